@@ -1,0 +1,351 @@
+"""Seeded synthetic inputs for the tree-verify hot path.
+
+This module only draws random numbers and lays them out; it holds none of the
+method's arithmetic (no ancestor tables, no attention, no argmax, no
+acceptance, no commit, no path scores).  Both the CPU oracle (through the
+tests) and the CUDA path read the arrays it returns, so the two sides always
+see identical bits.
+
+Shapes follow the five verify workloads:
+
+* ``tiny``    B=1, Hq=Hkv=4, D=64, prefix 128, 15-node random tree
+              (depth <= 4, <= 3 children), V=1000, logits N(0,1), match 0.5.
+* ``8b``      B=1, Hq=32, Hkv=8, D=128, prefix 4096, 63-node static
+              level-order tree (depth 6), V=128256, logits N(0,2), match 0.7.
+* ``ragged``  B=16, Hq=32, Hkv=8, D=128, prefix ~ U[512, 8192], 31-node random
+              trees (depth <= 5), V=32000, logits N(0,1), match 0.6.
+* ``70b``     B=4, Hq=64, Hkv=8, D=128, prefix 32768, 127-node random trees
+              (depth <= 8), V=128256, logits N(0,2), match 0.7, paged cache
+              with a shuffled block table.
+* ``bastion`` B=8, K=16 draft positions, V=32000, draft marginals
+              softmax(N(0,2)) in fp32; the verify layer is the 8B shape with
+              prefix 2048.
+
+N(0,2) is read as variance 2.  Every row of target logits carries one planted
+target token whose logit is set to (row maximum + 1), so the target's greedy
+choice for each node is known by construction; a draft token "matches" when
+it equals the planted target of its parent.
+
+bf16 tensors are returned as ``uint16`` bit patterns (round to nearest even
+from an fp32 draw).
+"""
+
+from __future__ import annotations
+
+import dataclasses
+from typing import Dict, List, Optional
+
+import numpy as np
+
+PAGE = 16  # tokens per KV-cache block
+
+# --------------------------------------------------------------------------
+# primitive draws
+# --------------------------------------------------------------------------
+
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round fp32 values to bf16 (nearest, ties to even); return uint16 bits."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    rounded = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return rounded.astype(np.uint16)
+
+
+def normal_bf16(rng: np.random.Generator, shape, std: float = 1.0) -> np.ndarray:
+    x = rng.standard_normal(size=shape, dtype=np.float32)
+    if std != 1.0:
+        x *= np.float32(std)
+    return bf16_bits(x)
+
+
+def random_tree(rng: np.random.Generator, n: int, max_depth: int,
+                max_children: Optional[int] = None) -> np.ndarray:
+    """Parent array (root parent = -1).  Node i>0 picks its parent uniformly
+    among earlier nodes whose depth is < max_depth and (optionally) that have
+    fewer than max_children children."""
+    parent = np.full(n, -1, dtype=np.int32)
+    depth = [0]
+    kids = [0]
+    for i in range(1, n):
+        ok = [j for j in range(i)
+              if depth[j] < max_depth and (max_children is None or kids[j] < max_children)]
+        if not ok:
+            raise ValueError("tree constraints leave no parent for node %d" % i)
+        p = ok[int(rng.integers(len(ok)))]
+        parent[i] = p
+        depth.append(depth[p] + 1)
+        kids.append(0)
+        kids[p] += 1
+    return parent
+
+
+def level_order_tree(level_sizes: List[int], fanouts: List[List[int]]) -> np.ndarray:
+    """Static tree given level sizes and, for each level, the child counts of
+    that level's first nodes (the highest-ranked ones)."""
+    assert level_sizes[0] == 1
+    parent = [-1]
+    prev = [0]
+    nxt = 1
+    for lvl in range(1, len(level_sizes)):
+        counts = fanouts[lvl - 1]
+        assert sum(counts) == level_sizes[lvl], (lvl, counts)
+        cur = []
+        for rank, c in enumerate(counts):
+            for _ in range(c):
+                parent.append(prev[rank])
+                cur.append(nxt)
+                nxt += 1
+        prev = cur
+    return np.asarray(parent, dtype=np.int32)
+
+
+# Our own static shape for the 8B workload: level sizes 1, 8, 16, 16, 10, 8, 4.
+STATIC_8B_LEVELS = [1, 8, 16, 16, 10, 8, 4]
+STATIC_8B_FANOUT = [
+    [8],
+    [4, 3, 2, 2, 2, 1, 1, 1],
+    [4, 3, 2, 2, 1, 1, 1, 1, 1],
+    [3, 2, 2, 1, 1, 1],
+    [2, 2, 1, 1, 1, 1],
+    [1, 1, 1, 1],
+]
+
+
+def static_8b_tree() -> np.ndarray:
+    return level_order_tree(STATIC_8B_LEVELS, STATIC_8B_FANOUT)
+
+
+def chain_tree(n: int) -> np.ndarray:
+    p = np.arange(-1, n - 1, dtype=np.int32)
+    return p
+
+
+def relabel(rng: np.random.Generator, parent: np.ndarray) -> np.ndarray:
+    """Randomly permute the ids of nodes 1..n-1 (root stays 0), so parents may
+    come after their children."""
+    n = len(parent)
+    perm = np.concatenate([[0], 1 + rng.permutation(n - 1)]).astype(np.int64)
+    out = np.full(n, -1, dtype=np.int32)
+    for old in range(1, n):
+        out[perm[old]] = perm[parent[old]]
+    return out
+
+
+def plant_targets(logits: np.ndarray, targets: np.ndarray) -> None:
+    """In place: for each row r, set logits[r, targets[r]] = max(row) + 1."""
+    flat = logits.reshape(-1, logits.shape[-1])
+    t = targets.reshape(-1)
+    mx = flat.max(axis=1)
+    flat[np.arange(flat.shape[0]), t] = mx + np.float32(1.0)
+
+
+def draft_tokens(rng: np.random.Generator, parent: np.ndarray, targets: np.ndarray,
+                 p_match: float, vocab: int) -> np.ndarray:
+    """tokens[i] = targets[parent[i]] with probability p_match, else uniform.
+    The root's token is uniform (it is the token emitted by the last step)."""
+    n = len(parent)
+    tok = rng.integers(0, vocab, size=n, dtype=np.int64)
+    coin = rng.random(n)
+    for i in range(1, n):
+        if parent[i] >= 0 and coin[i] < p_match:
+            tok[i] = targets[parent[i]]
+    return tok.astype(np.int32)
+
+
+# --------------------------------------------------------------------------
+# paged KV cache
+# --------------------------------------------------------------------------
+
+
+@dataclasses.dataclass
+class PagedCache:
+    k: np.ndarray            # uint16 [num_blocks][Hkv][PAGE][D]
+    v: np.ndarray            # uint16 [num_blocks][Hkv][PAGE][D]
+    block_table: np.ndarray  # int32 [B][max_blocks]
+    num_blocks: int
+    max_blocks: int
+
+
+def paged_cache(rng: np.random.Generator, prefix_len: np.ndarray, n_nodes: np.ndarray,
+                hkv: int, d: int, shuffle: bool, spare_blocks: int = 0) -> PagedCache:
+    """Cache pool holding, for each sequence b, slots [0, P_b + N_b): the
+    committed prefix followed by the draft tree's own K/V (slot P_b + i holds
+    real node i).  Every slot in the pool is N(0,1) bf16."""
+    B = len(prefix_len)
+    need = [(int(prefix_len[b]) + int(n_nodes[b]) + PAGE - 1) // PAGE for b in range(B)]
+    max_blocks = max(need) if B else 1
+    num_blocks = sum(need) + spare_blocks
+    ids = np.arange(num_blocks, dtype=np.int32)
+    if shuffle:
+        ids = rng.permutation(num_blocks).astype(np.int32)
+    table = np.zeros((B, max_blocks), dtype=np.int32)
+    pos = 0
+    for b in range(B):
+        table[b, :need[b]] = ids[pos:pos + need[b]]
+        pos += need[b]
+    k = normal_bf16(rng, (num_blocks, hkv, PAGE, d))
+    v = normal_bf16(rng, (num_blocks, hkv, PAGE, d))
+    return PagedCache(k=k, v=v, block_table=table, num_blocks=num_blocks, max_blocks=max_blocks)
+
+
+# --------------------------------------------------------------------------
+# workloads
+# --------------------------------------------------------------------------
+
+
+@dataclasses.dataclass
+class VerifyInputs:
+    name: str
+    B: int
+    N_max: int
+    Hq: int
+    Hkv: int
+    D: int
+    V: int
+    D_max: int
+    parent: np.ndarray       # int32 [B][N_max]
+    n_nodes: np.ndarray      # int32 [B]
+    prefix_len: np.ndarray   # int32 [B]
+    tokens: np.ndarray       # int32 [B][N_max]
+    logits: np.ndarray       # float32 [B][N_max][V]
+    q: np.ndarray            # uint16 [B][N_max][Hq][D]
+    cache: PagedCache
+    targets: np.ndarray      # int32 [B][N_max] planted target token per node
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / float(np.sqrt(self.D))
+
+
+WORKLOADS = {
+    # name: (B, Hq, Hkv, D, prefix, N, V, D_max, logit_std, p_match)
+    "tiny": (1, 4, 4, 64, 128, 15, 1000, 4, 1.0, 0.5),
+    "8b": (1, 32, 8, 128, 4096, 63, 128256, 6, float(np.sqrt(2.0)), 0.7),
+    "ragged": (16, 32, 8, 128, None, 31, 32000, 5, 1.0, 0.6),
+    "70b": (4, 64, 8, 128, 32768, 127, 128256, 8, float(np.sqrt(2.0)), 0.7),
+}
+SEEDS = {"tiny": 0, "8b": 1, "ragged": 2, "70b": 3, "bastion": 4}
+
+
+def _trees_for(name: str, rng: np.random.Generator, B: int, N: int) -> np.ndarray:
+    if name == "tiny":
+        return np.stack([random_tree(rng, N, 4, 3) for _ in range(B)])
+    if name == "8b":
+        return np.stack([static_8b_tree() for _ in range(B)])
+    if name == "ragged":
+        return np.stack([random_tree(rng, N, 5) for _ in range(B)])
+    if name == "70b":
+        return np.stack([random_tree(rng, N, 8) for _ in range(B)])
+    raise KeyError(name)
+
+
+def verify_workload(name: str, seed: Optional[int] = None, with_logits: bool = True) -> VerifyInputs:
+    """One of the four fixed-tree verify workloads, fully materialised."""
+    B, Hq, Hkv, D, prefix, N, V, D_max, lstd, pm = WORKLOADS[name]
+    rng = np.random.default_rng(SEEDS[name] if seed is None else seed)
+    parent = _trees_for(name, rng, B, N)
+    n_nodes = np.full(B, N, dtype=np.int32)
+    if prefix is None:
+        prefix_len = rng.integers(512, 8192, size=B, endpoint=True).astype(np.int32)
+    else:
+        prefix_len = np.full(B, prefix, dtype=np.int32)
+    targets = rng.integers(0, V, size=(B, N)).astype(np.int32)
+    tokens = np.stack([draft_tokens(rng, parent[b], targets[b], pm, V) for b in range(B)])
+    if with_logits:
+        logits = rng.standard_normal(size=(B, N, V), dtype=np.float32)
+        if lstd != 1.0:
+            logits *= np.float32(lstd)
+        plant_targets(logits, targets)
+    else:
+        logits = np.zeros((0,), dtype=np.float32)
+    q = normal_bf16(rng, (B, N, Hq, D))
+    cache = paged_cache(rng, prefix_len, n_nodes, Hkv, D, shuffle=(name == "70b"))
+    return VerifyInputs(name=name, B=B, N_max=N, Hq=Hq, Hkv=Hkv, D=D, V=V, D_max=D_max,
+                        parent=parent, n_nodes=n_nodes, prefix_len=prefix_len, tokens=tokens,
+                        logits=logits, q=q, cache=cache, targets=targets)
+
+
+# BASTION-style budgeted trees -------------------------------------------------
+
+BASTION = dict(B=8, K=16, V=32000, Hq=32, Hkv=8, D=128, prefix=2048, p_match=0.6,
+               budgets=(16, 32, 64, 128, 256))
+
+
+def bastion_marginals(seed: Optional[int] = None):
+    """Per-sequence draft marginals q[B][K][V] = softmax(z), z ~ N(0,2).  The
+    softmax is taken in fp64 and rounded once to fp32; both sides read that
+    fp32 array.  Also returns the root tokens (uniform)."""
+    c = BASTION
+    rng = np.random.default_rng(SEEDS["bastion"] if seed is None else seed)
+    z = rng.standard_normal(size=(c["B"], c["K"], c["V"])) * np.sqrt(2.0)
+    z -= z.max(axis=-1, keepdims=True)
+    e = np.exp(z)
+    q = (e / e.sum(axis=-1, keepdims=True)).astype(np.float32)
+    root = rng.integers(0, c["V"], size=c["B"]).astype(np.int32)
+    return q, root
+
+
+def bastion_verify_inputs(parent: np.ndarray, tokens: np.ndarray, depth: np.ndarray,
+                          draft_top1: np.ndarray, seed: Optional[int] = None) -> VerifyInputs:
+    """Verify-layer inputs for a built budgeted tree.
+
+    ``parent``/``tokens``/``depth`` describe the tree [B][N]; ``draft_top1``
+    [B][K] is the draft's most likely token at each position (supplied by the
+    caller).  For node i the planted target is draft_top1[depth(i)+1] with
+    probability 0.6 (when that position exists), else a uniform token."""
+    c = BASTION
+    B, N = parent.shape
+    rng = np.random.default_rng((SEEDS["bastion"] if seed is None else seed) * 1000 + N)
+    targets = rng.integers(0, c["V"], size=(B, N)).astype(np.int32)
+    coin = rng.random((B, N))
+    for b in range(B):
+        for i in range(N):
+            pos = int(depth[b, i]) + 1
+            if pos <= c["K"] and coin[b, i] < c["p_match"]:
+                targets[b, i] = draft_top1[b, pos - 1]
+    logits = rng.standard_normal(size=(B, N, c["V"]), dtype=np.float32) * np.float32(np.sqrt(2.0))
+    plant_targets(logits, targets)
+    q = normal_bf16(rng, (B, N, c["Hq"], c["D"]))
+    prefix_len = np.full(B, c["prefix"], dtype=np.int32)
+    n_nodes = np.full(B, N, dtype=np.int32)
+    cache = paged_cache(rng, prefix_len, n_nodes, c["Hkv"], c["D"], shuffle=False)
+    return VerifyInputs(name="bastion%d" % N, B=B, N_max=N, Hq=c["Hq"], Hkv=c["Hkv"], D=c["D"],
+                        V=c["V"], D_max=min(16, N - 1), parent=parent.astype(np.int32),
+                        n_nodes=n_nodes, prefix_len=prefix_len, tokens=tokens.astype(np.int32),
+                        logits=logits, q=q, cache=cache, targets=targets)
+
+
+def random_small(seed: int, B: int, N_max: int, Hq: int, Hkv: int, D: int, V: int,
+                 prefix_lo: int, prefix_hi: int, max_depth: int, p_match: float = 0.6,
+                 ragged_nodes: bool = True, shuffle_blocks: bool = True,
+                 relabel_ids: bool = True, logit_std: float = 1.0) -> VerifyInputs:
+    """Randomised small verify inputs for parity sweeps: ragged node counts
+    (padding rows), arbitrary parent order, shuffled pages."""
+    rng = np.random.default_rng(seed)
+    if ragged_nodes:
+        n_nodes = rng.integers(1, N_max, size=B, endpoint=True).astype(np.int32)
+    else:
+        n_nodes = np.full(B, N_max, dtype=np.int32)
+    parent = np.full((B, N_max), 0, dtype=np.int32)
+    for b in range(B):
+        nb = int(n_nodes[b])
+        p = random_tree(rng, nb, max_depth)
+        if relabel_ids and nb > 2:
+            p = relabel(rng, p)
+        parent[b, :nb] = p
+        # padding entries hold junk that must be ignored
+        parent[b, nb:] = rng.integers(-5, 2 * N_max, size=N_max - nb)
+    prefix_len = rng.integers(prefix_lo, prefix_hi, size=B, endpoint=True).astype(np.int32)
+    targets = rng.integers(0, V, size=(B, N_max)).astype(np.int32)
+    tokens = np.zeros((B, N_max), dtype=np.int32)
+    for b in range(B):
+        nb = int(n_nodes[b])
+        tokens[b, :nb] = draft_tokens(rng, parent[b, :nb], targets[b, :nb], p_match, V)
+        tokens[b, nb:] = rng.integers(0, V, size=N_max - nb)
+    logits = rng.standard_normal(size=(B, N_max, V), dtype=np.float32) * np.float32(logit_std)
+    plant_targets(logits, targets)
+    q = normal_bf16(rng, (B, N_max, Hq, D))
+    cache = paged_cache(rng, prefix_len, n_nodes, Hkv, D, shuffle=shuffle_blocks, spare_blocks=3)
+    return VerifyInputs(name="random%d" % seed, B=B, N_max=N_max, Hq=Hq, Hkv=Hkv, D=D, V=V,
+                        D_max=max_depth, parent=parent, n_nodes=n_nodes, prefix_len=prefix_len,
+                        tokens=tokens, logits=logits, q=q, cache=cache, targets=targets)

@@ -1,0 +1,73 @@
+"""Commit of the accepted path's K/V into the committed cache.
+
+Follows [EP-zh] 2.1 (branchable KV cache: length-based commit keeps the prefix
+and the first A steps of the chosen branch; path-index commit reorders the
+cache along the accepted path; the prefix-sharing fast reorder moves only the
+newly accepted segment, and only when needed) and [EP-pt] section 2 (the fast
+reorder preserves the accepted prefix to avoid needless memory movement).
+
+Readings taken where the pages are silent:
+
+* Before the call, sequence b's draft tree K/V sit in the paged cache at slot
+  P_b + i for real node i (the speculative tail after the committed prefix).
+* For k = 0..A: slot P_b + k receives the entry of slot P_b + (path[k] - 1).
+  An entry already in place (path[k] - 1 == k) is not copied.  The root
+  (k = 0) is always in place.
+* All sources are read before any destination is written (a destination can
+  be the source of a later path element).
+* new_len[b] = P_b + A + 1; moved[b] = number of k with path[k] - 1 != k.
+* A sequence with err != 0 commits nothing: new_len = P_b, moved = 0.
+* Slots >= new_len are unspecified afterwards.
+* The cache may hold several layers: [L][num_blocks][Hkv][16][D]; every layer
+  is committed with the same path.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+PAGE = 16
+
+
+def commit_path(k_cache, v_cache, block_table, prefix_len, accept_len, path, err):
+    """Returns (k_new, v_new, new_len, moved); inputs are not modified."""
+    k_new = np.array(k_cache, copy=True)
+    v_new = np.array(v_cache, copy=True)
+    layered = k_new.ndim == 5
+    if not layered:
+        k_new = k_new[None]
+        v_new = v_new[None]
+    B = len(prefix_len)
+    new_len = np.zeros(B, dtype=np.int32)
+    moved = np.zeros(B, dtype=np.int32)
+
+    def where(b, slot):
+        return int(block_table[b, slot // PAGE]), slot % PAGE
+
+    for b in range(B):
+        P = int(prefix_len[b])
+        if int(err[b]) != 0:
+            new_len[b] = P
+            continue
+        A = int(accept_len[b])
+        copies = []
+        for k in range(A + 1):
+            src = P + int(path[b, k]) - 1
+            dst = P + k
+            if src != dst:
+                copies.append((dst, src))
+        # read every source first
+        staged = []
+        for dst, src in copies:
+            pg, row = where(b, src)
+            staged.append((dst, k_new[:, pg, :, row, :].copy(), v_new[:, pg, :, row, :].copy()))
+        for dst, kk, vv in staged:
+            pg, row = where(b, dst)
+            k_new[:, pg, :, row, :] = kk
+            v_new[:, pg, :, row, :] = vv
+        new_len[b] = P + A + 1
+        moved[b] = len(copies)
+    if not layered:
+        k_new = k_new[0]
+        v_new = v_new[0]
+    return k_new, v_new, new_len, moved
