@@ -1,0 +1,511 @@
+#!/usr/bin/env python3
+"""Benchmark of the tree-verify hot path on one GB300 per rank.
+
+One step = ancestors (a1) + tree attention (a2) + greedy verify (a3) + KV
+commit (a4) for the whole batch of one layer, back to back on one stream
+(plus the best-first tree build a5 for the budgeted-tree workloads).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 8b]
+  python bench.py --impl reference ...   # the CPU oracle arm
+
+Prints ONE JSON line (rank 0).  Inputs are synthetic (seeded, the shapes of
+the named workload) and resident in HBM before timing; L2 is flushed between
+timed steps by writing a 256 MiB buffer outside the timed events.  Under
+torchrun every rank runs its own replica (sequences are independent units;
+no data-path collective): value = all ranks' steps / max-over-ranks time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import gen  # noqa: E402
+
+METRIC = "tree-verify steps/s (attn+accept+commit) and achieved HBM GB/s vs GB300 peak"
+FALLBACK_HBM_GBS = 6800.0
+FLUSH_BYTES = 256 << 20
+DESCRIPTIONS = {
+    "tiny": "tiny verify layer: B=1, Hq=Hkv=4, D=64, prefix 128, 15-node random tree, V=1000",
+    "8b": "Llama-3-8B-shaped verify layer: B=1, Hq=32, Hkv=8, D=128, prefix 4096, 63-node static "
+          "tree (depth 6), V=128256",
+    "ragged": "batched ragged verify layer: B=16, Hq=32, Hkv=8, D=128, prefix U[512,8192], "
+              "31-node random trees (depth<=5), V=32000",
+    "70b": "long-context 70B-shaped verify layer: B=4, Hq=64, Hkv=8, D=128, prefix 32768, "
+           "127-node random trees (depth<=8), V=128256, paged cache with shuffled 16-token blocks",
+}
+
+
+def workload_inputs(name):
+    """Host arrays for a workload (numpy), and a description."""
+    if name.startswith("bastion"):
+        N = int(name[len("bastion"):])
+        q, root = gen.bastion_marginals()
+        return ("bastion", N, q, root), ("BASTION-style budgeted tree: B=8, K=16, V=32000 "
+                                         "marginals, best-first budget N=%d, verify on Hq=32, "
+                                         "Hkv=8, D=128, prefix 2048" % N)
+    return gen.verify_workload(name), DESCRIPTIONS[name]
+
+
+def algorithmic_bytes(inp, moved_total):
+    """Per-kernel algorithmic bytes of one step (what each kernel must move at
+    least once)."""
+    B, N, Hq, Hkv, D, V, Dm = inp.B, inp.N_max, inp.Hq, inp.Hkv, inp.D, inp.V, inp.D_max
+    W = (N + 31) // 32
+    slots = int((inp.prefix_len.astype(np.int64) + inp.n_nodes).sum())
+    a1 = 4 * (B * N + B + B * (N + 1) * (Dm + 1) + B * N + B * N * W + B)
+    a2 = 4 * Hkv * D * slots + 4 * B * N * Hq * D + 4 * B * N * Hq
+    a3 = 4 * B * N * V
+    a4 = 8 * Hkv * D * int(moved_total)
+    return {"tree_build_ancestors": a1, "tree_attn_fwd": a2, "tree_verify_greedy": a3,
+            "kv_commit_path": a4}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)", pk
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 measurement)", {}
+
+
+def kernel_sources_digest():
+    csrc = os.path.join(ROOT, "tree_speculative_decoding_virtual_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key, workload):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
+    the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic_%s_%s.md" % (kernel_key, workload))
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    d = re.search(r"kernel_sources_sha256_16:\s*([0-9a-f]+)", text)
+    if not m or not d or d.group(1) != kernel_sources_digest():
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    def __init__(self, index):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench.csv")
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index),
+                 "--query-gpu=timestamp,clocks.sm,clocks.max.sm,power.draw,"
+                 "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+                 "clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        self.marks = []
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[2]) if v == "Active"})
+        loaded = [r[0] for r in rows]
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg and reference arm)
+# ---------------------------------------------------------------------------
+
+ORACLE_CHILD = r"""
+import json, os, sys, time
+sys.path.insert(0, %(root)r)
+import numpy as np
+import gen, oracle
+name, steps, frac = %(name)r, %(steps)d, %(frac)f
+inp = gen.verify_workload(name)
+rng = np.random.default_rng(0)
+rows = [(b, i, h) for b in range(inp.B) for i in range(int(inp.n_nodes[b])) for h in range(inp.Hq)]
+pick = rng.choice(len(rows), size=max(1, int(round(frac * len(rows)))), replace=False)
+sample = [rows[j] for j in sorted(pick)]
+c = inp.cache
+t_attn = t_rest = 0.0
+for s in range(steps):
+    t0 = time.perf_counter()
+    anc, depth, mask, err = oracle.build_ancestors(inp.parent, inp.n_nodes, inp.D_max)
+    t1 = time.perf_counter()
+    out, lse = oracle.tree_attention(inp.q, c.k, c.v, c.block_table, inp.prefix_len, inp.n_nodes,
+                                     inp.parent, err, inp.scale, sample=sample)
+    t2 = time.perf_counter()
+    am, A, leaf, path, bonus = oracle.verify_greedy(inp.logits, inp.tokens, inp.parent,
+                                                    inp.n_nodes, err, inp.D_max)
+    k1, v1, nl, mv = oracle.commit_path(c.k, c.v, c.block_table, inp.prefix_len, A, path, err)
+    t3 = time.perf_counter()
+    t_attn += t2 - t1
+    t_rest += (t1 - t0) + (t3 - t2)
+per_step_full = (t_rest + t_attn / (len(sample) / len(rows))) / steps
+print(json.dumps({"sec_per_full_step": per_step_full, "steps": steps, "sample_rows": len(sample),
+                  "total_rows": len(rows), "wall": t_attn + t_rest}))
+"""
+
+
+def run_oracle_child(name, steps, frac, threads):
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = str(threads)
+    code = ORACLE_CHILD % {"root": ROOT, "name": name, "steps": steps, "frac": frac}
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                       timeout=1800)
+    if r.returncode != 0:
+        raise RuntimeError("oracle child failed: " + r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def oracle_sample_fraction(name):
+    # attention rows evaluated per oracle step (the rest of the step runs in full)
+    return {"tiny": 1.0, "8b": 0.125, "ragged": 0.05, "70b": 0.004}.get(name, 0.05)
+
+
+def cpu_baseline(name, budget_steps=3):
+    threads = os.cpu_count() or 1
+    frac = oracle_sample_fraction(name)
+    res = run_oracle_child(name, budget_steps, frac, threads)
+    value = 1.0 / res["sec_per_full_step"]
+    return {"value": value, "unit": "steps/s", "cores": threads, "kind": "oracle",
+            "sample": "%d oracle steps of the %s workload; each runs ancestors, verify and commit "
+                      "in full and attention on %d of %d (seq, node, q-head) rows, scaled to the "
+                      "full row count" % (res["steps"], name, res["sample_rows"],
+                                           res["total_rows"])}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def gpu_arm(args, rank, world):
+    import torch
+    import torch.distributed as dist
+
+    import tree_speculative_decoding_virtual_gb300 as tsd
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+
+    w, desc = workload_inputs(args.workload)
+    bastion = isinstance(w, tuple)
+
+    def T(a, dtype=None):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if dtype is not None:
+            t = t.view(dtype)
+        return t.to(dev)
+
+    if bastion:
+        _, N_b, q_marg, root = w
+        qd, rootd = T(q_marg), T(root)
+        bf_ws = torch.empty(tsd.best_first_workspace_bytes(*q_marg.shape, N_b), dtype=torch.uint8,
+                            device=dev)
+        bf_out = [torch.empty((q_marg.shape[0], N_b), dtype=torch.int32, device=dev) for _ in range(3)]
+        rho = torch.empty((q_marg.shape[0], N_b), dtype=torch.float32, device=dev)
+        ahat = torch.empty((q_marg.shape[0],), dtype=torch.float64, device=dev)
+        tsd.best_first_tree_build(qd, rootd, N_b, *bf_out, rho, ahat, workspace=bf_ws)
+        torch.cuda.synchronize()
+        par_h, tok_h, dep_h = [x.cpu().numpy() for x in bf_out]
+        top1 = np.argmax(q_marg, axis=-1)  # input synthesis only: plants target choices
+        inp = gen.bastion_verify_inputs(par_h, tok_h, dep_h, top1)
+    else:
+        inp = w
+
+    B, N, Hq, Hkv, D, V, Dm = inp.B, inp.N_max, inp.Hq, inp.Hkv, inp.D, inp.V, inp.D_max
+    c = inp.cache
+    parent, n_nodes, prefix = T(inp.parent), T(inp.n_nodes), T(inp.prefix_len)
+    tokens, logits, q = T(inp.tokens), T(inp.logits), T(inp.q, torch.bfloat16)
+    table = T(c.block_table)
+    kc, vc = T(c.k, torch.bfloat16), T(c.v, torch.bfloat16)
+    max_slots = int((inp.prefix_len + inp.n_nodes).max())
+    W = (N + 31) // 32
+    i32 = dict(dtype=torch.int32, device=dev)
+    anc = torch.empty((B, N + 1, Dm + 1), **i32)
+    depth = torch.empty((B, N), **i32)
+    mask = torch.empty((B, N, W), **i32)
+    err = torch.empty((B,), **i32)
+    out = torch.empty((B, N, Hq, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, N, Hq), dtype=torch.float32, device=dev)
+    attn_ws = torch.empty((tsd.tree_attn_workspace_bytes(B, N, Hq, Hkv, D, max_slots),),
+                          dtype=torch.uint8, device=dev)
+    ver_ws = torch.zeros((tsd.tree_verify_workspace_bytes(B, N, V),), dtype=torch.uint8, device=dev)
+    am = torch.empty((B, N), **i32)
+    A = torch.empty((B,), **i32)
+    leaf = torch.empty((B,), **i32)
+    path = torch.empty((B, Dm + 1), **i32)
+    bonus = torch.empty((B,), **i32)
+    new_len = torch.empty((B,), **i32)
+    moved = torch.empty((B,), **i32)
+    status = torch.zeros((1,), **i32)
+    flush = torch.empty((FLUSH_BYTES,), dtype=torch.uint8, device=dev)
+
+    names = (["best_first_tree_build"] if bastion else []) + [
+        "tree_build_ancestors", "tree_attn_fwd", "tree_verify_greedy", "kv_commit_path"]
+    launches_per_step = (2 if bastion else 0) + 1 + 2 + 1 + 1
+
+    def step(ev=None):
+        k = 0
+        if ev is not None:
+            ev[k].record(stream)
+        if bastion:
+            tsd.best_first_tree_build(qd, rootd, N_b, *bf_out, rho, ahat, workspace=bf_ws)
+            k += 1
+            if ev is not None:
+                ev[k].record(stream)
+        tsd.tree_build_ancestors(parent, n_nodes, Dm, anc, depth, mask, err)
+        if ev is not None:
+            ev[k + 1].record(stream)
+        tsd.tree_attn_fwd(q, kc, vc, table, prefix, n_nodes, mask, err, max_slots, out=out, lse=lse,
+                          workspace=attn_ws, status=status)
+        if ev is not None:
+            ev[k + 2].record(stream)
+        tsd.tree_verify_greedy(logits, tokens, parent, anc, depth, mask, n_nodes, err, Dm, am, A,
+                               leaf, path, bonus, workspace=ver_ws)
+        if ev is not None:
+            ev[k + 3].record(stream)
+        tsd.kv_commit_path(kc, vc, table, prefix, n_nodes, A, path, err, N, Dm, new_len=new_len,
+                           moved=moved, status=status)
+        if ev is not None:
+            ev[k + 4].record(stream)
+
+    nev = len(names) + 1
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    moved_total = int(moved.sum().item())
+    assert int(status.item()) == 0, "device status %d" % int(status.item())
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    for s in range(args.steps):
+        flush.zero_()
+        step(events[s])
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        dist.barrier()
+    per_kernel = {n: 0.0 for n in names}
+    total_ms = 0.0
+    for ev in events:
+        for j, n in enumerate(names):
+            per_kernel[n] += ev[j].elapsed_time(ev[j + 1])
+        total_ms += ev[0].elapsed_time(ev[-1])
+    ms_per_step = total_ms / args.steps
+    if world > 1:
+        t = torch.tensor([ms_per_step], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+    kernel_us = {n: 1000.0 * v / args.steps for n, v in per_kernel.items()}
+
+    # ---- e2e: host buffers through the public API, copies inside the timing ----
+    h_in = {"q": q, "logits": logits, "parent": parent, "tokens": tokens, "n_nodes": n_nodes,
+            "prefix_len": prefix}
+    pinned = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in h_in.items()}
+    for k, v in h_in.items():
+        pinned[k].copy_(v.cpu())
+    h_out_src = {"out": out, "argmax": am, "accept_len": A, "leaf": leaf, "path": path,
+                 "bonus": bonus, "new_len": new_len}
+    h_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in h_out_src.items()}
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+    d2h = sum(v.numel() * v.element_size() for v in h_out.values())
+    e2e_steps = max(3, min(args.steps, 200))
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(e2e_steps)]
+    for s in range(e2e_steps + 3):
+        flush.zero_()
+        if s >= 3:
+            e2e_ev[s - 3][0].record(stream)
+        for k, v in h_in.items():
+            v.copy_(pinned[k], non_blocking=True)
+        step()
+        for k, v in h_out_src.items():
+            h_out[k].copy_(v, non_blocking=True)
+        if s >= 3:
+            e2e_ev[s - 3][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    clocks = sampler.stop() if sampler else None
+
+    if rank != 0:
+        return None
+    peak, peak_src, _ = load_peaks()
+    abytes = algorithmic_bytes(inp, moved_total)
+    step_bytes = sum(abytes.values())
+    dom = max(["tree_attn_fwd", "tree_verify_greedy"], key=lambda n: kernel_us[n])
+    achieved = abytes[dom] / (kernel_us[dom] * 1e-6) / 1e9
+    kernels = {}
+    for n in names:
+        entry = {"us": round(kernel_us[n], 3)}
+        if n in abytes:
+            gbs = abytes[n] / (kernel_us[n] * 1e-6) / 1e9 if kernel_us[n] > 0 else 0.0
+            entry.update({"algorithmic_bytes": abytes[n], "gbs": round(gbs, 1),
+                          "frac_of_hbm_peak": round(gbs / peak, 4)})
+        kernels[n] = entry
+    launches = launches_per_step * args.steps
+    result = {
+        "metric": METRIC,
+        "value": round(world * 1000.0 / ms_per_step, 2),
+        "unit": "steps/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 (attention, fp32 accumulate); f32 (logits argmax); int32 (tree, paths)",
+        "data": "synthetic (seeded; shapes and distributions of the named workload)",
+        "config": {"workload": desc, "name": args.workload, "global_batch": B * world,
+                   "seq_len": max_slots, "parallelism": "replicas (dp%d)" % world,
+                   "l2": "flushed between timed steps (256 MiB write outside the timed events)",
+                   "timing": "CUDA events per kernel on the launching stream; per-step sum"},
+        "hbm_gbs_step": round(step_bytes / (ms_per_step * 1e-3) / 1e9, 1),
+        "kernels": kernels,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": ncu_traffic(dom, args.workload), "peak_source": peak_src,
+                     "algorithmic_bytes_per_launch": abytes[dom]},
+        "e2e": {"value": round(1000.0 * world / e2e_ms, 2), "unit": "steps/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "wall_s_timed_region": round(t_wall, 4),
+        "mean_accept_len": float(A.float().mean().item()),
+    }
+    if args.workload == "70b":
+        # tensor-pipe bound on this shape: report the binding roofline too
+        flops = 4.0 * Hq * D * N * float(inp.prefix_len.astype(np.int64).sum())
+        result["attention_tflops"] = round(flops / (kernel_us["tree_attn_fwd"] * 1e-6) / 1e12, 1)
+    return result
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="8b")
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(reference_arm(args, world)), flush=True)
+        return 0
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.workload.startswith("bastion"):
+        base = cpu_baseline(args.workload)
+    res = gpu_arm(args, rank, world)
+    if rank == 0:
+        res["cpu_baseline"] = base
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def reference_arm(args, world):
+    """The oracle, as it stands, on the host cores: each step is a bounded
+    sample of the workload (attention on a sample of rows, the rest in full),
+    scaled to full-step units."""
+    name = args.workload if not args.workload.startswith("bastion") else "8b"
+    threads = os.cpu_count() or 1
+    frac = oracle_sample_fraction(name)
+    # size the run to a few minutes at most: measure one sampled step first
+    probe = run_oracle_child(name, 1, frac, threads)
+    per_sample = probe["wall"]
+    budget = 150.0
+    steps = max(1, min(args.steps, int(budget / max(per_sample, 1e-3)) - args.warmup))
+    res = run_oracle_child(name, steps, frac, threads)
+    sec = res["sec_per_full_step"]
+    _, desc = workload_inputs(name)
+    value = 1.0 / sec
+    sample = ("%d oracle steps of the %s workload (of %d requested); each runs ancestors, verify "
+              "and commit in full and attention on %d of %d (seq, node, q-head) rows, scaled to "
+              "the full row count" % (steps, name, args.steps, res["sample_rows"], res["total_rows"]))
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s",
+            "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": 1000.0 * sec,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; shapes and distributions of the named workload)",
+            "config": {"workload": desc, "name": name, "global_batch": None,
+                       "parallelism": "host cores"},
+            "cpu_baseline": {"value": value, "unit": "steps/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,236 @@
+/*
+ * tsd.h -- C ABI of the tree-speculative-decoding verify path (libtsd.so).
+ *
+ * The library runs, on one GPU, the target model's verification of a draft
+ * tree: safe ancestor tables with a virtual root, tree-masked attention over a
+ * paged KV cache, greedy longest-accepted-path search, and the fast-reorder
+ * commit of the accepted K/V.  An optional entry point builds best-first
+ * budgeted draft trees from per-position marginals.
+ *
+ * Sources (page title, section):
+ *   [EP-zh]   "EAGLE-Pangu: Accelerator-Safe Tree Speculative Decoding on
+ *             Ascend NPUs", technical summary (gist.science/zh/paper/2603.08088),
+ *             2.1 branchable KV cache, 2.2 accelerator-safe tree tensor
+ *             semantics, 2.3 fused tree-masked teacher execution.
+ *   [EP-pt]   the same paper's Portuguese technical summary, section 2.
+ *   [BASTION] "Resumo Técnico: BASTION" (gist.science/pt/paper/2605.29727),
+ *             Methodology 1 and 2.
+ *   [Blog]    "Speculative Decoding Hierárquico: Medusa, EAGLE-2 e
+ *             Multi-Token Prediction" (produtoramaxvision.com.br), sections
+ *             on Medusa tree attention and on vLLM PagedAttention.
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ * - Every array argument is a DEVICE pointer to memory the caller owns and
+ *   allocated.  The library allocates nothing, frees nothing and never
+ *   synchronises: all work is enqueued on `stream` (a cudaStream_t; NULL is
+ *   the legacy default stream) in launch order, and results are ready when
+ *   the stream reaches that point.
+ * - Return value: a host-detected status (TSD_OK or a negative TSD_ERR_*).
+ *   On a non-zero return nothing was launched (TSD_ERR_CUDA: a launch failed;
+ *   the CUDA error is left for the caller to query).
+ * - Problems the host cannot see (device-resident lengths, block ids, paths)
+ *   are reported on the device: per-sequence error bits in err[b], and a
+ *   device status word `status` (OR of TSD_STATUS_* bits; the caller zeroes it
+ *   when it wants a fresh reading).  Such sequences are skipped, never read or
+ *   written out of bounds (fail closed).
+ * - Node ids: callers give real ids 0..N_b-1; node 0 is the tree root (the
+ *   last emitted token, whose K/V is the first tree slot) with parent -1.
+ *   Tables built by the library use safe ids s = i + 1 with the virtual root at
+ *   0, so every gather index lies in [0, N_max] ([EP-zh] 2.2).
+ * - bf16 arrays are passed as uint16_t bit patterns.
+ * - KV cache: paged, 16 token slots per block, layout
+ *   [num_blocks][Hkv][16][D]; token slot t of sequence b lives in block
+ *   block_table[b * max_blocks + t / 16], row t % 16.  Sequence b's committed
+ *   prefix is slots [0, P_b); the draft tree's own K/V sit at slot P_b + i for
+ *   real node i ([EP-zh] 2.1 committed vs speculative state; [Blog] paged
+ *   blocks).
+ * - Limits (TSD_ERR_LIMIT): 1 <= N_max <= 256, 0 <= D_max <= 32,
+ *   D in {64, 128}, Hq % Hkv == 0, Hq / Hkv <= 16, B <= 65535.
+ */
+#ifndef TSD_H_
+#define TSD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *tsd_stream_t; /* same handle as cudaStream_t */
+
+/* host-detected status */
+enum {
+  TSD_OK = 0,
+  TSD_ERR_ARG = -1,       /* null pointer, negative size, misaligned pointer */
+  TSD_ERR_LIMIT = -2,     /* a size outside the limits listed above */
+  TSD_ERR_WORKSPACE = -3, /* workspace missing or smaller than required */
+  TSD_ERR_CUDA = -4       /* a kernel launch failed */
+};
+
+/* err[b] bits written by tsd_tree_build_ancestors ([EP-zh] 2.2 checks) */
+#define TSD_TREE_RANGE 1   /* non-root parent outside [0, N_max) (incl. a second -1) */
+#define TSD_TREE_CYCLE 2   /* walking up from a node does not reach the root */
+#define TSD_TREE_TOO_DEEP 4 /* a node deeper than D_max */
+#define TSD_TREE_CLOSURE 8 /* a valid node whose parent is a padding node */
+#define TSD_TREE_ROOT 16   /* parent[0] != -1 */
+#define TSD_TREE_COUNT 32  /* n_nodes[b] outside [1, N_max] */
+
+/* device status word bits */
+#define TSD_STATUS_BAD_PAGE 1 /* a block id outside [0, num_blocks): sequence skipped */
+#define TSD_STATUS_BAD_LEN 2  /* P_b < 0 or P_b + N_b beyond max_slots / the table */
+#define TSD_STATUS_BAD_PATH 4 /* accept_len / path inconsistent with the tree */
+
+/* Library version string (static storage). */
+const char *tsd_version(void);
+
+/*
+ * a1. Accelerator-safe tree tensors ([EP-zh] 2.2; [EP-pt] section 2,
+ *     "Semântica de Tensores em Árvore Segura").
+ *
+ * Replaces the root's -1 sentinel by a virtual root row 0, builds the
+ * ancestor index table, the per-node ancestor bitmask and the depth, and runs
+ * the range / acyclicity / validity-closure checks before any fused kernel.
+ *
+ * parent   int32 [B][N_max]  real ids; parent[b][0] must be -1; entries of
+ *                             padding nodes (i >= n_nodes[b]) are ignored.
+ *                             Any order is allowed (no topological order).
+ * n_nodes  int32 [B] or NULL (NULL: every sequence has N_max nodes).
+ * anc      int32 [B][N_max+1][D_max+1]  out.  anc[b][s][d] = safe id of the
+ *                             depth-d ancestor of safe node s (d <= depth),
+ *                             0 beyond; row 0 (virtual root) and padding rows
+ *                             are all 0.
+ * depth    int32 [B][N_max]  out.  depth(root) = 0; padding rows 0.
+ * mask     uint32 [B][N_max][W], W = ceil(N_max / 32)  out.  Bit j of row i is
+ *                             set iff real node j is i or an ancestor of i.
+ * err      int32 [B]  out.  OR of TSD_TREE_* bits; a sequence with err != 0
+ *                             gets all-zero rows and is skipped by the other
+ *                             entry points.
+ * One thread block per sequence.
+ */
+int tsd_tree_build_ancestors(const int32_t *parent, const int32_t *n_nodes, int B, int N_max,
+                             int D_max, int32_t *anc, int32_t *depth, uint32_t *mask, int32_t *err,
+                             tsd_stream_t stream);
+
+/*
+ * a2. Tree-masked attention for all tree nodes in one pass ([EP-zh] 2.3:
+ *     node k attends only to its ancestor path and itself, no cross-branch
+ *     leakage; [Blog] Medusa tree attention mask).
+ *
+ * For every valid (b, node i, q head h):
+ *   out = softmax(scale * q . K^T) V over the keys of kv head h / (Hq/Hkv):
+ *   every prefix slot [0, P_b), plus tail slot P_b + j iff bit j of
+ *   mask[b][i] is set.  fp32 accumulation, out rounded to bf16 (nearest
+ *   even).  lse (optional) = natural log of the sum of exp(scale * q . k).
+ * No positional rotation is applied (rotate q/k with position P_b + depth).
+ *
+ * q           bf16 [B][N_max][Hq][D]
+ * k_cache,
+ * v_cache     bf16 [num_blocks][Hkv][16][D]   (see conventions)
+ * block_table int32 [B][max_blocks]
+ * prefix_len  int32 [B]   P_b
+ * n_nodes     int32 [B] or NULL
+ * mask        uint32 [B][N_max][W]   from tsd_tree_build_ancestors
+ * err         int32 [B] or NULL      sequences with err != 0 are skipped
+ * max_slots   host upper bound on P_b + N_b over the batch; it sizes the
+ *             split-KV grid.  A sequence exceeding it sets
+ *             TSD_STATUS_BAD_LEN and is skipped.
+ * out         bf16 [B][N_max][Hq][D]  out.  Skipped / padding rows are 0.
+ * lse         float [B][N_max][Hq] or NULL  out.  Skipped rows -inf.
+ * workspace   device scratch of ws_bytes >= tsd_tree_attn_workspace_bytes()
+ *             (fp32 split-KV partials; no initial contents required).
+ * status      int32 device word (see TSD_STATUS_*), may be NULL.
+ */
+size_t tsd_tree_attn_workspace_bytes(int B, int N_max, int Hq, int Hkv, int D, int max_slots);
+int tsd_tree_attn_fwd(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                      const int32_t *block_table, int max_blocks, int num_blocks,
+                      const int32_t *prefix_len, const int32_t *n_nodes, const uint32_t *mask,
+                      const int32_t *err, int B, int N_max, int Hq, int Hkv, int D, int max_slots,
+                      float scale, uint16_t *out, float *lse, void *workspace, size_t ws_bytes,
+                      int32_t *status, tsd_stream_t stream);
+
+/*
+ * a3. Greedy verification ([Blog] Medusa: the target evaluates every branch
+ *     in one parallel pass and the longest valid path is selected; [EP-zh]
+ *     lay summary section 3).
+ *
+ * argmax[b][i] = first index of the maximum of logits[b][i][0..V) (exact fp32
+ * compares, lowest index on ties, +0 == -0).  Acceptance: the root is
+ * accepted; node i is accepted iff its parent is and tokens[b][i] ==
+ * argmax[b][parent(i)].  leaf = deepest accepted node (lowest id on ties);
+ * accept_len = depth(leaf); path[b][k] = anc[b][leaf+1][k] for k <= accept_len,
+ * 0 beyond; bonus = argmax[b][leaf].
+ *
+ * logits  float [B][N_max][V]; tokens, parent int32 [B][N_max];
+ * anc, depth, mask, err  from tsd_tree_build_ancestors; n_nodes int32 [B] or NULL.
+ * argmax  int32 [B][N_max] out (-1 for padding rows and skipped sequences);
+ * accept_len, leaf, bonus int32 [B] out; path int32 [B][D_max+1] out.
+ * A sequence with err != 0: accept_len 0, leaf -1, bonus -1, path 0.
+ * workspace  >= tsd_tree_verify_workspace_bytes() bytes, ZERO-FILLED before
+ *            its first use; every call leaves it zero-filled again.  Calls
+ *            sharing one workspace must not overlap on the GPU.
+ * One fused launch: a grid-wide argmax scan over V, and the block that
+ * finishes a sequence's last chunk runs its acceptance search.
+ */
+size_t tsd_tree_verify_workspace_bytes(int B, int N_max, int V);
+int tsd_tree_verify_greedy(const float *logits, const int32_t *tokens, const int32_t *parent,
+                           const int32_t *anc, const int32_t *depth, const uint32_t *mask,
+                           const int32_t *n_nodes, const int32_t *err, int B, int N_max, int V,
+                           int D_max, int32_t *argmax, int32_t *accept_len, int32_t *leaf,
+                           int32_t *path, int32_t *bonus, void *workspace, size_t ws_bytes,
+                           tsd_stream_t stream);
+
+/*
+ * a4. Commit of the accepted path with the prefix-sharing fast reorder
+ *     ([EP-zh] 2.1: path-index commit reorders the cache along the accepted
+ *     path and moves only the newly accepted segment, only when needed;
+ *     length-based commit is the case where nothing moves; [EP-pt] section 2).
+ *
+ * For k = 0..accept_len[b]: slot P_b + k receives the entry of slot
+ * P_b + path[b][k] - 1, for every layer and kv head, skipped when the two are
+ * equal.  All sources are read before any destination is written.
+ * new_len[b] = P_b + accept_len[b] + 1; moved[b] = entries copied per
+ * (layer, head).  err != 0: nothing is written, new_len = P_b, moved = 0.
+ *
+ * k_cache, v_cache  bf16, num_layers consecutive pools of
+ *                   [num_blocks][Hkv][16][D], layer_stride elements apart.
+ * block_table, prefix_len, n_nodes (or NULL: N_max nodes), accept_len, path,
+ *                   err (or NULL) as produced above; path int32 [B][D_max+1].
+ * new_len int32 [B] out; moved int32 [B] out or NULL; status as in a2
+ * (BAD_PATH / BAD_PAGE / BAD_LEN sequences are skipped, new_len = P_b).
+ */
+int tsd_kv_commit_path(uint16_t *k_cache, uint16_t *v_cache, int num_layers, int64_t layer_stride,
+                       const int32_t *block_table, int max_blocks, int num_blocks,
+                       const int32_t *prefix_len, const int32_t *n_nodes, const int32_t *accept_len,
+                       const int32_t *path, const int32_t *err, int B, int N_max, int Hkv, int D,
+                       int D_max, int32_t *new_len, int32_t *moved, int32_t *status,
+                       tsd_stream_t stream);
+
+/*
+ * a5. Best-first budgeted tree construction ([BASTION] Methodology 1: path
+ *     score rho(i) = prod_k q_k(x_ik); Methodology 2: surrogate
+ *     A_hat = sum rho, best-first expansion adds the valid node with the
+ *     largest rho).
+ *
+ * q           float [B][K][V] per-position draft marginals (non-negative).
+ * root_token  int32 [B]
+ * N           node budget including the root, 1 <= N <= 256, and no larger
+ *             than 1 + the number of distinct paths of length <= K.
+ * parent, tokens, depth int32 [B][N] out (insertion order: parents first);
+ * rho float [B][N] out, rho(child) = fl32(rho(parent) * q), rho(root) = 1;
+ * ahat double [B] out, sum of rho over non-root nodes in insertion order.
+ * Ties: (rho desc, depth asc, parent index asc, token rank asc); a
+ * position's token rank sorts q descending, lower token id first on ties.
+ * workspace  >= tsd_best_first_workspace_bytes() bytes (no initial contents).
+ */
+size_t tsd_best_first_workspace_bytes(int B, int K, int V, int N);
+int tsd_best_first_tree_build(const float *q, const int32_t *root_token, int B, int K, int V, int N,
+                              int32_t *parent, int32_t *tokens, int32_t *depth, float *rho,
+                              double *ahat, void *workspace, size_t ws_bytes, tsd_stream_t stream);
+
+#ifdef __cplusplus
+} /* extern "C" */
+#endif
+
+#endif /* TSD_H_ */

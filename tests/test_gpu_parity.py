@@ -1,0 +1,198 @@
+"""GPU parity: the CUDA path through the C ABI against the oracle on the same
+seeded inputs.  Bit-exact for ancestors, masks, error bits, argmax, accepted
+length / leaf / path / bonus, commit lengths and the whole committed cache
+pool; attention within max-abs 1e-2 and mean-abs 2e-3 over valid elements.
+
+Covers the five verify workloads at their full sizes (the 70B-shaped one on a
+sample of attention rows the oracle computes one by one), randomised small
+shapes across tile boundaries, node counts and prefixes, and the degenerate
+and fail-closed cases."""
+
+import numpy as np
+import pytest
+
+import gen
+import oracle
+
+from _gpu_path import compare, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tsd():
+    import torch
+    import tree_speculative_decoding_virtual_gb300 as m
+    torch.cuda.set_device(0)
+    return m
+
+
+@pytest.mark.parametrize("name", ["tiny", "8b", "ragged"])
+def test_workload_full(tsd, name):
+    inp = gen.verify_workload(name)
+    g = run_gpu(tsd, inp)
+    o = run_oracle(inp)
+    mx, mean = compare(inp, g, o)
+    assert g["status"] == 0
+    assert o["accept_len"].min() >= 0
+
+
+def test_workload_70b_sampled(tsd):
+    inp = gen.verify_workload("70b")
+    rng = np.random.default_rng(0)
+    sample = set()
+    for b in range(inp.B):
+        for h in rng.choice(inp.Hq, size=6, replace=False):
+            for i in range(inp.N_max):
+                sample.add((b, i, int(h)))
+        for _ in range(64):
+            sample.add((b, int(rng.integers(inp.N_max)), int(rng.integers(inp.Hq))))
+    sample = sorted(sample)
+    g = run_gpu(tsd, inp)
+    o = run_oracle(inp, sample_attention=sample)
+    compare(inp, g, o, sample=sample)
+    assert g["status"] == 0
+
+
+@pytest.mark.parametrize("N", [16, 32, 64, 128, 256])
+def test_bastion_budget(tsd, N):
+    import torch
+    from _gpu_path import dev_tensor, to_np
+    q, root = gen.bastion_marginals()
+    bf = tsd.best_first_tree_build(dev_tensor(q), dev_tensor(root), N)
+    torch.cuda.synchronize()
+    got = [to_np(x) for x in bf]
+    ref = oracle.best_first_tree(q, root, N)
+    for name, x, y in zip(["parent", "tokens", "depth", "rho", "ahat"], got, ref):
+        assert np.array_equal(x, y), name
+    # verify the built tree on the 8B-shaped layer
+    top1 = np.stack([[oracle.ranked_tokens(q[b, k])[0] for k in range(q.shape[1])]
+                     for b in range(q.shape[0])])
+    inp = gen.bastion_verify_inputs(ref[0], ref[1], ref[2], top1)
+    g = run_gpu(tsd, inp)
+    o = run_oracle(inp)
+    compare(inp, g, o)
+
+
+SWEEP = [
+    # B, N_max, Hq, Hkv, D, V, P range, depth
+    (2, 1, 4, 4, 64, 100, (0, 40), 1),
+    (3, 2, 8, 2, 128, 257, (0, 3), 2),
+    (2, 31, 32, 8, 128, 1000, (15, 17), 6),
+    (2, 32, 8, 1, 64, 1001, (16, 16), 8),
+    (3, 33, 16, 2, 128, 4099, (1, 130), 9),
+    (2, 64, 8, 8, 64, 5000, (63, 65), 12),
+    (1, 255, 4, 4, 128, 300, (0, 0), 20),
+    (2, 256, 8, 1, 128, 2048, (100, 300), 32),
+    (4, 47, 12, 3, 64, 777, (0, 700), 7),
+]
+
+
+@pytest.mark.parametrize("case", range(len(SWEEP)))
+def test_random_sweep(tsd, case):
+    B, N, Hq, Hkv, D, V, (plo, phi), dmax = SWEEP[case]
+    inp = gen.random_small(1000 + case, B=B, N_max=N, Hq=Hq, Hkv=Hkv, D=D, V=V, prefix_lo=plo,
+                           prefix_hi=phi, max_depth=dmax, p_match=0.8)
+    g = run_gpu(tsd, inp)
+    o = run_oracle(inp)
+    compare(inp, g, o)
+    assert g["status"] == 0
+
+
+def test_chain_and_single_node(tsd):
+    """A chain tree at the depth limit (causal attention) and single-node
+    trees (plain decode)."""
+    rng = np.random.default_rng(3)
+    for N in (1, 33):
+        inp = gen.random_small(77 + N, B=2, N_max=N, Hq=8, Hkv=2, D=128, V=300, prefix_lo=0,
+                               prefix_hi=90, max_depth=N - 1, ragged_nodes=False,
+                               relabel_ids=False)
+        inp.parent[:] = gen.chain_tree(N)
+        inp.tokens[:] = np.stack([gen.draft_tokens(rng, inp.parent[b], inp.targets[b], 0.9, 300)
+                                  for b in range(2)])
+        g = run_gpu(tsd, inp)
+        o = run_oracle(inp)
+        compare(inp, g, o)
+
+
+def test_malformed_trees_fail_closed(tsd):
+    """Error bits match the oracle exactly; bad sequences are skipped by every
+    downstream kernel (zero output, nothing accepted, nothing committed) and
+    good sequences in the same batch are unaffected."""
+    inp = gen.random_small(5, B=6, N_max=12, Hq=4, Hkv=2, D=64, V=64, prefix_lo=3, prefix_hi=40,
+                           max_depth=4, ragged_nodes=False)
+    inp.parent[1, 5] = 5                 # self loop
+    inp.parent[2, 0] = 3                 # root with a parent
+    inp.parent[3, 7] = 40                # out of range
+    inp.n_nodes[4] = 0                   # empty tree
+    inp.parent[5, :] = gen.chain_tree(12)  # depth 11 > D_max 4
+    g = run_gpu(tsd, inp)
+    o = run_oracle(inp)
+    assert o["err"][0] == 0 and (o["err"][1:] != 0).all()
+    compare(inp, g, o)
+    assert (g["accept_len"][1:] == 0).all() and (g["bonus"][1:] == -1).all()
+    assert (g["new_len"][1:] == inp.prefix_len[1:]).all()
+
+
+def test_argmax_ties_across_chunks(tsd):
+    """Maxima planted in several chunks of a long row: the lowest index wins;
+    +0.0 and -0.0 tie; a non-multiple-of-4 vocabulary takes the scalar path."""
+    import torch
+    from _gpu_path import dev_tensor, to_np
+    for V in (128256, 32003):
+        B, N = 2, 5
+        rng = np.random.default_rng(V)
+        logits = rng.standard_normal((B, N, V)).astype(np.float32)
+        logits[0, 0, [V - 1, 70000 % V, 12345]] = 9.0
+        logits[0, 1, :] = -1.0
+        logits[0, 1, [V - 3, 5]] = 0.0
+        logits[0, 1, 5] = -0.0
+        logits[0, 1, 2] = -0.0
+        logits[1, 2, :] = 3.0
+        parent = np.array([[-1, 0, 1, 2, 3]] * B, dtype=np.int32)
+        tokens = np.zeros((B, N), dtype=np.int32)
+        n_nodes = np.full(B, N, dtype=np.int32)
+        anc, depth, mask, err = tsd.tree_build_ancestors(dev_tensor(parent), dev_tensor(n_nodes), 4)
+        am, *_ = tsd.tree_verify_greedy(dev_tensor(logits), dev_tensor(tokens), dev_tensor(parent),
+                                        anc, depth, mask, dev_tensor(n_nodes), err, 4)
+        torch.cuda.synchronize()
+        ref = oracle.verify_greedy(logits, tokens, parent, n_nodes, np.zeros(B, np.int32), 4)[0]
+        assert np.array_equal(to_np(am), ref)
+        assert to_np(am)[0, 0] == min(V - 1, 70000 % V, 12345)
+        assert to_np(am)[0, 1] == 2 and to_np(am)[1, 2] == 0
+
+
+def test_bad_block_id_is_reported(tsd):
+    """A block id outside the pool is caught by the kernels' bounds checks:
+    the status word says so and no memory outside the pool is touched."""
+    inp = gen.random_small(8, B=2, N_max=8, Hq=4, Hkv=2, D=64, V=50, prefix_lo=20, prefix_hi=30,
+                           max_depth=3, ragged_nodes=False, shuffle_blocks=False)
+    inp.cache.block_table[1, 0] = inp.cache.num_blocks + 1000
+    g = run_gpu(tsd, inp)
+    assert g["status"] & 1  # TSD_STATUS_BAD_PAGE
+
+
+def test_commit_layers_stacked(tsd):
+    """All layers committed in one launch, bit-exact with the oracle."""
+    import torch
+    from _gpu_path import dev_tensor, to_np
+    inp = gen.random_small(9, B=3, N_max=20, Hq=4, Hkv=2, D=128, V=30, prefix_lo=0, prefix_hi=60,
+                           max_depth=6, p_match=0.95)
+    L = 5
+    rng = np.random.default_rng(1)
+    K = np.stack([gen.normal_bf16(rng, inp.cache.k.shape) for _ in range(L)])
+    Vv = np.stack([gen.normal_bf16(rng, inp.cache.v.shape) for _ in range(L)])
+    anc, depth, mask, err = oracle.build_ancestors(inp.parent, inp.n_nodes, inp.D_max)
+    _, A, _, path, _ = oracle.verify_greedy(inp.logits, inp.tokens, inp.parent, inp.n_nodes, err,
+                                            inp.D_max)
+    k1, v1, new_len, moved = oracle.commit_path(K, Vv, inp.cache.block_table, inp.prefix_len, A,
+                                                path, err)
+    kd = dev_tensor(K, torch.bfloat16)
+    vd = dev_tensor(Vv, torch.bfloat16)
+    nl, mv = tsd.kv_commit_path(kd, vd, dev_tensor(inp.cache.block_table),
+                                dev_tensor(inp.prefix_len), dev_tensor(inp.n_nodes), dev_tensor(A),
+                                dev_tensor(path), dev_tensor(err), inp.N_max, inp.D_max)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_np(kd, np.uint16), k1) and np.array_equal(to_np(vd, np.uint16), v1)
+    assert np.array_equal(to_np(nl), new_len) and np.array_equal(to_np(mv), moved)
+    assert moved.sum() > 0

@@ -1,0 +1,256 @@
+"""Python binding of libtsd.so, the GB300 tree-speculative-decoding verify path.
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+PyTorch supplies device memory and the current stream.  Each call has the
+name of its C entry point without the ``tsd_`` prefix; outputs and workspaces
+may be passed in (no allocation inside the call, e.g. under CUDA-graph
+capture) or are allocated here when omitted.
+
+Importing the package loads the shared library and fails loudly if it has not
+been built (``tree_speculative_decoding_virtual_gb300._build.build()``).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from ._build import LIB as _LIB_PATH
+
+TSD_OK, TSD_ERR_ARG, TSD_ERR_LIMIT, TSD_ERR_WORKSPACE, TSD_ERR_CUDA = 0, -1, -2, -3, -4
+_ERR_NAMES = {TSD_ERR_ARG: "TSD_ERR_ARG", TSD_ERR_LIMIT: "TSD_ERR_LIMIT",
+              TSD_ERR_WORKSPACE: "TSD_ERR_WORKSPACE", TSD_ERR_CUDA: "TSD_ERR_CUDA"}
+
+TREE_RANGE, TREE_CYCLE, TREE_TOO_DEEP, TREE_CLOSURE, TREE_ROOT, TREE_COUNT = 1, 2, 4, 8, 16, 32
+STATUS_BAD_PAGE, STATUS_BAD_LEN, STATUS_BAD_PATH = 1, 2, 4
+
+# C signatures: (name, restype, argtypes)
+_P, _I, _I64, _SZ, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+SIGNATURES = {
+    "tsd_version": (ctypes.c_char_p, []),
+    "tsd_tree_build_ancestors": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "tsd_tree_attn_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "tsd_tree_attn_fwd": (_I, [_P, _P, _P, _P, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F,
+                               _P, _P, _P, _SZ, _P, _P]),
+    "tsd_tree_verify_workspace_bytes": (_SZ, [_I, _I, _I]),
+    "tsd_tree_verify_greedy": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P,
+                                    _P, _P, _SZ, _P]),
+    "tsd_kv_commit_path": (_I, [_P, _P, _I, _I64, _P, _I, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I,
+                                _I, _P, _P, _P, _P]),
+    "tsd_best_first_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
+    "tsd_best_first_tree_build": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+}
+
+
+class TsdError(RuntimeError):
+    pass
+
+
+def _load():
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError("libtsd.so is not built at %s; run "
+                          "tree_speculative_decoding_virtual_gb300._build.build()" % _LIB_PATH)
+    lib = ctypes.CDLL(_LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()
+LIB_PATH = _LIB_PATH
+
+
+def _check(rc: int, what: str):
+    if rc != TSD_OK:
+        raise TsdError("%s failed: %s" % (what, _ERR_NAMES.get(rc, rc)))
+
+
+def _ptr(t: Optional[torch.Tensor], dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise TsdError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise TsdError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TsdError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _empty(shape, dtype, like):
+    return torch.empty(shape, dtype=dtype, device=like.device)
+
+
+# ---------------------------------------------------------------------------
+# a1
+# ---------------------------------------------------------------------------
+
+def tree_build_ancestors(parent, n_nodes, D_max, anc=None, depth=None, mask=None, err=None,
+                         stream=None):
+    """parent int32 [B][N_max]; n_nodes int32 [B] or None.  Returns
+    (anc [B][N_max+1][D_max+1], depth [B][N_max], mask uint32-as-int32
+    [B][N_max][W], err [B])."""
+    B, N_max = parent.shape
+    W = (N_max + 31) // 32
+    anc = anc if anc is not None else _empty((B, N_max + 1, D_max + 1), torch.int32, parent)
+    depth = depth if depth is not None else _empty((B, N_max), torch.int32, parent)
+    mask = mask if mask is not None else _empty((B, N_max, W), torch.int32, parent)
+    err = err if err is not None else _empty((B,), torch.int32, parent)
+    rc = lib.tsd_tree_build_ancestors(_ptr(parent, torch.int32, "parent"),
+                                      _ptr(n_nodes, torch.int32, "n_nodes"), B, N_max, D_max,
+                                      _ptr(anc, torch.int32, "anc"), _ptr(depth, torch.int32, "depth"),
+                                      _ptr(mask, torch.int32, "mask"), _ptr(err, torch.int32, "err"),
+                                      _stream(stream))
+    _check(rc, "tree_build_ancestors")
+    return anc, depth, mask, err
+
+
+# ---------------------------------------------------------------------------
+# a2
+# ---------------------------------------------------------------------------
+
+def tree_attn_workspace_bytes(B, N_max, Hq, Hkv, D, max_slots) -> int:
+    return int(lib.tsd_tree_attn_workspace_bytes(B, N_max, Hq, Hkv, D, max_slots))
+
+
+def tree_attn_fwd(q, k_cache, v_cache, block_table, prefix_len, n_nodes, mask, err, max_slots,
+                  scale=None, out=None, lse=None, want_lse=True, workspace=None, status=None,
+                  stream=None):
+    """q bf16 [B][N_max][Hq][D]; caches bf16 [num_blocks][Hkv][16][D];
+    block_table int32 [B][max_blocks].  Returns (out bf16 [B][N_max][Hq][D],
+    lse float32 [B][N_max][Hq] or None)."""
+    B, N_max, Hq, D = q.shape
+    num_blocks, Hkv = k_cache.shape[0], k_cache.shape[1]
+    max_blocks = block_table.shape[1]
+    if scale is None:
+        scale = 1.0 / float(D) ** 0.5
+    out = out if out is not None else _empty(q.shape, torch.bfloat16, q)
+    if lse is None and want_lse:
+        lse = _empty((B, N_max, Hq), torch.float32, q)
+    need = tree_attn_workspace_bytes(B, N_max, Hq, Hkv, D, max_slots)
+    if workspace is None:
+        workspace = _empty((max(need, 1),), torch.uint8, q)
+    rc = lib.tsd_tree_attn_fwd(
+        _ptr(q, torch.bfloat16, "q"), _ptr(k_cache, torch.bfloat16, "k_cache"),
+        _ptr(v_cache, torch.bfloat16, "v_cache"), _ptr(block_table, torch.int32, "block_table"),
+        max_blocks, num_blocks, _ptr(prefix_len, torch.int32, "prefix_len"),
+        _ptr(n_nodes, torch.int32, "n_nodes"), _ptr(mask, torch.int32, "mask"),
+        _ptr(err, torch.int32, "err"), B, N_max, Hq, Hkv, D, int(max_slots), float(scale),
+        _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"),
+        _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+        _ptr(status, torch.int32, "status"), _stream(stream))
+    _check(rc, "tree_attn_fwd")
+    return out, lse
+
+
+# ---------------------------------------------------------------------------
+# a3
+# ---------------------------------------------------------------------------
+
+def tree_verify_workspace_bytes(B, N_max, V) -> int:
+    return int(lib.tsd_tree_verify_workspace_bytes(B, N_max, V))
+
+
+def tree_verify_greedy(logits, tokens, parent, anc, depth, mask, n_nodes, err, D_max,
+                       argmax=None, accept_len=None, leaf=None, path=None, bonus=None,
+                       workspace=None, stream=None):
+    """logits float32 [B][N_max][V].  Returns (argmax [B][N_max], accept_len
+    [B], leaf [B], path [B][D_max+1], bonus [B]).  A workspace passed in must
+    be zero-filled before its first use (the call leaves it zero-filled)."""
+    B, N_max, V = logits.shape
+    argmax = argmax if argmax is not None else _empty((B, N_max), torch.int32, logits)
+    accept_len = accept_len if accept_len is not None else _empty((B,), torch.int32, logits)
+    leaf = leaf if leaf is not None else _empty((B,), torch.int32, logits)
+    path = path if path is not None else _empty((B, D_max + 1), torch.int32, logits)
+    bonus = bonus if bonus is not None else _empty((B,), torch.int32, logits)
+    need = tree_verify_workspace_bytes(B, N_max, V)
+    if workspace is None:
+        workspace = torch.zeros((max(need, 1),), dtype=torch.uint8, device=logits.device)
+    rc = lib.tsd_tree_verify_greedy(
+        _ptr(logits, torch.float32, "logits"), _ptr(tokens, torch.int32, "tokens"),
+        _ptr(parent, torch.int32, "parent"), _ptr(anc, torch.int32, "anc"),
+        _ptr(depth, torch.int32, "depth"), _ptr(mask, torch.int32, "mask"),
+        _ptr(n_nodes, torch.int32, "n_nodes"), _ptr(err, torch.int32, "err"), B, N_max, V, D_max,
+        _ptr(argmax, torch.int32, "argmax"), _ptr(accept_len, torch.int32, "accept_len"),
+        _ptr(leaf, torch.int32, "leaf"), _ptr(path, torch.int32, "path"),
+        _ptr(bonus, torch.int32, "bonus"), _ptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "tree_verify_greedy")
+    return argmax, accept_len, leaf, path, bonus
+
+
+# ---------------------------------------------------------------------------
+# a4
+# ---------------------------------------------------------------------------
+
+def kv_commit_path(k_cache, v_cache, block_table, prefix_len, n_nodes, accept_len, path, err,
+                   N_max, D_max, num_layers=1, new_len=None, moved=None, status=None,
+                   stream=None):
+    """Caches bf16 [num_layers][num_blocks][Hkv][16][D] (or without the layer
+    axis).  Commits in place.  Returns (new_len [B], moved [B])."""
+    if k_cache.dim() == 5:
+        num_layers = k_cache.shape[0]
+        num_blocks, Hkv, _, D = k_cache.shape[1:]
+        layer_stride = k_cache.stride(0)
+    else:
+        num_blocks, Hkv, _, D = k_cache.shape
+        layer_stride = k_cache.numel()
+    B, max_blocks = block_table.shape
+    new_len = new_len if new_len is not None else _empty((B,), torch.int32, k_cache)
+    moved = moved if moved is not None else _empty((B,), torch.int32, k_cache)
+    rc = lib.tsd_kv_commit_path(
+        _ptr(k_cache, torch.bfloat16, "k_cache"), _ptr(v_cache, torch.bfloat16, "v_cache"),
+        num_layers, layer_stride, _ptr(block_table, torch.int32, "block_table"), max_blocks,
+        num_blocks, _ptr(prefix_len, torch.int32, "prefix_len"),
+        _ptr(n_nodes, torch.int32, "n_nodes"), _ptr(accept_len, torch.int32, "accept_len"),
+        _ptr(path, torch.int32, "path"), _ptr(err, torch.int32, "err"), B, N_max, Hkv, D, D_max,
+        _ptr(new_len, torch.int32, "new_len"), _ptr(moved, torch.int32, "moved"),
+        _ptr(status, torch.int32, "status"), _stream(stream))
+    _check(rc, "kv_commit_path")
+    return new_len, moved
+
+
+# ---------------------------------------------------------------------------
+# a5
+# ---------------------------------------------------------------------------
+
+def best_first_workspace_bytes(B, K, V, N) -> int:
+    return int(lib.tsd_best_first_workspace_bytes(B, K, V, N))
+
+
+def best_first_tree_build(q, root_token, N, parent=None, tokens=None, depth=None, rho=None,
+                          ahat=None, workspace=None, stream=None):
+    """q float32 [B][K][V] marginals.  Returns (parent, tokens, depth int32
+    [B][N], rho float32 [B][N], ahat float64 [B])."""
+    B, K, V = q.shape
+    parent = parent if parent is not None else _empty((B, N), torch.int32, q)
+    tokens = tokens if tokens is not None else _empty((B, N), torch.int32, q)
+    depth = depth if depth is not None else _empty((B, N), torch.int32, q)
+    rho = rho if rho is not None else _empty((B, N), torch.float32, q)
+    ahat = ahat if ahat is not None else _empty((B,), torch.float64, q)
+    need = best_first_workspace_bytes(B, K, V, N)
+    if workspace is None:
+        workspace = _empty((max(need, 1),), torch.uint8, q)
+    rc = lib.tsd_best_first_tree_build(
+        _ptr(q, torch.float32, "q"), _ptr(root_token, torch.int32, "root_token"), B, K, V, N,
+        _ptr(parent, torch.int32, "parent"), _ptr(tokens, torch.int32, "tokens"),
+        _ptr(depth, torch.int32, "depth"), _ptr(rho, torch.float32, "rho"),
+        _ptr(ahat, torch.float64, "ahat"), _ptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "best_first_tree_build")
+    return parent, tokens, depth, rho, ahat
+
+
+def version() -> str:
+    return lib.tsd_version().decode()
