@@ -182,6 +182,32 @@ int tsd_tree_verify_greedy(const float *logits, const int32_t *tokens, const int
                            tsd_stream_t stream);
 
 /*
+ * Allocation-free variant of tsd_tree_verify_greedy (the pages have no
+ * counterpart; it exists for callers that cannot allocate device memory).
+ *
+ * Some callers cannot call cudaMalloc: a plugin inside another engine that
+ * owns all device memory and offers no workspace, or a latency-critical path
+ * where an allocation, which may synchronise the device, is not allowed.
+ * This call takes the same arguments and produces the same results as
+ * tsd_tree_verify_greedy, without a workspace: its scratch is a fixed array
+ * of tsd_tree_verify_static_capacity() bytes (1 MiB) in device memory that
+ * every GPU loading the library holds until the process exits.  Sizes whose
+ * scratch (B tickets plus B * N_max * chunks argmax partials) exceeds it
+ * return TSD_ERR_LIMIT.  The call itself allocates nothing.
+ * - The first call on a device looks up the array's device address (with
+ *   that device current); make that first call before any stream capture.
+ * - Every call zeroes the array's tickets on `stream` before its kernel runs.
+ *   All calls share the one array: calls that overlap on the GPU race.
+ */
+size_t tsd_tree_verify_static_capacity(void);
+int tsd_tree_verify_greedy_static(const float *logits, const int32_t *tokens,
+                                  const int32_t *parent, const int32_t *anc, const int32_t *depth,
+                                  const uint32_t *mask, const int32_t *n_nodes, const int32_t *err,
+                                  int B, int N_max, int V, int D_max, int32_t *argmax,
+                                  int32_t *accept_len, int32_t *leaf, int32_t *path,
+                                  int32_t *bonus, tsd_stream_t stream);
+
+/*
  * a4. Commit of the accepted path with the prefix-sharing fast reorder
  *     ([EP-zh] 2.1: path-index commit reorders the cache along the accepted
  *     path and moves only the newly accepted segment, only when needed;

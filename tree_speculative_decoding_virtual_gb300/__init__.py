@@ -38,6 +38,9 @@ SIGNATURES = {
     "tsd_tree_verify_workspace_bytes": (_SZ, [_I, _I, _I]),
     "tsd_tree_verify_greedy": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P,
                                     _P, _P, _SZ, _P]),
+    "tsd_tree_verify_static_capacity": (_SZ, []),
+    "tsd_tree_verify_greedy_static": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P,
+                                           _P, _P, _P, _P]),
     "tsd_kv_commit_path": (_I, [_P, _P, _I, _I64, _P, _I, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I,
                                 _I, _P, _P, _P, _P]),
     "tsd_best_first_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
@@ -187,6 +190,35 @@ def tree_verify_greedy(logits, tokens, parent, anc, depth, mask, n_nodes, err, D
         _ptr(bonus, torch.int32, "bonus"), _ptr(workspace, None, "workspace"),
         workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "tree_verify_greedy")
+    return argmax, accept_len, leaf, path, bonus
+
+
+def tree_verify_static_capacity() -> int:
+    return int(lib.tsd_tree_verify_static_capacity())
+
+
+def tree_verify_greedy_static(logits, tokens, parent, anc, depth, mask, n_nodes, err, D_max,
+                              argmax=None, accept_len=None, leaf=None, path=None, bonus=None,
+                              stream=None):
+    """tree_verify_greedy without a workspace, for callers that cannot
+    allocate device memory: the library's fixed device array serves as
+    scratch (calls that overlap on the GPU race on it).  Outputs passed in
+    are written in place; omitted ones are allocated here."""
+    B, N_max, V = logits.shape
+    argmax = argmax if argmax is not None else _empty((B, N_max), torch.int32, logits)
+    accept_len = accept_len if accept_len is not None else _empty((B,), torch.int32, logits)
+    leaf = leaf if leaf is not None else _empty((B,), torch.int32, logits)
+    path = path if path is not None else _empty((B, D_max + 1), torch.int32, logits)
+    bonus = bonus if bonus is not None else _empty((B,), torch.int32, logits)
+    rc = lib.tsd_tree_verify_greedy_static(
+        _ptr(logits, torch.float32, "logits"), _ptr(tokens, torch.int32, "tokens"),
+        _ptr(parent, torch.int32, "parent"), _ptr(anc, torch.int32, "anc"),
+        _ptr(depth, torch.int32, "depth"), _ptr(mask, torch.int32, "mask"),
+        _ptr(n_nodes, torch.int32, "n_nodes"), _ptr(err, torch.int32, "err"), B, N_max, V, D_max,
+        _ptr(argmax, torch.int32, "argmax"), _ptr(accept_len, torch.int32, "accept_len"),
+        _ptr(leaf, torch.int32, "leaf"), _ptr(path, torch.int32, "path"),
+        _ptr(bonus, torch.int32, "bonus"), _stream(stream))
+    _check(rc, "tree_verify_greedy_static")
     return argmax, accept_len, leaf, path, bonus
 
 

@@ -272,3 +272,78 @@ TSD_API int tsd_tree_verify_greedy(const float *logits, const int32_t *tokens,
       vec_ok, argmax, accept_len, leaf, path, bonus, part, counter);
   return launch_status();
 }
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of tsd_tree_verify_greedy.
+//
+// Some callers cannot call cudaMalloc: a plugin running inside another
+// engine that owns every byte of device memory and hands out no workspace,
+// or a latency-critical path where an allocation (which may synchronise the
+// device) is not acceptable.  This entry point keeps its scratch (the
+// per-sequence tickets and the per-chunk argmax partials) in a fixed array
+// in device global memory, loaded with the library: every GPU that loads
+// libtsd.so holds kStaticScratchBytes of it until the process exits.
+//
+// In host code `g_verify_scratch` names a host-side shadow, not device
+// memory, so its device address is looked up once per device with
+// cudaGetSymbolAddress (with that device current) and cached.  The first
+// call on a device performs that look-up, so make it before any stream
+// capture.  All calls share the one array: each call zeroes the tickets on
+// its stream before its kernel runs, and calls that overlap on the GPU (two
+// streams, or two devices' contexts racing on one array) race on it.
+// ---------------------------------------------------------------------------
+
+namespace tsd {
+namespace {
+
+constexpr size_t kStaticScratchBytes = 1u << 20;  // 1 MiB
+__device__ __align__(256) unsigned char g_verify_scratch[kStaticScratchBytes];
+
+void *static_scratch_ptr() {
+  static void *ptrs[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!ptrs[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_verify_scratch) != cudaSuccess) return nullptr;
+    ptrs[dev] = p;
+  }
+  return ptrs[dev];
+}
+
+}  // namespace
+}  // namespace tsd
+
+TSD_API size_t tsd_tree_verify_static_capacity(void) { return tsd::kStaticScratchBytes; }
+
+TSD_API int tsd_tree_verify_greedy_static(const float *logits, const int32_t *tokens,
+                                          const int32_t *parent, const int32_t *anc,
+                                          const int32_t *depth, const uint32_t *mask,
+                                          const int32_t *n_nodes, const int32_t *err, int B,
+                                          int N_max, int V, int D_max, int32_t *argmax,
+                                          int32_t *accept_len, int32_t *leaf, int32_t *path,
+                                          int32_t *bonus, tsd_stream_t stream) {
+  using namespace tsd;
+  if (B < 0 || V < 1) return B < 0 ? TSD_ERR_ARG : TSD_ERR_LIMIT;
+  if (N_max < 1 || N_max > kMaxNodes || D_max < 0 || D_max > kMaxDepth || B > 65535)
+    return TSD_ERR_LIMIT;
+  if (B == 0) return TSD_OK;
+  if (!logits || !tokens || !parent || !anc || !depth || !mask || !argmax || !accept_len ||
+      !leaf || !path || !bonus)
+    return TSD_ERR_ARG;
+  const VerifyPlan p = plan_verify(B, N_max, V);
+  if (p.counter_bytes + p.part_bytes > kStaticScratchBytes) return TSD_ERR_LIMIT;
+  void *scratch = static_scratch_ptr();
+  if (!scratch) return TSD_ERR_CUDA;
+  if (cudaMemsetAsync(scratch, 0, p.counter_bytes, as_cuda(stream)) != cudaSuccess)
+    return TSD_ERR_CUDA;
+  unsigned *counter = static_cast<unsigned *>(scratch);
+  Partial *part = reinterpret_cast<Partial *>(static_cast<char *>(scratch) + p.counter_bytes);
+  const int W = (N_max + 31) / 32;
+  const int vec_ok = (V % 4 == 0) && aligned(logits, 16);
+  dim3 grid(p.C, N_max, B);
+  verify_greedy_kernel<<<grid, kThreads, 0, as_cuda(stream)>>>(
+      logits, tokens, parent, anc, depth, mask, n_nodes, err, N_max, V, D_max, W, p.chunk, p.C,
+      vec_ok, argmax, accept_len, leaf, path, bonus, part, counter);
+  return launch_status();
+}
