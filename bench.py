@@ -294,32 +294,26 @@ def gpu_arm(args, rank, world):
         "tree_build_ancestors", "tree_attn_fwd", "tree_verify_greedy", "kv_commit_path"]
     launches_per_step = (2 if bastion else 0) + 1 + 2 + 1 + 1
 
-    def step(ev=None):
-        k = 0
-        if ev is not None:
-            ev[k].record(stream)
-        if bastion:
-            tsd.best_first_tree_build(qd, rootd, N_b, *bf_out, rho, ahat, workspace=bf_ws)
-            k += 1
-            if ev is not None:
-                ev[k].record(stream)
-        tsd.tree_build_ancestors(parent, n_nodes, Dm, anc, depth, mask, err)
-        if ev is not None:
-            ev[k + 1].record(stream)
-        tsd.tree_attn_fwd(q, kc, vc, table, prefix, n_nodes, mask, err, max_slots, out=out, lse=lse,
-                          workspace=attn_ws, status=status)
-        if ev is not None:
-            ev[k + 2].record(stream)
-        tsd.tree_verify_greedy(logits, tokens, parent, anc, depth, mask, n_nodes, err, Dm, am, A,
-                               leaf, path, bonus, workspace=ver_ws)
-        if ev is not None:
-            ev[k + 3].record(stream)
-        tsd.kv_commit_path(kc, vc, table, prefix, n_nodes, A, path, err, N, Dm, new_len=new_len,
-                           moved=moved, status=status)
-        if ev is not None:
-            ev[k + 4].record(stream)
+    calls = {}
+    if bastion:
+        calls["best_first_tree_build"] = lambda: tsd.best_first_tree_build(
+            qd, rootd, N_b, *bf_out, rho, ahat, workspace=bf_ws)
+    calls["tree_build_ancestors"] = lambda: tsd.tree_build_ancestors(
+        parent, n_nodes, Dm, anc, depth, mask, err)
+    calls["tree_attn_fwd"] = lambda: tsd.tree_attn_fwd(
+        q, kc, vc, table, prefix, n_nodes, mask, err, max_slots, out=out, lse=lse,
+        workspace=attn_ws, status=status)
+    calls["tree_verify_greedy"] = lambda: tsd.tree_verify_greedy(
+        logits, tokens, parent, anc, depth, mask, n_nodes, err, Dm, am, A, leaf, path, bonus,
+        workspace=ver_ws)
+    calls["kv_commit_path"] = lambda: tsd.kv_commit_path(
+        kc, vc, table, prefix, n_nodes, A, path, err, N, Dm, new_len=new_len, moved=moved,
+        status=status)
 
-    nev = len(names) + 1
+    def step():
+        for n in names:
+            calls[n]()
+
     for _ in range(args.warmup):
         flush.zero_()
         step()
@@ -327,30 +321,61 @@ def gpu_arm(args, rank, world):
     moved_total = int(moved.sum().item())
     assert int(status.item()) == 0, "device status %d" % int(status.item())
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    # CUDA graphs: the whole step, and each entry point on its own (timing
+    # without host launch gaps; the kernels are the same launches)
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            fn()
+        torch.cuda.current_stream().wait_stream(side)
+        with torch.cuda.graph(g):
+            fn()
+        return g
+
+    g_step = capture(step)
+    g_one = {n: capture(calls[n]) for n in names}
+    torch.cuda.synchronize()
+
     sampler = ClockSampler(local) if rank == 0 else None
+    # ---- timed region 1: whole steps (the headline value) ----
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.perf_counter()
     for s in range(args.steps):
         flush.zero_()
-        step(events[s])
+        ev[s][0].record(stream)
+        g_step.replay()
+        ev[s][1].record(stream)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
     if world > 1:
         dist.barrier()
-    per_kernel = {n: 0.0 for n in names}
-    total_ms = 0.0
-    for ev in events:
-        for j, n in enumerate(names):
-            per_kernel[n] += ev[j].elapsed_time(ev[j + 1])
-        total_ms += ev[0].elapsed_time(ev[-1])
-    ms_per_step = total_ms / args.steps
+    ms_per_step = sum(a.elapsed_time(b) for a, b in ev) / args.steps
     if world > 1:
         t = torch.tensor([ms_per_step], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_per_step = float(t.item())
+
+    # ---- timed region 2: per entry point (roofline of the dominant kernel) ----
+    nev = len(names) + 1
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for s in range(args.steps):
+        flush.zero_()
+        kev[s][0].record(stream)
+        for j, n in enumerate(names):
+            g_one[n].replay()
+            kev[s][j + 1].record(stream)
+    torch.cuda.synchronize()
+    per_kernel = {n: 0.0 for n in names}
+    for e in kev:
+        for j, n in enumerate(names):
+            per_kernel[n] += e[j].elapsed_time(e[j + 1])
     kernel_us = {n: 1000.0 * v / args.steps for n, v in per_kernel.items()}
 
     # ---- e2e: host buffers through the public API, copies inside the timing ----
@@ -373,7 +398,7 @@ def gpu_arm(args, rank, world):
             e2e_ev[s - 3][0].record(stream)
         for k, v in h_in.items():
             v.copy_(pinned[k], non_blocking=True)
-        step()
+        step()  # the public API calls, launched from Python
         for k, v in h_out_src.items():
             h_out[k].copy_(v, non_blocking=True)
         if s >= 3:
@@ -418,7 +443,8 @@ def gpu_arm(args, rank, world):
         "config": {"workload": desc, "name": args.workload, "global_batch": B * world,
                    "seq_len": max_slots, "parallelism": "replicas (dp%d)" % world,
                    "l2": "flushed between timed steps (256 MiB write outside the timed events)",
-                   "timing": "CUDA events per kernel on the launching stream; per-step sum"},
+                   "timing": "CUDA events on the launching stream around CUDA-graph replays of "
+                             "the whole step (value) and of each entry point (kernels)"},
         "hbm_gbs_step": round(step_bytes / (ms_per_step * 1e-3) / 1e9, 1),
         "kernels": kernels,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
@@ -431,6 +457,7 @@ def gpu_arm(args, rank, world):
         "gpu_launches": launches,
         "clocks": clocks,
         "wall_s_timed_region": round(t_wall, 4),
+        "kernel_sum_us": round(sum(kernel_us.values()), 3),
         "mean_accept_len": float(A.float().mean().item()),
     }
     if args.workload == "70b":
@@ -443,7 +470,7 @@ def gpu_arm(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="8b")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])

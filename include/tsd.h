@@ -81,9 +81,30 @@ enum {
 #define TSD_STATUS_BAD_PAGE 1 /* a block id outside [0, num_blocks): sequence skipped */
 #define TSD_STATUS_BAD_LEN 2  /* P_b < 0 or P_b + N_b beyond max_slots / the table */
 #define TSD_STATUS_BAD_PATH 4 /* accept_len / path inconsistent with the tree */
+#define TSD_STATUS_TIMEOUT 8  /* a bounded wait inside a kernel ran out: outputs unspecified */
 
 /* Library version string (static storage). */
 const char *tsd_version(void);
+
+/*
+ * Process-wide options (host state, read at each launch; not thread-safe
+ * against concurrent launches).  No page counterpart: they exist for tests
+ * and measurement.
+ *   TSD_OPT_WAIT_LIMIT_NS  limit of every bounded wait inside a kernel, in
+ *                          ns (default 2e9).  When a wait runs out the kernel
+ *                          sets TSD_STATUS_TIMEOUT, drains its in-flight copies
+ *                          and MMAs (bounded), frees its tensor memory and
+ *                          returns; 0 makes every wait that is not already
+ *                          satisfied run out.
+ *   TSD_OPT_ATTN_KERNEL    0: tcgen05/TMA tree attention (default);
+ *                          1: the mma.sync kernel kept for comparison.
+ * Returns TSD_ERR_ARG for an unknown key or value.
+ */
+#define TSD_OPT_WAIT_LIMIT_NS 0
+#define TSD_OPT_ATTN_KERNEL 1
+#define TSD_OPT_COUNT 2
+int tsd_set_option(int key, int64_t value);
+int64_t tsd_get_option(int key);
 
 /*
  * a1. Accelerator-safe tree tensors ([EP-zh] 2.2; [EP-pt] section 2,

@@ -25,12 +25,15 @@ _ERR_NAMES = {TSD_ERR_ARG: "TSD_ERR_ARG", TSD_ERR_LIMIT: "TSD_ERR_LIMIT",
               TSD_ERR_WORKSPACE: "TSD_ERR_WORKSPACE", TSD_ERR_CUDA: "TSD_ERR_CUDA"}
 
 TREE_RANGE, TREE_CYCLE, TREE_TOO_DEEP, TREE_CLOSURE, TREE_ROOT, TREE_COUNT = 1, 2, 4, 8, 16, 32
-STATUS_BAD_PAGE, STATUS_BAD_LEN, STATUS_BAD_PATH = 1, 2, 4
+STATUS_BAD_PAGE, STATUS_BAD_LEN, STATUS_BAD_PATH, STATUS_TIMEOUT = 1, 2, 4, 8
+OPT_WAIT_LIMIT_NS, OPT_ATTN_KERNEL = 0, 1
 
 # C signatures: (name, restype, argtypes)
 _P, _I, _I64, _SZ, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
 SIGNATURES = {
     "tsd_version": (ctypes.c_char_p, []),
+    "tsd_set_option": (_I, [_I, _I64]),
+    "tsd_get_option": (_I64, [_I]),
     "tsd_tree_build_ancestors": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "tsd_tree_attn_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "tsd_tree_attn_fwd": (_I, [_P, _P, _P, _P, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F,
@@ -282,6 +285,15 @@ def best_first_tree_build(q, root_token, N, parent=None, tokens=None, depth=None
         workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "best_first_tree_build")
     return parent, tokens, depth, rho, ahat
+
+
+def set_option(key: int, value: int) -> None:
+    """Process-wide library option (OPT_WAIT_LIMIT_NS, OPT_ATTN_KERNEL)."""
+    _check(lib.tsd_set_option(key, value), "set_option")
+
+
+def get_option(key: int) -> int:
+    return int(lib.tsd_get_option(key))
 
 
 def version() -> str:

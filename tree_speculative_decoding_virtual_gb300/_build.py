@@ -19,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtsd.so")
 
-SOURCES = ["ancestors.cu", "attention.cu", "verify.cu", "commit.cu", "best_first.cu"]
+SOURCES = ["runtime.cu", "ancestors.cu", "attention.cu", "verify.cu", "commit.cu",
+           "best_first.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

@@ -11,8 +11,6 @@
 // steps, which also detects cycles), and the ancestor rows are assembled in
 // shared memory and written out with coalesced stores.
 
-#include <cstdio>
-
 #include "tsd_common.cuh"
 
 namespace tsd {
@@ -119,21 +117,7 @@ ancestors_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict__
 
 }  // namespace
 
-int sm_count() {
-  static int cached[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
-  if (dev < 64 && cached[dev] > 0) return cached[dev];
-  int n = 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-    n = 148;
-  if (dev < 64) cached[dev] = n;
-  return n;
-}
-
 }  // namespace tsd
-
-TSD_API const char *tsd_version(void) { return "tsd 0.1 (sm_103a)"; }
 
 TSD_API int tsd_tree_build_ancestors(const int32_t *parent, const int32_t *n_nodes, int B,
                                      int N_max, int D_max, int32_t *anc, int32_t *depth,

@@ -21,10 +21,13 @@
 // partials (O, running max, running sum); a combine kernel merges them,
 // normalises and rounds to bf16.
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
 #include <cmath>
 
+#include "sm100_ptx.cuh"
 #include "tsd_common.cuh"
 
 namespace tsd {
@@ -53,6 +56,7 @@ struct AttnParams {
   uint16_t *out;
   float *lse;
   int32_t *status;
+  uint64_t wait_limit_ns;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -341,6 +345,372 @@ tree_attn_split_kernel(const AttnParams p) {
   }
 }
 
+
+// ===========================================================================
+// tcgen05 path.  One block = 128 query rows x one split of the key range of
+// one (sequence, kv head).  Warp 0 issues TMA loads of paged K/V tiles (128
+// keys = 8 blocks of 16 slots, 128-byte swizzle, two stages); warp 1 owns
+// the tensor memory and issues the MMAs (one thread); warps 2-5 run the
+// softmax, one TMEM lane (= one query row) per thread.
+//   S_j = Q K_j^T   (M=128, N=128, K=D; A and B K-major) -> TMEM, 2 buffers
+//   P_j = exp2(S_j * scale * log2e - m) as bf16 -> shared memory, 2 buffers
+//   O  += P_j V_j   (M=128, N=D, K=128; V MN-major)     -> TMEM
+// The running max is raised lazily: O and the row sum are rescaled (in
+// TMEM) only when a tile's max exceeds the one in use by more than 2^8, so
+// P never exceeds 256 and the result is the same softmax.  S_{j+1} is
+// issued before P_j V_j so the tensor core works while the softmax runs.
+// Every wait is bounded; on expiry the block flags TSD_STATUS_TIMEOUT,
+// drains what it issued, frees its tensor memory and returns.
+// ===========================================================================
+
+constexpr int kTcThreads = 192;
+constexpr int kTcBM = 128;
+constexpr int kTcBN = 128;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint64_t kDrainLimitNs = 100000000ull;  // 100 ms
+
+template <int D>
+struct TcLayout {
+  static constexpr int kHalves = D / 64;                      // 128-byte column blocks
+  static constexpr uint32_t kHalfBytes = 128 * 128;           // one column block of 128 rows
+  static constexpr uint32_t kTile = kTcBN * D * 2;            // one K or V tile
+  static constexpr uint32_t kQ = 0;
+  static constexpr uint32_t kK = kTcBM * D * 2;
+  static constexpr uint32_t kV = kK + 2 * kTile;
+  static constexpr uint32_t kP = kV + 2 * kTile;
+  static constexpr uint32_t kPBytes = kTcBM * kTcBN * 2;
+  static constexpr uint32_t kBytes = kP + 2 * kPBytes;
+  static constexpr uint32_t kAlloc = kBytes + 1024;           // + alignment slack
+  static constexpr uint32_t kTmemS = 0;                       // two 128-column S buffers
+  static constexpr uint32_t kTmemO = 256;                     // D columns of O
+};
+
+struct TcShared {
+  uint64_t k_full[2], v_full[2], kv_empty[2], s_full[2], s_free[2], p_full[2], p_free[2];
+  uint64_t q_full, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ bool tc_wait(uint64_t &bar, uint32_t parity, uint64_t limit,
+                                        volatile int *abort) {
+  using namespace sm100;
+  if (mbar_wait(smem_addr(&bar), parity, limit)) return true;
+  *abort = 1;
+  return false;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kTcThreads, 1)
+tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap tmap_k,
+                   const __grid_constant__ CUtensorMap tmap_v) {
+  using namespace sm100;
+  using L = TcLayout<D>;
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ TcShared sh;
+
+  const int rt = blockIdx.x;
+  const int split = blockIdx.y;
+  const int z = blockIdx.z;
+  const int b = z / p.Hkv;
+  const int hkv = z % p.Hkv;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  int P, nb;
+  if (!seq_ok(p, b, P, nb)) {
+    if (rt == 0 && split == 0 && hkv == 0 && tid == 0 && p.status) {
+      const int e = p.err ? p.err[b] : 0;
+      const int nbb = p.n_nodes ? p.n_nodes[b] : p.N_max;
+      if (e == 0 && nbb >= 1 && nbb <= p.N_max) atomicOr(p.status, TSD_STATUS_BAD_LEN);
+    }
+    return;
+  }
+  const int rows_valid = nb * p.g;
+  const int seq_len = P + nb;
+  const int k_begin = split * p.chunk;
+  if (rt * kTcBM >= rows_valid || k_begin >= seq_len) return;
+  const int k_end = min(seq_len, k_begin + p.chunk);
+  const int ntiles = (k_end - k_begin + kTcBN - 1) / kTcBN;
+
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  unsigned char *gbase = smem_raw + (base - raw);
+  volatile int *abort = &sh.abort;
+  const uint64_t lim = p.wait_limit_ns;
+
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_addr(&sh.k_full[i]), 1);
+      mbar_init(smem_addr(&sh.v_full[i]), 1);
+      mbar_init(smem_addr(&sh.kv_empty[i]), 1);
+      mbar_init(smem_addr(&sh.s_full[i]), 1);
+      mbar_init(smem_addr(&sh.s_free[i]), 4);
+      mbar_init(smem_addr(&sh.p_full[i]), 4);
+      mbar_init(smem_addr(&sh.p_free[i]), 1);
+    }
+    mbar_init(smem_addr(&sh.q_full), 4);
+    mbar_init(smem_addr(&sh.drain), 1);
+    sh.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(smem_addr(&sh.tmem_base), kTmemCols);
+  if (tid == 32 * 0) {
+    tma_prefetch_desc(&tmap_k);
+    tma_prefetch_desc(&tmap_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------ TMA producer ------------------------------
+    if (lane == 0) {
+      const int32_t *trow = p.table + (size_t)b * p.max_blocks;
+      const int last_page = (seq_len - 1) / kPage;
+      int last_issued[2] = {-1, -1};
+      bool bad = false;
+      for (int j = 0; j < ntiles && !*abort; ++j) {
+        const int st = j & 1;
+        if (j >= 2 && !tc_wait(sh.kv_empty[st], ((j >> 1) - 1) & 1, lim, abort)) break;
+        const int pg0 = (k_begin + j * kTcBN) / kPage;
+        int ys[kTcBN / kPage];
+#pragma unroll
+        for (int g = 0; g < kTcBN / kPage; ++g) {
+          int page = __ldg(trow + min(pg0 + g, last_page));
+          if (page < 0 || page >= p.num_blocks) {
+            bad = true;
+            page = 0;
+          }
+          ys[g] = (page * p.Hkv + hkv) * kPage;
+        }
+        mbar_arrive_expect_tx(smem_addr(&sh.k_full[st]), L::kTile);
+#pragma unroll
+        for (int g = 0; g < kTcBN / kPage; ++g)
+#pragma unroll
+          for (int h = 0; h < L::kHalves; ++h)
+            tma_load_2d(base + L::kK + st * L::kTile + h * L::kHalfBytes + g * kPage * 128, &tmap_k,
+                        h * 64, ys[g], smem_addr(&sh.k_full[st]));
+        mbar_arrive_expect_tx(smem_addr(&sh.v_full[st]), L::kTile);
+#pragma unroll
+        for (int g = 0; g < kTcBN / kPage; ++g)
+#pragma unroll
+          for (int h = 0; h < L::kHalves; ++h)
+            tma_load_2d(base + L::kV + st * L::kTile + h * L::kHalfBytes + g * kPage * 128, &tmap_v,
+                        h * 64, ys[g], smem_addr(&sh.v_full[st]));
+        last_issued[st] = j;
+      }
+      // drain: the last loads issued into each stage have landed
+      for (int st = 0; st < 2; ++st)
+        if (last_issued[st] >= 0) {
+          const uint32_t par = (last_issued[st] >> 1) & 1;
+          mbar_wait(smem_addr(&sh.k_full[st]), par, kDrainLimitNs);
+          mbar_wait(smem_addr(&sh.v_full[st]), par, kDrainLimitNs);
+        }
+      if (bad && p.status) atomicOr(p.status, TSD_STATUS_BAD_PAGE);
+    }
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer ------------------------------
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(kTcBM, kTcBN, false, false);
+      constexpr uint32_t idPV = idesc_bf16_f32(kTcBM, D, false, true);
+      auto issue_s = [&](int j) -> bool {
+        const int st = j & 1;
+        if (!tc_wait(sh.k_full[st], (j >> 1) & 1, lim, abort)) return false;
+        if (j >= 2 && !tc_wait(sh.s_free[st], ((j >> 1) - 1) & 1, lim, abort)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
+          umma_bf16(tmem + L::kTmemS + st * kTcBN, smem_desc_sw128(base + L::kQ + koff, 16, 1024),
+                    smem_desc_sw128(base + L::kK + st * L::kTile + koff, 16, 1024), idS, kk > 0);
+        }
+        umma_commit(smem_addr(&sh.s_full[st]));
+        return true;
+      };
+      auto issue_pv = [&](int j) -> bool {
+        const int st = j & 1;
+        if (!tc_wait(sh.p_full[st], (j >> 1) & 1, lim, abort)) return false;
+        if (!tc_wait(sh.v_full[st], (j >> 1) & 1, lim, abort)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kTcBN / 16; ++kk) {
+          const uint32_t aoff = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
+          umma_bf16(tmem + L::kTmemO, smem_desc_sw128(base + L::kP + st * L::kPBytes + aoff, 16, 1024),
+                    smem_desc_sw128(base + L::kV + st * L::kTile + kk * 16 * 128, L::kHalfBytes, 1024),
+                    idPV, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(smem_addr(&sh.p_free[st]));
+        umma_commit(smem_addr(&sh.kv_empty[st]));
+        return true;
+      };
+      bool ok = tc_wait(sh.q_full, 0, lim, abort) && issue_s(0);
+      for (int j = 1; ok && j < ntiles; ++j) ok = !*abort && issue_s(j) && issue_pv(j - 1);
+      if (ok) ok = issue_pv(ntiles - 1);
+      // drain: every MMA issued above has completed
+      umma_commit(smem_addr(&sh.drain));
+      mbar_wait(smem_addr(&sh.drain), 0, kDrainLimitNs);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------ softmax ------------------------------
+    const int quarter = warp & 3;                     // TMEM lanes 32*quarter .. +31
+    const int rl = quarter * 32 + lane;               // row within the tile
+    const int row = rt * kTcBM + rl;
+    const bool rvalid = row < rows_valid;
+    const int node = rvalid ? row / p.g : 0;
+    const int head = hkv * p.g + (rvalid ? row % p.g : 0);
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t *mrow = p.mask + ((size_t)b * p.N_max + node) * p.W;
+
+    // Q row -> shared memory, 128-byte swizzle
+    const uint4 *qsrc =
+        reinterpret_cast<const uint4 *>(p.q + (((size_t)b * p.N_max + node) * p.Hq + head) * D);
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) {
+      const uint4 v = rvalid ? __ldg(qsrc + c) : make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4 *>(gbase + L::kQ + (c >> 3) * L::kHalfBytes + sw128_offset(rl, c & 7)) = v;
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&sh.q_full));
+
+    // waits are taken by every lane and their outcome made warp-uniform, so the
+    // .sync.aligned TMEM accesses below are never reached by a partial warp
+    auto warp_wait = [&](uint64_t &bar, uint32_t parity) -> bool {
+      const bool got = !*abort && tc_wait(bar, parity, lim, abort);
+      return __all_sync(0xffffffffu, got);
+    };
+    float m_use = -INFINITY, l_sum = 0.f;
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      const int st = j & 1;
+      if (!warp_wait(sh.s_full[st], (j >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t r[4][32];
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(tmem + L::kTmemS + st * kTcBN + lane_off + c4 * 32, r[c4]);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&sh.s_free[st]));
+
+      const int ts = k_begin + j * kTcBN;
+      const bool full = (ts + kTcBN <= P) && (ts + kTcBN <= k_end);
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t vis = 0xFFFFFFFFu;
+        if (!full) {
+          vis = 0u;
+          for (int i = 0; i < 32; ++i) {
+            const int slot = ts + c4 * 32 + i;
+            bool v = slot < k_end;
+            if (v && slot >= P) {
+              const int jj = slot - P;
+              v = rvalid && ((__ldg(mrow + (jj >> 5)) >> (jj & 31)) & 1u);
+            }
+            vis |= (v ? 1u : 0u) << i;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          float x = __uint_as_float(r[c4][i]) * p.scale_log2;
+          x = ((vis >> i) & 1u) ? x : -INFINITY;
+          r[c4][i] = __float_as_uint(x);
+          mt = fmaxf(mt, x);
+        }
+      }
+      const float m_new = fmaxf(m_use, mt);
+      const bool upd = m_new > m_use + 8.f;  // first visible key, or the max grew by > 2^8
+      const float alpha = upd ? exp2f(m_use - m_new) : 1.f;
+      if (j > 0 && __any_sync(0xffffffffu, upd)) {
+        // O holds tiles < j: wait for P_{j-1} V_{j-1}, rescale O in TMEM (whole warp)
+        if (!warp_wait(sh.p_free[(j - 1) & 1], ((j - 1) >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tmem + L::kTmemO + lane_off + c * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tmem + L::kTmemO + lane_off + c * 32, o);
+        }
+        tmem_wait_st();
+      }
+      if (upd) {
+        l_sum *= alpha;
+        m_use = m_new;
+      }
+      const float mb = m_use == -INFINITY ? 0.f : m_use;
+      // P_j must not overwrite buffer st before P_{j-2} V_{j-2} has read it
+      if (j >= 2 && !warp_wait(sh.p_free[st], ((j >> 1) - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      float rs = 0.f;
+      unsigned char *pbuf = gbase + L::kP + st * L::kPBytes;
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {  // 8 keys = one 16-byte chunk
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float a = exp2f(__uint_as_float(r[c4][q8 * 8 + 2 * e]) - mb);
+            const float c = exp2f(__uint_as_float(r[c4][q8 * 8 + 2 * e + 1]) - mb);
+            rs += a + c;
+            w[e] = pack_bf16(a, c);
+          }
+          const int chunk = c4 * 4 + q8;  // 0..15 across 128 keys
+          *reinterpret_cast<uint4 *>(pbuf + (chunk >> 3) * L::kHalfBytes + sw128_offset(rl, chunk & 7)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+      l_sum += rs;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&sh.p_full[st]));
+    }
+
+    // ---- epilogue: unnormalised O, running max (log2 units) and row sum ----
+    if (ok && warp_wait(sh.p_free[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1)) {
+      tc_fence_after();
+      const size_t prow = ((size_t)z * p.splits + split) * p.rows_pad + rt * kTcBM + rl;
+      float4 *po = reinterpret_cast<float4 *>(p.part_o + prow * D);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tmem + L::kTmemO + lane_off + c * 32, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          po[c * 8 + i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
+                                      __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
+      }
+      p.part_ml[prow] = make_float2(m_use, l_sum);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort && tid == 0 && p.status) atomicOr(p.status, TSD_STATUS_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 // One warp per output row (b, node, q head): merge the splits.
 template <int D>
 __global__ void __launch_bounds__(256) tree_attn_combine_kernel(const AttnParams p, int B) {
@@ -394,24 +764,44 @@ __global__ void __launch_bounds__(256) tree_attn_combine_kernel(const AttnParams
 }
 
 struct AttnPlan {
-  int row_tiles, rows_pad, splits, chunk;
+  int impl;  // 0 tcgen05, 1 mma.sync
+  int bm, bn, row_tiles, rows_pad, splits, chunk;
   size_t o_bytes, ml_bytes;
 };
 
 AttnPlan plan_attn(int B, int N_max, int Hq, int Hkv, int D, int max_slots) {
   AttnPlan a;
+  a.impl = (int)option(TSD_OPT_ATTN_KERNEL);
+  a.bm = a.impl == 0 ? kTcBM : kBM;
+  a.bn = a.impl == 0 ? kTcBN : kBN;
   const int g = Hq / Hkv;
-  a.row_tiles = (N_max * g + kBM - 1) / kBM;
-  a.rows_pad = a.row_tiles * kBM;
+  a.row_tiles = (N_max * g + a.bm - 1) / a.bm;
+  a.rows_pad = a.row_tiles * a.bm;
   const long units = (long)B * Hkv * a.row_tiles;
-  const long target = 2L * sm_count();
-  long splits = (target + units - 1) / units;
-  const long max_splits = (max_slots + kBN - 1) / kBN;
-  if (splits > max_splits) splits = max_splits;
-  if (splits < 1) splits = 1;
-  long chunk = (max_slots + splits - 1) / splits;
-  chunk = (chunk + kBN - 1) / kBN * kBN;
-  if (chunk < kBN) chunk = kBN;
+  const long nsm = sm_count();
+  const long max_tiles = (max_slots + a.bn - 1) / a.bn;
+  long best_s = 1;
+  if (a.impl == 0) {
+    // one resident block per SM: estimated time = waves x (tiles per block +
+    // a fixed cost of about four tiles for the prologue and the partials)
+    double best_t = 1e30;
+    for (long s = 1; s <= max_tiles && s <= 64; ++s) {
+      const long waves = (units * s + nsm - 1) / nsm;
+      const long per = (max_tiles + s - 1) / s;
+      const double t = (double)waves * (double)(per + 4);
+      if (t < best_t - 1e-9) {
+        best_t = t;
+        best_s = s;
+      }
+    }
+  } else {
+    const long target = 2L * nsm;
+    best_s = (target + units - 1) / units;
+    if (best_s > max_tiles) best_s = max_tiles;
+    if (best_s < 1) best_s = 1;
+  }
+  long chunk = (max_slots + best_s - 1) / best_s;
+  chunk = (chunk + a.bn - 1) / a.bn * a.bn;
   a.chunk = (int)chunk;
   a.splits = (int)((max_slots + chunk - 1) / chunk);
   if (a.splits < 1) a.splits = 1;
@@ -421,21 +811,68 @@ AttnPlan plan_attn(int B, int N_max, int Hq, int Hkv, int D, int max_slots) {
   return a;
 }
 
-template <int D>
-int launch_attn(AttnParams &p, int B, cudaStream_t s) {
-  const size_t smem = (size_t)(kBM + 4 * kBN) * D * 2;
-  static unsigned long long configured = 0ull;  // one bit per device
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return TSD_ERR_CUDA;
-  const unsigned long long bit = 1ull << (dev & 63);
-  if (!(configured & bit)) {
-    if (cudaFuncSetAttribute(tree_attn_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
-      return TSD_ERR_CUDA;
-    configured |= bit;
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void *f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
   }
+  return fn;
+}
+
+// 2-D view of a paged cache: rows = (block, kv head, slot), columns = D.
+bool make_cache_map(CUtensorMap *m, const uint16_t *cache, int num_blocks, int Hkv, int D) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)num_blocks * Hkv * kPage};
+  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)kPage};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(cache), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Opt a kernel in to more than 48 KB of dynamic shared memory, once per
+// (kernel, device).
+bool set_smem(const void *kernel, size_t bytes) {
+  struct Entry {
+    const void *fn;
+    int dev;
+  };
+  static Entry done[64];
+  static int n_done = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  for (int i = 0; i < n_done; ++i)
+    if (done[i].fn == kernel && done[i].dev == dev) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+      cudaSuccess)
+    return false;
+  if (n_done < 64) done[n_done++] = Entry{kernel, dev};
+  return true;
+}
+
+template <int D>
+int launch_attn(AttnParams &p, const AttnPlan &a, int B, int num_blocks, cudaStream_t s) {
   dim3 grid(p.row_tiles, p.splits, B * p.Hkv);
-  tree_attn_split_kernel<D><<<grid, kAttnThreads, smem, s>>>(p);
+  if (a.impl == 0) {
+    CUtensorMap mk, mv;
+    if (!make_cache_map(&mk, p.k, num_blocks, p.Hkv, D) ||
+        !make_cache_map(&mv, p.v, num_blocks, p.Hkv, D))
+      return TSD_ERR_CUDA;
+    if (!set_smem((const void *)tree_attn_split_tc<D>, TcLayout<D>::kAlloc)) return TSD_ERR_CUDA;
+    tree_attn_split_tc<D><<<grid, kTcThreads, TcLayout<D>::kAlloc, s>>>(p, mk, mv);
+  } else {
+    const size_t smem = (size_t)(kBM + 4 * kBN) * D * 2;
+    if (!set_smem((const void *)tree_attn_split_kernel<D>, smem)) return TSD_ERR_CUDA;
+    tree_attn_split_kernel<D><<<grid, kAttnThreads, smem, s>>>(p);
+  }
   if (cudaGetLastError() != cudaSuccess) return TSD_ERR_CUDA;
   const long rows = (long)B * p.N_max * p.Hq;
   const int blocks = (int)((rows * 32 + 255) / 256);
@@ -476,6 +913,7 @@ TSD_API int tsd_tree_attn_fwd(const uint16_t *q, const uint16_t *k_cache, const 
     return TSD_ERR_ARG;
   if (max_blocks < 1 || num_blocks < 1 || !(scale > 0.f) || !std::isfinite(scale))
     return TSD_ERR_ARG;
+  if ((long long)num_blocks * Hkv * kPage > 0x7FFFFFFFLL) return TSD_ERR_LIMIT;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
     return TSD_ERR_ARG;
   const AttnPlan a = plan_attn(B, N_max, Hq, Hkv, D, max_slots);
@@ -508,5 +946,7 @@ TSD_API int tsd_tree_attn_fwd(const uint16_t *q, const uint16_t *k_cache, const 
   p.out = out;
   p.lse = lse;
   p.status = status;
-  return D == 128 ? launch_attn<128>(p, B, as_cuda(stream)) : launch_attn<64>(p, B, as_cuda(stream));
+  p.wait_limit_ns = (uint64_t)option(TSD_OPT_WAIT_LIMIT_NS);
+  return D == 128 ? launch_attn<128>(p, a, B, num_blocks, as_cuda(stream))
+                  : launch_attn<64>(p, a, B, num_blocks, as_cuda(stream));
 }

@@ -1,0 +1,39 @@
+// Host-side state shared by the entry points: device properties, process-wide
+// options, version.
+
+#include "tsd_common.cuh"
+
+namespace tsd {
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 148;
+  if (dev < 64) cached[dev] = n;
+  return n;
+}
+
+static int64_t g_options[TSD_OPT_COUNT] = {
+    2000000000LL,  // TSD_OPT_WAIT_LIMIT_NS: 2 s
+    0,             // TSD_OPT_ATTN_KERNEL: tcgen05
+};
+
+int64_t option(int key) { return (key >= 0 && key < TSD_OPT_COUNT) ? g_options[key] : 0; }
+
+}  // namespace tsd
+
+TSD_API const char *tsd_version(void) { return "tsd 0.2 (sm_103a)"; }
+
+TSD_API int tsd_set_option(int key, int64_t value) {
+  if (key < 0 || key >= TSD_OPT_COUNT) return TSD_ERR_ARG;
+  if (key == TSD_OPT_WAIT_LIMIT_NS && value < 0) return TSD_ERR_ARG;
+  if (key == TSD_OPT_ATTN_KERNEL && (value < 0 || value > 1)) return TSD_ERR_ARG;
+  tsd::g_options[key] = value;
+  return TSD_OK;
+}
+
+TSD_API int64_t tsd_get_option(int key) { return tsd::option(key); }

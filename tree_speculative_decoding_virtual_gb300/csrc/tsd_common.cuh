@@ -23,6 +23,9 @@ inline int launch_status() {
 // Streaming multiprocessor count of the current device (cached per device).
 int sm_count();
 
+// Process-wide option (see tsd_set_option).
+int64_t option(int key);
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 inline bool aligned(const void *p, size_t a) {
