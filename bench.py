@@ -234,6 +234,7 @@ def gpu_arm(args, rank, world):
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
+    tsd.set_option(tsd.OPT_ATTN_KERNEL, 0 if args.attn_kernel == "tc" else 1)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
 
@@ -444,7 +445,8 @@ def gpu_arm(args, rank, world):
                    "seq_len": max_slots, "parallelism": "replicas (dp%d)" % world,
                    "l2": "flushed between timed steps (256 MiB write outside the timed events)",
                    "timing": "CUDA events on the launching stream around CUDA-graph replays of "
-                             "the whole step (value) and of each entry point (kernels)"},
+                             "the whole step (value) and of each entry point (kernels)",
+                   "attention_kernel": "tcgen05" if args.attn_kernel == "tc" else "mma.sync"},
         "hbm_gbs_step": round(step_bytes / (ms_per_step * 1e-3) / 1e9, 1),
         "kernels": kernels,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
@@ -475,6 +477,8 @@ def main():
     ap.add_argument("--workload", default="8b")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--attn-kernel", default="tc", choices=["tc", "mma"],
+                    help="tree attention kernel: tcgen05 (default) or the mma.sync one")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 

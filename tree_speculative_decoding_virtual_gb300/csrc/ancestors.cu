@@ -28,6 +28,8 @@ ancestors_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict__
   __shared__ int s_err;
   extern __shared__ int s_anc[];  // [(N_max + 1) * (D_max + 1)]
 
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x;
   const int t = threadIdx.x;
   const int cols = D_max + 1;
@@ -129,7 +131,8 @@ TSD_API int tsd_tree_build_ancestors(const int32_t *parent, const int32_t *n_nod
   if (!parent || !anc || !depth || !mask || !err) return TSD_ERR_ARG;
   const int W = (N_max + 31) / 32;
   const size_t smem = sizeof(int) * (size_t)(N_max + 1) * (D_max + 1);
-  ancestors_kernel<<<B, kThreads, smem, as_cuda(stream)>>>(parent, n_nodes, N_max, D_max, W, anc,
-                                                           depth, mask, err);
-  return launch_status();
+  if (launch(ancestors_kernel, dim3(B), dim3(kThreads), smem, as_cuda(stream), parent, n_nodes,
+             N_max, D_max, W, anc, depth, mask, err) != cudaSuccess)
+    return TSD_ERR_CUDA;
+  return TSD_OK;
 }

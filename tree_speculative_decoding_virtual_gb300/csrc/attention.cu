@@ -125,6 +125,8 @@ tree_attn_split_kernel(const AttnParams p) {
   unsigned char *sK = smem + kBM * D * 2;
   unsigned char *sV = sK + 2 * kBN * D * 2;
 
+  pdl_trigger();
+  pdl_wait();
   const int rt = blockIdx.x;
   const int split = blockIdx.y;
   const int z = blockIdx.z;
@@ -348,45 +350,58 @@ tree_attn_split_kernel(const AttnParams p) {
 
 // ===========================================================================
 // tcgen05 path.  One block = 128 query rows x one split of the key range of
-// one (sequence, kv head).  Warp 0 issues TMA loads of paged K/V tiles (128
-// keys = 8 blocks of 16 slots, 128-byte swizzle, two stages); warp 1 owns
-// the tensor memory and issues the MMAs (one thread); warps 2-5 run the
-// softmax, one TMEM lane (= one query row) per thread.
-//   S_j = Q K_j^T   (M=128, N=128, K=D; A and B K-major) -> TMEM, 2 buffers
-//   P_j = exp2(S_j * scale * log2e - m) as bf16 -> shared memory, 2 buffers
-//   O  += P_j V_j   (M=128, N=D, K=128; V MN-major)     -> TMEM
-// The running max is raised lazily: O and the row sum are rescaled (in
-// TMEM) only when a tile's max exceeds the one in use by more than 2^8, so
-// P never exceeds 256 and the result is the same softmax.  S_{j+1} is
-// issued before P_j V_j so the tensor core works while the softmax runs.
-// Every wait is bounded; on expiry the block flags TSD_STATUS_TIMEOUT,
-// drains what it issued, frees its tensor memory and returns.
+// one (sequence, kv head), walked in 64-key tiles.
+//   warp 0:    reads the split's block ids, then lane 0 loads K tiles and lane
+//              1 loads V tiles with TMA (4-stage rings; a K stage is refilled
+//              as soon as the Q K^T that read it completes, a V stage after P V)
+//   warp 1:    owns 256 TMEM columns; lane 0 issues every MMA
+//   warps 2-5: softmax, one TMEM lane (= one query row) per thread
+// Per tile j:
+//   S_j = Q K_j^T  (M=128, N=64, K=D; A and B K-major)  -> TMEM, 2 buffers
+//   P_j = exp2(S_j * scale * log2e - m) as bf16          -> smem, 2 buffers
+//   O  += P_j V_j  (M=128, N=D, K=64; V read MN-major)   -> TMEM
+// S_{j+1} is issued before P_j V_j, so the tensor core works while the
+// softmax of tile j runs.  The running max is raised lazily: O and the row
+// sum are rescaled (in TMEM) only when a tile's max exceeds the one in use by
+// more than 2^8, so P never exceeds 256 and the result is the same softmax.
+// K and V tiles are read straight from the paged cache by TMA (4-D view
+// [block][kv head][slot][D], 128-byte swizzle): when the four 16-slot blocks
+// of a 64-key tile are consecutive one box fetches them, otherwise one box
+// per block.  Measured on GB300 this beat a cp.async gather of the same tiles.
+// Every wait is bounded; on expiry the block flags TSD_STATUS_TIMEOUT, drains
+// what it issued, frees its tensor memory and returns.
 // ===========================================================================
 
 constexpr int kTcThreads = 192;
 constexpr int kTcBM = 128;
-constexpr int kTcBN = 128;
-constexpr uint32_t kTmemCols = 512;
+constexpr int kTcBN = 64;
+constexpr int kTcStages = 4;
+constexpr uint32_t kTmemCols = 256;
 constexpr uint64_t kDrainLimitNs = 100000000ull;  // 100 ms
 
 template <int D>
 struct TcLayout {
-  static constexpr int kHalves = D / 64;                      // 128-byte column blocks
-  static constexpr uint32_t kHalfBytes = 128 * 128;           // one column block of 128 rows
-  static constexpr uint32_t kTile = kTcBN * D * 2;            // one K or V tile
+  static constexpr int kHalves = D / 64;                  // 128-byte column blocks of a row
+  static constexpr uint32_t kQHalf = kTcBM * 128;         // one column block of Q (128 rows)
+  static constexpr uint32_t kKVHalf = kTcBN * 128;        // one column block of a K/V tile
+  static constexpr uint32_t kTile = kTcBN * D * 2;        // one K or V tile
   static constexpr uint32_t kQ = 0;
   static constexpr uint32_t kK = kTcBM * D * 2;
-  static constexpr uint32_t kV = kK + 2 * kTile;
-  static constexpr uint32_t kP = kV + 2 * kTile;
-  static constexpr uint32_t kPBytes = kTcBM * kTcBN * 2;
+  static constexpr uint32_t kV = kK + kTcStages * kTile;
+  static constexpr uint32_t kP = kV + kTcStages * kTile;
+  static constexpr uint32_t kPBytes = kTcBM * kTcBN * 2;  // 128 rows x 64 keys bf16
   static constexpr uint32_t kBytes = kP + 2 * kPBytes;
-  static constexpr uint32_t kAlloc = kBytes + 1024;           // + alignment slack
-  static constexpr uint32_t kTmemS = 0;                       // two 128-column S buffers
-  static constexpr uint32_t kTmemO = 256;                     // D columns of O
+  static constexpr uint32_t kAlloc = kBytes + 1024;       // + alignment slack
+  static constexpr uint32_t kTmemS = 0;                   // two 64-column S buffers
+  static constexpr uint32_t kTmemO = 128;                 // D columns of O
 };
 
+constexpr int kTcMaxPages = 2048;  // block ids of one split held in shared memory
+
 struct TcShared {
-  uint64_t k_full[2], v_full[2], kv_empty[2], s_full[2], s_free[2], p_full[2], p_free[2];
+  int32_t rows[kTcMaxPages];  // tensor-map row of each block of the split (y coordinate)
+  uint64_t k_full[kTcStages], k_empty[kTcStages], v_full[kTcStages], v_empty[kTcStages];
+  uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
   uint64_t q_full, drain;
   uint32_t tmem_base;
   int abort;
@@ -400,15 +415,43 @@ __device__ __forceinline__ bool tc_wait(uint64_t &bar, uint32_t parity, uint64_t
   return false;
 }
 
+// Visibility of 32 consecutive key slots for one query row: bit i covers the
+// slot whose tail index (slot - P) is j0 + i.  Prefix slots (j0 + i < 0) are
+// visible; tail slot j is visible iff bit j of the row's ancestor mask is set;
+// slots at or past the split's end (i >= remaining) are not.
+__device__ __forceinline__ uint32_t visible_bits(const uint32_t *mrow, int W, int j0, int remaining,
+                                                 bool row_valid) {
+  uint32_t bits;
+  if (j0 <= -32) {
+    bits = 0xFFFFFFFFu;
+  } else if (j0 < 0) {
+    const int sh = -j0;  // 1..31 prefix slots first
+    const uint32_t tail = row_valid ? __ldg(mrow) : 0u;
+    bits = ((1u << sh) - 1u) | (tail << sh);
+  } else if (!row_valid) {
+    bits = 0u;
+  } else {
+    const int w0 = j0 >> 5;
+    const uint32_t lo = w0 < W ? __ldg(mrow + w0) : 0u;
+    const uint32_t hi = w0 + 1 < W ? __ldg(mrow + w0 + 1) : 0u;
+    bits = __funnelshift_r(lo, hi, j0 & 31);
+  }
+  if (remaining < 32) bits &= remaining <= 0 ? 0u : ((1u << remaining) - 1u);
+  return bits;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
-tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap tmap_k,
-                   const __grid_constant__ CUtensorMap tmap_v) {
+tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k1,
+                   const __grid_constant__ CUtensorMap map_k4, const __grid_constant__ CUtensorMap map_v1,
+                   const __grid_constant__ CUtensorMap map_v4) {
   using namespace sm100;
   using L = TcLayout<D>;
   extern __shared__ unsigned char smem_raw[];
   __shared__ TcShared sh;
 
+  pdl_trigger();
+  pdl_wait();
   const int rt = blockIdx.x;
   const int split = blockIdx.y;
   const int z = blockIdx.z;
@@ -441,10 +484,13 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap tmap_
   const uint64_t lim = p.wait_limit_ns;
 
   if (tid == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kTcStages; ++i) {
       mbar_init(smem_addr(&sh.k_full[i]), 1);
+      mbar_init(smem_addr(&sh.k_empty[i]), 1);
       mbar_init(smem_addr(&sh.v_full[i]), 1);
-      mbar_init(smem_addr(&sh.kv_empty[i]), 1);
+      mbar_init(smem_addr(&sh.v_empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(smem_addr(&sh.s_full[i]), 1);
       mbar_init(smem_addr(&sh.s_free[i]), 4);
       mbar_init(smem_addr(&sh.p_full[i]), 4);
@@ -454,101 +500,117 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap tmap_
     mbar_init(smem_addr(&sh.drain), 1);
     sh.abort = 0;
     fence_mbar_init();
+    tma_prefetch_desc(&map_k1);
+    tma_prefetch_desc(&map_k4);
+    tma_prefetch_desc(&map_v1);
+    tma_prefetch_desc(&map_v4);
   }
   if (warp == 1) tmem_alloc(smem_addr(&sh.tmem_base), kTmemCols);
-  if (tid == 32 * 0) {
-    tma_prefetch_desc(&tmap_k);
-    tma_prefetch_desc(&tmap_v);
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
 
   if (warp == 0) {
-    // ------------------------------ TMA producer ------------------------------
-    if (lane == 0) {
-      const int32_t *trow = p.table + (size_t)b * p.max_blocks;
-      const int last_page = (seq_len - 1) / kPage;
-      int last_issued[2] = {-1, -1};
-      bool bad = false;
+    // --------------------------- loaders (TMA) ---------------------------
+    // every block id of the split is read once, by the whole warp, up front
+    const int32_t *trow = p.table + (size_t)b * p.max_blocks;
+    const int pg_first = k_begin / kPage;
+    const int pg_last = (k_end - 1) / kPage;
+    const int npg = pg_last - pg_first + 1;  // <= chunk / 16 <= kTcMaxPages (host check)
+    bool bad = false;
+    for (int i = lane; i < npg; i += 32) {
+      int page = __ldg(trow + pg_first + i);
+      if (page < 0 || page >= p.num_blocks) {
+        bad = true;
+        page = 0;
+      }
+      sh.rows[i] = page;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0 && p.status) atomicOr(p.status, TSD_STATUS_BAD_PAGE);
+    __syncwarp();
+    if (lane < 2) {
+      const bool is_k = lane == 0;
+      const CUtensorMap *m1 = is_k ? &map_k1 : &map_v1;
+      const CUtensorMap *m4 = is_k ? &map_k4 : &map_v4;
+      uint64_t *full = is_k ? sh.k_full : sh.v_full;
+      uint64_t *empty = is_k ? sh.k_empty : sh.v_empty;
+      const uint32_t ring = base + (is_k ? L::kK : L::kV);
+      int last_issued[kTcStages];
+#pragma unroll
+      for (int i = 0; i < kTcStages; ++i) last_issued[i] = -1;
       for (int j = 0; j < ntiles && !*abort; ++j) {
-        const int st = j & 1;
-        if (j >= 2 && !tc_wait(sh.kv_empty[st], ((j >> 1) - 1) & 1, lim, abort)) break;
-        const int pg0 = (k_begin + j * kTcBN) / kPage;
-        int ys[kTcBN / kPage];
+        const int st = j % kTcStages;
+        if (j >= kTcStages && !tc_wait(empty[st], ((j / kTcStages) - 1) & 1, lim, abort)) break;
+        const int g0 = j * (kTcBN / kPage);
+        int pg[kTcBN / kPage];
 #pragma unroll
-        for (int g = 0; g < kTcBN / kPage; ++g) {
-          int page = __ldg(trow + min(pg0 + g, last_page));
-          if (page < 0 || page >= p.num_blocks) {
-            bad = true;
-            page = 0;
+        for (int g = 0; g < kTcBN / kPage; ++g) pg[g] = sh.rows[min(g0 + g, npg - 1)];
+        const bool run = pg[1] == pg[0] + 1 && pg[2] == pg[0] + 2 && pg[3] == pg[0] + 3;
+        const uint32_t bar = smem_addr(&full[st]);
+        mbar_arrive_expect_tx(bar, L::kTile);
+#pragma unroll
+        for (int h = 0; h < L::kHalves; ++h) {
+          const uint32_t dst = ring + st * L::kTile + h * L::kKVHalf;
+          if (run) {
+            tma_load_4d(dst, m4, h * 64, 0, hkv, pg[0], bar);
+          } else {
+#pragma unroll
+            for (int g = 0; g < kTcBN / kPage; ++g)
+              tma_load_4d(dst + g * kPage * 128, m1, h * 64, 0, hkv, pg[g], bar);
           }
-          ys[g] = (page * p.Hkv + hkv) * kPage;
         }
-        mbar_arrive_expect_tx(smem_addr(&sh.k_full[st]), L::kTile);
-#pragma unroll
-        for (int g = 0; g < kTcBN / kPage; ++g)
-#pragma unroll
-          for (int h = 0; h < L::kHalves; ++h)
-            tma_load_2d(base + L::kK + st * L::kTile + h * L::kHalfBytes + g * kPage * 128, &tmap_k,
-                        h * 64, ys[g], smem_addr(&sh.k_full[st]));
-        mbar_arrive_expect_tx(smem_addr(&sh.v_full[st]), L::kTile);
-#pragma unroll
-        for (int g = 0; g < kTcBN / kPage; ++g)
-#pragma unroll
-          for (int h = 0; h < L::kHalves; ++h)
-            tma_load_2d(base + L::kV + st * L::kTile + h * L::kHalfBytes + g * kPage * 128, &tmap_v,
-                        h * 64, ys[g], smem_addr(&sh.v_full[st]));
         last_issued[st] = j;
       }
       // drain: the last loads issued into each stage have landed
-      for (int st = 0; st < 2; ++st)
-        if (last_issued[st] >= 0) {
-          const uint32_t par = (last_issued[st] >> 1) & 1;
-          mbar_wait(smem_addr(&sh.k_full[st]), par, kDrainLimitNs);
-          mbar_wait(smem_addr(&sh.v_full[st]), par, kDrainLimitNs);
-        }
-      if (bad && p.status) atomicOr(p.status, TSD_STATUS_BAD_PAGE);
+#pragma unroll
+      for (int st = 0; st < kTcStages; ++st)
+        if (last_issued[st] >= 0)
+          mbar_wait(smem_addr(&full[st]), (last_issued[st] / kTcStages) & 1, kDrainLimitNs);
     }
   } else if (warp == 1) {
-    // ------------------------------ MMA issuer ------------------------------
+    // ------------------------------ MMA issuer ------------------------------ ------------------------------
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(kTcBM, kTcBN, false, false);
       constexpr uint32_t idPV = idesc_bf16_f32(kTcBM, D, false, true);
       auto issue_s = [&](int j) -> bool {
-        const int st = j & 1;
-        if (!tc_wait(sh.k_full[st], (j >> 1) & 1, lim, abort)) return false;
-        if (j >= 2 && !tc_wait(sh.s_free[st], ((j >> 1) - 1) & 1, lim, abort)) return false;
+        const int st = j % kTcStages, sb = j & 1;
+        if (!tc_wait(sh.k_full[st], (j / kTcStages) & 1, lim, abort)) return false;
+        if (j >= 2 && !tc_wait(sh.s_free[sb], ((j >> 1) - 1) & 1, lim, abort)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
-          umma_bf16(tmem + L::kTmemS + st * kTcBN, smem_desc_sw128(base + L::kQ + koff, 16, 1024),
-                    smem_desc_sw128(base + L::kK + st * L::kTile + koff, 16, 1024), idS, kk > 0);
+          umma_bf16(tmem + L::kTmemS + sb * kTcBN,
+                    smem_desc_sw128(base + L::kQ + (kk >> 2) * L::kQHalf + (kk & 3) * 32, 16, 1024),
+                    smem_desc_sw128(base + L::kK + st * L::kTile + (kk >> 2) * L::kKVHalf +
+                                        (kk & 3) * 32, 16, 1024),
+                    idS, kk > 0);
         }
-        umma_commit(smem_addr(&sh.s_full[st]));
+        umma_commit(smem_addr(&sh.s_full[sb]));
+        umma_commit(smem_addr(&sh.k_empty[st]));
         return true;
       };
       auto issue_pv = [&](int j) -> bool {
-        const int st = j & 1;
-        if (!tc_wait(sh.p_full[st], (j >> 1) & 1, lim, abort)) return false;
-        if (!tc_wait(sh.v_full[st], (j >> 1) & 1, lim, abort)) return false;
+        const int st = j % kTcStages, pb = j & 1;
+        if (!tc_wait(sh.p_full[pb], (j >> 1) & 1, lim, abort)) return false;
+        if (!tc_wait(sh.v_full[st], (j / kTcStages) & 1, lim, abort)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTcBN / 16; ++kk) {
-          const uint32_t aoff = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
-          umma_bf16(tmem + L::kTmemO, smem_desc_sw128(base + L::kP + st * L::kPBytes + aoff, 16, 1024),
-                    smem_desc_sw128(base + L::kV + st * L::kTile + kk * 16 * 128, L::kHalfBytes, 1024),
+          umma_bf16(tmem + L::kTmemO,
+                    smem_desc_sw128(base + L::kP + pb * L::kPBytes + kk * 32, 16, 1024),
+                    smem_desc_sw128(base + L::kV + st * L::kTile + kk * 16 * 128, L::kKVHalf, 1024),
                     idPV, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(smem_addr(&sh.p_free[st]));
-        umma_commit(smem_addr(&sh.kv_empty[st]));
+        umma_commit(smem_addr(&sh.p_free[pb]));
+        umma_commit(smem_addr(&sh.v_empty[st]));
         return true;
       };
       bool ok = tc_wait(sh.q_full, 0, lim, abort) && issue_s(0);
-      for (int j = 1; ok && j < ntiles; ++j) ok = !*abort && issue_s(j) && issue_pv(j - 1);
-      if (ok) ok = issue_pv(ntiles - 1);
+      for (int j = 0; ok && j < ntiles; ++j) {
+        if (j + 1 < ntiles) ok = !*abort && issue_s(j + 1);
+        if (ok) ok = issue_pv(j);
+      }
       // drain: every MMA issued above has completed
       umma_commit(smem_addr(&sh.drain));
       mbar_wait(smem_addr(&sh.drain), 0, kDrainLimitNs);
@@ -571,7 +633,7 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap tmap_
 #pragma unroll
     for (int c = 0; c < D / 8; ++c) {
       const uint4 v = rvalid ? __ldg(qsrc + c) : make_uint4(0u, 0u, 0u, 0u);
-      *reinterpret_cast<uint4 *>(gbase + L::kQ + (c >> 3) * L::kHalfBytes + sw128_offset(rl, c & 7)) = v;
+      *reinterpret_cast<uint4 *>(gbase + L::kQ + (c >> 3) * L::kQHalf + sw128_offset(rl, c & 7)) = v;
     }
     fence_proxy_async_smem();
     __syncwarp();
@@ -586,46 +648,40 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap tmap_
     float m_use = -INFINITY, l_sum = 0.f;
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
-      const int st = j & 1;
-      if (!warp_wait(sh.s_full[st], (j >> 1) & 1)) {
+      const int sb = j & 1;
+      if (!warp_wait(sh.s_full[sb], (j >> 1) & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t r[4][32];
+      uint32_t r[2][32];
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(tmem + L::kTmemS + st * kTcBN + lane_off + c4 * 32, r[c4]);
+      for (int c2 = 0; c2 < 2; ++c2) tmem_ld32(tmem + L::kTmemS + sb * kTcBN + lane_off + c2 * 32, r[c2]);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&sh.s_free[st]));
+      if (lane == 0) mbar_arrive(smem_addr(&sh.s_free[sb]));
 
       const int ts = k_begin + j * kTcBN;
       const bool full = (ts + kTcBN <= P) && (ts + kTcBN <= k_end);
-      float mt = -INFINITY;
+      // masked scores become -inf; the max is taken on raw scores (scale > 0)
+      if (!full) {
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t vis = 0xFFFFFFFFu;
-        if (!full) {
-          vis = 0u;
-          for (int i = 0; i < 32; ++i) {
-            const int slot = ts + c4 * 32 + i;
-            bool v = slot < k_end;
-            if (v && slot >= P) {
-              const int jj = slot - P;
-              v = rvalid && ((__ldg(mrow + (jj >> 5)) >> (jj & 31)) & 1u);
-            }
-            vis |= (v ? 1u : 0u) << i;
-          }
-        }
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const uint32_t vis =
+              visible_bits(mrow, p.W, ts + c2 * 32 - P, k_end - (ts + c2 * 32), rvalid);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float x = __uint_as_float(r[c4][i]) * p.scale_log2;
-          x = ((vis >> i) & 1u) ? x : -INFINITY;
-          r[c4][i] = __float_as_uint(x);
-          mt = fmaxf(mt, x);
+          for (int i = 0; i < 32; ++i)
+            if (!((vis >> i) & 1u)) r[c2][i] = __float_as_uint(-INFINITY);
         }
       }
+      float mx[8];
+#pragma unroll
+      for (int a = 0; a < 8; ++a) mx[a] = __uint_as_float(r[0][a]);
+#pragma unroll
+      for (int i = 8; i < 64; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(r[i >> 5][i & 31]));
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * p.scale_log2;
       const float m_new = fmaxf(m_use, mt);
       const bool upd = m_new > m_use + 8.f;  // first visible key, or the max grew by > 2^8
       const float alpha = upd ? exp2f(m_use - m_new) : 1.f;
@@ -652,35 +708,36 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap tmap_
         m_use = m_new;
       }
       const float mb = m_use == -INFINITY ? 0.f : m_use;
-      // P_j must not overwrite buffer st before P_{j-2} V_{j-2} has read it
-      if (j >= 2 && !warp_wait(sh.p_free[st], ((j >> 1) - 1) & 1)) {
+      // P_j must not overwrite buffer sb before P_{j-2} V_{j-2} has read it
+      if (j >= 2 && !warp_wait(sh.p_free[sb], ((j >> 1) - 1) & 1)) {
         ok = false;
         break;
       }
-      float rs = 0.f;
-      unsigned char *pbuf = gbase + L::kP + st * L::kPBytes;
+      float rsum[4] = {0.f, 0.f, 0.f, 0.f};
+      unsigned char *pbuf = gbase + L::kP + sb * L::kPBytes;
+      const float sc = p.scale_log2;
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
+      for (int c2 = 0; c2 < 2; ++c2) {
 #pragma unroll
         for (int q8 = 0; q8 < 4; ++q8) {  // 8 keys = one 16-byte chunk
           uint32_t w[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float a = exp2f(__uint_as_float(r[c4][q8 * 8 + 2 * e]) - mb);
-            const float c = exp2f(__uint_as_float(r[c4][q8 * 8 + 2 * e + 1]) - mb);
-            rs += a + c;
+            const float a = ex2_approx(fmaf(__uint_as_float(r[c2][q8 * 8 + 2 * e]), sc, -mb));
+            const float c = ex2_approx(fmaf(__uint_as_float(r[c2][q8 * 8 + 2 * e + 1]), sc, -mb));
+            rsum[e] += a + c;
             w[e] = pack_bf16(a, c);
           }
-          const int chunk = c4 * 4 + q8;  // 0..15 across 128 keys
-          *reinterpret_cast<uint4 *>(pbuf + (chunk >> 3) * L::kHalfBytes + sw128_offset(rl, chunk & 7)) =
+          *reinterpret_cast<uint4 *>(pbuf + sw128_offset(rl, c2 * 4 + q8)) =
               make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
+      const float rs = (rsum[0] + rsum[1]) + (rsum[2] + rsum[3]);
       l_sum += rs;
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&sh.p_full[st]));
+      if (lane == 0) mbar_arrive(smem_addr(&sh.p_full[sb]));
     }
 
     // ---- epilogue: unnormalised O, running max (log2 units) and row sum ----
@@ -711,10 +768,14 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap tmap_
   }
 }
 
-// One warp per output row (b, node, q head): merge the splits.
+// One warp per output row (b, node, q head): merge the splits.  Lane s reads
+// split s's (max, sum); every lane then accumulates its D/32 columns over the
+// splits with all loads independent.
 template <int D>
 __global__ void __launch_bounds__(256) tree_attn_combine_kernel(const AttnParams p, int B) {
   constexpr int kPer = D / 32;
+  pdl_trigger();
+  pdl_wait();
   const int warp = (blockIdx.x * 256 + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const long total = (long)B * p.N_max * p.Hq;
@@ -727,39 +788,59 @@ __global__ void __launch_bounds__(256) tree_attn_combine_kernel(const AttnParams
   int P, nb;
   const bool ok = seq_ok(p, b, P, nb) && node < nb;
   if (!ok) {
-#pragma unroll
-    for (int x = 0; x < kPer; ++x) dst[x] = 0;
+    if (kPer == 4)
+      *reinterpret_cast<uint2 *>(dst) = make_uint2(0u, 0u);
+    else
+      *reinterpret_cast<uint32_t *>(dst) = 0u;
     if (p.lse && lane == 0) p.lse[warp] = -INFINITY;
     return;
   }
   const int hkv = hq / p.g;
   const int row = node * p.g + (hq % p.g);
-  const int z = b * p.Hkv + hkv;
-  const int ns = (P + nb + p.chunk - 1) / p.chunk;
-  float M = -INFINITY;
-  for (int s = 0; s < ns; ++s) {
-    const float2 ml = p.part_ml[((size_t)z * p.splits + s) * p.rows_pad + row];
-    M = fmaxf(M, ml.x);
-  }
-  float L = 0.f;
+  const size_t r0 = (size_t)(b * p.Hkv + hkv) * p.splits * p.rows_pad + row;
+  const int ns = (P + nb + p.chunk - 1) / p.chunk;  // <= 32 (host check)
+  const float2 ml = lane < ns ? p.part_ml[r0 + (size_t)lane * p.rows_pad]
+                              : make_float2(-INFINITY, 0.f);
+  float M = ml.x;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  const float w = lane < ns ? exp2f(ml.x - M) : 0.f;
+  float L = ml.y * w;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
   float acc[kPer];
 #pragma unroll
   for (int x = 0; x < kPer; ++x) acc[x] = 0.f;
-  for (int s = 0; s < ns; ++s) {
-    const size_t r = ((size_t)z * p.splits + s) * p.rows_pad + row;
-    const float2 ml = p.part_ml[r];
-    const float w = exp2f(ml.x - M);
-    L += ml.y * w;
-    const float *src = p.part_o + r * D + lane * kPer;
+  for (int s0 = 0; s0 < ns; s0 += 8) {
+    float v[8][kPer];
+    float ws[8];
 #pragma unroll
-    for (int x = 0; x < kPer; ++x) acc[x] += src[x] * w;
+    for (int u = 0; u < 8; ++u) {
+      const int s = s0 + u;
+      ws[u] = __shfl_sync(0xffffffffu, w, s & 31);
+      const float *src = p.part_o + (r0 + (size_t)min(s, ns - 1) * p.rows_pad) * D + lane * kPer;
+      if (kPer == 4) {
+        const float4 t = __ldcg(reinterpret_cast<const float4 *>(src));
+        v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
+      } else {
+        const float2 t = __ldcg(reinterpret_cast<const float2 *>(src));
+        v[u][0] = t.x; v[u][1] = t.y;
+      }
+      if (s >= ns) ws[u] = 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+#pragma unroll
+      for (int x = 0; x < kPer; ++x) acc[x] += v[u][x] * ws[u];
   }
   const float inv = 1.f / L;
+  uint32_t packed[kPer / 2];
 #pragma unroll
-  for (int x = 0; x < kPer; ++x) {
-    const __nv_bfloat16 h = __float2bfloat16_rn(acc[x] * inv);
-    dst[x] = *reinterpret_cast<const uint16_t *>(&h);
-  }
+  for (int x = 0; x < kPer / 2; ++x) packed[x] = pack_bf16(acc[2 * x] * inv, acc[2 * x + 1] * inv);
+  if (kPer == 4)
+    *reinterpret_cast<uint2 *>(dst) = make_uint2(packed[0], packed[1]);
+  else
+    *reinterpret_cast<uint32_t *>(dst) = packed[0];
   if (p.lse && lane == 0) p.lse[warp] = (M + log2f(L)) * 0.6931471805599453f;
 }
 
@@ -783,12 +864,12 @@ AttnPlan plan_attn(int B, int N_max, int Hq, int Hkv, int D, int max_slots) {
   long best_s = 1;
   if (a.impl == 0) {
     // one resident block per SM: estimated time = waves x (tiles per block +
-    // a fixed cost of about four tiles for the prologue and the partials)
+    // a fixed cost of about eight 64-key tiles for the prologue and partials)
     double best_t = 1e30;
-    for (long s = 1; s <= max_tiles && s <= 64; ++s) {
+    for (long s = 1; s <= max_tiles && s <= 32; ++s) {
       const long waves = (units * s + nsm - 1) / nsm;
       const long per = (max_tiles + s - 1) / s;
-      const double t = (double)waves * (double)(per + 4);
+      const double t = (double)waves * (double)(per + 8);
       if (t < best_t - 1e-9) {
         best_t = t;
         best_s = s;
@@ -802,6 +883,8 @@ AttnPlan plan_attn(int B, int N_max, int Hq, int Hkv, int D, int max_slots) {
   }
   long chunk = (max_slots + best_s - 1) / best_s;
   chunk = (chunk + a.bn - 1) / a.bn * a.bn;
+  if (a.impl == 0 && chunk > (long)kTcMaxPages * kPage) chunk = (long)kTcMaxPages * kPage;
+  while ((max_slots + chunk - 1) / chunk > 32) chunk += a.bn;
   a.chunk = (int)chunk;
   a.splits = (int)((max_slots + chunk - 1) / chunk);
   if (a.splits < 1) a.splits = 1;
@@ -825,15 +908,18 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 2-D view of a paged cache: rows = (block, kv head, slot), columns = D.
-bool make_cache_map(CUtensorMap *m, const uint16_t *cache, int num_blocks, int Hkv, int D) {
+// 4-D view [block][kv head][slot][D] of a paged cache; a box covers 64
+// columns of 16 slots of `pages` consecutive blocks of one head.
+bool make_cache_map(CUtensorMap *m, const uint16_t *cache, int num_blocks, int Hkv, int D,
+                    int pages) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)num_blocks * Hkv * kPage};
-  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)kPage};
-  cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(cache), dims, strides,
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)kPage, (cuuint64_t)Hkv, (cuuint64_t)num_blocks};
+  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)kPage * D * 2,
+                           (cuuint64_t)Hkv * kPage * D * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)kPage, 1, (cuuint32_t)pages};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t *>(cache), dims, strides,
              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -862,22 +948,28 @@ template <int D>
 int launch_attn(AttnParams &p, const AttnPlan &a, int B, int num_blocks, cudaStream_t s) {
   dim3 grid(p.row_tiles, p.splits, B * p.Hkv);
   if (a.impl == 0) {
-    CUtensorMap mk, mv;
-    if (!make_cache_map(&mk, p.k, num_blocks, p.Hkv, D) ||
-        !make_cache_map(&mv, p.v, num_blocks, p.Hkv, D))
+    CUtensorMap k1, k4, v1, v4;
+    if (!make_cache_map(&k1, p.k, num_blocks, p.Hkv, D, 1) ||
+        !make_cache_map(&k4, p.k, num_blocks, p.Hkv, D, kTcBN / kPage) ||
+        !make_cache_map(&v1, p.v, num_blocks, p.Hkv, D, 1) ||
+        !make_cache_map(&v4, p.v, num_blocks, p.Hkv, D, kTcBN / kPage))
       return TSD_ERR_CUDA;
     if (!set_smem((const void *)tree_attn_split_tc<D>, TcLayout<D>::kAlloc)) return TSD_ERR_CUDA;
-    tree_attn_split_tc<D><<<grid, kTcThreads, TcLayout<D>::kAlloc, s>>>(p, mk, mv);
+    if (launch(tree_attn_split_tc<D>, grid, dim3(kTcThreads), TcLayout<D>::kAlloc, s, p, k1, k4, v1,
+               v4) != cudaSuccess)
+      return TSD_ERR_CUDA;
   } else {
     const size_t smem = (size_t)(kBM + 4 * kBN) * D * 2;
     if (!set_smem((const void *)tree_attn_split_kernel<D>, smem)) return TSD_ERR_CUDA;
-    tree_attn_split_kernel<D><<<grid, kAttnThreads, smem, s>>>(p);
+    if (launch(tree_attn_split_kernel<D>, grid, dim3(kAttnThreads), smem, s, p) != cudaSuccess)
+      return TSD_ERR_CUDA;
   }
   if (cudaGetLastError() != cudaSuccess) return TSD_ERR_CUDA;
   const long rows = (long)B * p.N_max * p.Hq;
   const int blocks = (int)((rows * 32 + 255) / 256);
-  tree_attn_combine_kernel<D><<<blocks, 256, 0, s>>>(p, B);
-  return launch_status();
+  if (launch(tree_attn_combine_kernel<D>, dim3(blocks), dim3(256), 0, s, p, B) != cudaSuccess)
+    return TSD_ERR_CUDA;
+  return TSD_OK;
 }
 
 }  // namespace

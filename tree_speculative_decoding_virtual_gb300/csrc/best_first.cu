@@ -67,6 +67,8 @@ topk_kernel(const float *__restrict__ q, int K, int V, int M, int32_t *__restric
   __shared__ unsigned s_warp[32];
   __shared__ unsigned long long s_sel[256];
 
+  pdl_trigger();
+  pdl_wait();
   const int k = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
   const float *row = q + ((size_t)b * K + k) * (size_t)V;
 
@@ -179,6 +181,8 @@ expand_kernel(const int32_t *__restrict__ top_tok, const float *__restrict__ top
   int32_t *s_tt = reinterpret_cast<int32_t *>(s_tq + (size_t)K * M);  // [K][M]
   __shared__ float s_rho[kMaxNodes];
 
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x, t = threadIdx.x;
   for (int x = t; x < K * M; x += kExpandThreads) {
     s_tq[x] = top_q[(size_t)b * K * M + x];
@@ -344,8 +348,9 @@ TSD_API int tsd_best_first_tree_build(const float *q, const int32_t *root_token,
   float *top_q = reinterpret_cast<float *>(static_cast<char *>(workspace) + p.tok_bytes);
   cudaStream_t s = as_cuda(stream);
   if (p.M > 0) {
-    topk_kernel<<<dim3(K, B), kTopThreads, 0, s>>>(q, K, V, p.M, top_tok, top_q);
-    if (cudaGetLastError() != cudaSuccess) return TSD_ERR_CUDA;
+    if (launch(topk_kernel, dim3(K, B), dim3(kTopThreads), 0, s, q, K, V, p.M, top_tok, top_q) !=
+        cudaSuccess)
+      return TSD_ERR_CUDA;
   }
   const size_t smem = (size_t)K * (p.M > 0 ? p.M : 0) * (sizeof(float) + sizeof(int32_t));
   if (smem > 48 * 1024) {
@@ -353,7 +358,8 @@ TSD_API int tsd_best_first_tree_build(const float *q, const int32_t *root_token,
                              (int)smem) != cudaSuccess)
       return TSD_ERR_CUDA;
   }
-  expand_kernel<<<B, kExpandThreads, smem, s>>>(top_tok, top_q, root_token, K, p.M, N, parent,
-                                                tokens, depth, rho, ahat);
-  return launch_status();
+  if (launch(expand_kernel, dim3(B), dim3(kExpandThreads), smem, s, top_tok, top_q, root_token, K,
+             p.M, N, parent, tokens, depth, rho, ahat) != cudaSuccess)
+    return TSD_ERR_CUDA;
+  return TSD_OK;
 }

@@ -35,6 +35,8 @@ commit_kernel(uint16_t *__restrict__ k_cache, uint16_t *__restrict__ v_cache,
   __shared__ long long s_dst[kMaxMoves];
   __shared__ int s_n;
 
+  pdl_trigger();
+  pdl_wait();
   const int h = blockIdx.x;
   const int b = blockIdx.y;
   const int layer = blockIdx.z;
@@ -132,13 +134,12 @@ TSD_API int tsd_kv_commit_path(uint16_t *k_cache, uint16_t *v_cache, int num_lay
   const int64_t pool = (int64_t)num_blocks * Hkv * kPage * D;
   if (num_layers > 1 && (layer_stride < pool || layer_stride % 8 != 0)) return TSD_ERR_ARG;
   dim3 grid(Hkv, B, num_layers);
-  if (D == 128)
-    commit_kernel<128><<<grid, kThreads, 0, as_cuda(stream)>>>(
-        k_cache, v_cache, layer_stride, block_table, max_blocks, num_blocks, prefix_len, n_nodes,
-        accept_len, path, err, N_max, Hkv, D_max, new_len, moved, status);
-  else
-    commit_kernel<64><<<grid, kThreads, 0, as_cuda(stream)>>>(
-        k_cache, v_cache, layer_stride, block_table, max_blocks, num_blocks, prefix_len, n_nodes,
-        accept_len, path, err, N_max, Hkv, D_max, new_len, moved, status);
-  return launch_status();
+  const cudaError_t e =
+      D == 128 ? launch(commit_kernel<128>, grid, dim3(kThreads), 0, as_cuda(stream), k_cache,
+                        v_cache, layer_stride, block_table, max_blocks, num_blocks, prefix_len,
+                        n_nodes, accept_len, path, err, N_max, Hkv, D_max, new_len, moved, status)
+               : launch(commit_kernel<64>, grid, dim3(kThreads), 0, as_cuda(stream), k_cache,
+                        v_cache, layer_stride, block_table, max_blocks, num_blocks, prefix_len,
+                        n_nodes, accept_len, path, err, N_max, Hkv, D_max, new_len, moved, status);
+  return e == cudaSuccess ? TSD_OK : TSD_ERR_CUDA;
 }

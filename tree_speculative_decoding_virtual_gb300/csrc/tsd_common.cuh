@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "tsd.h"
 
 #define TSD_API extern "C" __attribute__((visibility("default")))
@@ -27,6 +29,31 @@ int sm_count();
 int64_t option(int key);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Programmatic dependent launch: every kernel of the library is launched so
+// that it may start while the previous kernel on the stream finishes; each
+// kernel lets its own dependents launch at entry (pdl_trigger) and waits for
+// the previous grid's completion and memory (pdl_wait) before it touches
+// global memory.  After a kernel that does not trigger, this is an ordinary
+// stream-ordered launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 inline bool aligned(const void *p, size_t a) {
   return (reinterpret_cast<uintptr_t>(p) % a) == 0;

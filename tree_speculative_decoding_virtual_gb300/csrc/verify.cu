@@ -23,7 +23,7 @@ namespace tsd {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 4;
+constexpr int kBatch = 8;  // independent 16-byte loads in flight per thread
 
 struct Partial {
   float v;
@@ -37,6 +37,10 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
 
 __device__ __forceinline__ float4 ld_stream(const float4 *p) { return __ldcs(p); }
 
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+  asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p));
+}
+
 __global__ void __launch_bounds__(kThreads)
 verify_greedy_kernel(const float *__restrict__ logits, const int32_t *__restrict__ tokens,
                      const int32_t *__restrict__ parent, const int32_t *__restrict__ anc,
@@ -47,6 +51,8 @@ verify_greedy_kernel(const float *__restrict__ logits, const int32_t *__restrict
                      int32_t *__restrict__ leaf_out, int32_t *__restrict__ path,
                      int32_t *__restrict__ bonus, Partial *__restrict__ part,
                      unsigned *__restrict__ counter) {
+  pdl_trigger();
+  pdl_wait();
   const int c = blockIdx.x;
   const int i = blockIdx.y;
   const int b = blockIdx.z;
@@ -62,6 +68,21 @@ verify_greedy_kernel(const float *__restrict__ logits, const int32_t *__restrict
   __shared__ int s_i[kThreads / 32];
   __shared__ bool s_last;
 
+  // The first block of each sequence pulls the acceptance inputs into L2 so
+  // the block that finishes the sequence finds them there.
+  if (c == 0 && i == 0 && seq_ok) {
+    const char *lines[4] = {reinterpret_cast<const char *>(tokens + (size_t)b * N_max),
+                            reinterpret_cast<const char *>(parent + (size_t)b * N_max),
+                            reinterpret_cast<const char *>(depth + (size_t)b * N_max),
+                            reinterpret_cast<const char *>(mask + (size_t)b * N_max * W)};
+    const int bytes[4] = {N_max * 4, N_max * 4, N_max * 4, N_max * W * 4};
+    for (int a = 0; a < 4; ++a)
+      for (int off = t * 128; off < bytes[a]; off += kThreads * 128) prefetch_l2(lines[a] + off);
+    const char *ab = reinterpret_cast<const char *>(anc + (size_t)b * (N_max + 1) * (D_max + 1));
+    for (int off = t * 128; off < (N_max + 1) * (D_max + 1) * 4; off += kThreads * 128)
+      prefetch_l2(ab + off);
+  }
+
   // ---- phase 1: argmax of one chunk of row (b, i) ----
   if (seq_ok && i < nb) {
     float bv = -INFINITY;
@@ -70,29 +91,27 @@ verify_greedy_kernel(const float *__restrict__ logits, const int32_t *__restrict
     const int lo = c * chunk;
     const int hi = min(V, lo + chunk);
     if (vec_ok) {
+      // passes of kBatch independent 16-byte loads per thread
       const float4 *r4 = reinterpret_cast<const float4 *>(row + lo);
       const int n4 = (hi - lo) >> 2;
-      int k = t;
-      for (; k + (kUnroll - 1) * kThreads < n4; k += kUnroll * kThreads) {
-        float4 a[kUnroll];
+      for (int k0 = 0; k0 < n4; k0 += kBatch * kThreads) {
+        float4 a[kBatch];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) a[u] = ld_stream(r4 + k + u * kThreads);
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-          const int x = lo + 4 * (k + u * kThreads);
-          if (better(a[u].x, x, bv, bi)) { bv = a[u].x; bi = x; }
-          if (better(a[u].y, x + 1, bv, bi)) { bv = a[u].y; bi = x + 1; }
-          if (better(a[u].z, x + 2, bv, bi)) { bv = a[u].z; bi = x + 2; }
-          if (better(a[u].w, x + 3, bv, bi)) { bv = a[u].w; bi = x + 3; }
+        for (int u = 0; u < kBatch; ++u) {
+          const int k = k0 + u * kThreads + t;
+          a[u] = k < n4 ? ld_stream(r4 + k) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
         }
-      }
-      for (; k < n4; k += kThreads) {
-        const float4 a = ld_stream(r4 + k);
-        const int x = lo + 4 * k;
-        if (better(a.x, x, bv, bi)) { bv = a.x; bi = x; }
-        if (better(a.y, x + 1, bv, bi)) { bv = a.y; bi = x + 1; }
-        if (better(a.z, x + 2, bv, bi)) { bv = a.z; bi = x + 2; }
-        if (better(a.w, x + 3, bv, bi)) { bv = a.w; bi = x + 3; }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int k = k0 + u * kThreads + t;
+          if (k < n4) {
+            const int x = lo + 4 * k;
+            if (better(a[u].x, x, bv, bi)) { bv = a[u].x; bi = x; }
+            if (better(a[u].y, x + 1, bv, bi)) { bv = a[u].y; bi = x + 1; }
+            if (better(a[u].z, x + 2, bv, bi)) { bv = a[u].z; bi = x + 2; }
+            if (better(a[u].w, x + 3, bv, bi)) { bv = a[u].w; bi = x + 3; }
+          }
+        }
       }
       for (int x = lo + 4 * n4 + t; x < hi; x += kThreads) {
         const float v = __ldcs(row + x);
@@ -139,6 +158,17 @@ verify_greedy_kernel(const float *__restrict__ logits, const int32_t *__restrict
   __shared__ int s_key[kThreads / 32];
 
   const int cols = D_max + 1;
+  // independent loads first, so their latencies overlap
+  int my_parent = 0, my_token = 0, my_depth = 0;
+  uint32_t my_mask[kMaxNodes / 32];
+  if (seq_ok && t < nb) {
+    my_parent = parent[(size_t)b * N_max + t];
+    my_token = tokens[(size_t)b * N_max + t];
+    my_depth = depth[(size_t)b * N_max + t];
+#pragma unroll
+    for (int w = 0; w < kMaxNodes / 32; ++w)
+      my_mask[w] = w < W ? mask[((size_t)b * N_max + t) * W + w] : 0u;
+  }
   int am = -1;
   if (seq_ok && t < nb) {
     float bv = -INFINITY;
@@ -158,12 +188,7 @@ verify_greedy_kernel(const float *__restrict__ logits, const int32_t *__restrict
   // matched(i): root, or token equals the target's choice at the parent
   bool match = false;
   if (seq_ok && t < nb) {
-    if (t == 0) {
-      match = true;
-    } else {
-      const int p = parent[(size_t)b * N_max + t];
-      match = tokens[(size_t)b * N_max + t] == s_am[p];
-    }
+    match = t == 0 || my_token == s_am[my_parent];
   }
   const unsigned ballot = __ballot_sync(0xffffffffu, match);
   if (lane == 0 && warp < kMaxNodes / 32) s_match[warp] = ballot;
@@ -172,10 +197,11 @@ verify_greedy_kernel(const float *__restrict__ logits, const int32_t *__restrict
   // accepted(i): every node on the ancestor path (bitmask row) matched
   int key = -1;
   if (seq_ok && t < nb) {
-    const uint32_t *mrow = mask + ((size_t)b * N_max + t) * W;
     bool acc = true;
-    for (int w = 0; w < W; ++w) acc = acc && ((mrow[w] & ~s_match[w]) == 0u);
-    if (acc) key = (depth[(size_t)b * N_max + t] << 16) | (0xFFFF - t);
+#pragma unroll
+    for (int w = 0; w < kMaxNodes / 32; ++w)
+      acc = acc && (w >= W || (my_mask[w] & ~s_match[w]) == 0u);
+    if (acc) key = (my_depth << 16) | (0xFFFF - t);
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) key = max(key, __shfl_xor_sync(0xffffffffu, key, off));
@@ -220,15 +246,13 @@ struct VerifyPlan {
 VerifyPlan plan_verify(int B, int N_max, int V) {
   VerifyPlan p;
   const long rows = (long)B * N_max;
-  const long target = 4L * sm_count();
-  long per_row = (target + rows - 1) / rows;
-  if (per_row < 1) per_row = 1;
-  const long max_per_row = (V + 2047) / 2048;
-  if (per_row > max_per_row) per_row = max_per_row;
-  if (per_row < 1) per_row = 1;
-  long chunk = (V + per_row - 1) / per_row;
-  chunk = (chunk + 3) / 4 * 4;
-  if (chunk < 4) chunk = 4;
+  const long total = rows * (long)V;
+  const long resident = 4L * sm_count();  // blocks of 256 threads resident at once
+  const long per_pass = (long)kBatch * kThreads * 4;
+  long chunk = (total + resident - 1) / resident;
+  chunk = (chunk + per_pass - 1) / per_pass * per_pass;  // whole passes
+  if (chunk < per_pass) chunk = per_pass;
+  if (chunk > V) chunk = (V + 3) / 4 * 4;
   p.chunk = (int)chunk;
   p.C = (int)((V + chunk - 1) / chunk);
   p.counter_bytes = align_up(sizeof(unsigned) * (size_t)B, 256);
@@ -266,11 +290,11 @@ TSD_API int tsd_tree_verify_greedy(const float *logits, const int32_t *tokens,
   Partial *part = reinterpret_cast<Partial *>(static_cast<char *>(workspace) + p.counter_bytes);
   const int W = (N_max + 31) / 32;
   const int vec_ok = (V % 4 == 0) && aligned(logits, 16);
-  dim3 grid(p.C, N_max, B);
-  verify_greedy_kernel<<<grid, kThreads, 0, as_cuda(stream)>>>(
-      logits, tokens, parent, anc, depth, mask, n_nodes, err, N_max, V, D_max, W, p.chunk, p.C,
-      vec_ok, argmax, accept_len, leaf, path, bonus, part, counter);
-  return launch_status();
+  if (launch(verify_greedy_kernel, dim3(p.C, N_max, B), dim3(kThreads), 0, as_cuda(stream), logits,
+             tokens, parent, anc, depth, mask, n_nodes, err, N_max, V, D_max, W, p.chunk, p.C,
+             vec_ok, argmax, accept_len, leaf, path, bonus, part, counter) != cudaSuccess)
+    return TSD_ERR_CUDA;
+  return TSD_OK;
 }
 
 // ---------------------------------------------------------------------------
@@ -341,9 +365,9 @@ TSD_API int tsd_tree_verify_greedy_static(const float *logits, const int32_t *to
   Partial *part = reinterpret_cast<Partial *>(static_cast<char *>(scratch) + p.counter_bytes);
   const int W = (N_max + 31) / 32;
   const int vec_ok = (V % 4 == 0) && aligned(logits, 16);
-  dim3 grid(p.C, N_max, B);
-  verify_greedy_kernel<<<grid, kThreads, 0, as_cuda(stream)>>>(
-      logits, tokens, parent, anc, depth, mask, n_nodes, err, N_max, V, D_max, W, p.chunk, p.C,
-      vec_ok, argmax, accept_len, leaf, path, bonus, part, counter);
-  return launch_status();
+  if (launch(verify_greedy_kernel, dim3(p.C, N_max, B), dim3(kThreads), 0, as_cuda(stream), logits,
+             tokens, parent, anc, depth, mask, n_nodes, err, N_max, V, D_max, W, p.chunk, p.C,
+             vec_ok, argmax, accept_len, leaf, path, bonus, part, counter) != cudaSuccess)
+    return TSD_ERR_CUDA;
+  return TSD_OK;
 }
