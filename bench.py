@@ -10,7 +10,9 @@ commit (a4) for the whole batch of one layer, back to back on one stream
 
 Prints ONE JSON line (rank 0).  Inputs are synthetic (seeded, the shapes of
 the named workload) and resident in HBM before timing; L2 is flushed between
-timed steps by writing a 256 MiB buffer outside the timed events.  Under
+timed steps (a 256 MiB write, then a 256 MiB read of another buffer, so the
+step starts cold with no dirty lines to write back), outside the timed
+events.  Under
 torchrun every rank runs its own replica (sequences are independent units;
 no data-path collective): value = all ranks' steps / max-over-ranks time.
 """
@@ -223,6 +225,27 @@ def cpu_baseline(name, budget_steps=3):
 
 
 # ---------------------------------------------------------------------------
+# multi-rank aggregation (replicas: every rank runs the whole workload)
+# ---------------------------------------------------------------------------
+
+def max_over_ranks(value: float, world: int, device="cpu") -> float:
+    """The slowest rank's time: every rank contributes its own, rank 0 reports
+    the max (the job is done when the last replica is)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(ms_per_step_max: float, world: int) -> float:
+    """Steps per second of the whole job: all ranks' steps over the max time."""
+    return world * 1000.0 / ms_per_step_max
+
+
+# ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
 
@@ -290,6 +313,14 @@ def gpu_arm(args, rank, world):
     moved = torch.empty((B,), **i32)
     status = torch.zeros((1,), **i32)
     flush = torch.empty((FLUSH_BYTES,), dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones((FLUSH_BYTES // 8,), dtype=torch.int64, device=dev)
+
+    def flush_l2():
+        # write one buffer larger than L2, then read another: the timed step
+        # starts with a cold L2 holding clean lines, so no write-back of the
+        # flush's dirty lines is charged to the kernels
+        flush.zero_()
+        flush_rd.sum()
 
     names = (["best_first_tree_build"] if bastion else []) + [
         "tree_build_ancestors", "tree_attn_fwd", "tree_verify_greedy", "kv_commit_path"]
@@ -316,7 +347,7 @@ def gpu_arm(args, rank, world):
             calls[n]()
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2()
         step()
     torch.cuda.synchronize()
     moved_total = int(moved.sum().item())
@@ -348,7 +379,7 @@ def gpu_arm(args, rank, world):
     torch.cuda.synchronize()
     t_wall0 = time.perf_counter()
     for s in range(args.steps):
-        flush.zero_()
+        flush_l2()
         ev[s][0].record(stream)
         g_step.replay()
         ev[s][1].record(stream)
@@ -356,18 +387,14 @@ def gpu_arm(args, rank, world):
     t_wall = time.perf_counter() - t_wall0
     if world > 1:
         dist.barrier()
-    ms_per_step = sum(a.elapsed_time(b) for a, b in ev) / args.steps
-    if world > 1:
-        t = torch.tensor([ms_per_step], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_per_step = float(t.item())
+    ms_per_step = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev) / args.steps, world, dev)
 
     # ---- timed region 2: per entry point (roofline of the dominant kernel) ----
     nev = len(names) + 1
     kev = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
     torch.cuda.synchronize()
     for s in range(args.steps):
-        flush.zero_()
+        flush_l2()
         kev[s][0].record(stream)
         for j, n in enumerate(names):
             g_one[n].replay()
@@ -394,7 +421,7 @@ def gpu_arm(args, rank, world):
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(e2e_steps)]
     for s in range(e2e_steps + 3):
-        flush.zero_()
+        flush_l2()
         if s >= 3:
             e2e_ev[s - 3][0].record(stream)
         for k, v in h_in.items():
@@ -405,11 +432,7 @@ def gpu_arm(args, rank, world):
         if s >= 3:
             e2e_ev[s - 3][1].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev) / e2e_steps, world, dev)
     clocks = sampler.stop() if sampler else None
 
     if rank != 0:
@@ -430,7 +453,7 @@ def gpu_arm(args, rank, world):
     launches = launches_per_step * args.steps
     result = {
         "metric": METRIC,
-        "value": round(world * 1000.0 / ms_per_step, 2),
+        "value": round(whole_job_rate(ms_per_step, world), 2),
         "unit": "steps/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -443,7 +466,8 @@ def gpu_arm(args, rank, world):
         "data": "synthetic (seeded; shapes and distributions of the named workload)",
         "config": {"workload": desc, "name": args.workload, "global_batch": B * world,
                    "seq_len": max_slots, "parallelism": "replicas (dp%d)" % world,
-                   "l2": "flushed between timed steps (256 MiB write outside the timed events)",
+                   "l2": "flushed between timed steps: 256 MiB write then 256 MiB read of another "
+                         "buffer, outside the timed events (cold, clean L2)",
                    "timing": "CUDA events on the launching stream around CUDA-graph replays of "
                              "the whole step (value) and of each entry point (kernels)",
                    "attention_kernel": "tcgen05" if args.attn_kernel == "tc" else "mma.sync"},
@@ -453,7 +477,7 @@ def gpu_arm(args, rank, world):
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": ncu_traffic(dom, args.workload), "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": abytes[dom]},
-        "e2e": {"value": round(1000.0 * world / e2e_ms, 2), "unit": "steps/s",
+        "e2e": {"value": round(whole_job_rate(e2e_ms, world), 2), "unit": "steps/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4)},
         "gpu_launches": launches,
@@ -469,7 +493,7 @@ def gpu_arm(args, rank, world):
     return result
 
 
-def main():
+def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10000)
@@ -479,7 +503,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--attn-kernel", default="tc", choices=["tc", "mma"],
                     help="tree attention kernel: tcgen05 (default) or the mma.sync one")
-    args = ap.parse_args()
+    args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
