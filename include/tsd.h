@@ -98,11 +98,16 @@ const char *tsd_version(void);
  *                          satisfied run out.
  *   TSD_OPT_ATTN_KERNEL    0: tcgen05/TMA tree attention (default);
  *                          1: the mma.sync kernel kept for comparison.
+ *   TSD_OPT_TEST_STALL     1: the tcgen05 attention's MMA thread first waits
+ *                          on a barrier nothing ever signals, so that wait
+ *                          runs out after TSD_OPT_WAIT_LIMIT_NS and the
+ *                          timeout path runs (tests only; default 0).
  * Returns TSD_ERR_ARG for an unknown key or value.
  */
 #define TSD_OPT_WAIT_LIMIT_NS 0
 #define TSD_OPT_ATTN_KERNEL 1
-#define TSD_OPT_COUNT 2
+#define TSD_OPT_TEST_STALL 2
+#define TSD_OPT_COUNT 3
 int tsd_set_option(int key, int64_t value);
 int64_t tsd_get_option(int key);
 

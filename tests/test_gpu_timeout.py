@@ -1,8 +1,9 @@
 """Failure detection without a GPU fault: every wait inside the tree-attention
-kernel is bounded.  With the limit set to 0 each wait that is not already
-satisfied runs out; the kernel must report TSD_STATUS_TIMEOUT through its
-status word, drain what it issued, free its tensor memory and return, and the
-context must stay usable: the next call with the normal limit is correct."""
+kernel is bounded.  With the test stall on, the kernel's MMA thread first
+waits on a barrier that nothing signals; with a 1 ms limit that wait runs
+out, and the kernel must report TSD_STATUS_TIMEOUT through its status word,
+drain what it issued, free its tensor memory and return.  The context must
+stay usable: the next call with the normal settings is correct."""
 
 import numpy as np
 import pytest
@@ -27,7 +28,8 @@ def test_wait_limit_expiry_reports_timeout_and_recovers():
     anc, depth, mask, err = tsd.tree_build_ancestors(parent, n_nodes, inp.D_max)
     old = tsd.get_option(tsd.OPT_WAIT_LIMIT_NS)
     try:
-        tsd.set_option(tsd.OPT_WAIT_LIMIT_NS, 0)
+        tsd.set_option(tsd.OPT_WAIT_LIMIT_NS, 1_000_000)
+        tsd.set_option(tsd.OPT_TEST_STALL, 1)
         tsd.tree_attn_fwd(dev_tensor(inp.q, torch.bfloat16), dev_tensor(c.k, torch.bfloat16),
                           dev_tensor(c.v, torch.bfloat16), dev_tensor(c.block_table),
                           dev_tensor(inp.prefix_len), n_nodes, mask, err,
@@ -35,6 +37,7 @@ def test_wait_limit_expiry_reports_timeout_and_recovers():
         torch.cuda.synchronize()  # returns: no hang, no fault
         assert int(status.item()) & tsd.STATUS_TIMEOUT
     finally:
+        tsd.set_option(tsd.OPT_TEST_STALL, 0)
         tsd.set_option(tsd.OPT_WAIT_LIMIT_NS, old)
     # the context is healthy: the same inputs give the oracle's answer
     g = run_gpu(tsd, inp)

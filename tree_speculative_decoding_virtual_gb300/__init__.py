@@ -26,7 +26,7 @@ _ERR_NAMES = {TSD_ERR_ARG: "TSD_ERR_ARG", TSD_ERR_LIMIT: "TSD_ERR_LIMIT",
 
 TREE_RANGE, TREE_CYCLE, TREE_TOO_DEEP, TREE_CLOSURE, TREE_ROOT, TREE_COUNT = 1, 2, 4, 8, 16, 32
 STATUS_BAD_PAGE, STATUS_BAD_LEN, STATUS_BAD_PATH, STATUS_TIMEOUT = 1, 2, 4, 8
-OPT_WAIT_LIMIT_NS, OPT_ATTN_KERNEL = 0, 1
+OPT_WAIT_LIMIT_NS, OPT_ATTN_KERNEL, OPT_TEST_STALL = 0, 1, 2
 
 # C signatures: (name, restype, argtypes)
 _P, _I, _I64, _SZ, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
@@ -288,7 +288,7 @@ def best_first_tree_build(q, root_token, N, parent=None, tokens=None, depth=None
 
 
 def set_option(key: int, value: int) -> None:
-    """Process-wide library option (OPT_WAIT_LIMIT_NS, OPT_ATTN_KERNEL)."""
+    """Process-wide library option (OPT_WAIT_LIMIT_NS, OPT_ATTN_KERNEL, OPT_TEST_STALL)."""
     _check(lib.tsd_set_option(key, value), "set_option")
 
 

@@ -24,6 +24,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <cmath>
 
@@ -51,12 +52,14 @@ struct AttnParams {
   int N_max, Hq, Hkv, g, W, max_slots;
   float scale_log2;
   int chunk, splits, row_tiles, rows_pad;
-  float *part_o;    // [B*Hkv][splits][rows_pad][D]
-  float2 *part_ml;  // [B*Hkv][splits][rows_pad]  (max in log2 units, sum)
+  uint16_t *part_o;  // [B*Hkv][splits][rows_pad][D] fp16: the split's O / (l * c)
+  float4 *part_ml;   // [B*Hkv][splits][rows_pad]  (max in log2 units, sum l, scale c, 0)
   uint16_t *out;
   float *lse;
   int32_t *status;
   uint64_t wait_limit_ns;
+  int test_stall;  // wait on a barrier nothing signals (exercises the timeout path)
+  int swizzled;    // partial rows hold 16-byte chunk k at position k ^ (row % (D/8))
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -95,6 +98,18 @@ __device__ __forceinline__ void mma_bf16(float *c, const uint32_t *a, uint32_t b
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&h);
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+// Power of two c with |x| / c < 1 for every |x| <= amax (1 when amax is 0).
+// Split partials are stored as fp16 values of O / (l c): always in range, with
+// an 11-bit significand, whatever the magnitude of V.
+__device__ __forceinline__ float pow2_above(float amax) {
+  if (!(amax > 0.f) || !isfinite(amax)) return 1.f;
+  const int e = ((__float_as_uint(amax) >> 23) & 0xFF) - 127 + 1;  // 2^e > amax
+  return __uint_as_float((uint32_t)(min(max(e, -126), 127) + 127) << 23);
 }
 
 // byte offset of 16-byte chunk `ch` of row `row` in a swizzled [rows][D] bf16 tile
@@ -332,77 +347,101 @@ tree_attn_split_kernel(const AttnParams p) {
     l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
   }
   const size_t base = ((size_t)z * p.splits + split) * p.rows_pad + rt * kBM;
-  float *po = p.part_o + base * D;
+  uint16_t *po = p.part_o + base * D;
   const int ca = 2 * (lane & 3);
+  float inv_a = l_run[0] > 0.f ? 1.f / l_run[0] : 0.f;
+  float inv_b = l_run[1] > 0.f ? 1.f / l_run[1] : 0.f;
+  float amax_a = 0.f, amax_b = 0.f;
 #pragma unroll
   for (int dt = 0; dt < kDT; ++dt) {
-    *reinterpret_cast<float2 *>(po + (size_t)ra_local * D + dt * 8 + ca) =
-        make_float2(o[dt][0], o[dt][1]);
-    *reinterpret_cast<float2 *>(po + (size_t)(ra_local + 8) * D + dt * 8 + ca) =
-        make_float2(o[dt][2], o[dt][3]);
+    amax_a = fmaxf(amax_a, fmaxf(fabsf(o[dt][0]), fabsf(o[dt][1])));
+    amax_b = fmaxf(amax_b, fmaxf(fabsf(o[dt][2]), fabsf(o[dt][3])));
+  }
+#pragma unroll
+  for (int off = 1; off <= 2; off <<= 1) {  // the four threads holding a row
+    amax_a = fmaxf(amax_a, __shfl_xor_sync(0xffffffffu, amax_a, off));
+    amax_b = fmaxf(amax_b, __shfl_xor_sync(0xffffffffu, amax_b, off));
+  }
+  const float c_a = pow2_above(amax_a * inv_a), c_b = pow2_above(amax_b * inv_b);
+  inv_a /= c_a;
+  inv_b /= c_b;
+#pragma unroll
+  for (int dt = 0; dt < kDT; ++dt) {
+    *reinterpret_cast<uint32_t *>(po + (size_t)ra_local * D + dt * 8 + ca) =
+        pack_f16(o[dt][0] * inv_a, o[dt][1] * inv_a);
+    *reinterpret_cast<uint32_t *>(po + (size_t)(ra_local + 8) * D + dt * 8 + ca) =
+        pack_f16(o[dt][2] * inv_b, o[dt][3] * inv_b);
   }
   if ((lane & 3) == 0) {
-    p.part_ml[base + ra_local] = make_float2(m_run[0], l_run[0]);
-    p.part_ml[base + ra_local + 8] = make_float2(m_run[1], l_run[1]);
+    p.part_ml[base + ra_local] = make_float4(m_run[0], l_run[0], c_a, 0.f);
+    p.part_ml[base + ra_local + 8] = make_float4(m_run[1], l_run[1], c_b, 0.f);
   }
 }
 
 
 // ===========================================================================
-// tcgen05 path.  One block = 128 query rows x one split of the key range of
-// one (sequence, kv head), walked in 64-key tiles.
-//   warp 0:    reads the split's block ids, then lane 0 loads K tiles and lane
-//              1 loads V tiles with TMA (4-stage rings; a K stage is refilled
-//              as soon as the Q K^T that read it completes, a V stage after P V)
-//   warp 1:    owns 256 TMEM columns; lane 0 issues every MMA
-//   warps 2-5: softmax, one TMEM lane (= one query row) per thread
-// Per tile j:
-//   S_j = Q K_j^T  (M=128, N=64, K=D; A and B K-major)  -> TMEM, 2 buffers
-//   P_j = exp2(S_j * scale * log2e - m) as bf16          -> smem, 2 buffers
-//   O  += P_j V_j  (M=128, N=D, K=64; V read MN-major)   -> TMEM
-// S_{j+1} is issued before P_j V_j, so the tensor core works while the
+// tcgen05 path.  One block = up to 256 query rows (two 128-row tiles, A and
+// B) x one split of the key range of one (sequence, kv head), walked in
+// 64-key tiles.  Both row tiles consume every K/V tile, so each K/V byte
+// brought to the SM feeds 256 rows (the GQA group of up to 256/g nodes).
+//   warp 0:    reads the split's block ids; lane 0 then loads K tiles and
+//              lane 1 V tiles with TMA into 3-stage rings (a K stage is
+//              refilled once both Q K^T that read it completed, a V stage
+//              once both P V did)
+//   warp 1:    owns 512 TMEM columns; lane 0 issues every MMA
+//   warps 2-5: softmax of row tile A, warps 6-9: of row tile B; one TMEM lane
+//              (= one query row) per thread
+// Per 64-key tile j and row tile t:
+//   S_tj = Q_t K_j^T  (M=128, N=64, K=D; A and B K-major) -> TMEM, 2 buffers
+//   P_tj = exp2(S_tj * scale * log2e - m) as bf16         -> shared memory
+//   O_t += P_tj V_j   (M=128, N=D, K=64; V read MN-major)  -> TMEM
+// S_{t,j+1} is issued before P_tj V_j, so the tensor core works while the
 // softmax of tile j runs.  The running max is raised lazily: O and the row
 // sum are rescaled (in TMEM) only when a tile's max exceeds the one in use by
 // more than 2^8, so P never exceeds 256 and the result is the same softmax.
 // K and V tiles are read straight from the paged cache by TMA (4-D view
 // [block][kv head][slot][D], 128-byte swizzle): when the four 16-slot blocks
 // of a 64-key tile are consecutive one box fetches them, otherwise one box
-// per block.  Measured on GB300 this beat a cp.async gather of the same tiles.
+// per block.  The epilogue writes O / l rounded to bf16, staged in shared
+// memory and stored with one bulk copy, plus the row's (max, sum).
 // Every wait is bounded; on expiry the block flags TSD_STATUS_TIMEOUT, drains
 // what it issued, frees its tensor memory and returns.
 // ===========================================================================
 
-constexpr int kTcThreads = 192;
-constexpr int kTcBM = 128;
-constexpr int kTcBN = 64;
-constexpr int kTcStages = 4;
-constexpr uint32_t kTmemCols = 256;
+constexpr int kTcThreads = 320;
+constexpr int kTcBM = 128;          // rows of one row tile (one MMA M)
+constexpr int kTcRows = 256;        // rows of one block (two row tiles)
+constexpr int kTcBN = 64;           // keys per tile
+constexpr int kTcStages = 3;
+constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kDrainLimitNs = 100000000ull;  // 100 ms
+constexpr int kTcMaxPages = 512;    // block ids of one split held in shared memory
 
 template <int D>
 struct TcLayout {
-  static constexpr int kHalves = D / 64;                  // 128-byte column blocks of a row
-  static constexpr uint32_t kQHalf = kTcBM * 128;         // one column block of Q (128 rows)
-  static constexpr uint32_t kKVHalf = kTcBN * 128;        // one column block of a K/V tile
-  static constexpr uint32_t kTile = kTcBN * D * 2;        // one K or V tile
-  static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kK = kTcBM * D * 2;
+  static constexpr int kHalves = D / 64;                   // 128-byte column blocks of a row
+  static constexpr uint32_t kQHalf = kTcBM * 128;          // one column block of a Q row tile
+  static constexpr uint32_t kQTile = kTcBM * D * 2;        // one Q row tile
+  static constexpr uint32_t kKVHalf = kTcBN * 128;         // one column block of a K/V tile
+  static constexpr uint32_t kTile = kTcBN * D * 2;         // one K or V tile
+  static constexpr uint32_t kQ = 0;                        // Q_A, Q_B
+  static constexpr uint32_t kK = 2 * kQTile;
   static constexpr uint32_t kV = kK + kTcStages * kTile;
-  static constexpr uint32_t kP = kV + kTcStages * kTile;
-  static constexpr uint32_t kPBytes = kTcBM * kTcBN * 2;  // 128 rows x 64 keys bf16
+  static constexpr uint32_t kP = kV + kTcStages * kTile;   // P_A, P_B
+  static constexpr uint32_t kPBytes = kTcBM * kTcBN * 2;   // 128 rows x 64 keys bf16
   static constexpr uint32_t kBytes = kP + 2 * kPBytes;
-  static constexpr uint32_t kAlloc = kBytes + 1024;       // + alignment slack
-  static constexpr uint32_t kTmemS = 0;                   // two 64-column S buffers
-  static constexpr uint32_t kTmemO = 128;                 // D columns of O
+  static constexpr uint32_t kAlloc = kBytes + 1024;        // + alignment slack
+  static constexpr uint32_t kStaging = kK;                 // epilogue reuses the K/V rings
+  static_assert(2 * kTcStages * kTile >= kTcRows * D * 2, "epilogue staging fits the rings");
+  static constexpr uint32_t kTmemS = 0;                    // [row tile][2 buffers] x 64 columns
+  static constexpr uint32_t kTmemO = 256;                  // [row tile] x 128 columns
 };
 
-constexpr int kTcMaxPages = 2048;  // block ids of one split held in shared memory
-
 struct TcShared {
-  int32_t rows[kTcMaxPages];  // tensor-map row of each block of the split (y coordinate)
+  int32_t pages[kTcMaxPages];  // block ids of the split
   uint64_t k_full[kTcStages], k_empty[kTcStages], v_full[kTcStages], v_empty[kTcStages];
-  uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
-  uint64_t q_full, drain;
+  uint64_t s_full[2][2], s_free[2][2], p_full[2], p_free[2];
+  uint64_t q_full[2], drain, never;
   uint32_t tmem_base;
   int abort;
 };
@@ -440,6 +479,50 @@ __device__ __forceinline__ uint32_t visible_bits(const uint32_t *mrow, int W, in
   return bits;
 }
 
+// Before the previous kernel on the stream has finished (programmatic launch),
+// start pulling this block's inputs into L2: its Q rows, and the K/V of the
+// first blocks of its split.  Only lines are prefetched (through the load/
+// store unit: queuing prefetch boxes on the TMA unit delayed the real tile
+// loads behind them); nothing read here is used, so inputs the previous
+// kernel is still writing are harmless (L2 is the point of coherence for
+// their later writes).
+constexpr int kPrefetchPages = 16;  // 4 tiles of 64 keys
+
+template <int D>
+__device__ __forceinline__ void attn_prefetch(const AttnParams &p, const CUtensorMap *mk,
+                                              const CUtensorMap *mv, int b, int hkv, int rt,
+                                              int split, int warp, int lane) {
+  using namespace sm100;
+  const int P = p.prefix_len[b];
+  const int nb = p.n_nodes ? p.n_nodes[b] : p.N_max;
+  if (P < 0 || nb < 1 || nb > p.N_max || (long)P + nb > (long)p.max_slots ||
+      (long)P + nb > (long)p.max_blocks * kPage)
+    return;
+  const int k_begin = split * p.chunk;
+  if (k_begin >= P + nb) return;
+  if (warp < 2) {
+    // warp 0 prefetches K, warp 1 V: one 16-slot block of one head is 16*D*2
+    // contiguous bytes; lane l covers lines l, l+32, ... of each block
+    const uint16_t *cache = warp == 0 ? p.k : p.v;
+    const int pg_first = k_begin / kPage;
+    const int pg_last = min((min(P + nb, k_begin + p.chunk) - 1) / kPage, pg_first + kPrefetchPages - 1);
+    for (int i = pg_first; i <= pg_last; ++i) {
+      const int page = p.table[(size_t)b * p.max_blocks + i];
+      if (page < 0 || page >= p.num_blocks) continue;
+      const char *blk =
+          reinterpret_cast<const char *>(cache + ((size_t)page * p.Hkv + hkv) * kPage * D);
+      for (int off = lane * 128; off < kPage * D * 2; off += 32 * 128) prefetch_l2(blk + off);
+    }
+  } else if (warp >= 2) {
+    const int row = rt * kTcRows + ((warp - 2) >> 2) * kTcBM + (warp & 3) * 32 + lane;
+    if (row < nb * p.g) {
+      const char *q = reinterpret_cast<const char *>(
+          p.q + (((size_t)b * p.N_max + row / p.g) * p.Hq + hkv * p.g + row % p.g) * D);
+      for (int off = 0; off < D * 2; off += 128) prefetch_l2(q + off);
+    }
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k1,
@@ -451,6 +534,8 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
   __shared__ TcShared sh;
 
   pdl_trigger();
+  attn_prefetch<D>(p, &map_k1, &map_v1, blockIdx.z / p.Hkv, blockIdx.z % p.Hkv, blockIdx.x,
+                   blockIdx.y, threadIdx.x >> 5, threadIdx.x & 31);
   pdl_wait();
   const int rt = blockIdx.x;
   const int split = blockIdx.y;
@@ -473,7 +558,8 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
   const int rows_valid = nb * p.g;
   const int seq_len = P + nb;
   const int k_begin = split * p.chunk;
-  if (rt * kTcBM >= rows_valid || k_begin >= seq_len) return;
+  if (rt * kTcRows >= rows_valid || k_begin >= seq_len) return;
+  const int ntile_rows = rt * kTcRows + kTcBM < rows_valid ? 2 : 1;  // row tiles with valid rows
   const int k_end = min(seq_len, k_begin + p.chunk);
   const int ntiles = (k_end - k_begin + kTcBN - 1) / kTcBN;
 
@@ -490,14 +576,17 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
       mbar_init(smem_addr(&sh.v_full[i]), 1);
       mbar_init(smem_addr(&sh.v_empty[i]), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_addr(&sh.s_full[i]), 1);
-      mbar_init(smem_addr(&sh.s_free[i]), 4);
-      mbar_init(smem_addr(&sh.p_full[i]), 4);
-      mbar_init(smem_addr(&sh.p_free[i]), 1);
+    for (int t = 0; t < 2; ++t) {
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(smem_addr(&sh.s_full[t][i]), 1);
+        mbar_init(smem_addr(&sh.s_free[t][i]), 4);
+      }
+      mbar_init(smem_addr(&sh.p_full[t]), 4);
+      mbar_init(smem_addr(&sh.p_free[t]), 1);
+      mbar_init(smem_addr(&sh.q_full[t]), 4);
     }
-    mbar_init(smem_addr(&sh.q_full), 4);
     mbar_init(smem_addr(&sh.drain), 1);
+    mbar_init(smem_addr(&sh.never), 1);
     sh.abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&map_k1);
@@ -513,7 +602,6 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
 
   if (warp == 0) {
     // --------------------------- loaders (TMA) ---------------------------
-    // every block id of the split is read once, by the whole warp, up front
     const int32_t *trow = p.table + (size_t)b * p.max_blocks;
     const int pg_first = k_begin / kPage;
     const int pg_last = (k_end - 1) / kPage;
@@ -525,7 +613,7 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
         bad = true;
         page = 0;
       }
-      sh.rows[i] = page;
+      sh.pages[i] = page;
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0 && p.status) atomicOr(p.status, TSD_STATUS_BAD_PAGE);
     __syncwarp();
@@ -545,7 +633,7 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
         const int g0 = j * (kTcBN / kPage);
         int pg[kTcBN / kPage];
 #pragma unroll
-        for (int g = 0; g < kTcBN / kPage; ++g) pg[g] = sh.rows[min(g0 + g, npg - 1)];
+        for (int g = 0; g < kTcBN / kPage; ++g) pg[g] = sh.pages[min(g0 + g, npg - 1)];
         const bool run = pg[1] == pg[0] + 1 && pg[2] == pg[0] + 2 && pg[3] == pg[0] + 3;
         const uint32_t bar = smem_addr(&full[st]);
         mbar_arrive_expect_tx(bar, L::kTile);
@@ -568,45 +656,54 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
         if (last_issued[st] >= 0)
           mbar_wait(smem_addr(&full[st]), (last_issued[st] / kTcStages) & 1, kDrainLimitNs);
     }
+    __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------ MMA issuer ------------------------------ ------------------------------
+    // ------------------------------ MMA issuer ------------------------------
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(kTcBM, kTcBN, false, false);
       constexpr uint32_t idPV = idesc_bf16_f32(kTcBM, D, false, true);
       auto issue_s = [&](int j) -> bool {
         const int st = j % kTcStages, sb = j & 1;
         if (!tc_wait(sh.k_full[st], (j / kTcStages) & 1, lim, abort)) return false;
-        if (j >= 2 && !tc_wait(sh.s_free[sb], ((j >> 1) - 1) & 1, lim, abort)) return false;
-        tc_fence_after();
+        for (int t = 0; t < ntile_rows; ++t) {
+          if (j >= 2 && !tc_wait(sh.s_free[t][sb], ((j >> 1) - 1) & 1, lim, abort)) return false;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          umma_bf16(tmem + L::kTmemS + sb * kTcBN,
-                    smem_desc_sw128(base + L::kQ + (kk >> 2) * L::kQHalf + (kk & 3) * 32, 16, 1024),
-                    smem_desc_sw128(base + L::kK + st * L::kTile + (kk >> 2) * L::kKVHalf +
-                                        (kk & 3) * 32, 16, 1024),
-                    idS, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            umma_bf16(tmem + L::kTmemS + (t * 2 + sb) * kTcBN,
+                      smem_desc_sw128(base + L::kQ + t * L::kQTile + (kk >> 2) * L::kQHalf +
+                                          (kk & 3) * 32, 16, 1024),
+                      smem_desc_sw128(base + L::kK + st * L::kTile + (kk >> 2) * L::kKVHalf +
+                                          (kk & 3) * 32, 16, 1024),
+                      idS, kk > 0);
+          }
+          umma_commit(smem_addr(&sh.s_full[t][sb]));
         }
-        umma_commit(smem_addr(&sh.s_full[sb]));
         umma_commit(smem_addr(&sh.k_empty[st]));
         return true;
       };
       auto issue_pv = [&](int j) -> bool {
-        const int st = j % kTcStages, pb = j & 1;
-        if (!tc_wait(sh.p_full[pb], (j >> 1) & 1, lim, abort)) return false;
+        const int st = j % kTcStages;
         if (!tc_wait(sh.v_full[st], (j / kTcStages) & 1, lim, abort)) return false;
-        tc_fence_after();
+        for (int t = 0; t < ntile_rows; ++t) {
+          if (!tc_wait(sh.p_full[t], j & 1, lim, abort)) return false;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kTcBN / 16; ++kk) {
-          umma_bf16(tmem + L::kTmemO,
-                    smem_desc_sw128(base + L::kP + pb * L::kPBytes + kk * 32, 16, 1024),
-                    smem_desc_sw128(base + L::kV + st * L::kTile + kk * 16 * 128, L::kKVHalf, 1024),
-                    idPV, (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kTcBN / 16; ++kk) {
+            umma_bf16(tmem + L::kTmemO + t * 128,
+                      smem_desc_sw128(base + L::kP + t * L::kPBytes + kk * 32, 16, 1024),
+                      smem_desc_sw128(base + L::kV + st * L::kTile + kk * 16 * 128, L::kKVHalf, 1024),
+                      idPV, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(smem_addr(&sh.p_free[t]));
         }
-        umma_commit(smem_addr(&sh.p_free[pb]));
         umma_commit(smem_addr(&sh.v_empty[st]));
         return true;
       };
-      bool ok = tc_wait(sh.q_full, 0, lim, abort) && issue_s(0);
+      bool ok = !p.test_stall || tc_wait(sh.never, 0, lim, abort);
+      ok = ok && tc_wait(sh.q_full[0], 0, lim, abort);
+      ok = ok && (ntile_rows < 2 || tc_wait(sh.q_full[1], 0, lim, abort));
+      ok = ok && issue_s(0);
       for (int j = 0; ok && j < ntiles; ++j) {
         if (j + 1 < ntiles) ok = !*abort && issue_s(j + 1);
         if (ok) ok = issue_pv(j);
@@ -618,26 +715,18 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
     __syncwarp();
   } else {
     // ------------------------------ softmax ------------------------------
+    const int t = (warp - 2) >> 2;                    // row tile of this warp group
     const int quarter = warp & 3;                     // TMEM lanes 32*quarter .. +31
-    const int rl = quarter * 32 + lane;               // row within the tile
-    const int row = rt * kTcBM + rl;
+    const int rl = quarter * 32 + lane;               // row within the row tile
+    const int row = rt * kTcRows + t * kTcBM + rl;
+    const bool active = t < ntile_rows;
     const bool rvalid = row < rows_valid;
     const int node = rvalid ? row / p.g : 0;
     const int head = hkv * p.g + (rvalid ? row % p.g : 0);
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t *mrow = p.mask + ((size_t)b * p.N_max + node) * p.W;
-
-    // Q row -> shared memory, 128-byte swizzle
-    const uint4 *qsrc =
-        reinterpret_cast<const uint4 *>(p.q + (((size_t)b * p.N_max + node) * p.Hq + head) * D);
-#pragma unroll
-    for (int c = 0; c < D / 8; ++c) {
-      const uint4 v = rvalid ? __ldg(qsrc + c) : make_uint4(0u, 0u, 0u, 0u);
-      *reinterpret_cast<uint4 *>(gbase + L::kQ + (c >> 3) * L::kQHalf + sw128_offset(rl, c & 7)) = v;
-    }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&sh.q_full));
+    const uint32_t tS = tmem + L::kTmemS + t * 2 * kTcBN;
+    const uint32_t tO = tmem + L::kTmemO + t * 128;
 
     // waits are taken by every lane and their outcome made warp-uniform, so the
     // .sync.aligned TMEM accesses below are never reached by a partial warp
@@ -646,119 +735,170 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
       return __all_sync(0xffffffffu, got);
     };
     float m_use = -INFINITY, l_sum = 0.f;
-    bool ok = true;
-    for (int j = 0; j < ntiles; ++j) {
-      const int sb = j & 1;
-      if (!warp_wait(sh.s_full[sb], (j >> 1) & 1)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t r[2][32];
+    bool ok = active;
+    if (active) {
+      // Q rows -> shared memory (128-byte swizzle) with cp.async: every copy is
+      // in flight at once.  Each warp stages its 32 rows; one instruction
+      // covers 32 / (D/8) consecutive rows, so global reads are contiguous.
+      // Rows past the valid ones copy row 0 of the sequence (finite, unused).
+      const uint32_t qt = base + L::kQ + t * L::kQTile;
+      constexpr int kCh = D / 8;               // 16-byte chunks per row
+      constexpr int kRowsPer = 32 / kCh;       // rows per warp instruction
+      const int ch = lane % kCh;
 #pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) tmem_ld32(tmem + L::kTmemS + sb * kTcBN + lane_off + c2 * 32, r[c2]);
-      tmem_wait_ld();
-      tc_fence_before();
+      for (int i = 0; i < 32 / kRowsPer; ++i) {
+        const int r_in = quarter * 32 + i * kRowsPer + lane / kCh;  // row within the tile
+        const int grow = rt * kTcRows + t * kTcBM + r_in;
+        const int gr = grow < rows_valid ? grow : 0;
+        const uint16_t *src =
+            p.q + (((size_t)b * p.N_max + gr / p.g) * p.Hq + hkv * p.g + gr % p.g) * D + ch * 8;
+        cp_async_16(qt + (ch >> 3) * L::kQHalf + sw128_offset(r_in, ch & 7), src);
+      }
+      cp_async_wait_all();
+      fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&sh.s_free[sb]));
+      if (lane == 0) mbar_arrive(smem_addr(&sh.q_full[t]));
 
-      const int ts = k_begin + j * kTcBN;
-      const bool full = (ts + kTcBN <= P) && (ts + kTcBN <= k_end);
-      // masked scores become -inf; the max is taken on raw scores (scale > 0)
-      if (!full) {
-#pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          const uint32_t vis =
-              visible_bits(mrow, p.W, ts + c2 * 32 - P, k_end - (ts + c2 * 32), rvalid);
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (!((vis >> i) & 1u)) r[c2][i] = __float_as_uint(-INFINITY);
-        }
-      }
-      float mx[8];
-#pragma unroll
-      for (int a = 0; a < 8; ++a) mx[a] = __uint_as_float(r[0][a]);
-#pragma unroll
-      for (int i = 8; i < 64; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(r[i >> 5][i & 31]));
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * p.scale_log2;
-      const float m_new = fmaxf(m_use, mt);
-      const bool upd = m_new > m_use + 8.f;  // first visible key, or the max grew by > 2^8
-      const float alpha = upd ? exp2f(m_use - m_new) : 1.f;
-      if (j > 0 && __any_sync(0xffffffffu, upd)) {
-        // O holds tiles < j: wait for P_{j-1} V_{j-1}, rescale O in TMEM (whole warp)
-        if (!warp_wait(sh.p_free[(j - 1) & 1], ((j - 1) >> 1) & 1)) {
+      for (int j = 0; j < ntiles; ++j) {
+        const int sb = j & 1;
+        if (!warp_wait(sh.s_full[t][sb], (j >> 1) & 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        uint32_t r[2][32];
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tmem + L::kTmemO + lane_off + c * 32, o);
-          tmem_wait_ld();
+        for (int c2 = 0; c2 < 2; ++c2) tmem_ld32(tS + sb * kTcBN + lane_off + c2 * 32, r[c2]);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&sh.s_free[t][sb]));
+
+        const int ts = k_begin + j * kTcBN;
+        const bool full = (ts + kTcBN <= P) && (ts + kTcBN <= k_end);
+        // masked scores become -inf; the max is taken on raw scores (scale > 0)
+        if (!full) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(tmem + L::kTmemO + lane_off + c * 32, o);
-        }
-        tmem_wait_st();
-      }
-      if (upd) {
-        l_sum *= alpha;
-        m_use = m_new;
-      }
-      const float mb = m_use == -INFINITY ? 0.f : m_use;
-      // P_j must not overwrite buffer sb before P_{j-2} V_{j-2} has read it
-      if (j >= 2 && !warp_wait(sh.p_free[sb], ((j >> 1) - 1) & 1)) {
-        ok = false;
-        break;
-      }
-      float rsum[4] = {0.f, 0.f, 0.f, 0.f};
-      unsigned char *pbuf = gbase + L::kP + sb * L::kPBytes;
-      const float sc = p.scale_log2;
+          for (int c2 = 0; c2 < 2; ++c2) {
+            const uint32_t vis =
+                visible_bits(mrow, p.W, ts + c2 * 32 - P, k_end - (ts + c2 * 32), rvalid);
 #pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
-#pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8) {  // 8 keys = one 16-byte chunk
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float a = ex2_approx(fmaf(__uint_as_float(r[c2][q8 * 8 + 2 * e]), sc, -mb));
-            const float c = ex2_approx(fmaf(__uint_as_float(r[c2][q8 * 8 + 2 * e + 1]), sc, -mb));
-            rsum[e] += a + c;
-            w[e] = pack_bf16(a, c);
+            for (int i = 0; i < 32; ++i)
+              if (!((vis >> i) & 1u)) r[c2][i] = __float_as_uint(-INFINITY);
           }
-          *reinterpret_cast<uint4 *>(pbuf + sw128_offset(rl, c2 * 4 + q8)) =
-              make_uint4(w[0], w[1], w[2], w[3]);
         }
+        float mx[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) mx[a] = __uint_as_float(r[0][a]);
+#pragma unroll
+        for (int i = 8; i < 64; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(r[i >> 5][i & 31]));
+        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * p.scale_log2;
+        const float m_new = fmaxf(m_use, mt);
+        const bool upd = m_new > m_use + 8.f;  // first visible key, or the max grew by > 2^8
+        const float alpha = upd ? exp2f(m_use - m_new) : 1.f;
+        // P_{t,j-1} V_{j-1} must be complete before O is rescaled or P_t rewritten
+        if (j > 0 && !warp_wait(sh.p_free[t], (j - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        if (j > 0 && __any_sync(0xffffffffu, upd)) {
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + lane_off + c * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tO + lane_off + c * 32, o);
+          }
+          tmem_wait_st();
+        }
+        if (upd) {
+          l_sum *= alpha;
+          m_use = m_new;
+        }
+        const float mb = m_use == -INFINITY ? 0.f : m_use;
+        float rsum[4] = {0.f, 0.f, 0.f, 0.f};
+        unsigned char *pbuf = gbase + L::kP + t * L::kPBytes;
+        const float sc = p.scale_log2;
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+#pragma unroll
+          for (int q8 = 0; q8 < 4; ++q8) {  // 8 keys = one 16-byte chunk
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float a = ex2_approx(fmaf(__uint_as_float(r[c2][q8 * 8 + 2 * e]), sc, -mb));
+              const float c = ex2_approx(fmaf(__uint_as_float(r[c2][q8 * 8 + 2 * e + 1]), sc, -mb));
+              rsum[e] += a + c;
+              w[e] = pack_bf16(a, c);
+            }
+            *reinterpret_cast<uint4 *>(pbuf + sw128_offset(rl, c2 * 4 + q8)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        l_sum += (rsum[0] + rsum[1]) + (rsum[2] + rsum[3]);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&sh.p_full[t]));
       }
-      const float rs = (rsum[0] + rsum[1]) + (rsum[2] + rsum[3]);
-      l_sum += rs;
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&sh.p_full[sb]));
+      if (ok) ok = warp_wait(sh.p_free[t], (ntiles - 1) & 1);  // this row tile's last P V
     }
 
-    // ---- epilogue: unnormalised O, running max (log2 units) and row sum ----
-    if (ok && warp_wait(sh.p_free[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1)) {
+    // ---- epilogue: O / l in bf16 through shared memory, (max, sum) per row ----
+    // Both row tiles' MMAs must be complete before the K/V rings are reused.
+    const int nthr = ntile_rows * 128;
+    if (active) asm volatile("bar.sync 1, %0;\n" ::"r"(nthr) : "memory");
+    const bool all_ok = __all_sync(0xffffffffu, active && !*abort);
+    if (all_ok) {
       tc_fence_after();
-      const size_t prow = ((size_t)z * p.splits + split) * p.rows_pad + rt * kTcBM + rl;
-      float4 *po = reinterpret_cast<float4 *>(p.part_o + prow * D);
+      float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+      float amax = 0.f;  // pass 1: the row's largest |O|
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
-        tmem_ld32(tmem + L::kTmemO + lane_off + c * 32, o);
+        tmem_ld32(tO + lane_off + c * 32, o);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          po[c * 8 + i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
-                                      __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(__uint_as_float(o[i])));
       }
-      p.part_ml[prow] = make_float2(m_use, l_sum);
+      const float cs = pow2_above(amax * inv);
+      inv /= cs;
+      // staged row-major, 16-byte chunk k of a row at position k ^ (row % (D/8)),
+      // so the 32 rows a warp writes at once hit distinct banks
+      const int swz_mask = D / 8 - 1;
+      unsigned char *srow = gbase + L::kStaging + (size_t)(t * kTcBM + rl) * D * 2;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {  // pass 2: scale, round to fp16, stage
+        uint32_t o[32];
+        tmem_ld32(tO + lane_off + c * 32, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {
+          uint4 v;
+          v.x = pack_f16(__uint_as_float(o[q8 * 8 + 0]) * inv, __uint_as_float(o[q8 * 8 + 1]) * inv);
+          v.y = pack_f16(__uint_as_float(o[q8 * 8 + 2]) * inv, __uint_as_float(o[q8 * 8 + 3]) * inv);
+          v.z = pack_f16(__uint_as_float(o[q8 * 8 + 4]) * inv, __uint_as_float(o[q8 * 8 + 5]) * inv);
+          v.w = pack_f16(__uint_as_float(o[q8 * 8 + 6]) * inv, __uint_as_float(o[q8 * 8 + 7]) * inv);
+          *reinterpret_cast<uint4 *>(srow + (((c * 4 + q8) ^ (rl & swz_mask)) << 4)) = v;
+        }
+      }
+      const size_t prow = ((size_t)z * p.splits + split) * p.rows_pad + rt * kTcRows + t * kTcBM + rl;
+      p.part_ml[prow] = make_float4(m_use, l_sum, cs, 0.f);
+      fence_proxy_async_smem();
+    }
+    if (active) asm volatile("bar.sync 1, %0;\n" ::"r"(nthr) : "memory");
+    if (all_ok && warp == 2 && lane == 0) {
+      const size_t row0 = ((size_t)z * p.splits + split) * p.rows_pad + rt * kTcRows;
+      bulk_store(p.part_o + row0 * D, base + L::kStaging, (uint32_t)(nthr * D * 2));
+      bulk_wait_read();
     }
   }
 
+  __syncwarp();  // role code above diverges inside warps; reconverge first
   tc_fence_before();
   __syncthreads();
   if (*abort && tid == 0 && p.status) atomicOr(p.status, TSD_STATUS_TIMEOUT);
@@ -799,13 +939,14 @@ __global__ void __launch_bounds__(256) tree_attn_combine_kernel(const AttnParams
   const int row = node * p.g + (hq % p.g);
   const size_t r0 = (size_t)(b * p.Hkv + hkv) * p.splits * p.rows_pad + row;
   const int ns = (P + nb + p.chunk - 1) / p.chunk;  // <= 32 (host check)
-  const float2 ml = lane < ns ? p.part_ml[r0 + (size_t)lane * p.rows_pad]
-                              : make_float2(-INFINITY, 0.f);
+  const float4 ml = lane < ns ? p.part_ml[r0 + (size_t)lane * p.rows_pad]
+                              : make_float4(-INFINITY, 0.f, 0.f, 0.f);
   float M = ml.x;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  const float w = lane < ns ? exp2f(ml.x - M) : 0.f;
-  float L = ml.y * w;
+  const float wl = lane < ns ? exp2f(ml.x - M) * ml.y : 0.f;  // weight of split `lane`
+  float L = wl;
+  const float w = wl * ml.z;  // the split's partial holds O / (l c)
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
   float acc[kPer];
@@ -818,13 +959,20 @@ __global__ void __launch_bounds__(256) tree_attn_combine_kernel(const AttnParams
     for (int u = 0; u < 8; ++u) {
       const int s = s0 + u;
       ws[u] = __shfl_sync(0xffffffffu, w, s & 31);
-      const float *src = p.part_o + (r0 + (size_t)min(s, ns - 1) * p.rows_pad) * D + lane * kPer;
+      const size_t prow = r0 + (size_t)min(s, ns - 1) * p.rows_pad;
+      const int col = p.swizzled ? ((((lane * kPer) >> 3) ^ (int)(prow & (D / 8 - 1))) << 3) +
+                                       ((lane * kPer) & 7)
+                                 : lane * kPer;
+      const uint16_t *src = p.part_o + prow * D + col;
       if (kPer == 4) {
-        const float4 t = __ldcg(reinterpret_cast<const float4 *>(src));
-        v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
+        const uint2 t = __ldcg(reinterpret_cast<const uint2 *>(src));
+        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&t.x));
+        const float2 c = __half22float2(*reinterpret_cast<const __half2 *>(&t.y));
+        v[u][0] = a.x; v[u][1] = a.y; v[u][2] = c.x; v[u][3] = c.y;
       } else {
-        const float2 t = __ldcg(reinterpret_cast<const float2 *>(src));
-        v[u][0] = t.x; v[u][1] = t.y;
+        const uint32_t t = __ldcg(reinterpret_cast<const unsigned int *>(src));
+        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&t));
+        v[u][0] = a.x; v[u][1] = a.y;
       }
       if (s >= ns) ws[u] = 0.f;
     }
@@ -853,7 +1001,7 @@ struct AttnPlan {
 AttnPlan plan_attn(int B, int N_max, int Hq, int Hkv, int D, int max_slots) {
   AttnPlan a;
   a.impl = (int)option(TSD_OPT_ATTN_KERNEL);
-  a.bm = a.impl == 0 ? kTcBM : kBM;
+  a.bm = a.impl == 0 ? kTcRows : kBM;
   a.bn = a.impl == 0 ? kTcBN : kBN;
   const int g = Hq / Hkv;
   a.row_tiles = (N_max * g + a.bm - 1) / a.bm;
@@ -884,13 +1032,14 @@ AttnPlan plan_attn(int B, int N_max, int Hq, int Hkv, int D, int max_slots) {
   long chunk = (max_slots + best_s - 1) / best_s;
   chunk = (chunk + a.bn - 1) / a.bn * a.bn;
   if (a.impl == 0 && chunk > (long)kTcMaxPages * kPage) chunk = (long)kTcMaxPages * kPage;
+  if (a.impl == 0 && chunk > 64L * kTcBN) chunk = 64L * kTcBN;  // at most 64 tiles per block
   while ((max_slots + chunk - 1) / chunk > 32) chunk += a.bn;
   a.chunk = (int)chunk;
   a.splits = (int)((max_slots + chunk - 1) / chunk);
   if (a.splits < 1) a.splits = 1;
   const size_t rows = (size_t)B * Hkv * a.splits * a.rows_pad;
-  a.o_bytes = align_up(rows * D * sizeof(float), 256);
-  a.ml_bytes = rows * sizeof(float2);
+  a.o_bytes = align_up(rows * D * sizeof(uint16_t), 256);
+  a.ml_bytes = rows * sizeof(float4);
   return a;
 }
 
@@ -1033,12 +1182,14 @@ TSD_API int tsd_tree_attn_fwd(const uint16_t *q, const uint16_t *k_cache, const 
   p.splits = a.splits;
   p.row_tiles = a.row_tiles;
   p.rows_pad = a.rows_pad;
-  p.part_o = static_cast<float *>(workspace);
-  p.part_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) + a.o_bytes);
+  p.part_o = static_cast<uint16_t *>(workspace);
+  p.part_ml = reinterpret_cast<float4 *>(static_cast<char *>(workspace) + a.o_bytes);
   p.out = out;
   p.lse = lse;
   p.status = status;
   p.wait_limit_ns = (uint64_t)option(TSD_OPT_WAIT_LIMIT_NS);
+  p.test_stall = (int)option(TSD_OPT_TEST_STALL);
+  p.swizzled = a.impl == 0 ? 1 : 0;
   return D == 128 ? launch_attn<128>(p, a, B, num_blocks, as_cuda(stream))
                   : launch_attn<64>(p, a, B, num_blocks, as_cuda(stream));
 }

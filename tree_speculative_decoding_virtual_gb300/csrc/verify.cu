@@ -52,13 +52,23 @@ verify_greedy_kernel(const float *__restrict__ logits, const int32_t *__restrict
                      int32_t *__restrict__ bonus, Partial *__restrict__ part,
                      unsigned *__restrict__ counter) {
   pdl_trigger();
-  pdl_wait();
   const int c = blockIdx.x;
   const int i = blockIdx.y;
   const int b = blockIdx.z;
   const int t = threadIdx.x;
   const int lane = t & 31;
   const int warp = t >> 5;
+  {
+    // while the previous kernel finishes, pull this block's logits chunk into
+    // L2 (lines only; nothing read here is used)
+    const int nb_hint = n_nodes ? n_nodes[b] : N_max;
+    if (i < nb_hint) {
+      const char *row = reinterpret_cast<const char *>(logits + ((size_t)b * N_max + i) * (size_t)V);
+      const long lo = (long)c * chunk * 4, hi = min((long)V, (long)(c + 1) * chunk) * 4;
+      for (long off = lo + (long)t * 128; off < hi; off += (long)kThreads * 128) prefetch_l2(row + off);
+    }
+  }
+  pdl_wait();
 
   const int nb = n_nodes ? n_nodes[b] : N_max;
   const int eb = err ? err[b] : 0;
