@@ -193,11 +193,13 @@ int tsd_tree_attn_fwd(const uint16_t *q, const uint16_t *k_cache, const uint16_t
  * argmax  int32 [B][N_max] out (-1 for padding rows and skipped sequences);
  * accept_len, leaf, bonus int32 [B] out; path int32 [B][D_max+1] out.
  * A sequence with err != 0: accept_len 0, leaf -1, bonus -1, path 0.
- * workspace  >= tsd_tree_verify_workspace_bytes() bytes, ZERO-FILLED before
+ * workspace  >= tsd_tree_verify_workspace_bytes() bytes (a ticket per
+ *            sequence and a 64-bit argmax key per row), ZERO-FILLED before
  *            its first use; every call leaves it zero-filled again.  Calls
  *            sharing one workspace must not overlap on the GPU.
- * One fused launch: a grid-wide argmax scan over V, and the block that
- * finishes a sequence's last chunk runs its acceptance search.
+ * One fused launch: each sequence's rows are streamed in equal ranges, one
+ * per block, and the block that retires a sequence's last range runs its
+ * acceptance search.
  */
 size_t tsd_tree_verify_workspace_bytes(int B, int N_max, int V);
 int tsd_tree_verify_greedy(const float *logits, const int32_t *tokens, const int32_t *parent,
@@ -218,11 +220,12 @@ int tsd_tree_verify_greedy(const float *logits, const int32_t *tokens, const int
  * tsd_tree_verify_greedy, without a workspace: its scratch is a fixed array
  * of tsd_tree_verify_static_capacity() bytes (1 MiB) in device memory that
  * every GPU loading the library holds until the process exits.  Sizes whose
- * scratch (B tickets plus B * N_max * chunks argmax partials) exceeds it
- * return TSD_ERR_LIMIT.  The call itself allocates nothing.
+ * scratch (B tickets plus B * N_max 8-byte argmax keys) exceeds it return
+ * TSD_ERR_LIMIT.  The call itself allocates nothing.
  * - The first call on a device looks up the array's device address (with
  *   that device current); make that first call before any stream capture.
- * - Every call zeroes the array's tickets on `stream` before its kernel runs.
+ * - Every call zeroes the tickets and keys it uses on `stream` before its
+ *   kernel runs.
  *   All calls share the one array: calls that overlap on the GPU race.
  */
 size_t tsd_tree_verify_static_capacity(void);

@@ -63,7 +63,7 @@ def test_static_scratch_matches_workspace_entry_point():
 
 def test_static_scratch_rejects_oversized_batches():
     import tree_speculative_decoding_virtual_gb300 as tsd
-    # 65535 sequences x 256 rows of partials cannot fit in 1 MiB
+    # 65535 sequences x 256 rows of 8-byte argmax keys cannot fit in 1 MiB
     rc = tsd.lib.tsd_tree_verify_greedy_static(1, 1, 1, 1, 1, 1, None, None, 65535, 256, 128256, 8,
                                                1, 1, 1, 1, 1, None)
     assert rc == -2  # TSD_ERR_LIMIT, nothing launched

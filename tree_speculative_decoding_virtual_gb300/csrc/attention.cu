@@ -385,18 +385,21 @@ tree_attn_split_kernel(const AttnParams p) {
 // 64-key tiles.  Both row tiles consume every K/V tile, so each K/V byte
 // brought to the SM feeds 256 rows (the GQA group of up to 256/g nodes).
 //   warp 0:    reads the split's block ids; lane 0 then loads K tiles and
-//              lane 1 V tiles with TMA into 3-stage rings (a K stage is
+//              lane 1 V tiles with TMA into 4-stage rings (a K stage is
 //              refilled once both Q K^T that read it completed, a V stage
 //              once both P V did)
-//   warp 1:    owns 512 TMEM columns; lane 0 issues every MMA
+//   warp 1:    owns 512 TMEM columns; lane 0 issues every MMA, taking each
+//              one as soon as its inputs are ready (it polls, so a late K
+//              tile never holds back a P V that is ready, or the reverse)
 //   warps 2-5: softmax of row tile A, warps 6-9: of row tile B; one TMEM lane
 //              (= one query row) per thread
 // Per 64-key tile j and row tile t:
 //   S_tj = Q_t K_j^T  (M=128, N=64, K=D; A and B K-major) -> TMEM, 2 buffers
-//   P_tj = exp2(S_tj * scale * log2e - m) as bf16         -> shared memory
-//   O_t += P_tj V_j   (M=128, N=D, K=64; V read MN-major)  -> TMEM
-// S_{t,j+1} is issued before P_tj V_j, so the tensor core works while the
-// softmax of tile j runs.  The running max is raised lazily: O and the row
+//   P_tj = exp2(S_tj * scale * log2e - m) as bf16         -> TMEM, over S_tj
+//   O_t += P_tj V_j   (M=128, N=D, K=64; A from TMEM, V read MN-major)
+// S_{t,j+1} is computed while the softmax of tile j runs; the softmax waits
+// for P_{t,j-1} V_{j-1} only when it has to rescale O.  The running max is
+// raised lazily: O and the row
 // sum are rescaled (in TMEM) only when a tile's max exceeds the one in use by
 // more than 2^8, so P never exceeds 256 and the result is the same softmax.
 // K and V tiles are read straight from the paged cache by TMA (4-D view
@@ -412,7 +415,7 @@ constexpr int kTcThreads = 320;
 constexpr int kTcBM = 128;          // rows of one row tile (one MMA M)
 constexpr int kTcRows = 256;        // rows of one block (two row tiles)
 constexpr int kTcBN = 64;           // keys per tile
-constexpr int kTcStages = 3;
+constexpr int kTcStages = 4;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kDrainLimitNs = 100000000ull;  // 100 ms
 constexpr int kTcMaxPages = 512;    // block ids of one split held in shared memory
@@ -427,20 +430,20 @@ struct TcLayout {
   static constexpr uint32_t kQ = 0;                        // Q_A, Q_B
   static constexpr uint32_t kK = 2 * kQTile;
   static constexpr uint32_t kV = kK + kTcStages * kTile;
-  static constexpr uint32_t kP = kV + kTcStages * kTile;   // P_A, P_B
-  static constexpr uint32_t kPBytes = kTcBM * kTcBN * 2;   // 128 rows x 64 keys bf16
-  static constexpr uint32_t kBytes = kP + 2 * kPBytes;
+  static constexpr uint32_t kBytes = kV + kTcStages * kTile;
   static constexpr uint32_t kAlloc = kBytes + 1024;        // + alignment slack
   static constexpr uint32_t kStaging = kK;                 // epilogue reuses the K/V rings
   static_assert(2 * kTcStages * kTile >= kTcRows * D * 2, "epilogue staging fits the rings");
-  static constexpr uint32_t kTmemS = 0;                    // [row tile][2 buffers] x 64 columns
+  // [row tile][2 buffers] x 64 columns of S; P (bf16 pairs) overwrites the
+  // first 32 columns of its own S buffer
+  static constexpr uint32_t kTmemS = 0;
   static constexpr uint32_t kTmemO = 256;                  // [row tile] x 128 columns
 };
 
 struct TcShared {
   int32_t pages[kTcMaxPages];  // block ids of the split
   uint64_t k_full[kTcStages], k_empty[kTcStages], v_full[kTcStages], v_empty[kTcStages];
-  uint64_t s_full[2][2], s_free[2][2], p_full[2], p_free[2];
+  uint64_t s_full[2][2], p_full[2][2], o_done[2], o_final[2];
   uint64_t q_full[2], drain, never;
   uint32_t tmem_base;
   int abort;
@@ -579,10 +582,10 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
     for (int t = 0; t < 2; ++t) {
       for (int i = 0; i < 2; ++i) {
         mbar_init(smem_addr(&sh.s_full[t][i]), 1);
-        mbar_init(smem_addr(&sh.s_free[t][i]), 4);
+        mbar_init(smem_addr(&sh.p_full[t][i]), 4);
       }
-      mbar_init(smem_addr(&sh.p_full[t]), 4);
-      mbar_init(smem_addr(&sh.p_free[t]), 1);
+      mbar_init(smem_addr(&sh.o_done[t]), 1);
+      mbar_init(smem_addr(&sh.o_final[t]), 1);
       mbar_init(smem_addr(&sh.q_full[t]), 4);
     }
     mbar_init(smem_addr(&sh.drain), 1);
@@ -659,15 +662,16 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ------------------------------
+    // Barrier phases: every waiter below knows that the barrier it tests is
+    // at most one phase ahead of the one it wants (the issue order bounds it),
+    // so a parity test is unambiguous.
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(kTcBM, kTcBN, false, false);
       constexpr uint32_t idPV = idesc_bf16_f32(kTcBM, D, false, true);
-      auto issue_s = [&](int j) -> bool {
+      auto issue_s = [&](int j) {  // K_j has landed; both S buffers j&1 are free
         const int st = j % kTcStages, sb = j & 1;
-        if (!tc_wait(sh.k_full[st], (j / kTcStages) & 1, lim, abort)) return false;
+        tc_fence_after();
         for (int t = 0; t < ntile_rows; ++t) {
-          if (j >= 2 && !tc_wait(sh.s_free[t][sb], ((j >> 1) - 1) & 1, lim, abort)) return false;
-          tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             umma_bf16(tmem + L::kTmemS + (t * 2 + sb) * kTcBN,
@@ -680,33 +684,57 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
           umma_commit(smem_addr(&sh.s_full[t][sb]));
         }
         umma_commit(smem_addr(&sh.k_empty[st]));
-        return true;
       };
-      auto issue_pv = [&](int j) -> bool {
-        const int st = j % kTcStages;
-        if (!tc_wait(sh.v_full[st], (j / kTcStages) & 1, lim, abort)) return false;
-        for (int t = 0; t < ntile_rows; ++t) {
-          if (!tc_wait(sh.p_full[t], j & 1, lim, abort)) return false;
-          tc_fence_after();
+      auto issue_pv = [&](int t, int j) {  // V_j has landed; P_tj is in TMEM
+        const int st = j % kTcStages, sb = j & 1;
+        tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < kTcBN / 16; ++kk) {
-            umma_bf16(tmem + L::kTmemO + t * 128,
-                      smem_desc_sw128(base + L::kP + t * L::kPBytes + kk * 32, 16, 1024),
-                      smem_desc_sw128(base + L::kV + st * L::kTile + kk * 16 * 128, L::kKVHalf, 1024),
-                      idPV, (j > 0 || kk > 0) ? 1u : 0u);
-          }
-          umma_commit(smem_addr(&sh.p_free[t]));
+        for (int kk = 0; kk < kTcBN / 16; ++kk) {
+          umma_bf16_ta(tmem + L::kTmemO + t * 128, tmem + L::kTmemS + (t * 2 + sb) * kTcBN + kk * 8,
+                       smem_desc_sw128(base + L::kV + st * L::kTile + kk * 16 * 128, L::kKVHalf, 1024),
+                       idPV, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(smem_addr(&sh.v_empty[st]));
-        return true;
+        umma_commit(smem_addr(&sh.o_done[t]));
+        if (j == ntiles - 1) umma_commit(smem_addr(&sh.o_final[t]));
       };
       bool ok = !p.test_stall || tc_wait(sh.never, 0, lim, abort);
       ok = ok && tc_wait(sh.q_full[0], 0, lim, abort);
       ok = ok && (ntile_rows < 2 || tc_wait(sh.q_full[1], 0, lim, abort));
-      ok = ok && issue_s(0);
-      for (int j = 0; ok && j < ntiles; ++j) {
-        if (j + 1 < ntiles) ok = !*abort && issue_s(j + 1);
-        if (ok) ok = issue_pv(j);
+      int ns = 0;                                   // next S tile
+      int npv[2] = {0, ntile_rows > 1 ? 0 : ntiles};  // next P V tile per row tile
+      int nv = 0;                                   // next V stage to hand back
+      uint64_t t_prog = global_timer_ns();
+      while (ok) {
+        const int mpv = min(npv[0], npv[1]);
+        if (mpv >= ntiles) break;
+        bool prog = false;
+        // S_j reuses the S buffers of tile j-2, read by P_{j-2} V_{j-2}
+        if (ns < ntiles && ns <= mpv + 1 &&
+            mbar_test(smem_addr(&sh.k_full[ns % kTcStages]), (ns / kTcStages) & 1)) {
+          issue_s(ns++);
+          prog = true;
+        }
+        for (int t = 0; t < ntile_rows; ++t) {
+          const int j = npv[t];
+          if (j < ns && mbar_test(smem_addr(&sh.v_full[j % kTcStages]), (j / kTcStages) & 1) &&
+              mbar_test(smem_addr(&sh.p_full[t][j & 1]), (j >> 1) & 1)) {
+            issue_pv(t, j);
+            ++npv[t];
+            prog = true;
+          }
+        }
+        for (const int m2 = min(npv[0], npv[1]); nv < m2; ++nv)
+          umma_commit(smem_addr(&sh.v_empty[nv % kTcStages]));
+        if (prog) {
+          t_prog = global_timer_ns();
+        } else if (*abort) {
+          ok = false;
+        } else if (global_timer_ns() - t_prog > lim) {
+          *abort = 1;
+          ok = false;
+        } else {
+          __nanosleep(32);
+        }
       }
       // drain: every MMA issued above has completed
       umma_commit(smem_addr(&sh.drain));
@@ -770,9 +798,6 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2) tmem_ld32(tS + sb * kTcBN + lane_off + c2 * 32, r[c2]);
         tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&sh.s_free[t][sb]));
 
         const int ts = k_begin + j * kTcBN;
         const bool full = (ts + kTcBN <= P) && (ts + kTcBN <= k_end);
@@ -797,12 +822,13 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
         const float m_new = fmaxf(m_use, mt);
         const bool upd = m_new > m_use + 8.f;  // first visible key, or the max grew by > 2^8
         const float alpha = upd ? exp2f(m_use - m_new) : 1.f;
-        // P_{t,j-1} V_{j-1} must be complete before O is rescaled or P_t rewritten
-        if (j > 0 && !warp_wait(sh.p_free[t], (j - 1) & 1)) {
+        // O may be rescaled only once P_{t,j-1} V_{j-1} has completed
+        const bool resc = j > 0 && __any_sync(0xffffffffu, upd);
+        if (resc && !warp_wait(sh.o_done[t], (j - 1) & 1)) {
           ok = false;
           break;
         }
-        if (j > 0 && __any_sync(0xffffffffu, upd)) {
+        if (resc) {
           tc_fence_after();
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
@@ -821,31 +847,23 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
         }
         const float mb = m_use == -INFINITY ? 0.f : m_use;
         float rsum[4] = {0.f, 0.f, 0.f, 0.f};
-        unsigned char *pbuf = gbase + L::kP + t * L::kPBytes;
         const float sc = p.scale_log2;
+        uint32_t pk[32];  // P row as bf16 pairs: column i holds keys 2i, 2i+1
 #pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-#pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8) {  // 8 keys = one 16-byte chunk
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float a = ex2_approx(fmaf(__uint_as_float(r[c2][q8 * 8 + 2 * e]), sc, -mb));
-              const float c = ex2_approx(fmaf(__uint_as_float(r[c2][q8 * 8 + 2 * e + 1]), sc, -mb));
-              rsum[e] += a + c;
-              w[e] = pack_bf16(a, c);
-            }
-            *reinterpret_cast<uint4 *>(pbuf + sw128_offset(rl, c2 * 4 + q8)) =
-                make_uint4(w[0], w[1], w[2], w[3]);
-          }
+        for (int i = 0; i < 32; ++i) {
+          const float a = ex2_approx(fmaf(__uint_as_float(r[i >> 4][(2 * i) & 31]), sc, -mb));
+          const float c = ex2_approx(fmaf(__uint_as_float(r[i >> 4][(2 * i + 1) & 31]), sc, -mb));
+          rsum[i & 3] += a + c;
+          pk[i] = pack_bf16(a, c);
         }
         l_sum += (rsum[0] + rsum[1]) + (rsum[2] + rsum[3]);
-        fence_proxy_async_smem();
+        tmem_st32(tS + sb * kTcBN + lane_off, pk);
+        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&sh.p_full[t]));
+        if (lane == 0) mbar_arrive(smem_addr(&sh.p_full[t][sb]));
       }
-      if (ok) ok = warp_wait(sh.p_free[t], (ntiles - 1) & 1);  // this row tile's last P V
+      if (ok) ok = warp_wait(sh.o_final[t], 0);  // this row tile's last P V
     }
 
     // ---- epilogue: O / l in bf16 through shared memory, (max, sum) per row ----
@@ -1071,26 +1089,6 @@ bool make_cache_map(CUtensorMap *m, const uint16_t *cache, int num_blocks, int H
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t *>(cache), dims, strides,
              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// Opt a kernel in to more than 48 KB of dynamic shared memory, once per
-// (kernel, device).
-bool set_smem(const void *kernel, size_t bytes) {
-  struct Entry {
-    const void *fn;
-    int dev;
-  };
-  static Entry done[64];
-  static int n_done = 0;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  for (int i = 0; i < n_done; ++i)
-    if (done[i].fn == kernel && done[i].dev == dev) return true;
-  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
-      cudaSuccess)
-    return false;
-  if (n_done < 64) done[n_done++] = Entry{kernel, dev};
-  return true;
 }
 
 template <int D>

@@ -25,6 +25,24 @@ static int64_t g_options[TSD_OPT_COUNT] = {
 
 int64_t option(int key) { return (key >= 0 && key < TSD_OPT_COUNT) ? g_options[key] : 0; }
 
+bool set_smem(const void *kernel, size_t bytes) {
+  struct Entry {
+    const void *fn;
+    int dev;
+  };
+  static Entry done[64];
+  static int n_done = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  for (int i = 0; i < n_done; ++i)
+    if (done[i].fn == kernel && done[i].dev == dev) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+      cudaSuccess)
+    return false;
+  if (n_done < 64) done[n_done++] = Entry{kernel, dev};
+  return true;
+}
+
 }  // namespace tsd
 
 TSD_API const char *tsd_version(void) { return "tsd 0.2 (sm_103a)"; }

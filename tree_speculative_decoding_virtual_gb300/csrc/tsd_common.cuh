@@ -55,6 +55,10 @@ inline cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Opt a kernel in to `bytes` of dynamic shared memory (needed once static
+// plus dynamic exceeds 48 KB), once per (kernel, device).
+bool set_smem(const void *kernel, size_t bytes);
+
 inline bool aligned(const void *p, size_t a) {
   return (reinterpret_cast<uintptr_t>(p) % a) == 0;
 }

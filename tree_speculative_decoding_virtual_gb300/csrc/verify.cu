@@ -6,66 +6,87 @@
 // draft token is accepted when it equals the target's most likely token at
 // its parent, and its parent was accepted.
 //
-// One fused launch.  Grid (chunk, node, sequence): each block scans one
-// chunk of one logits row with 16-byte streaming loads and writes its
-// (max, first index) partial.  The block that retires a sequence's last
-// chunk (ticket counter per sequence, no waiting) reduces the partials of
-// every row, evaluates acceptance with the ancestor bitmasks, and writes
-// leaf / accept_len / path / bonus.  The counter is reset by that block, so
-// the workspace is zero again when the launch ends.
+// One fused launch.  Grid (Gs, sequence): the valid rows of sequence b,
+// nb * V floats laid end to end, are cut into Gs equal ranges, one per
+// block, so every block streams the same number of bytes.  Each thread reads
+// its part in passes of 8 independent 16-byte loads (32 KB per block in
+// flight, four blocks per SM) and keeps a running (max, first index) for
+// each row its range touches (at most two); the block then folds each row's
+// candidate into a per-row 64-bit key with one atomicMax (key order = value,
+// then lower index).  The block that takes a sequence's last ticket reads
+// the row keys (resetting them), evaluates acceptance with the ancestor
+// bitmasks and writes leaf / accept_len / path / bonus; it also resets the
+// ticket, so the workspace is zero again when the launch ends.
 
 #include <climits>
 #include <cmath>
 
+#include "sm100_ptx.cuh"
 #include "tsd_common.cuh"
 
 namespace tsd {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kBatch = 8;  // independent 16-byte loads in flight per thread
-
-struct Partial {
-  float v;
-  int idx;
-};
+constexpr int kBatch = 8;        // 16-byte loads in flight per thread
+constexpr int kBlocksPerSm = 4;  // 1024 threads x 64 registers per SM
 
 // (v, i) beats (bv, bi): larger value, or equal value and lower index.
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
   return v > bv || (v == bv && i < bi);
 }
 
-__device__ __forceinline__ float4 ld_stream(const float4 *p) { return __ldcs(p); }
-
-__device__ __forceinline__ void prefetch_l2(const void *p) {
-  asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p));
+// Order-preserving 64-bit key: larger value first, then lower index; -0 and
+// +0 share one key so they tie on value.
+__device__ __forceinline__ unsigned long long arg_key(float v, int i) {
+  if (v == 0.f) v = 0.f;
+  uint32_t u = __float_as_uint(v);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)i);
 }
 
-__global__ void __launch_bounds__(kThreads)
+__device__ __forceinline__ void take4(const float4 &a, int x, float &bv, int &bi) {
+  if (better(a.x, x, bv, bi)) { bv = a.x; bi = x; }
+  if (better(a.y, x + 1, bv, bi)) { bv = a.y; bi = x + 1; }
+  if (better(a.z, x + 2, bv, bi)) { bv = a.z; bi = x + 2; }
+  if (better(a.w, x + 3, bv, bi)) { bv = a.w; bi = x + 3; }
+}
+
+__global__ void __launch_bounds__(kThreads, kBlocksPerSm)
 verify_greedy_kernel(const float *__restrict__ logits, const int32_t *__restrict__ tokens,
                      const int32_t *__restrict__ parent, const int32_t *__restrict__ anc,
                      const int32_t *__restrict__ depth, const uint32_t *__restrict__ mask,
                      const int32_t *__restrict__ n_nodes, const int32_t *__restrict__ err,
-                     int N_max, int V, int D_max, int W, int chunk, int C, int vec_ok,
+                     int N_max, int V, int D_max, int W, int vec,
                      int32_t *__restrict__ argmax_out, int32_t *__restrict__ accept_len,
                      int32_t *__restrict__ leaf_out, int32_t *__restrict__ path,
-                     int32_t *__restrict__ bonus, Partial *__restrict__ part,
+                     int32_t *__restrict__ bonus, unsigned long long *__restrict__ row_key,
                      unsigned *__restrict__ counter) {
+  using namespace sm100;
+  __shared__ float s_v[2][kThreads / 32];
+  __shared__ int s_i[2][kThreads / 32];
+  __shared__ bool s_last;
+
   pdl_trigger();
-  const int c = blockIdx.x;
-  const int i = blockIdx.y;
-  const int b = blockIdx.z;
+  const int g = blockIdx.x;
+  const int Gs = gridDim.x;
+  const int b = blockIdx.y;
   const int t = threadIdx.x;
   const int lane = t & 31;
   const int warp = t >> 5;
+  const float *seq = logits + (size_t)b * N_max * (size_t)V;
   {
-    // while the previous kernel finishes, pull this block's logits chunk into
-    // L2 (lines only; nothing read here is used)
+    // while the previous kernel finishes, pull the first pass of this
+    // block's range into L2 (lines only; nothing read here is used)
     const int nb_hint = n_nodes ? n_nodes[b] : N_max;
-    if (i < nb_hint) {
-      const char *row = reinterpret_cast<const char *>(logits + ((size_t)b * N_max + i) * (size_t)V);
-      const long lo = (long)c * chunk * 4, hi = min((long)V, (long)(c + 1) * chunk) * 4;
-      for (long off = lo + (long)t * 128; off < hi; off += (long)kThreads * 128) prefetch_l2(row + off);
+    if (nb_hint >= 1 && nb_hint <= N_max) {
+      const long total = (long)nb_hint * V;
+      const long lo = (total * g / Gs) & ~3L;
+      const long hi = min(g + 1 == Gs ? total : (total * (g + 1) / Gs) & ~3L,
+                          lo + (long)kBatch * kThreads * 4);
+      const char *base = reinterpret_cast<const char *>(seq);
+      for (long off = lo * 4 + (long)t * 128; off < hi * 4; off += (long)kThreads * 128)
+        prefetch_l2(base + off);
     }
   }
   pdl_wait();
@@ -74,80 +95,96 @@ verify_greedy_kernel(const float *__restrict__ logits, const int32_t *__restrict
   const int eb = err ? err[b] : 0;
   const bool seq_ok = eb == 0 && nb >= 1 && nb <= N_max;
 
-  __shared__ float s_v[kThreads / 32];
-  __shared__ int s_i[kThreads / 32];
-  __shared__ bool s_last;
+  // Block-wide fold of up to two candidates (rows r and r + 1) into the row
+  // keys.  Every thread calls it with the same `two`.
+  auto fold = [&](int r, bool two, float v0, int i0, float v1, int i1) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov0 = __shfl_xor_sync(0xffffffffu, v0, off);
+      const int oi0 = __shfl_xor_sync(0xffffffffu, i0, off);
+      if (better(ov0, oi0, v0, i0)) { v0 = ov0; i0 = oi0; }
+      const float ov1 = __shfl_xor_sync(0xffffffffu, v1, off);
+      const int oi1 = __shfl_xor_sync(0xffffffffu, i1, off);
+      if (better(ov1, oi1, v1, i1)) { v1 = ov1; i1 = oi1; }
+    }
+    if (lane == 0) {
+      s_v[0][warp] = v0; s_i[0][warp] = i0;
+      s_v[1][warp] = v1; s_i[1][warp] = i1;
+    }
+    __syncthreads();
+    if (t < 2 && (t == 0 || two)) {
+      float bv = s_v[t][0];
+      int bi = s_i[t][0];
+      for (int w = 1; w < kThreads / 32; ++w)
+        if (better(s_v[t][w], s_i[t][w], bv, bi)) { bv = s_v[t][w]; bi = s_i[t][w]; }
+      atomicMax(&row_key[(size_t)b * N_max + r + t], arg_key(bv, bi));
+    }
+    __syncthreads();
+  };
 
-  // The first block of each sequence pulls the acceptance inputs into L2 so
-  // the block that finishes the sequence finds them there.
-  if (c == 0 && i == 0 && seq_ok) {
-    const char *lines[4] = {reinterpret_cast<const char *>(tokens + (size_t)b * N_max),
-                            reinterpret_cast<const char *>(parent + (size_t)b * N_max),
-                            reinterpret_cast<const char *>(depth + (size_t)b * N_max),
-                            reinterpret_cast<const char *>(mask + (size_t)b * N_max * W)};
-    const int bytes[4] = {N_max * 4, N_max * 4, N_max * 4, N_max * W * 4};
-    for (int a = 0; a < 4; ++a)
-      for (int off = t * 128; off < bytes[a]; off += kThreads * 128) prefetch_l2(lines[a] + off);
-    const char *ab = reinterpret_cast<const char *>(anc + (size_t)b * (N_max + 1) * (D_max + 1));
-    for (int off = t * 128; off < (N_max + 1) * (D_max + 1) * 4; off += kThreads * 128)
-      prefetch_l2(ab + off);
-  }
-
-  // ---- phase 1: argmax of one chunk of row (b, i) ----
-  if (seq_ok && i < nb) {
-    float bv = -INFINITY;
-    int bi = INT_MAX;
-    const float *row = logits + ((size_t)b * N_max + i) * (size_t)V;
-    const int lo = c * chunk;
-    const int hi = min(V, lo + chunk);
-    if (vec_ok) {
-      // passes of kBatch independent 16-byte loads per thread
-      const float4 *r4 = reinterpret_cast<const float4 *>(row + lo);
-      const int n4 = (hi - lo) >> 2;
-      for (int k0 = 0; k0 < n4; k0 += kBatch * kThreads) {
-        float4 a[kBatch];
+  // ---- phase 1: argmax over this block's range of the sequence's rows ----
+  if (seq_ok) {
+    const long total = (long)nb * V;
+    const long lo = (total * g / Gs) & ~3L;
+    const long hi = g + 1 == Gs ? total : (total * (g + 1) / Gs) & ~3L;
+    if (lo < hi && vec && hi - lo <= V) {
+      // the range touches rows r0 and (if it crosses end0) r0 + 1; a float4
+      // never straddles a row end since V is a multiple of 4
+      const int r0 = (int)(lo / V);
+      const long end0 = (long)(r0 + 1) * V;
+      const bool two = hi > end0;
+      float v0 = -INFINITY, v1 = -INFINITY;
+      int i0 = INT_MAX, i1 = INT_MAX;
+      // 32-bit offsets from the range start: the range is at most one row
+      const float4 *src = reinterpret_cast<const float4 *>(seq) + (lo >> 2);
+      const int n4 = (int)((hi - lo) >> 2);
+      const int e4 = (int)((end0 - lo) >> 2);  // first float4 of row r0 + 1
+      const int x0 = (int)(lo - (long)r0 * V);  // column of src[0] in row r0
+      const int x1 = (int)(lo - end0);          // ... and in row r0 + 1 (negative)
+      constexpr int kStride = kBatch * kThreads;
+      const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      // passes of kBatch independent loads per thread
+      float4 a[kBatch];
+      for (int p4 = 0; p4 < n4; p4 += kStride) {
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
-          const int k = k0 + u * kThreads + t;
-          a[u] = k < n4 ? ld_stream(r4 + k) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+          const int q = p4 + u * kThreads + t;
+          a[u] = q < n4 ? __ldcs(src + q) : ninf;
         }
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
-          const int k = k0 + u * kThreads + t;
-          if (k < n4) {
-            const int x = lo + 4 * k;
-            if (better(a[u].x, x, bv, bi)) { bv = a[u].x; bi = x; }
-            if (better(a[u].y, x + 1, bv, bi)) { bv = a[u].y; bi = x + 1; }
-            if (better(a[u].z, x + 2, bv, bi)) { bv = a[u].z; bi = x + 2; }
-            if (better(a[u].w, x + 3, bv, bi)) { bv = a[u].w; bi = x + 3; }
+          const int q = p4 + u * kThreads + t;
+          if (q < n4) {
+            if (q < e4)
+              take4(a[u], x0 + 4 * q, v0, i0);
+            else
+              take4(a[u], x1 + 4 * q, v1, i1);
           }
         }
       }
-      for (int x = lo + 4 * n4 + t; x < hi; x += kThreads) {
-        const float v = __ldcs(row + x);
-        if (better(v, x, bv, bi)) { bv = v; bi = x; }
+      fold(r0, two, v0, i0, v1, i1);
+    } else if (lo < hi) {
+      // general case (rows shorter than the range, or unaligned rows): one
+      // row segment at a time with plain loads
+      for (long p = lo; p < hi;) {
+        const int r = (int)(p / V);
+        const long e = min(hi, (long)(r + 1) * V);
+        float bv = -INFINITY;
+        int bi = INT_MAX;
+        const long rs = (long)r * V;
+        if (vec) {  // p, e and the row start are multiples of 4
+          const float4 *s4 = reinterpret_cast<const float4 *>(seq);
+          for (long q = (p >> 2) + t; q < (e >> 2); q += kThreads)
+            take4(__ldcs(s4 + q), (int)(4 * q - rs), bv, bi);
+        } else {
+          for (long q = p + t; q < e; q += kThreads) {
+            const float v = __ldcs(seq + q);
+            if (better(v, (int)(q - rs), bv, bi)) { bv = v; bi = (int)(q - rs); }
+          }
+        }
+        fold(r, false, bv, bi, -INFINITY, INT_MAX);
+        p = e;
       }
-    } else {
-      for (int x = lo + t; x < hi; x += kThreads) {
-        const float v = __ldcs(row + x);
-        if (better(v, x, bv, bi)) { bv = v; bi = x; }
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-    }
-    if (lane == 0) { s_v[warp] = bv; s_i[warp] = bi; }
-    __syncthreads();
-    if (t == 0) {
-      for (int w = 1; w < kThreads / 32; ++w)
-        if (better(s_v[w], s_i[w], bv, bi)) { bv = s_v[w]; bi = s_i[w]; }
-      Partial pr;
-      pr.v = bv;
-      pr.idx = bi;
-      part[((size_t)b * N_max + i) * C + c] = pr;
     }
   }
 
@@ -155,7 +192,7 @@ verify_greedy_kernel(const float *__restrict__ logits, const int32_t *__restrict
   if (t == 0) {
     __threadfence();
     const unsigned ticket = atomicAdd(&counter[b], 1u);
-    s_last = ticket == (unsigned)(N_max * C - 1);
+    s_last = ticket == (unsigned)(Gs - 1);
   }
   __syncthreads();
   if (!s_last) return;
@@ -170,8 +207,10 @@ verify_greedy_kernel(const float *__restrict__ logits, const int32_t *__restrict
   const int cols = D_max + 1;
   // independent loads first, so their latencies overlap
   int my_parent = 0, my_token = 0, my_depth = 0;
+  unsigned long long my_key = 0ull;
   uint32_t my_mask[kMaxNodes / 32];
   if (seq_ok && t < nb) {
+    my_key = __ldcg(&row_key[(size_t)b * N_max + t]);
     my_parent = parent[(size_t)b * N_max + t];
     my_token = tokens[(size_t)b * N_max + t];
     my_depth = depth[(size_t)b * N_max + t];
@@ -181,20 +220,12 @@ verify_greedy_kernel(const float *__restrict__ logits, const int32_t *__restrict
   }
   int am = -1;
   if (seq_ok && t < nb) {
-    float bv = -INFINITY;
-    int bi = INT_MAX;
-    const Partial *pr = part + ((size_t)b * N_max + t) * C;
-    for (int k = 0; k < C; ++k) {
-      const float v = __ldcg(&pr[k].v);
-      const int x = __ldcg(&pr[k].idx);
-      if (better(v, x, bv, bi)) { bv = v; bi = x; }
-    }
-    am = bi;
+    row_key[(size_t)b * N_max + t] = 0ull;  // zero again for the next call
+    am = my_key ? (int)(0xFFFFFFFFu - (uint32_t)(my_key & 0xFFFFFFFFull)) : -1;
   }
   if (t < kMaxNodes) s_am[t] = am;
   if (t < N_max) argmax_out[(size_t)b * N_max + t] = am;
   __syncthreads();
-
   // matched(i): root, or token equals the target's choice at the parent
   bool match = false;
   if (seq_ok && t < nb) {
@@ -247,27 +278,42 @@ verify_greedy_kernel(const float *__restrict__ logits, const int32_t *__restrict
 }
 
 struct VerifyPlan {
-  int chunk;
-  int C;
-  size_t counter_bytes;
-  size_t part_bytes;
+  int Gs;                // blocks per sequence
+  size_t counter_bytes;  // one ticket per sequence
+  size_t key_bytes;      // one 64-bit argmax key per row
 };
 
 VerifyPlan plan_verify(int B, int N_max, int V) {
   VerifyPlan p;
-  const long rows = (long)B * N_max;
-  const long total = rows * (long)V;
-  const long resident = 4L * sm_count();  // blocks of 256 threads resident at once
-  const long per_pass = (long)kBatch * kThreads * 4;
-  long chunk = (total + resident - 1) / resident;
-  chunk = (chunk + per_pass - 1) / per_pass * per_pass;  // whole passes
-  if (chunk < per_pass) chunk = per_pass;
-  if (chunk > V) chunk = (V + 3) / 4 * 4;
-  p.chunk = (int)chunk;
-  p.C = (int)((V + chunk - 1) / chunk);
+  // about one resident wave of blocks, each with at least 4096 floats; at
+  // least N_max blocks per sequence, so a block's range spans at most two rows
+  const long resident = (long)kBlocksPerSm * sm_count();
+  long gs = resident / B;
+  const long min_chunks = ((long)N_max * V + 4095) / 4096;
+  if (gs > min_chunks) gs = min_chunks;
+  if (gs < N_max) gs = N_max;
+  if (gs > 65535) gs = 65535;
+  p.Gs = (int)gs;
   p.counter_bytes = align_up(sizeof(unsigned) * (size_t)B, 256);
-  p.part_bytes = sizeof(Partial) * (size_t)B * N_max * p.C;
+  p.key_bytes = sizeof(unsigned long long) * (size_t)B * N_max;
   return p;
+}
+
+int launch_verify(const float *logits, const int32_t *tokens, const int32_t *parent,
+                  const int32_t *anc, const int32_t *depth, const uint32_t *mask,
+                  const int32_t *n_nodes, const int32_t *err, int B, int N_max, int V, int D_max,
+                  int32_t *argmax, int32_t *accept_len, int32_t *leaf, int32_t *path,
+                  int32_t *bonus, void *scratch, const VerifyPlan &p, cudaStream_t s) {
+  unsigned *counter = static_cast<unsigned *>(scratch);
+  unsigned long long *keys =
+      reinterpret_cast<unsigned long long *>(static_cast<char *>(scratch) + p.counter_bytes);
+  const int W = (N_max + 31) / 32;
+  const int vec = (V % 4 == 0) && aligned(logits, 16);
+  if (launch(verify_greedy_kernel, dim3(p.Gs, B), dim3(kThreads), 0, s, logits, tokens, parent,
+             anc, depth, mask, n_nodes, err, N_max, V, D_max, W, vec, argmax, accept_len, leaf,
+             path, bonus, keys, counter) != cudaSuccess)
+    return TSD_ERR_CUDA;
+  return TSD_OK;
 }
 
 }  // namespace
@@ -276,7 +322,7 @@ VerifyPlan plan_verify(int B, int N_max, int V) {
 TSD_API size_t tsd_tree_verify_workspace_bytes(int B, int N_max, int V) {
   if (B <= 0 || N_max <= 0 || V <= 0) return 0;
   const tsd::VerifyPlan p = tsd::plan_verify(B, N_max, V);
-  return p.counter_bytes + p.part_bytes;
+  return p.counter_bytes + p.key_bytes;
 }
 
 TSD_API int tsd_tree_verify_greedy(const float *logits, const int32_t *tokens,
@@ -294,17 +340,10 @@ TSD_API int tsd_tree_verify_greedy(const float *logits, const int32_t *tokens,
       !leaf || !path || !bonus)
     return TSD_ERR_ARG;
   const VerifyPlan p = plan_verify(B, N_max, V);
-  if (!workspace || ws_bytes < p.counter_bytes + p.part_bytes || !aligned(workspace, 16))
+  if (!workspace || ws_bytes < p.counter_bytes + p.key_bytes || !aligned(workspace, 16))
     return TSD_ERR_WORKSPACE;
-  unsigned *counter = static_cast<unsigned *>(workspace);
-  Partial *part = reinterpret_cast<Partial *>(static_cast<char *>(workspace) + p.counter_bytes);
-  const int W = (N_max + 31) / 32;
-  const int vec_ok = (V % 4 == 0) && aligned(logits, 16);
-  if (launch(verify_greedy_kernel, dim3(p.C, N_max, B), dim3(kThreads), 0, as_cuda(stream), logits,
-             tokens, parent, anc, depth, mask, n_nodes, err, N_max, V, D_max, W, p.chunk, p.C,
-             vec_ok, argmax, accept_len, leaf, path, bonus, part, counter) != cudaSuccess)
-    return TSD_ERR_CUDA;
-  return TSD_OK;
+  return launch_verify(logits, tokens, parent, anc, depth, mask, n_nodes, err, B, N_max, V, D_max,
+                       argmax, accept_len, leaf, path, bonus, workspace, p, as_cuda(stream));
 }
 
 // ---------------------------------------------------------------------------
@@ -314,7 +353,7 @@ TSD_API int tsd_tree_verify_greedy(const float *logits, const int32_t *tokens,
 // engine that owns every byte of device memory and hands out no workspace,
 // or a latency-critical path where an allocation (which may synchronise the
 // device) is not acceptable.  This entry point keeps its scratch (the
-// per-sequence tickets and the per-chunk argmax partials) in a fixed array
+// per-sequence tickets and the per-row argmax keys) in a fixed array
 // in device global memory, loaded with the library: every GPU that loads
 // libtsd.so holds kStaticScratchBytes of it until the process exits.
 //
@@ -322,9 +361,10 @@ TSD_API int tsd_tree_verify_greedy(const float *logits, const int32_t *tokens,
 // memory, so its device address is looked up once per device with
 // cudaGetSymbolAddress (with that device current) and cached.  The first
 // call on a device performs that look-up, so make it before any stream
-// capture.  All calls share the one array: each call zeroes the tickets on
-// its stream before its kernel runs, and calls that overlap on the GPU (two
-// streams, or two devices' contexts racing on one array) race on it.
+// capture.  All calls share the one array: each call zeroes the tickets and
+// row keys it uses on its stream before its kernel runs, and calls that
+// overlap on the GPU (two streams, or two devices' contexts racing on one
+// array) race on it.
 // ---------------------------------------------------------------------------
 
 namespace tsd {
@@ -366,18 +406,11 @@ TSD_API int tsd_tree_verify_greedy_static(const float *logits, const int32_t *to
       !leaf || !path || !bonus)
     return TSD_ERR_ARG;
   const VerifyPlan p = plan_verify(B, N_max, V);
-  if (p.counter_bytes + p.part_bytes > kStaticScratchBytes) return TSD_ERR_LIMIT;
+  if (p.counter_bytes + p.key_bytes > kStaticScratchBytes) return TSD_ERR_LIMIT;
   void *scratch = static_scratch_ptr();
   if (!scratch) return TSD_ERR_CUDA;
-  if (cudaMemsetAsync(scratch, 0, p.counter_bytes, as_cuda(stream)) != cudaSuccess)
+  if (cudaMemsetAsync(scratch, 0, p.counter_bytes + p.key_bytes, as_cuda(stream)) != cudaSuccess)
     return TSD_ERR_CUDA;
-  unsigned *counter = static_cast<unsigned *>(scratch);
-  Partial *part = reinterpret_cast<Partial *>(static_cast<char *>(scratch) + p.counter_bytes);
-  const int W = (N_max + 31) / 32;
-  const int vec_ok = (V % 4 == 0) && aligned(logits, 16);
-  if (launch(verify_greedy_kernel, dim3(p.C, N_max, B), dim3(kThreads), 0, as_cuda(stream), logits,
-             tokens, parent, anc, depth, mask, n_nodes, err, N_max, V, D_max, W, p.chunk, p.C,
-             vec_ok, argmax, accept_len, leaf, path, bonus, part, counter) != cudaSuccess)
-    return TSD_ERR_CUDA;
-  return TSD_OK;
+  return launch_verify(logits, tokens, parent, anc, depth, mask, n_nodes, err, B, N_max, V, D_max,
+                       argmax, accept_len, leaf, path, bonus, scratch, p, as_cuda(stream));
 }
