@@ -927,11 +927,15 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
 }
 
 // One warp per output row (b, node, q head): merge the splits.  Lane s reads
-// split s's (max, sum); every lane then accumulates its D/32 columns over the
-// splits with all loads independent.
-template <int D>
+// split s's (max, sum, scale).  A split's partial row is D/8 16-byte chunks,
+// so one warp-wide load covers 32/(D/8) splits: lane l reads chunk l % (D/8)
+// of split (l / (D/8)) + round * 32/(D/8).  Every load of every round is
+// issued before any is used, so the merge costs one memory round trip; lanes
+// holding the same chunk for different splits are then summed by shuffles.
+template <int D, int R>  // R: rounds of loads (R * 32 / (D/8) >= number of splits)
 __global__ void __launch_bounds__(256) tree_attn_combine_kernel(const AttnParams p, int B) {
-  constexpr int kPer = D / 32;
+  constexpr int kChunks = D / 8;            // 16-byte chunks of a partial row
+  constexpr int kPerRound = 32 / kChunks;   // splits covered by one warp-wide load
   pdl_trigger();
   pdl_wait();
   const int warp = (blockIdx.x * 256 + threadIdx.x) >> 5;
@@ -941,24 +945,34 @@ __global__ void __launch_bounds__(256) tree_attn_combine_kernel(const AttnParams
   const int hq = warp % p.Hq;
   const int node = (warp / p.Hq) % p.N_max;
   const int b = warp / (p.Hq * p.N_max);
-  uint16_t *dst = p.out + (size_t)warp * D + lane * kPer;
+  const int c = lane % kChunks;   // logical chunk of this lane
+  const int so = lane / kChunks;  // split offset within a round
+  uint16_t *dst = p.out + (size_t)warp * D + c * 8;
 
   int P, nb;
   const bool ok = seq_ok(p, b, P, nb) && node < nb;
   if (!ok) {
-    if (kPer == 4)
-      *reinterpret_cast<uint2 *>(dst) = make_uint2(0u, 0u);
-    else
-      *reinterpret_cast<uint32_t *>(dst) = 0u;
+    if (so == 0) *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
     if (p.lse && lane == 0) p.lse[warp] = -INFINITY;
     return;
   }
   const int hkv = hq / p.g;
   const int row = node * p.g + (hq % p.g);
   const size_t r0 = (size_t)(b * p.Hkv + hkv) * p.splits * p.rows_pad + row;
-  const int ns = (P + nb + p.chunk - 1) / p.chunk;  // <= 32 (host check)
-  const float4 ml = lane < ns ? p.part_ml[r0 + (size_t)lane * p.rows_pad]
+  const int ns = (P + nb + p.chunk - 1) / p.chunk;  // <= R * kPerRound (host check)
+  // rows_pad is a multiple of 16, so every split's copy of this row has the
+  // same swizzle phase
+  const int pc = p.swizzled ? (c ^ (int)(r0 & (kChunks - 1))) : c;
+  const float4 ml = lane < ns ? __ldcg(&p.part_ml[r0 + (size_t)lane * p.rows_pad])
                               : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+  uint4 raw[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int sp = r * kPerRound + so;
+    raw[r] = sp < ns ? __ldcg(reinterpret_cast<const uint4 *>(
+                           p.part_o + (r0 + (size_t)sp * p.rows_pad) * D + pc * 8))
+                     : make_uint4(0u, 0u, 0u, 0u);
+  }
   float M = ml.x;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
@@ -967,47 +981,45 @@ __global__ void __launch_bounds__(256) tree_attn_combine_kernel(const AttnParams
   const float w = wl * ml.z;  // the split's partial holds O / (l c)
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-  float acc[kPer];
+  float acc[8];
 #pragma unroll
-  for (int x = 0; x < kPer; ++x) acc[x] = 0.f;
-  for (int s0 = 0; s0 < ns; s0 += 8) {
-    float v[8][kPer];
-    float ws[8];
+  for (int x = 0; x < 8; ++x) acc[x] = 0.f;
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int s = s0 + u;
-      ws[u] = __shfl_sync(0xffffffffu, w, s & 31);
-      const size_t prow = r0 + (size_t)min(s, ns - 1) * p.rows_pad;
-      const int col = p.swizzled ? ((((lane * kPer) >> 3) ^ (int)(prow & (D / 8 - 1))) << 3) +
-                                       ((lane * kPer) & 7)
-                                 : lane * kPer;
-      const uint16_t *src = p.part_o + prow * D + col;
-      if (kPer == 4) {
-        const uint2 t = __ldcg(reinterpret_cast<const uint2 *>(src));
-        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&t.x));
-        const float2 c = __half22float2(*reinterpret_cast<const __half2 *>(&t.y));
-        v[u][0] = a.x; v[u][1] = a.y; v[u][2] = c.x; v[u][3] = c.y;
-      } else {
-        const uint32_t t = __ldcg(reinterpret_cast<const unsigned int *>(src));
-        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&t));
-        v[u][0] = a.x; v[u][1] = a.y;
+  for (int r = 0; r < R; ++r) {
+    const int sp = r * kPerRound + so;
+    const float ws = __shfl_sync(0xffffffffu, w, sp & 31);
+    if (sp < ns) {
+      const uint32_t h[4] = {raw[r].x, raw[r].y, raw[r].z, raw[r].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h[k]));
+        acc[2 * k] += f.x * ws;
+        acc[2 * k + 1] += f.y * ws;
       }
-      if (s >= ns) ws[u] = 0.f;
     }
-#pragma unroll
-    for (int u = 0; u < 8; ++u)
-#pragma unroll
-      for (int x = 0; x < kPer; ++x) acc[x] += v[u][x] * ws[u];
   }
-  const float inv = 1.f / L;
-  uint32_t packed[kPer / 2];
 #pragma unroll
-  for (int x = 0; x < kPer / 2; ++x) packed[x] = pack_bf16(acc[2 * x] * inv, acc[2 * x + 1] * inv);
-  if (kPer == 4)
-    *reinterpret_cast<uint2 *>(dst) = make_uint2(packed[0], packed[1]);
-  else
-    *reinterpret_cast<uint32_t *>(dst) = packed[0];
+  for (int off = kChunks; off < 32; off <<= 1)
+#pragma unroll
+    for (int x = 0; x < 8; ++x) acc[x] += __shfl_xor_sync(0xffffffffu, acc[x], off);
+  if (so == 0) {
+    const float inv = 1.f / L;
+    *reinterpret_cast<uint4 *>(dst) =
+        make_uint4(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv),
+                   pack_bf16(acc[4] * inv, acc[5] * inv), pack_bf16(acc[6] * inv, acc[7] * inv));
+  }
   if (p.lse && lane == 0) p.lse[warp] = (M + log2f(L)) * 0.6931471805599453f;
+}
+
+template <int D>
+cudaError_t launch_combine(const AttnParams &p, int B, cudaStream_t s) {
+  constexpr int kPerRound = 32 / (D / 8);
+  const long rows = (long)B * p.N_max * p.Hq;
+  const dim3 grid((unsigned)((rows * 32 + 255) / 256));
+  const int rounds = (p.splits + kPerRound - 1) / kPerRound;
+  if (rounds <= 4) return launch(tree_attn_combine_kernel<D, 4>, grid, dim3(256), 0, s, p, B);
+  if (rounds <= 8) return launch(tree_attn_combine_kernel<D, 8>, grid, dim3(256), 0, s, p, B);
+  return launch(tree_attn_combine_kernel<D, 32 / kPerRound>, grid, dim3(256), 0, s, p, B);
 }
 
 struct AttnPlan {
@@ -1112,10 +1124,7 @@ int launch_attn(AttnParams &p, const AttnPlan &a, int B, int num_blocks, cudaStr
       return TSD_ERR_CUDA;
   }
   if (cudaGetLastError() != cudaSuccess) return TSD_ERR_CUDA;
-  const long rows = (long)B * p.N_max * p.Hq;
-  const int blocks = (int)((rows * 32 + 255) / 256);
-  if (launch(tree_attn_combine_kernel<D>, dim3(blocks), dim3(256), 0, s, p, B) != cudaSuccess)
-    return TSD_ERR_CUDA;
+  if (launch_combine<D>(p, B, s) != cudaSuccess) return TSD_ERR_CUDA;
   return TSD_OK;
 }
 
