@@ -382,40 +382,48 @@ tree_attn_split_kernel(const AttnParams p) {
 // ===========================================================================
 // tcgen05 path.  One block = up to 256 query rows (two 128-row tiles, A and
 // B) x one split of the key range of one (sequence, kv head), walked in
-// 64-key tiles.  Both row tiles consume every K/V tile, so each K/V byte
+// 128-key tiles.  Both row tiles consume every K/V tile, so each K/V byte
 // brought to the SM feeds 256 rows (the GQA group of up to 256/g nodes).
-//   warp 0:    reads the split's block ids; lane 0 then loads K tiles and
-//              lane 1 V tiles with TMA into 4-stage rings (a K stage is
-//              refilled once both Q K^T that read it completed, a V stage
-//              once both P V did)
-//   warp 1:    owns 512 TMEM columns; lane 0 issues every MMA, taking each
-//              one as soon as its inputs are ready (it polls, so a late K
-//              tile never holds back a P V that is ready, or the reverse)
+//   warp 0:    reads the split's block ids; lane 0 then loads K tiles with
+//              TMA into a 2-stage ring (a stage is refilled once both
+//              Q K^T that read it completed)
+//   warp 10:   lane 0 loads V tiles the same way (refilled once both P V
+//              that read a stage completed); a warp of its own, so K and V
+//              loads never wait on each other
+//   warp 1:    owns 512 TMEM columns; lane 0 issues every MMA
 //   warps 2-5: softmax of row tile A, warps 6-9: of row tile B; one TMEM lane
 //              (= one query row) per thread
-// Per 64-key tile j and row tile t:
-//   S_tj = Q_t K_j^T  (M=128, N=64, K=D; A and B K-major) -> TMEM, 2 buffers
-//   P_tj = exp2(S_tj * scale * log2e - m) as bf16         -> TMEM, over S_tj
-//   O_t += P_tj V_j   (M=128, N=D, K=64; A from TMEM, V read MN-major)
-// S_{t,j+1} is computed while the softmax of tile j runs; the softmax waits
-// for P_{t,j-1} V_{j-1} only when it has to rescale O.  The running max is
-// raised lazily: O and the row
-// sum are rescaled (in TMEM) only when a tile's max exceeds the one in use by
-// more than 2^8, so P never exceeds 256 and the result is the same softmax.
+// Per 128-key tile j and row tile t:
+//   S_tj = Q_t K_j^T  (M=128, N=128, K=D; A and B K-major) -> TMEM
+//   P_tj = exp2(S_tj * scale * log2e - m) as bf16          -> TMEM, over S_tj
+//   O_t += P_tj V_j   (M=128, N=D, K=128; A from TMEM, V read MN-major)
+// The MMAs of a row tile form one chain (S_t0, P_t0 V_0, S_t1, P_t1 V_1, ...)
+// and the two chains alternate on the tensor core, so the softmax of one row
+// tile runs while the other's MMAs execute.  S_{t,j+1} is issued right
+// behind P_tj V_j and MMAs complete in issue order, so when the softmax sees
+// S_tj complete, every earlier MMA of the row tile has completed too: O may
+// be rescaled and S_tj overwritten by P_tj with no further wait.  The
+// running max is raised lazily: O and the row sum are rescaled (in TMEM)
+// only when a max exceeds the one in use by more than 2^8, so P never
+// exceeds 256 and the result is the same softmax.  A tile's row is handled
+// in two 64-key halves; if the second half raises the max, the first half's
+// P (already in TMEM) is rescaled too.
 // K and V tiles are read straight from the paged cache by TMA (4-D view
-// [block][kv head][slot][D], 128-byte swizzle): when the four 16-slot blocks
-// of a 64-key tile are consecutive one box fetches them, otherwise one box
-// per block.  The epilogue writes O / l rounded to bf16, staged in shared
-// memory and stored with one bulk copy, plus the row's (max, sum).
+// [block][kv head][slot][D], 128-byte swizzle): when the eight 16-slot
+// blocks of a tile are consecutive one box fetches them, otherwise one box
+// per block.  The epilogue writes O / (l c) in fp16 (c a power of two per
+// row), staged in shared memory and stored with one bulk copy, plus the
+// row's (max, sum, c).
 // Every wait is bounded; on expiry the block flags TSD_STATUS_TIMEOUT, drains
 // what it issued, frees its tensor memory and returns.
 // ===========================================================================
 
-constexpr int kTcThreads = 320;
+constexpr int kTcThreads = 352;     // 11 warps
 constexpr int kTcBM = 128;          // rows of one row tile (one MMA M)
 constexpr int kTcRows = 256;        // rows of one block (two row tiles)
-constexpr int kTcBN = 64;           // keys per tile
-constexpr int kTcStages = 4;
+constexpr int kTcBN = 128;          // keys per tile
+constexpr int kTcPagesPerTile = kTcBN / kPage;
+constexpr int kTcStages = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kDrainLimitNs = 100000000ull;  // 100 ms
 constexpr int kTcMaxPages = 512;    // block ids of one split held in shared memory
@@ -434,17 +442,19 @@ struct TcLayout {
   static constexpr uint32_t kAlloc = kBytes + 1024;        // + alignment slack
   static constexpr uint32_t kStaging = kK;                 // epilogue reuses the K/V rings
   static_assert(2 * kTcStages * kTile >= kTcRows * D * 2, "epilogue staging fits the rings");
-  // [row tile][2 buffers] x 64 columns of S; P (bf16 pairs) overwrites the
-  // first 32 columns of its own S buffer
+  // per row tile t: S_t (128 columns; P_t, bf16 pairs, overwrites its first
+  // 64) at t * 256, O_t (D columns) at t * 256 + 128
   static constexpr uint32_t kTmemS = 0;
-  static constexpr uint32_t kTmemO = 256;                  // [row tile] x 128 columns
+  static constexpr uint32_t kTmemO = 128;
+  static constexpr uint32_t kTmemTile = 256;
 };
 
 struct TcShared {
   int32_t pages[kTcMaxPages];  // block ids of the split
   uint64_t k_full[kTcStages], k_empty[kTcStages], v_full[kTcStages], v_empty[kTcStages];
-  uint64_t s_full[2][2], p_full[2][2], o_done[2], o_final[2];
-  uint64_t q_full[2], drain, never;
+  uint64_t s_full[2], p_full[2], o_final[2], q_full[2];
+  uint64_t drain, never;
+  float4 mrg[kTcBM];           // group 1's (m, l_sum, l_ex, -) per row (kv2)
   uint32_t tmem_base;
   int abort;
 };
@@ -489,11 +499,10 @@ __device__ __forceinline__ uint32_t visible_bits(const uint32_t *mrow, int W, in
 // loads behind them); nothing read here is used, so inputs the previous
 // kernel is still writing are harmless (L2 is the point of coherence for
 // their later writes).
-constexpr int kPrefetchPages = 16;  // 4 tiles of 64 keys
+constexpr int kPrefetchPages = 16;  // 2 tiles of 128 keys
 
 template <int D>
-__device__ __forceinline__ void attn_prefetch(const AttnParams &p, const CUtensorMap *mk,
-                                              const CUtensorMap *mv, int b, int hkv, int rt,
+__device__ __forceinline__ void attn_prefetch(const AttnParams &p, int b, int hkv, int rt,
                                               int split, int warp, int lane) {
   using namespace sm100;
   const int P = p.prefix_len[b];
@@ -516,7 +525,7 @@ __device__ __forceinline__ void attn_prefetch(const AttnParams &p, const CUtenso
           reinterpret_cast<const char *>(cache + ((size_t)page * p.Hkv + hkv) * kPage * D);
       for (int off = lane * 128; off < kPage * D * 2; off += 32 * 128) prefetch_l2(blk + off);
     }
-  } else if (warp >= 2) {
+  } else if (warp < 10) {
     const int row = rt * kTcRows + ((warp - 2) >> 2) * kTcBM + (warp & 3) * 32 + lane;
     if (row < nb * p.g) {
       const char *q = reinterpret_cast<const char *>(
@@ -526,20 +535,106 @@ __device__ __forceinline__ void attn_prefetch(const AttnParams &p, const CUtenso
   }
 }
 
+// One loader thread: TMA loads of K (or V) tiles 0..ntiles-1 into a ring,
+// waiting for a stage to be released before refilling it, then a drain so no
+// copy is in flight when the block exits.
 template <int D>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__device__ __forceinline__ void tc_load_tiles(const CUtensorMap *m1, const CUtensorMap *m8,
+                                              uint64_t *full, uint64_t *empty, uint32_t ring,
+                                              const int32_t *pages, int npg, int ntiles, int hkv,
+                                              uint64_t lim, volatile int *abort) {
+  using namespace sm100;
+  using L = TcLayout<D>;
+  int last_issued[kTcStages];
+#pragma unroll
+  for (int i = 0; i < kTcStages; ++i) last_issued[i] = -1;
+  for (int j = 0; j < ntiles && !*abort; ++j) {
+    const int st = j % kTcStages;
+    if (j >= kTcStages && !tc_wait(empty[st], ((j / kTcStages) - 1) & 1, lim, abort)) break;
+    const int g0 = j * kTcPagesPerTile;
+    int pg[kTcPagesPerTile];
+    bool run = true;
+#pragma unroll
+    for (int g = 0; g < kTcPagesPerTile; ++g) {
+      pg[g] = pages[min(g0 + g, npg - 1)];
+      run = run && pg[g] == pg[0] + g;
+    }
+    const uint32_t bar = smem_addr(&full[st]);
+    mbar_arrive_expect_tx(bar, L::kTile);
+#pragma unroll
+    for (int h = 0; h < L::kHalves; ++h) {
+      const uint32_t dst = ring + st * L::kTile + h * L::kKVHalf;
+      if (run) {
+        tma_load_4d(dst, m8, h * 64, 0, hkv, pg[0], bar);
+      } else {
+#pragma unroll
+        for (int g = 0; g < kTcPagesPerTile; ++g)
+          tma_load_4d(dst + g * kPage * 128, m1, h * 64, 0, hkv, pg[g], bar);
+      }
+    }
+    last_issued[st] = j;
+  }
+  // drain: the last loads issued into each stage have landed
+#pragma unroll
+  for (int st = 0; st < kTcStages; ++st)
+    if (last_issued[st] >= 0)
+      mbar_wait(smem_addr(&full[st]), (last_issued[st] / kTcStages) & 1, kDrainLimitNs);
+}
+
+// S_t = Q_q K^T for the K tile in stage st into the S columns of TMEM tile
+// t, then a commit to s_full.  Out of line: one copy of the code for every
+// call site.
+template <int D>
+__device__ __noinline__ void tc_issue_s(uint32_t tmem, uint32_t base, int q, int t, int st,
+                                        uint32_t s_full) {
+  using namespace sm100;
+  using L = TcLayout<D>;
+  constexpr uint32_t idS = idesc_bf16_f32(kTcBM, kTcBN, false, false);
+  tc_fence_after();
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    umma_bf16(tmem + t * L::kTmemTile + L::kTmemS,
+              smem_desc_sw128(base + L::kQ + q * L::kQTile + (kk >> 2) * L::kQHalf + (kk & 3) * 32,
+                              16, 1024),
+              smem_desc_sw128(base + L::kK + st * L::kTile + (kk >> 2) * L::kKVHalf + (kk & 3) * 32,
+                              16, 1024),
+              idS, kk > 0);
+  }
+  umma_commit(s_full);
+}
+
+// O_t += P_t V for the V tile in stage st (P read from tensor memory); a
+// commit to `final_bar` when it is nonzero.
+template <int D>
+__device__ __noinline__ void tc_issue_pv(uint32_t tmem, uint32_t base, int t, int st, bool accum,
+                                         uint32_t final_bar) {
+  using namespace sm100;
+  using L = TcLayout<D>;
+  constexpr uint32_t idPV = idesc_bf16_f32(kTcBM, D, false, true);
+  tc_fence_after();
+#pragma unroll
+  for (int kk = 0; kk < kTcBN / 16; ++kk) {
+    umma_bf16_ta(tmem + t * L::kTmemTile + L::kTmemO, tmem + t * L::kTmemTile + L::kTmemS + kk * 8,
+                 smem_desc_sw128(base + L::kV + st * L::kTile + kk * 16 * 128, L::kKVHalf, 1024),
+                 idPV, (accum || kk > 0) ? 1u : 0u);
+  }
+  if (final_bar) umma_commit(final_bar);
+}
+
+// __launch_bounds__ for 384 threads caps registers at 168, which keeps three
+// warps of 168 registers inside one SM sub-partition's register file; the
+// kernel runs 352 threads.
+template <int D>
+__global__ void __launch_bounds__(384, 1)
 tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k1,
-                   const __grid_constant__ CUtensorMap map_k4, const __grid_constant__ CUtensorMap map_v1,
-                   const __grid_constant__ CUtensorMap map_v4) {
+                   const __grid_constant__ CUtensorMap map_k8, const __grid_constant__ CUtensorMap map_v1,
+                   const __grid_constant__ CUtensorMap map_v8) {
   using namespace sm100;
   using L = TcLayout<D>;
   extern __shared__ unsigned char smem_raw[];
   __shared__ TcShared sh;
 
   pdl_trigger();
-  attn_prefetch<D>(p, &map_k1, &map_v1, blockIdx.z / p.Hkv, blockIdx.z % p.Hkv, blockIdx.x,
-                   blockIdx.y, threadIdx.x >> 5, threadIdx.x & 31);
-  pdl_wait();
   const int rt = blockIdx.x;
   const int split = blockIdx.y;
   const int z = blockIdx.z;
@@ -549,23 +644,8 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
-  int P, nb;
-  if (!seq_ok(p, b, P, nb)) {
-    if (rt == 0 && split == 0 && hkv == 0 && tid == 0 && p.status) {
-      const int e = p.err ? p.err[b] : 0;
-      const int nbb = p.n_nodes ? p.n_nodes[b] : p.N_max;
-      if (e == 0 && nbb >= 1 && nbb <= p.N_max) atomicOr(p.status, TSD_STATUS_BAD_LEN);
-    }
-    return;
-  }
-  const int rows_valid = nb * p.g;
-  const int seq_len = P + nb;
-  const int k_begin = split * p.chunk;
-  if (rt * kTcRows >= rows_valid || k_begin >= seq_len) return;
-  const int ntile_rows = rt * kTcRows + kTcBM < rows_valid ? 2 : 1;  // row tiles with valid rows
-  const int k_end = min(seq_len, k_begin + p.chunk);
-  const int ntiles = (k_end - k_begin + kTcBN - 1) / kTcBN;
-
+  // Set-up touches no global memory, so it runs while the previous kernel on
+  // the stream finishes (programmatic launch); so does the L2 prefetch.
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char *gbase = smem_raw + (base - raw);
@@ -580,11 +660,8 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
       mbar_init(smem_addr(&sh.v_empty[i]), 1);
     }
     for (int t = 0; t < 2; ++t) {
-      for (int i = 0; i < 2; ++i) {
-        mbar_init(smem_addr(&sh.s_full[t][i]), 1);
-        mbar_init(smem_addr(&sh.p_full[t][i]), 4);
-      }
-      mbar_init(smem_addr(&sh.o_done[t]), 1);
+      mbar_init(smem_addr(&sh.s_full[t]), 1);
+      mbar_init(smem_addr(&sh.p_full[t]), 4);
       mbar_init(smem_addr(&sh.o_final[t]), 1);
       mbar_init(smem_addr(&sh.q_full[t]), 4);
     }
@@ -593,9 +670,9 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
     sh.abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&map_k1);
-    tma_prefetch_desc(&map_k4);
+    tma_prefetch_desc(&map_k8);
     tma_prefetch_desc(&map_v1);
-    tma_prefetch_desc(&map_v4);
+    tma_prefetch_desc(&map_v8);
   }
   if (warp == 1) tmem_alloc(smem_addr(&sh.tmem_base), kTmemCols);
   tc_fence_before();
@@ -603,137 +680,126 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
 
-  if (warp == 0) {
+  attn_prefetch<D>(p, b, hkv, rt, split, warp, lane);
+  pdl_wait();
+
+  int P = 0, nb = 0;
+  bool run = seq_ok(p, b, P, nb);
+  if (!run && rt == 0 && split == 0 && hkv == 0 && tid == 0 && p.status) {
+    const int e = p.err ? p.err[b] : 0;
+    const int nbb = p.n_nodes ? p.n_nodes[b] : p.N_max;
+    if (e == 0 && nbb >= 1 && nbb <= p.N_max) atomicOr(p.status, TSD_STATUS_BAD_LEN);
+  }
+  const int rows_valid = nb * p.g;
+  const int seq_len = P + nb;
+  const int k_begin = split * p.chunk;
+  run = run && rt * kTcRows < rows_valid && k_begin < seq_len;
+  const int ntile_rows = rt * kTcRows + kTcBM < rows_valid ? 2 : 1;  // row tiles with valid rows
+  const int k_end = min(seq_len, k_begin + p.chunk);
+  const int ntiles = (k_end - k_begin + kTcBN - 1) / kTcBN;
+  const int pg_first = k_begin / kPage;
+  const int npg = run ? (k_end - 1) / kPage - pg_first + 1 : 0;  // <= kTcMaxPages (host check)
+  // One row tile and at least two key tiles: both softmax groups work on the
+  // same rows, each on every other key tile, and merge at the end.
+  const bool kv2 = ntile_rows == 1 && ntiles >= 2;
+
+  if (!run) {
+    // nothing to do for this block: straight to the teardown
+  } else if (warp == 0 || warp == 10) {
     // --------------------------- loaders (TMA) ---------------------------
-    const int32_t *trow = p.table + (size_t)b * p.max_blocks;
-    const int pg_first = k_begin / kPage;
-    const int pg_last = (k_end - 1) / kPage;
-    const int npg = pg_last - pg_first + 1;  // <= chunk / 16 <= kTcMaxPages (host check)
-    bool bad = false;
-    for (int i = lane; i < npg; i += 32) {
-      int page = __ldg(trow + pg_first + i);
-      if (page < 0 || page >= p.num_blocks) {
-        bad = true;
-        page = 0;
-      }
-      sh.pages[i] = page;
-    }
-    if (__any_sync(0xffffffffu, bad) && lane == 0 && p.status) atomicOr(p.status, TSD_STATUS_BAD_PAGE);
-    __syncwarp();
-    if (lane < 2) {
-      const bool is_k = lane == 0;
-      const CUtensorMap *m1 = is_k ? &map_k1 : &map_v1;
-      const CUtensorMap *m4 = is_k ? &map_k4 : &map_v4;
-      uint64_t *full = is_k ? sh.k_full : sh.v_full;
-      uint64_t *empty = is_k ? sh.k_empty : sh.v_empty;
-      const uint32_t ring = base + (is_k ? L::kK : L::kV);
-      int last_issued[kTcStages];
-#pragma unroll
-      for (int i = 0; i < kTcStages; ++i) last_issued[i] = -1;
-      for (int j = 0; j < ntiles && !*abort; ++j) {
-        const int st = j % kTcStages;
-        if (j >= kTcStages && !tc_wait(empty[st], ((j / kTcStages) - 1) & 1, lim, abort)) break;
-        const int g0 = j * (kTcBN / kPage);
-        int pg[kTcBN / kPage];
-#pragma unroll
-        for (int g = 0; g < kTcBN / kPage; ++g) pg[g] = sh.pages[min(g0 + g, npg - 1)];
-        const bool run = pg[1] == pg[0] + 1 && pg[2] == pg[0] + 2 && pg[3] == pg[0] + 3;
-        const uint32_t bar = smem_addr(&full[st]);
-        mbar_arrive_expect_tx(bar, L::kTile);
-#pragma unroll
-        for (int h = 0; h < L::kHalves; ++h) {
-          const uint32_t dst = ring + st * L::kTile + h * L::kKVHalf;
-          if (run) {
-            tma_load_4d(dst, m4, h * 64, 0, hkv, pg[0], bar);
-          } else {
-#pragma unroll
-            for (int g = 0; g < kTcBN / kPage; ++g)
-              tma_load_4d(dst + g * kPage * 128, m1, h * 64, 0, hkv, pg[g], bar);
-          }
+    if (warp == 0) {
+      const int32_t *trow = p.table + (size_t)b * p.max_blocks;
+      bool bad = false;
+      for (int i = lane; i < npg; i += 32) {
+        int page = __ldg(trow + pg_first + i);
+        if (page < 0 || page >= p.num_blocks) {
+          bad = true;
+          page = 0;
         }
-        last_issued[st] = j;
+        sh.pages[i] = page;
       }
-      // drain: the last loads issued into each stage have landed
-#pragma unroll
-      for (int st = 0; st < kTcStages; ++st)
-        if (last_issued[st] >= 0)
-          mbar_wait(smem_addr(&full[st]), (last_issued[st] / kTcStages) & 1, kDrainLimitNs);
+      if (__any_sync(0xffffffffu, bad) && lane == 0 && p.status) atomicOr(p.status, TSD_STATUS_BAD_PAGE);
+    }
+    asm volatile("bar.sync 2, 64;\n" ::: "memory");  // block ids visible to both loaders
+    if (lane == 0) {
+      if (warp == 0)
+        tc_load_tiles<D>(&map_k1, &map_k8, sh.k_full, sh.k_empty, base + L::kK, sh.pages, npg,
+                         ntiles, hkv, lim, abort);
+      else
+        tc_load_tiles<D>(&map_v1, &map_v8, sh.v_full, sh.v_empty, base + L::kV, sh.pages, npg,
+                         ntiles, hkv, lim, abort);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ------------------------------
-    // Barrier phases: every waiter below knows that the barrier it tests is
-    // at most one phase ahead of the one it wants (the issue order bounds it),
-    // so a parity test is unambiguous.
+    // Fixed order: S_t0 for each row tile, then for every tile j and row tile
+    // t: P_tj V_j followed by S_t,j+1.  Every wait is on a barrier at most one
+    // phase ahead of the one wanted (the order bounds it), so parities are
+    // unambiguous.
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(kTcBM, kTcBN, false, false);
       constexpr uint32_t idPV = idesc_bf16_f32(kTcBM, D, false, true);
-      auto issue_s = [&](int j) {  // K_j has landed; both S buffers j&1 are free
-        const int st = j % kTcStages, sb = j & 1;
-        tc_fence_after();
-        for (int t = 0; t < ntile_rows; ++t) {
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            umma_bf16(tmem + L::kTmemS + (t * 2 + sb) * kTcBN,
-                      smem_desc_sw128(base + L::kQ + t * L::kQTile + (kk >> 2) * L::kQHalf +
-                                          (kk & 3) * 32, 16, 1024),
-                      smem_desc_sw128(base + L::kK + st * L::kTile + (kk >> 2) * L::kKVHalf +
-                                          (kk & 3) * 32, 16, 1024),
-                      idS, kk > 0);
-          }
-          umma_commit(smem_addr(&sh.s_full[t][sb]));
-        }
-        umma_commit(smem_addr(&sh.k_empty[st]));
+      auto issue_s = [&](int t, int j) {  // K_j has landed; S_t is free
+        tc_issue_s<D>(tmem, base, kv2 ? 0 : t, t, j % kTcStages, smem_addr(&sh.s_full[t]));
       };
       auto issue_pv = [&](int t, int j) {  // V_j has landed; P_tj is in TMEM
-        const int st = j % kTcStages, sb = j & 1;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kTcBN / 16; ++kk) {
-          umma_bf16_ta(tmem + L::kTmemO + t * 128, tmem + L::kTmemS + (t * 2 + sb) * kTcBN + kk * 8,
-                       smem_desc_sw128(base + L::kV + st * L::kTile + kk * 16 * 128, L::kKVHalf, 1024),
-                       idPV, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(smem_addr(&sh.o_done[t]));
-        if (j == ntiles - 1) umma_commit(smem_addr(&sh.o_final[t]));
+        const bool last = kv2 ? j + 2 >= ntiles : j == ntiles - 1;
+        tc_issue_pv<D>(tmem, base, t, j % kTcStages, kv2 ? j >= 2 : j > 0,
+                       last ? smem_addr(&sh.o_final[t]) : 0u);
       };
       bool ok = !p.test_stall || tc_wait(sh.never, 0, lim, abort);
-      ok = ok && tc_wait(sh.q_full[0], 0, lim, abort);
-      ok = ok && (ntile_rows < 2 || tc_wait(sh.q_full[1], 0, lim, abort));
-      int ns = 0;                                   // next S tile
-      int npv[2] = {0, ntile_rows > 1 ? 0 : ntiles};  // next P V tile per row tile
-      int nv = 0;                                   // next V stage to hand back
-      uint64_t t_prog = global_timer_ns();
-      while (ok) {
-        const int mpv = min(npv[0], npv[1]);
-        if (mpv >= ntiles) break;
-        bool prog = false;
-        // S_j reuses the S buffers of tile j-2, read by P_{j-2} V_{j-2}
-        if (ns < ntiles && ns <= mpv + 1 &&
-            mbar_test(smem_addr(&sh.k_full[ns % kTcStages]), (ns / kTcStages) & 1)) {
-          issue_s(ns++);
-          prog = true;
-        }
-        for (int t = 0; t < ntile_rows; ++t) {
-          const int j = npv[t];
-          if (j < ns && mbar_test(smem_addr(&sh.v_full[j % kTcStages]), (j / kTcStages) & 1) &&
-              mbar_test(smem_addr(&sh.p_full[t][j & 1]), (j >> 1) & 1)) {
-            issue_pv(t, j);
-            ++npv[t];
-            prog = true;
+      if (kv2) {
+        // one row tile, two chains over alternate key tiles: tile j goes to
+        // TMEM tile (and softmax group) j & 1; K_j is released after S_j, V_j
+        // after P V_j
+        ok = ok && tc_wait(sh.q_full[0], 0, lim, abort);
+        for (int j = 0; ok && j < 2; ++j) {
+          ok = tc_wait(sh.k_full[j], 0, lim, abort);
+          if (ok) {
+            issue_s(j, j);
+            umma_commit(smem_addr(&sh.k_empty[j]));
           }
         }
-        for (const int m2 = min(npv[0], npv[1]); nv < m2; ++nv)
-          umma_commit(smem_addr(&sh.v_empty[nv % kTcStages]));
-        if (prog) {
-          t_prog = global_timer_ns();
-        } else if (*abort) {
-          ok = false;
-        } else if (global_timer_ns() - t_prog > lim) {
-          *abort = 1;
-          ok = false;
-        } else {
-          __nanosleep(32);
+        for (int j = 0; ok && j < ntiles; ++j) {
+          const int w = j & 1;
+          ok = !*abort && tc_wait(sh.p_full[w], (j >> 1) & 1, lim, abort);
+          ok = ok && tc_wait(sh.v_full[j % kTcStages], (j / kTcStages) & 1, lim, abort);
+          if (!ok) break;
+          issue_pv(w, j);
+          umma_commit(smem_addr(&sh.v_empty[j % kTcStages]));
+          if (j + 2 < ntiles) {
+            ok = tc_wait(sh.k_full[(j + 2) % kTcStages], ((j + 2) / kTcStages) & 1, lim, abort);
+            if (ok) {
+              issue_s(w, j + 2);
+              umma_commit(smem_addr(&sh.k_empty[(j + 2) % kTcStages]));
+            }
+          }
+        }
+      } else {
+        // one chain per row tile; the two chains alternate on the tensor core
+        ok = ok && tc_wait(sh.k_full[0], 0, lim, abort);
+        for (int t = 0; ok && t < ntile_rows; ++t) {
+          ok = tc_wait(sh.q_full[t], 0, lim, abort);
+          if (ok) issue_s(t, 0);
+        }
+        if (ok && ntiles == 1) umma_commit(smem_addr(&sh.k_empty[0]));
+        for (int j = 0; ok && j < ntiles; ++j) {
+          const bool next = j + 1 < ntiles;
+          for (int t = 0; ok && t < ntile_rows; ++t) {
+            ok = !*abort && tc_wait(sh.p_full[t], j & 1, lim, abort);
+            if (ok && t == 0) ok = tc_wait(sh.v_full[j % kTcStages], (j / kTcStages) & 1, lim, abort);
+            if (!ok) break;
+            issue_pv(t, j);
+            if (next) {
+              if (t == 0)
+                ok = tc_wait(sh.k_full[(j + 1) % kTcStages], ((j + 1) / kTcStages) & 1, lim, abort);
+              if (ok) issue_s(t, j + 1);
+            }
+          }
+          if (!ok) break;
+          umma_commit(smem_addr(&sh.v_empty[j % kTcStages]));  // both P V of tile j
+          if (next) umma_commit(smem_addr(&sh.k_empty[(j + 1) % kTcStages]));  // both S of j+1
+          if (j == 0 && next) umma_commit(smem_addr(&sh.k_empty[0]));
         }
       }
       // drain: every MMA issued above has completed
@@ -743,18 +809,18 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
     __syncwarp();
   } else {
     // ------------------------------ softmax ------------------------------
-    const int t = (warp - 2) >> 2;                    // row tile of this warp group
+    const int t = (warp - 2) >> 2;                    // group: TMEM tile and barriers
+    const int tr = kv2 ? 0 : t;                       // row tile of this group
     const int quarter = warp & 3;                     // TMEM lanes 32*quarter .. +31
     const int rl = quarter * 32 + lane;               // row within the row tile
-    const int row = rt * kTcRows + t * kTcBM + rl;
-    const bool active = t < ntile_rows;
+    const int row = rt * kTcRows + tr * kTcBM + rl;
+    const bool active = kv2 || t < ntile_rows;
     const bool rvalid = row < rows_valid;
     const int node = rvalid ? row / p.g : 0;
-    const int head = hkv * p.g + (rvalid ? row % p.g : 0);
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t *mrow = p.mask + ((size_t)b * p.N_max + node) * p.W;
-    const uint32_t tS = tmem + L::kTmemS + t * 2 * kTcBN;
-    const uint32_t tO = tmem + L::kTmemO + t * 128;
+    const uint32_t tS = tmem + t * L::kTmemTile + L::kTmemS + lane_off;
+    const uint32_t tO = tmem + t * L::kTmemTile + L::kTmemO + lane_off;
 
     // waits are taken by every lane and their outcome made warp-uniform, so the
     // .sync.aligned TMEM accesses below are never reached by a partial warp
@@ -762,21 +828,57 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
       const bool got = !*abort && tc_wait(bar, parity, lim, abort);
       return __all_sync(0xffffffffu, got);
     };
-    float m_use = -INFINITY, l_sum = 0.f;
+    // bf16 pair -> the two values' sum
+    auto pair_sum = [](uint32_t w) {
+      return __uint_as_float(w << 16) + __uint_as_float(w & 0xFFFF0000u);
+    };
+    // O (once a P V has written it) and this tile's first-half P, times alpha
+    // (threads whose max did not move pass alpha = 1); returns the sum of the
+    // first half's P as rounded again
+    auto rescale = [&](float alpha, bool with_o, bool with_p) -> float {
+      float psum = 0.f;
+      if (with_o) {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + c * 32, o);
+        }
+      }
+      if (with_p) {
+        tmem_wait_st();  // the first half's P stores have landed
+        uint32_t q[32];
+        tmem_ld32(tS, q);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&q[i]));
+          q[i] = pack_bf16(f.x * alpha, f.y * alpha);
+          psum += pair_sum(q[i]);
+        }
+        tmem_st32(tS, q);
+      }
+      tmem_wait_st();
+      return psum;
+    };
+    float m_use = -INFINITY, l_sum = 0.f, l_ex = 0.f;
     bool ok = active;
-    if (active) {
+    if (active && (!kv2 || t == 0)) {
       // Q rows -> shared memory (128-byte swizzle) with cp.async: every copy is
       // in flight at once.  Each warp stages its 32 rows; one instruction
       // covers 32 / (D/8) consecutive rows, so global reads are contiguous.
       // Rows past the valid ones copy row 0 of the sequence (finite, unused).
-      const uint32_t qt = base + L::kQ + t * L::kQTile;
+      const uint32_t qt = base + L::kQ + tr * L::kQTile;
       constexpr int kCh = D / 8;               // 16-byte chunks per row
       constexpr int kRowsPer = 32 / kCh;       // rows per warp instruction
       const int ch = lane % kCh;
 #pragma unroll
       for (int i = 0; i < 32 / kRowsPer; ++i) {
         const int r_in = quarter * 32 + i * kRowsPer + lane / kCh;  // row within the tile
-        const int grow = rt * kTcRows + t * kTcBM + r_in;
+        const int grow = rt * kTcRows + tr * kTcBM + r_in;
         const int gr = grow < rows_valid ? grow : 0;
         const uint16_t *src =
             p.q + (((size_t)b * p.N_max + gr / p.g) * p.Hq + hkv * p.g + gr % p.g) * D + ch * 8;
@@ -786,99 +888,131 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&sh.q_full[t]));
-
-      for (int j = 0; j < ntiles; ++j) {
-        const int sb = j & 1;
-        if (!warp_wait(sh.s_full[t][sb], (j >> 1) & 1)) {
+    }
+    if (active) {
+      const float sc = p.scale_log2;
+      // this group's tiles: all of them, or every other one (kv2); u counts them
+      for (int u = 0, j = kv2 ? t : 0; j < ntiles; ++u, j += kv2 ? 2 : 1) {
+        if (!warp_wait(sh.s_full[t], u & 1)) {
           ok = false;
           break;
         }
+        // S_tj is complete, and with it every earlier MMA of this row tile
         tc_fence_after();
-        uint32_t r[2][32];
-#pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) tmem_ld32(tS + sb * kTcBN + lane_off + c2 * 32, r[c2]);
-        tmem_wait_ld();
-
         const int ts = k_begin + j * kTcBN;
         const bool full = (ts + kTcBN <= P) && (ts + kTcBN <= k_end);
-        // masked scores become -inf; the max is taken on raw scores (scale > 0)
-        if (!full) {
+        // Two row sums: l_sum adds P exactly as rounded to bf16 for the P V
+        // product, so O / l_sum weighs every key alike; l_ex adds the fp32 P
+        // and gives the row's log-sum-exp and its weight against other
+        // splits.  Both hold the earlier tiles; lt / lte this tile's.
+        float lt = 0.f, lte = 0.f;
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {  // 64-key halves (one copy of the code)
+          uint32_t r[2][32];
+#pragma unroll
+          for (int c2 = 0; c2 < 2; ++c2) tmem_ld32(tS + h * 64 + c2 * 32, r[c2]);
+          tmem_wait_ld();
+          // masked scores become -inf; the max is taken on raw scores (scale > 0)
+          if (!full) {
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) {
+              const int k0 = ts + h * 64 + c2 * 32;
+              const uint32_t vis = visible_bits(mrow, p.W, k0 - P, k_end - k0, rvalid);
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (!((vis >> i) & 1u)) r[c2][i] = __float_as_uint(-INFINITY);
+            }
+          }
+          float mx[8];
+#pragma unroll
+          for (int a = 0; a < 8; ++a) mx[a] = __uint_as_float(r[0][a]);
+#pragma unroll
+          for (int i = 8; i < 64; ++i)
+            mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(r[i >> 5][i & 31]));
+          const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sc;
+          const float m_new = fmaxf(m_use, mt);
+          const bool upd = m_new > m_use + 8.f;  // first visible key, or the max grew by > 2^8
+          const float alpha = upd ? exp2f(m_use - m_new) : 1.f;
+          if (__any_sync(0xffffffffu, upd) && (u > 0 || h > 0)) {
+            const float s0 = rescale(alpha, u > 0, h > 0);
+            if (h > 0) lt = s0;  // the first half's P as rounded again
+          }
+          if (upd) {
+            l_sum *= alpha;
+            l_ex *= alpha;
+            lte *= alpha;  // (zero in the first half)
+            m_use = m_new;
+          }
+          const float mb = m_use == -INFINITY ? 0.f : m_use;
+          float esum[2] = {0.f, 0.f}, rsum[2] = {0.f, 0.f};
 #pragma unroll
           for (int c2 = 0; c2 < 2; ++c2) {
-            const uint32_t vis =
-                visible_bits(mrow, p.W, ts + c2 * 32 - P, k_end - (ts + c2 * 32), rvalid);
+            uint32_t pk[16];  // P as bf16 pairs: column i holds keys 2i, 2i+1 of the chunk
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (!((vis >> i) & 1u)) r[c2][i] = __float_as_uint(-INFINITY);
+            for (int i = 0; i < 16; ++i) {
+              const float a = ex2_approx(fmaf(__uint_as_float(r[c2][2 * i]), sc, -mb));
+              const float c = ex2_approx(fmaf(__uint_as_float(r[c2][2 * i + 1]), sc, -mb));
+              pk[i] = pack_bf16(a, c);
+              esum[i & 1] += a + c;
+              rsum[i & 1] += pair_sum(pk[i]);
+            }
+            tmem_st16(tS + h * 32 + c2 * 16, pk);
           }
+          lt += rsum[0] + rsum[1];
+          lte += esum[0] + esum[1];
         }
-        float mx[8];
-#pragma unroll
-        for (int a = 0; a < 8; ++a) mx[a] = __uint_as_float(r[0][a]);
-#pragma unroll
-        for (int i = 8; i < 64; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(r[i >> 5][i & 31]));
-        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * p.scale_log2;
-        const float m_new = fmaxf(m_use, mt);
-        const bool upd = m_new > m_use + 8.f;  // first visible key, or the max grew by > 2^8
-        const float alpha = upd ? exp2f(m_use - m_new) : 1.f;
-        // O may be rescaled only once P_{t,j-1} V_{j-1} has completed
-        const bool resc = j > 0 && __any_sync(0xffffffffu, upd);
-        if (resc && !warp_wait(sh.o_done[t], (j - 1) & 1)) {
-          ok = false;
-          break;
-        }
-        if (resc) {
-          tc_fence_after();
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + lane_off + c * 32, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(tO + lane_off + c * 32, o);
-          }
-          tmem_wait_st();
-        }
-        if (upd) {
-          l_sum *= alpha;
-          m_use = m_new;
-        }
-        const float mb = m_use == -INFINITY ? 0.f : m_use;
-        float rsum[4] = {0.f, 0.f, 0.f, 0.f};
-        const float sc = p.scale_log2;
-        uint32_t pk[32];  // P row as bf16 pairs: column i holds keys 2i, 2i+1
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float a = ex2_approx(fmaf(__uint_as_float(r[i >> 4][(2 * i) & 31]), sc, -mb));
-          const float c = ex2_approx(fmaf(__uint_as_float(r[i >> 4][(2 * i + 1) & 31]), sc, -mb));
-          rsum[i & 3] += a + c;
-          pk[i] = pack_bf16(a, c);
-        }
-        l_sum += (rsum[0] + rsum[1]) + (rsum[2] + rsum[3]);
-        tmem_st32(tS + sb * kTcBN + lane_off, pk);
+        l_sum += lt;
+        l_ex += lte;
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&sh.p_full[t][sb]));
+        if (lane == 0) mbar_arrive(smem_addr(&sh.p_full[t]));
       }
       if (ok) ok = warp_wait(sh.o_final[t], 0);  // this row tile's last P V
     }
 
-    // ---- epilogue: O / l in bf16 through shared memory, (max, sum) per row ----
-    // Both row tiles' MMAs must be complete before the K/V rings are reused.
-    const int nthr = ntile_rows * 128;
+    // ---- epilogue: O / (l c) in fp16 through shared memory, (m, l, c) per row ----
+    // Every MMA of the block must be complete before the K/V rings are reused.
+    // With kv2, group 1 hands its (m, l_sum, l_ex) to group 0 through shared
+    // memory and group 0 folds group 1's O into its own before writing.
+    const int nthr = kv2 ? 256 : ntile_rows * 128;
+    if (kv2 && t == 1) sh.mrg[rl] = make_float4(m_use, l_sum, l_ex, ok ? 0.f : 1.f);
     if (active) asm volatile("bar.sync 1, %0;\n" ::"r"(nthr) : "memory");
-    const bool all_ok = __all_sync(0xffffffffu, active && !*abort);
+    const bool writer = active && (!kv2 || t == 0);
+    const int nwr = kv2 ? 128 : nthr;  // threads that stage rows
+    const bool all_ok = __all_sync(0xffffffffu, writer && !*abort);
+    if (all_ok && kv2) {
+      tc_fence_after();
+      const float4 o1 = sh.mrg[rl];
+      const float m = fmaxf(m_use, o1.x);
+      const float a0 = m_use == -INFINITY ? 0.f : exp2f(m_use - m);
+      const float a1 = o1.x == -INFINITY ? 0.f : exp2f(o1.x - m);
+      l_sum = a0 * l_sum + a1 * o1.y;
+      l_ex = a0 * l_ex + a1 * o1.z;
+      m_use = m;
+      const uint32_t tO1 = tmem + L::kTmemTile + L::kTmemO + lane_off;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t x[32], y[32];
+        tmem_ld32(tO + c * 32, x);
+        tmem_ld32(tO1 + c * 32, y);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          x[i] = __float_as_uint(a0 * __uint_as_float(x[i]) + a1 * __uint_as_float(y[i]));
+        tmem_st32(tO + c * 32, x);
+      }
+      tmem_wait_st();
+    }
     if (all_ok) {
       tc_fence_after();
       float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
       float amax = 0.f;  // pass 1: the row's largest |O|
-#pragma unroll
+#pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
-        tmem_ld32(tO + lane_off + c * 32, o);
+        tmem_ld32(tO + c * 32, o);
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(__uint_as_float(o[i])));
@@ -888,11 +1022,11 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
       // staged row-major, 16-byte chunk k of a row at position k ^ (row % (D/8)),
       // so the 32 rows a warp writes at once hit distinct banks
       const int swz_mask = D / 8 - 1;
-      unsigned char *srow = gbase + L::kStaging + (size_t)(t * kTcBM + rl) * D * 2;
-#pragma unroll
+      unsigned char *srow = gbase + L::kStaging + (size_t)(tr * kTcBM + rl) * D * 2;
+#pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {  // pass 2: scale, round to fp16, stage
         uint32_t o[32];
-        tmem_ld32(tO + lane_off + c * 32, o);
+        tmem_ld32(tO + c * 32, o);
         tmem_wait_ld();
 #pragma unroll
         for (int q8 = 0; q8 < 4; ++q8) {
@@ -904,14 +1038,14 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
           *reinterpret_cast<uint4 *>(srow + (((c * 4 + q8) ^ (rl & swz_mask)) << 4)) = v;
         }
       }
-      const size_t prow = ((size_t)z * p.splits + split) * p.rows_pad + rt * kTcRows + t * kTcBM + rl;
-      p.part_ml[prow] = make_float4(m_use, l_sum, cs, 0.f);
+      const size_t prow = ((size_t)z * p.splits + split) * p.rows_pad + rt * kTcRows + tr * kTcBM + rl;
+      p.part_ml[prow] = make_float4(m_use, l_ex, cs, 0.f);
       fence_proxy_async_smem();
     }
-    if (active) asm volatile("bar.sync 1, %0;\n" ::"r"(nthr) : "memory");
+    if (writer) asm volatile("bar.sync 1, %0;\n" ::"r"(nwr) : "memory");
     if (all_ok && warp == 2 && lane == 0) {
       const size_t row0 = ((size_t)z * p.splits + split) * p.rows_pad + rt * kTcRows;
-      bulk_store(p.part_o + row0 * D, base + L::kStaging, (uint32_t)(nthr * D * 2));
+      bulk_store(p.part_o + row0 * D, base + L::kStaging, (uint32_t)(nwr * D * 2));
       bulk_wait_read();
     }
   }
@@ -1042,12 +1176,12 @@ AttnPlan plan_attn(int B, int N_max, int Hq, int Hkv, int D, int max_slots) {
   long best_s = 1;
   if (a.impl == 0) {
     // one resident block per SM: estimated time = waves x (tiles per block +
-    // a fixed cost of about eight 64-key tiles for the prologue and partials)
+    // a fixed cost of about four 128-key tiles for the prologue and partials)
     double best_t = 1e30;
     for (long s = 1; s <= max_tiles && s <= 32; ++s) {
       const long waves = (units * s + nsm - 1) / nsm;
       const long per = (max_tiles + s - 1) / s;
-      const double t = (double)waves * (double)(per + 8);
+      const double t = (double)waves * (double)(per + 4);
       if (t < best_t - 1e-9) {
         best_t = t;
         best_s = s;
@@ -1107,15 +1241,15 @@ template <int D>
 int launch_attn(AttnParams &p, const AttnPlan &a, int B, int num_blocks, cudaStream_t s) {
   dim3 grid(p.row_tiles, p.splits, B * p.Hkv);
   if (a.impl == 0) {
-    CUtensorMap k1, k4, v1, v4;
+    CUtensorMap k1, k8, v1, v8;
     if (!make_cache_map(&k1, p.k, num_blocks, p.Hkv, D, 1) ||
-        !make_cache_map(&k4, p.k, num_blocks, p.Hkv, D, kTcBN / kPage) ||
+        !make_cache_map(&k8, p.k, num_blocks, p.Hkv, D, kTcPagesPerTile) ||
         !make_cache_map(&v1, p.v, num_blocks, p.Hkv, D, 1) ||
-        !make_cache_map(&v4, p.v, num_blocks, p.Hkv, D, kTcBN / kPage))
+        !make_cache_map(&v8, p.v, num_blocks, p.Hkv, D, kTcPagesPerTile))
       return TSD_ERR_CUDA;
     if (!set_smem((const void *)tree_attn_split_tc<D>, TcLayout<D>::kAlloc)) return TSD_ERR_CUDA;
-    if (launch(tree_attn_split_tc<D>, grid, dim3(kTcThreads), TcLayout<D>::kAlloc, s, p, k1, k4, v1,
-               v4) != cudaSuccess)
+    if (launch(tree_attn_split_tc<D>, grid, dim3(kTcThreads), TcLayout<D>::kAlloc, s, p, k1, k8, v1,
+               v8) != cudaSuccess)
       return TSD_ERR_CUDA;
   } else {
     const size_t smem = (size_t)(kBM + 4 * kBN) * D * 2;
