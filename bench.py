@@ -39,6 +39,7 @@ import gen  # noqa: E402
 
 METRIC = "tree-verify steps/s (attn+accept+commit) and achieved HBM GB/s vs GB300 peak"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 FLUSH_BYTES = 256 << 20
 DESCRIPTIONS = {
     "tiny": "tiny verify layer: B=1, Hq=Hkv=4, D=64, prefix 128, 15-node random tree, V=1000",
@@ -74,6 +75,38 @@ def algorithmic_bytes(inp, moved_total):
     a4 = 8 * Hkv * D * int(moved_total)
     return {"tree_build_ancestors": a1, "tree_attn_fwd": a2, "tree_verify_greedy": a3,
             "kv_commit_path": a4}
+
+
+def tree_depths(parent_row, n):
+    """Depth of every node of one parent array (root depth 0)."""
+    d = np.zeros(n, dtype=np.int64)
+    for i in range(n):
+        j, k = i, 0
+        while parent_row[j] >= 0:
+            j = int(parent_row[j])
+            k += 1
+        d[i] = k
+    return d
+
+
+def attention_flops(inp):
+    """Algorithmic FLOPs of one tree_attn_fwd launch: each (node, q head) row
+    takes a D-long dot product and a D-long weighted sum (2 FLOPs per
+    multiply-add each) over the keys it sees, its prefix plus its ancestor
+    path (itself included)."""
+    keys = 0
+    for b in range(inp.B):
+        nb = int(inp.n_nodes[b])
+        keys += int(inp.prefix_len[b]) * nb + int((tree_depths(inp.parent[b], nb) + 1).sum())
+    return 4.0 * inp.D * inp.Hq * keys
+
+
+def load_tensor_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback (1.9 PFLOP/s bf16 burst, one earlier GB300 measurement)"
 
 
 def load_peaks():
@@ -442,6 +475,13 @@ def gpu_arm(args, rank, world):
     step_bytes = sum(abytes.values())
     dom = max(["tree_attn_fwd", "tree_verify_greedy"], key=lambda n: kernel_us[n])
     achieved = abytes[dom] / (kernel_us[dom] * 1e-6) / 1e9
+    attn_flops = attention_flops(inp)
+    tc_peak, tc_src = load_tensor_peak()
+    attn_tflops = attn_flops / (kernel_us["tree_attn_fwd"] * 1e-6) / 1e12
+    # the attention's binding roof: HBM when its bytes take longer at peak
+    # bandwidth than its FLOPs at peak tensor throughput, else the tensor pipe
+    tensor_bound = dom == "tree_attn_fwd" and (attn_flops / (tc_peak * 1e12)
+                                               > abytes[dom] / (peak * 1e9))
     kernels = {}
     for n in names:
         entry = {"us": round(kernel_us[n], 3)}
@@ -473,10 +513,21 @@ def gpu_arm(args, rank, world):
                    "attention_kernel": "tcgen05" if args.attn_kernel == "tc" else "mma.sync"},
         "hbm_gbs_step": round(step_bytes / (ms_per_step * 1e-3) / 1e9, 1),
         "kernels": kernels,
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
-                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": ncu_traffic(dom, args.workload), "peak_source": peak_src,
-                     "algorithmic_bytes_per_launch": abytes[dom]},
+        "roofline": ({"bound": "tensor", "kernel": dom, "achieved": round(attn_tflops, 1),
+                      "peak": tc_peak, "unit": "TFLOP/s", "frac": round(attn_tflops / tc_peak, 4),
+                      "traffic": ncu_traffic(dom, args.workload), "peak_source": tc_src,
+                      "algorithmic_flops_per_launch": attn_flops,
+                      "algorithmic_bytes_per_launch": abytes[dom],
+                      "hbm_frac": round(achieved / peak, 4)}
+                     if tensor_bound else
+                     {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
+                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                      "traffic": ncu_traffic(dom, args.workload), "peak_source": peak_src,
+                      "algorithmic_bytes_per_launch": abytes[dom],
+                      "algorithmic_flops_per_launch": attn_flops if dom == "tree_attn_fwd" else None,
+                      "tensor_frac": (round(attn_tflops / tc_peak, 4)
+                                      if dom == "tree_attn_fwd" else None)}),
+        "attention_tflops": round(attn_tflops, 1),
         "e2e": {"value": round(whole_job_rate(e2e_ms, world), 2), "unit": "steps/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4)},
@@ -486,10 +537,6 @@ def gpu_arm(args, rank, world):
         "kernel_sum_us": round(sum(kernel_us.values()), 3),
         "mean_accept_len": float(A.float().mean().item()),
     }
-    if args.workload == "70b":
-        # tensor-pipe bound on this shape: report the binding roofline too
-        flops = 4.0 * Hq * D * N * float(inp.prefix_len.astype(np.int64).sum())
-        result["attention_tflops"] = round(flops / (kernel_us["tree_attn_fwd"] * 1e-6) / 1e12, 1)
     return result
 
 
