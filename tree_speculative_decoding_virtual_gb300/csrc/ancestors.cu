@@ -6,10 +6,12 @@
 // table is precomputed; range, acyclicity and validity-closure checks run
 // before the fused kernels.
 //
-// One thread block per sequence, one thread per node.  The parent array is
-// staged in shared memory; each node walks up to the root (at most N_b
-// steps, which also detects cycles), and the ancestor rows are assembled in
-// shared memory and written out with coalesced stores.
+// One thread block per sequence, one thread per node, two barriers: the
+// parent array is staged in shared memory; then each node checks its own
+// parent (root, range, closure) and walks up to the root (at most N_b
+// steps, which also detects cycles), writing its ancestor row and bitmask
+// row into shared memory as it goes; then the rows are written out with
+// coalesced stores (all zero when the sequence is flagged).
 
 #include "tsd_common.cuh"
 
@@ -25,7 +27,8 @@ ancestors_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict__
                  int32_t *__restrict__ err) {
   __shared__ int s_par[kMaxNodes];
   __shared__ int s_depth[kMaxNodes];
-  __shared__ int s_err;
+  __shared__ uint32_t s_mask[kMaxNodes * (kMaxNodes / 32)];
+  __shared__ int s_serr, s_werr;
   extern __shared__ int s_anc[];  // [(N_max + 1) * (D_max + 1)]
 
   pdl_trigger();
@@ -36,84 +39,73 @@ ancestors_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict__
   const int nb = n_nodes ? n_nodes[b] : N_max;
   const bool count_ok = nb >= 1 && nb <= N_max;
 
-  if (t == 0) s_err = count_ok ? 0 : TSD_TREE_COUNT;
+  if (t == 0) {
+    s_serr = count_ok ? 0 : TSD_TREE_COUNT;
+    s_werr = 0;
+  }
   for (int i = t; i < N_max; i += kThreads) s_par[i] = parent[(size_t)b * N_max + i];
   for (int x = t; x < (N_max + 1) * cols; x += kThreads) s_anc[x] = 0;
+  for (int x = t; x < N_max * W; x += kThreads) s_mask[x] = 0u;
   __syncthreads();
 
-  // structural checks: root sentinel, range, closure
   if (count_ok) {
-    int e = 0;
+    int se = 0, we = 0;
     for (int i = t; i < nb; i += kThreads) {
+      // structural checks of this node's own parent: root sentinel, range, closure
       const int p = s_par[i];
       if (i == 0) {
-        if (p != -1) e |= TSD_TREE_ROOT;
+        if (p != -1) se |= TSD_TREE_ROOT;
       } else if (p < 0 || p >= N_max) {
-        e |= TSD_TREE_RANGE;
+        se |= TSD_TREE_RANGE;
       } else if (p >= nb) {
-        e |= TSD_TREE_CLOSURE;
+        se |= TSD_TREE_CLOSURE;
       }
-    }
-    if (e) atomicOr(&s_err, e);
-  }
-  __syncthreads();
-
-  // walk to the root: depth, cycle and depth checks
-  if (s_err == 0) {
-    int e = 0;
-    for (int i = t; i < nb; i += kThreads) {
+      // walk to the root: depth, cycle and depth checks (a parent outside
+      // [0, nb) on the way is some node's structural error; stop there)
       int j = i, steps = 0;
-      bool cycle = false;
+      bool cycle = false, broken = false;
       while (s_par[j] != -1) {
         if (steps == nb) {
           cycle = true;
           break;
         }
-        j = s_par[j];
+        const int pj = s_par[j];
+        if (pj < 0 || pj >= nb) {
+          broken = true;
+          break;
+        }
+        j = pj;
         ++steps;
       }
-      s_depth[i] = steps;
       if (cycle)
-        e |= TSD_TREE_CYCLE;
-      else if (steps > D_max)
-        e |= TSD_TREE_TOO_DEEP;
-    }
-    if (e) atomicOr(&s_err, e);
-  }
-  __syncthreads();
-  const int eb = s_err;
-
-  // ancestor rows in safe ids: row i+1, column d = safe id of the depth-d ancestor
-  if (eb == 0) {
-    for (int i = t; i < nb; i += kThreads) {
-      int j = i;
-      for (int d = s_depth[i]; d >= 0; --d) {
-        s_anc[(i + 1) * cols + d] = j + 1;
-        j = s_par[j];
-      }
-    }
-  }
-  __syncthreads();
-
-  int32_t *anc_b = anc + (size_t)b * (N_max + 1) * cols;
-  for (int x = t; x < (N_max + 1) * cols; x += kThreads) anc_b[x] = s_anc[x];
-
-  for (int i = t; i < N_max; i += kThreads) {
-    const bool valid = eb == 0 && i < nb;
-    const int d = valid ? s_depth[i] : 0;
-    depth_out[(size_t)b * N_max + i] = d;
-    uint32_t *mrow = mask + ((size_t)b * N_max + i) * W;
-    for (int w = 0; w < W; ++w) {
-      uint32_t bits = 0;
-      if (valid) {
-        for (int k = 0; k <= d; ++k) {
-          const int a = s_anc[(i + 1) * cols + k] - 1;
-          if ((a >> 5) == w) bits |= 1u << (a & 31);
+        we |= TSD_TREE_CYCLE;
+      else if (!broken && steps > D_max)
+        we |= TSD_TREE_TOO_DEEP;
+      s_depth[i] = steps;
+      if (!cycle && !broken && steps <= D_max) {
+        // ancestor row in safe ids (column d = the depth-d ancestor) and bitmask
+        int a = i;
+        for (int d = steps; d >= 0; --d) {
+          s_anc[(i + 1) * cols + d] = a + 1;
+          s_mask[i * W + (a >> 5)] |= 1u << (a & 31);
+          a = s_par[a];
         }
       }
-      mrow[w] = bits;
     }
+    if (se) atomicOr(&s_serr, se);
+    if (we) atomicOr(&s_werr, we);
   }
+  __syncthreads();
+  // range, closure and root errors are reported alone; cycle and depth
+  // errors only when those are clear
+  const int eb = s_serr ? s_serr : s_werr;
+
+  int32_t *anc_b = anc + (size_t)b * (N_max + 1) * cols;
+  for (int x = t; x < (N_max + 1) * cols; x += kThreads) anc_b[x] = eb ? 0 : s_anc[x];
+  for (int i = t; i < N_max; i += kThreads)
+    depth_out[(size_t)b * N_max + i] = (eb == 0 && i < nb) ? s_depth[i] : 0;
+  uint32_t *mask_b = mask + (size_t)b * N_max * W;
+  for (int x = t; x < N_max * W; x += kThreads) mask_b[x] = (eb == 0 && x < nb * W) ? s_mask[x] : 0u;
   if (t == 0) err[b] = eb;
 }
 
