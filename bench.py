@@ -245,12 +245,17 @@ def oracle_sample_fraction(name):
     return {"tiny": 1.0, "8b": 0.125, "ragged": 0.05, "70b": 0.004}.get(name, 0.05)
 
 
-def cpu_baseline(name, budget_steps=3):
+def cpu_baseline(name, budget_steps=3, single_thread=True):
     threads = os.cpu_count() or 1
     frac = oracle_sample_fraction(name)
     res = run_oracle_child(name, budget_steps, frac, threads)
     value = 1.0 / res["sec_per_full_step"]
+    one = None
+    if single_thread:
+        r1 = run_oracle_child(name, 1, frac, 1)
+        one = {"value": 1.0 / r1["sec_per_full_step"], "unit": "steps/s", "cores": 1}
     return {"value": value, "unit": "steps/s", "cores": threads, "kind": "oracle",
+            "single_thread": one,
             "sample": "%d oracle steps of the %s workload; each runs ancestors, verify and commit "
                       "in full and attention on %d of %d (seq, node, q-head) rows, scaled to the "
                       "full row count" % (res["steps"], name, res["sample_rows"],
@@ -439,6 +444,30 @@ def gpu_arm(args, rank, world):
             per_kernel[n] += e[j].elapsed_time(e[j + 1])
     kernel_us = {n: 1000.0 * v / args.steps for n, v in per_kernel.items()}
 
+    # ---- a4 layer-stacked: the step's accepted paths committed into L layers'
+    # caches in one launch (bandwidth is only meaningful this way; per layer the
+    # commit moves a few KB).  L = 80, or fewer when 80 layers of this cache
+    # would take more than 4 GB.
+    layer_bytes = 2 * kc.numel() * kc.element_size()
+    n_layers = int(max(1, min(80, (4 << 30) // max(layer_bytes, 1))))
+    kL = kc.unsqueeze(0).repeat(n_layers, 1, 1, 1, 1)
+    vL = vc.unsqueeze(0).repeat(n_layers, 1, 1, 1, 1)
+    stacked = lambda: tsd.kv_commit_path(kL, vL, table, prefix, n_nodes, A, path, err, N, Dm,
+                                         new_len=new_len, moved=moved, status=status)
+    stacked()
+    g_stacked = capture(stacked)
+    torch.cuda.synchronize()
+    sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(max(3, min(args.steps, 200)))]
+    for a_, b_ in sev:
+        flush_l2()
+        a_.record(stream)
+        g_stacked.replay()
+        b_.record(stream)
+    torch.cuda.synchronize()
+    stacked_us = 1000.0 * sum(a_.elapsed_time(b_) for a_, b_ in sev) / len(sev)
+    del kL, vL, g_stacked
+
     # ---- e2e: host buffers through the public API, copies inside the timing ----
     h_in = {"q": q, "logits": logits, "parent": parent, "tokens": tokens, "n_nodes": n_nodes,
             "prefix_len": prefix}
@@ -536,6 +565,12 @@ def gpu_arm(args, rank, world):
         "wall_s_timed_region": round(t_wall, 4),
         "kernel_sum_us": round(sum(kernel_us.values()), 3),
         "mean_accept_len": float(A.float().mean().item()),
+        "commit_layer_stacked": {
+            "layers": n_layers, "us": round(stacked_us, 3),
+            "algorithmic_bytes": abytes["kv_commit_path"] * n_layers,
+            "gbs": round(abytes["kv_commit_path"] * n_layers / (stacked_us * 1e-6) / 1e9, 1),
+            "frac_of_hbm_peak": round(abytes["kv_commit_path"] * n_layers
+                                      / (stacked_us * 1e-6) / 1e9 / peak, 4)},
     }
     return result
 
