@@ -14,8 +14,9 @@ Sources, cited by page title and section:
 * [EP-pt] the same paper's Portuguese technical summary
   (gist.science/pt/paper/2603.08088), section 2 "Metodologia e Arquitetura".
 * [BASTION] "Resumo Técnico: BASTION" (gist.science/pt/paper/2605.29727),
-  Methodology 1 (block-diffusion drafting, path score) and 2 (acceptance
-  surrogate and best-first expansion).
+  Methodology 1 (block-diffusion drafting, path score), 2 (acceptance
+  surrogate and best-first expansion) and 3 (hardware-aware online budget
+  controller).
 * [Blog] "Speculative Decoding Hierárquico: Medusa, EAGLE-2 e Multi-Token
   Prediction" (produtoramaxvision.com.br): sections on modified rejection
   sampling, the speed-up model and Medusa tree attention.
@@ -37,6 +38,7 @@ from .verify import verify_greedy
 from .commit import commit_path
 from .best_first import best_first_tree, ranked_tokens
 from .rejection import modified_rejection_step, residual_distribution
+from .budget import verify_step_cost, calibrate, budget_select, cost_table
 
 __all__ = [
     "ERR_RANGE", "ERR_CYCLE", "ERR_TOO_DEEP", "ERR_CLOSURE", "ERR_ROOT", "ERR_COUNT",
