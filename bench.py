@@ -575,6 +575,197 @@ def gpu_arm(args, rank, world):
     return result
 
 
+def budget_arm(args, rank, world):
+    """BASTION's online tree budget on its own workload (B=8 marginals over
+    16 positions, verify on the 8B-shaped layer with prefix 2048): the verify
+    step (a1-a4) is timed at N = 16..256, a roofline cost model is calibrated
+    on those times, and the budgeted step runs best-first construction at 256
+    nodes, the device-side choice of each sequence's size, and a1-a4 on the
+    chosen prefixes of the trees, all on one stream."""
+    import torch
+    import torch.distributed as dist
+
+    import tree_speculative_decoding_virtual_gb300 as tsd
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    hbm, hbm_src, _ = load_peaks()
+    tc, tc_src = load_tensor_peak()
+    q_m, root = gen.bastion_marginals()
+    c = gen.BASTION
+    qd, rootd = torch.from_numpy(q_m).to(dev), torch.from_numpy(root).to(dev)
+    flush = torch.empty((FLUSH_BYTES,), dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones((FLUSH_BYTES // 8,), dtype=torch.int64, device=dev)
+
+    def flush_l2():
+        flush.zero_()
+        flush_rd.sum()
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            fn()
+        torch.cuda.current_stream().wait_stream(side)
+        with torch.cuda.graph(g):
+            fn()
+        return g
+
+    def timed(g, reps):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)]
+        for a_, b_ in ev:
+            flush_l2()
+            a_.record(stream)
+            g.replay()
+            b_.record(stream)
+        torch.cuda.synchronize()
+        return 1000.0 * sum(a_.elapsed_time(b_) for a_, b_ in ev) / reps
+
+    def verify_setup(N):
+        """Best-first tree of N nodes on the GPU, the verify inputs built on it,
+        and the a1-a4 calls on device buffers."""
+        bf_ws = torch.empty(tsd.best_first_workspace_bytes(*q_m.shape, N), dtype=torch.uint8,
+                            device=dev)
+        outs = [torch.empty((c["B"], N), dtype=torch.int32, device=dev) for _ in range(3)]
+        rho = torch.empty((c["B"], N), dtype=torch.float32, device=dev)
+        ahat = torch.empty((c["B"],), dtype=torch.float64, device=dev)
+        bf = lambda: tsd.best_first_tree_build(qd, rootd, N, *outs, rho, ahat, workspace=bf_ws)
+        bf()
+        torch.cuda.synchronize()
+        par_h, tok_h, dep_h = [x.cpu().numpy() for x in outs]
+        top1 = np.argmax(q_m, axis=-1)  # input synthesis only: plants target choices
+        inp = gen.bastion_verify_inputs(par_h, tok_h, dep_h, top1)
+        T = lambda a, dt=None: (torch.from_numpy(np.ascontiguousarray(a)).view(dt)
+                                if dt is not None else torch.from_numpy(np.ascontiguousarray(a))).to(dev)
+        Bq, Nq, Hq, Hkv, D, V, Dm = inp.B, inp.N_max, inp.Hq, inp.Hkv, inp.D, inp.V, inp.D_max
+        d = dict(parent=T(inp.parent), n_nodes=T(inp.n_nodes), prefix=T(inp.prefix_len),
+                 tokens=T(inp.tokens), logits=T(inp.logits), q=T(inp.q, torch.bfloat16),
+                 table=T(inp.cache.block_table), kc=T(inp.cache.k, torch.bfloat16),
+                 vc=T(inp.cache.v, torch.bfloat16))
+        max_slots = int((inp.prefix_len + N).max())
+        W = (Nq + 31) // 32
+        i32 = dict(dtype=torch.int32, device=dev)
+        anc = torch.empty((Bq, Nq + 1, Dm + 1), **i32)
+        depth = torch.empty((Bq, Nq), **i32)
+        mask = torch.empty((Bq, Nq, W), **i32)
+        err = torch.empty((Bq,), **i32)
+        out = torch.empty((Bq, Nq, Hq, D), dtype=torch.bfloat16, device=dev)
+        attn_ws = torch.empty((tsd.tree_attn_workspace_bytes(Bq, Nq, Hq, Hkv, D, max_slots),),
+                              dtype=torch.uint8, device=dev)
+        ver_ws = torch.zeros((tsd.tree_verify_workspace_bytes(Bq, Nq, V),), dtype=torch.uint8,
+                             device=dev)
+        am = torch.empty((Bq, Nq), **i32)
+        A = torch.empty((Bq,), **i32)
+        leaf = torch.empty((Bq,), **i32)
+        path = torch.empty((Bq, Dm + 1), **i32)
+        bonus = torch.empty((Bq,), **i32)
+        new_len = torch.empty((Bq,), **i32)
+        moved = torch.empty((Bq,), **i32)
+        status = torch.zeros((1,), **i32)
+
+        def verify(n_nodes=None):
+            nn_ = d["n_nodes"] if n_nodes is None else n_nodes
+            tsd.tree_build_ancestors(d["parent"], nn_, Dm, anc, depth, mask, err)
+            tsd.tree_attn_fwd(d["q"], d["kc"], d["vc"], d["table"], d["prefix"], nn_, mask, err,
+                              max_slots, out=out, workspace=attn_ws, status=status)
+            tsd.tree_verify_greedy(d["logits"], d["tokens"], d["parent"], anc, depth, mask, nn_,
+                                   err, Dm, am, A, leaf, path, bonus, workspace=ver_ws)
+            tsd.kv_commit_path(d["kc"], d["vc"], d["table"], d["prefix"], nn_, A, path, err, Nq,
+                               Dm, new_len=new_len, moved=moved, status=status)
+        return inp, bf, rho, verify, status
+
+    reps = max(3, min(args.steps, 100))
+    Ns = [16, 32, 64, 128, 256]
+    t_verify, t_roof, t_bf = {}, {}, {}
+    keep = None
+    for N in Ns:
+        inp, bf, rho, verify, status = verify_setup(N)
+        for _ in range(args.warmup):
+            verify()
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        t_verify[N] = timed(capture(verify), reps)
+        t_bf[N] = timed(capture(bf), reps)
+        t_roof[N] = tsd.verify_step_cost(inp.B, inp.Hq, inp.Hkv, inp.D, inp.prefix_len, inp.V,
+                                         inp.D_max, N, hbm, tc)[2]
+        if N == Ns[-1]:
+            keep = (inp, bf, rho, verify, status)
+    alpha, beta = tsd.budget_calibrate([t_roof[N] for N in Ns], [t_verify[N] for N in Ns])
+    inp, bf, rho, verify, status = keep
+    n_max = Ns[-1]
+    roof_of = lambda n: tsd.verify_step_cost(inp.B, inp.Hq, inp.Hkv, inp.D, inp.prefix_len, inp.V,
+                                             min(16, max(n - 1, 0)), n, hbm, tc)[2]
+    t_draft = t_bf[n_max]          # the tree construction; the drafter's own pass is not modelled
+    l_ar = alpha * roof_of(1) + beta  # a 1-node tree is a plain decode step
+    cost_h = np.array([t_draft + alpha * roof_of(max(n, 1)) + beta for n in range(n_max + 1)])
+    cost = torch.from_numpy(cost_h.astype(np.float32)).to(dev)
+    n_opt = torch.empty((inp.B,), dtype=torch.int32, device=dev)
+    s_opt = torch.empty((inp.B,), dtype=torch.float32, device=dev)
+
+    def budgeted_step():
+        bf()
+        tsd.budget_select(rho, cost, l_ar, n_opt, s_opt)
+        verify(n_opt)
+
+    for _ in range(args.warmup):
+        budgeted_step()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    g_step = capture(budgeted_step)
+    g_sel = capture(lambda: tsd.budget_select(rho, cost, l_ar, n_opt, s_opt))
+    sampler = ClockSampler(local) if rank == 0 else None
+    if world > 1:
+        dist.barrier()
+    ms = max_over_ranks(timed(g_step, args.steps) / 1000.0, world, dev)
+    clocks = sampler.stop() if sampler else None
+    sel_us = timed(g_sel, reps)
+    n_h = n_opt.cpu().numpy()
+    if rank != 0:
+        return None
+    model = {N: alpha * t_roof[N] + beta for N in Ns}
+    step_bytes = sum(tsd.verify_step_cost(1, inp.Hq, inp.Hkv, inp.D, [int(inp.prefix_len[b])],
+                                          inp.V, inp.D_max, int(n_h[b]), hbm, tc)[0]
+                     for b in range(inp.B)) + 4.0 * q_m.size
+    return {
+        "metric": METRIC,
+        "value": round(whole_job_rate(ms, world), 2),
+        "unit": "steps/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp32 marginals, path scores and budget choice; bf16 attention; f32 logits",
+        "data": "synthetic (seeded; shapes and distributions of the named workload)",
+        "config": {"workload": "BASTION-style budgeted step: B=8, K=16, V=32000 marginals, "
+                               "best-first at 256 nodes, online size choice, verify on Hq=32, "
+                               "Hkv=8, D=128, prefix 2048", "name": "bastion-budget",
+                   "global_batch": inp.B * world, "parallelism": "replicas (dp%d)" % world,
+                   "l2": "flushed between timed steps (256 MiB write, 256 MiB read)"},
+        "budget": {"N": Ns, "t_verify_us": [round(t_verify[N], 3) for N in Ns],
+                   "t_roofline_us": [round(t_roof[N], 3) for N in Ns],
+                   "t_model_us": [round(model[N], 3) for N in Ns],
+                   "alpha": alpha, "beta_us": beta, "t_draft_us": round(t_draft, 3),
+                   "l_ar_us": round(l_ar, 3), "n_opt": n_h.tolist(),
+                   "s_opt": [round(float(x), 4) for x in s_opt.cpu().numpy()],
+                   "select_us": round(sel_us, 3),
+                   "peaks": {"hbm_gbs": hbm, "hbm_source": hbm_src, "bf16_tflops": tc,
+                             "tensor_source": tc_src}},
+        "roofline": {"bound": "hbm", "kernel": "whole budgeted step",
+                     "achieved": round(step_bytes / (ms * 1e-3) / 1e9, 1), "peak": hbm,
+                     "unit": "GB/s", "frac": round(step_bytes / (ms * 1e-3) / 1e9 / hbm, 4),
+                     "traffic": None, "peak_source": hbm_src},
+        "gpu_launches": 8 * args.steps,
+        "clocks": clocks,
+    }
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -603,7 +794,7 @@ def main(argv=None):
     base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.workload.startswith("bastion"):
         base = cpu_baseline(args.workload)
-    res = gpu_arm(args, rank, world)
+    res = (budget_arm if args.workload == "bastion-budget" else gpu_arm)(args, rank, world)
     if rank == 0:
         res["cpu_baseline"] = base
         print(json.dumps(res), flush=True)

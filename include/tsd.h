@@ -284,6 +284,47 @@ int tsd_best_first_tree_build(const float *q, const int32_t *root_token, int B, 
                               int32_t *parent, int32_t *tokens, int32_t *depth, float *rho,
                               double *ahat, void *workspace, size_t ws_bytes, tsd_stream_t stream);
 
+/*
+ * Tree budget ([BASTION] Methodology 3, hardware-aware online budget
+ * controller): T_verify(N) from a roofline model of bandwidth and compute,
+ * calibrated with measured step times; the tree grows until
+ * S(N) = A_hat(T_N) * L_AR / C(N) starts to decrease.
+ *
+ * tsd_verify_step_cost (host only, no GPU work): algorithmic bytes and FLOPs
+ * of one verify step (ancestor tables, attention over prefix and tree, logits,
+ * at most D_max moved entries per sequence) for N-node trees, and its roofline
+ * time max(bytes / BW, flops / TC) in microseconds.  prefix_len is a HOST
+ * array of B lengths; hbm_gbs in GB/s, tc_tflops in TFLOP/s.  Any output
+ * pointer may be NULL.  TSD_ERR_ARG on a non-positive size or peak.
+ *
+ * tsd_budget_calibrate (host only): least-squares line
+ * t_meas ~ alpha * t_roof + beta over `count` >= 2 HOST points; TSD_ERR_ARG
+ * without two distinct roofline times.
+ *
+ * tsd_budget_select (device, fp32 throughout): for every sequence, with A_hat(n)
+ * the fp32 running sum in insertion order of rho[b][1..n-1] (the non-root
+ * nodes among the first n) and S(n) = A_hat(n) * l_ar / cost[n], n_opt[b] =
+ * the largest n with S(1) <= ... <= S(n) (N_max when S never decreases),
+ * where S(n) < S(n-1) is tested as A_hat(n) * cost[n-1] < A_hat(n-1) * cost[n]
+ * with fp32 products; s_opt[b] = fl32(fl32(A_hat(n_opt) * l_ar) / cost[n_opt]).
+ *   rho    float [B][N_max] device, path scores in best-first insertion order
+ *          (as tsd_best_first_tree_build writes them);
+ *   cost   float [N_max + 1] device, cost[n] = C(n) = T_draft + T_verify(n)
+ *          > 0 for n = 1..N_max (entry 0 unused);
+ *   l_ar   > 0, the latency of one autoregressive step, in cost's unit;
+ *   n_opt  int32 [B] out; s_opt float [B] out or NULL.
+ * 1 <= N_max <= 256 and B <= 65535, else TSD_ERR_LIMIT.  The first n_opt[b]
+ * nodes of a best-first tree form a tree (parents come first), so n_opt can
+ * be passed on as n_nodes.
+ */
+int tsd_verify_step_cost(int B, int Hq, int Hkv, int D, const int32_t *prefix_len, int V,
+                         int D_max, int N, double hbm_gbs, double tc_tflops, double *bytes,
+                         double *flops, double *t_us);
+int tsd_budget_calibrate(const double *t_roof, const double *t_meas, int count, double *alpha,
+                         double *beta);
+int tsd_budget_select(const float *rho, int B, int N_max, const float *cost, float l_ar,
+                      int32_t *n_opt, float *s_opt, tsd_stream_t stream);
+
 #ifdef __cplusplus
 } /* extern "C" */
 #endif

@@ -22,7 +22,10 @@ Readings taken where the page is silent:
   inserted (best-first insertion order), accumulated in fp64 in that order.
 * "Starts to decrease": the chosen N is the largest n such that
   S(1) <= S(2) <= ... <= S(n) (equal values do not stop the growth); when S
-  never decreases, the whole budget.
+  never decreases, the whole budget.  The choice is taken in fp32: A_hat is
+  an fp32 running sum in insertion order, and S(n) < S(n-1) is tested as
+  A_hat(n) * C(n-1) < A_hat(n-1) * C(n) (L_AR > 0 cancels), each product
+  rounded to fp32; S at the chosen n is (A_hat * L_AR) / C, in fp32.
 """
 
 from __future__ import annotations
@@ -67,31 +70,31 @@ def calibrate(t_roof, t_meas):
 def budget_select(rho, cost, l_ar):
     """rho: [B][N_max] path scores in insertion order (rho[b][0] is the root);
     cost: [N_max + 1] with cost[n] = C(n) > 0 for n = 1..N_max; l_ar: L_AR.
-    Returns (n_opt int32 [B], s_opt float64 [B])."""
-    rho = np.asarray(rho, dtype=np.float32)
-    cost = np.asarray(cost, dtype=np.float64)
+    Returns (n_opt int32 [B], s_opt float32 [B])."""
+    f32 = np.float32
+    rho = np.asarray(rho, dtype=f32)
+    cost = np.asarray(cost, dtype=f32)
+    l_ar = f32(l_ar)
     B, n_max = rho.shape
     n_opt = np.zeros(B, dtype=np.int32)
-    s_opt = np.zeros(B, dtype=np.float64)
+    s_opt = np.zeros(B, dtype=f32)
     for b in range(B):
-        a_hat = 0.0
-        s_prev = a_hat * float(l_ar) / float(cost[1])
+        a_prev, c_prev = f32(0.0), cost[1]
         best = 1
         for n in range(2, n_max + 1):
-            a_hat += float(rho[b, n - 1])
-            s = a_hat * float(l_ar) / float(cost[n])
-            if s < s_prev:
+            a = f32(a_prev + rho[b, n - 1])
+            c = cost[n]
+            if f32(a * c_prev) < f32(a_prev * c):  # S(n) < S(n - 1)
                 break
-            s_prev = s
-            best = n
+            a_prev, c_prev, best = a, c, n
         n_opt[b] = best
-        s_opt[b] = s_prev
+        s_opt[b] = f32(f32(a_prev * l_ar) / c_prev)
     return n_opt, s_opt
 
 
 def cost_table(alpha, beta, t_draft, t_roof_of_n, n_max):
     """[n_max + 1] table of C(n) = t_draft + alpha * t_roof(n) + beta (entry 0
-    unused, set to C(1))."""
+    unused, set to C(1)), in fp64; the choice reads it rounded to fp32."""
     c = np.zeros(n_max + 1, dtype=np.float64)
     for n in range(1, n_max + 1):
         c[n] = float(t_draft) + float(alpha) * float(t_roof_of_n(n)) + float(beta)

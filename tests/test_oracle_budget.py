@@ -87,8 +87,8 @@ def test_budget_select_matches_exact_brute_force():
     rng = np.random.default_rng(11)
     for _ in range(200):
         n_max = int(rng.integers(1, 40))
-        # dyadic values: every sum and quotient below is exact in fp64 or
-        # compared only through an order that rounding cannot flip
+        # dyadic values with few significant bits: every sum and product the
+        # choice forms is exact in fp32, so it must match exact arithmetic
         rho = np.sort(rng.integers(0, 64, size=n_max) / 64.0)[::-1].astype(np.float32)
         rho[0] = 1.0
         cost = np.concatenate([[1.0], rng.integers(8, 512, size=n_max).astype(np.float64)])
@@ -97,7 +97,7 @@ def test_budget_select_matches_exact_brute_force():
         n_opt, s_opt = budget.budget_select(rho[None, :], cost, l_ar)
         n_ref, s_ref = _first_local_max_exact(rho, cost, l_ar)
         assert int(n_opt[0]) == n_ref
-        assert s_opt[0] == pytest.approx(float(s_ref), rel=1e-12)
+        assert s_opt[0] == pytest.approx(float(s_ref), rel=1e-6)
 
 
 def test_budget_select_closed_forms():

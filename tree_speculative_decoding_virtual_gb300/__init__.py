@@ -30,6 +30,7 @@ OPT_WAIT_LIMIT_NS, OPT_ATTN_KERNEL, OPT_TEST_STALL = 0, 1, 2
 
 # C signatures: (name, restype, argtypes)
 _P, _I, _I64, _SZ, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+_D = ctypes.c_double
 SIGNATURES = {
     "tsd_version": (ctypes.c_char_p, []),
     "tsd_set_option": (_I, [_I, _I64]),
@@ -48,6 +49,9 @@ SIGNATURES = {
                                 _I, _P, _P, _P, _P]),
     "tsd_best_first_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "tsd_best_first_tree_build": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "tsd_verify_step_cost": (_I, [_I, _I, _I, _I, _P, _I, _I, _I, _D, _D, _P, _P, _P]),
+    "tsd_budget_calibrate": (_I, [_P, _P, _I, _P, _P]),
+    "tsd_budget_select": (_I, [_P, _I, _I, _P, _F, _P, _P, _P]),
 }
 
 
@@ -285,6 +289,53 @@ def best_first_tree_build(q, root_token, N, parent=None, tokens=None, depth=None
         workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "best_first_tree_build")
     return parent, tokens, depth, rho, ahat
+
+
+# ---------------------------------------------------------------------------
+# tree budget
+# ---------------------------------------------------------------------------
+
+def verify_step_cost(B, Hq, Hkv, D, prefix_len, V, D_max, N, hbm_gbs, tc_tflops):
+    """Host-only: (bytes, flops, roofline microseconds) of one verify step with
+    N-node trees.  prefix_len: a sequence of B host integers."""
+    if len(prefix_len) != B:
+        raise TsdError("prefix_len must hold B lengths")
+    pl = (ctypes.c_int32 * B)(*[int(x) for x in prefix_len])
+    out = [ctypes.c_double(), ctypes.c_double(), ctypes.c_double()]
+    _check(lib.tsd_verify_step_cost(B, Hq, Hkv, D, ctypes.cast(pl, ctypes.c_void_p), V, D_max, N,
+                                    float(hbm_gbs), float(tc_tflops),
+                                    *[ctypes.cast(ctypes.byref(o), ctypes.c_void_p) for o in out]),
+           "verify_step_cost")
+    return tuple(o.value for o in out)
+
+
+def budget_calibrate(t_roof, t_meas):
+    """Host-only: least-squares (alpha, beta) of t_meas ~ alpha * t_roof + beta."""
+    n = len(t_roof)
+    x = (ctypes.c_double * n)(*[float(v) for v in t_roof])
+    y = (ctypes.c_double * n)(*[float(v) for v in t_meas])
+    a, b = ctypes.c_double(), ctypes.c_double()
+    _check(lib.tsd_budget_calibrate(ctypes.cast(x, ctypes.c_void_p), ctypes.cast(y, ctypes.c_void_p),
+                                    n, ctypes.cast(ctypes.byref(a), ctypes.c_void_p),
+                                    ctypes.cast(ctypes.byref(b), ctypes.c_void_p)),
+           "budget_calibrate")
+    return a.value, b.value
+
+
+def budget_select(rho, cost, l_ar, n_opt=None, s_opt=None, stream=None):
+    """rho float32 [B][N_max] (device), cost float32 [N_max + 1] (device).
+    Returns (n_opt int32 [B], s_opt float32 [B])."""
+    B, N_max = rho.shape
+    n_opt = n_opt if n_opt is not None else _empty((B,), torch.int32, rho)
+    s_opt = s_opt if s_opt is not None else _empty((B,), torch.float32, rho)
+    if cost.numel() != N_max + 1:
+        raise TsdError("cost must hold N_max + 1 entries")
+    _check(lib.tsd_budget_select(_ptr(rho, torch.float32, "rho"), B, N_max,
+                                 _ptr(cost, torch.float32, "cost"), float(l_ar),
+                                 _ptr(n_opt, torch.int32, "n_opt"),
+                                 _ptr(s_opt, torch.float32, "s_opt"), _stream(stream)),
+           "budget_select")
+    return n_opt, s_opt
 
 
 def set_option(key: int, value: int) -> None:

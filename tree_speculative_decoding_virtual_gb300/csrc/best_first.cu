@@ -8,13 +8,16 @@
 //
 // Kernel 1 (one block per (position, sequence)): the M = min(N-1, V) best
 // tokens of the position, ranked by (q desc, token id asc).  A 4-pass 8-bit
-// radix select finds the M-th largest key; the selection is gathered in
-// index order (deterministic) and bitonic-sorted in shared memory.
+// radix select finds the M-th largest key; the selection is gathered with
+// coalesced reads (its order does not matter) and bitonic-sorted in shared
+// memory by (q desc, index asc); ties at the threshold beyond the budget are
+// resolved in index order.
 // Kernel 2 (one block per sequence, one warp expanding): every inserted node
 // owns exactly one candidate, its best not-yet-inserted child (the next
 // rank at the next position); the child ranks of a node are consumed in
 // order because q is sorted.  Each step takes the best candidate with two
-// warp max-reductions (rho bits, then (depth, parent) as a tie key).
+// warp max-reductions (rho bits, then (depth, parent) as a tie key) over
+// candidate keys held in shared memory.
 
 #include "tsd_common.cuh"
 
@@ -31,40 +34,12 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Exclusive block scan of one unsigned per thread (blockDim.x == kTopThreads).
-__device__ unsigned block_excl_scan(unsigned v, unsigned *s_warp, unsigned *total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  unsigned x = v;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const unsigned y = __shfl_up_sync(0xffffffffu, x, off);
-    if (lane >= off) x += y;
-  }
-  if (lane == 31) s_warp[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    unsigned w = s_warp[lane];
-    unsigned z = w;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const unsigned y = __shfl_up_sync(0xffffffffu, z, off);
-      if (lane >= off) z += y;
-    }
-    s_warp[lane] = z - w;  // exclusive prefix of warp totals
-    if (lane == 31) *total = z;
-  }
-  __syncthreads();
-  const unsigned r = s_warp[warp] + x - v;
-  __syncthreads();
-  return r;
-}
-
 __global__ void __launch_bounds__(kTopThreads)
 topk_kernel(const float *__restrict__ q, int K, int V, int M, int32_t *__restrict__ top_tok,
             float *__restrict__ top_q) {
   __shared__ unsigned hist[256];
-  __shared__ unsigned s_prefix, s_remaining, s_total;
-  __shared__ unsigned s_warp[32];
+  __shared__ unsigned s_prefix, s_remaining, s_eq_total;
+  __shared__ unsigned s_ngt, s_neq;
   __shared__ unsigned long long s_sel[256];
 
   pdl_trigger();
@@ -107,6 +82,7 @@ topk_kernel(const float *__restrict__ q, int K, int V, int M, int32_t *__restric
         }
         s_prefix = prefix | ((unsigned)(255 - 8 * t - j) << shift);
         s_remaining = remaining - cum;
+        s_eq_total = c[j];  // after the last pass: the keys equal to T
       }
     }
     __syncthreads();
@@ -114,32 +90,44 @@ topk_kernel(const float *__restrict__ q, int K, int V, int M, int32_t *__restric
     remaining = s_remaining;
     pmask |= 0xFFu << shift;
   }
-  const unsigned T = prefix;
-  const unsigned need_eq = remaining;
-  const unsigned cnt_gt = (unsigned)M - need_eq;
+  const uint32_t T = prefix;
+  const unsigned need_eq = remaining;             // keys equal to T to take
+  const unsigned cnt_gt = (unsigned)M - need_eq;  // keys greater than T
+  // keys equal to T in the whole row (the last pass's bin count)
+  const bool all_eq = s_eq_total == need_eq;      // no excess ties at T
+  const int lane = t & 31, warp = t >> 5;
 
-  // gather in index order: contiguous segment per thread
-  const int seg = (V + kTopThreads - 1) / kTopThreads;
-  const int lo = min(V, t * seg), hi = min(V, lo + seg);
-  unsigned n_gt = 0u, n_eq = 0u;
-  for (int x = lo; x < hi; ++x) {
-    const uint32_t key = order_key(__ldg(row + x));
-    n_gt += key > T;
-    n_eq += key == T;
-  }
-  unsigned pos_gt = block_excl_scan(n_gt, s_warp, &s_total);
-  unsigned pos_eq = block_excl_scan(n_eq, s_warp, &s_total);
+  // gather: keys > T (and every key == T when all are taken) land in any
+  // order, the sort below orders them
   for (int x = t; x < 256; x += kTopThreads) s_sel[x] = 0ull;
+  if (t == 0) {
+    s_ngt = 0u;
+    s_neq = 0u;
+  }
   __syncthreads();
-  for (int x = lo; x < hi; ++x) {
-    const uint32_t key = order_key(__ldg(row + x));
+  auto take = [&](uint32_t key, int x) {
     const unsigned long long packed =
         ((unsigned long long)key << 32) | (unsigned long long)(0xFFFFFFFFu - (unsigned)x);
     if (key > T) {
-      s_sel[pos_gt++] = packed;
-    } else if (key == T) {
-      if (pos_eq < need_eq) s_sel[cnt_gt + pos_eq] = packed;
-      ++pos_eq;
+      s_sel[atomicAdd(&s_ngt, 1u)] = packed;
+    } else if (key == T && all_eq) {
+      s_sel[cnt_gt + atomicAdd(&s_neq, 1u)] = packed;
+    }
+  };
+  for (int x = t; x < V; x += kTopThreads) take(order_key(__ldg(row + x)), x);
+  if (!all_eq && warp == 0) {
+    // ties at T beyond the budget: the lowest indices win, so warp 0 walks the
+    // row in index order, 32 elements at a time
+    unsigned taken = 0u;
+    for (int x0 = 0; x0 < V && taken < need_eq; x0 += 32) {
+      const int x = x0 + lane;
+      const bool eq = x < V && order_key(__ldg(row + x)) == T;
+      const unsigned bal = __ballot_sync(0xffffffffu, eq);
+      const unsigned rank = __popc(bal & ((1u << lane) - 1u));
+      if (eq && taken + rank < need_eq)
+        s_sel[cnt_gt + taken + rank] =
+            ((unsigned long long)T << 32) | (unsigned long long)(0xFFFFFFFFu - (unsigned)x);
+      taken += __popc(bal);
     }
   }
   __syncthreads();
@@ -169,17 +157,38 @@ topk_kernel(const float *__restrict__ q, int K, int V, int M, int32_t *__restric
 }
 
 constexpr int kExpandThreads = 256;
-constexpr int kPerLane = kMaxNodes / 32;  // nodes owned by one lane
+constexpr int kPerLane = kMaxNodes / 32;  // candidate slots one lane scans
 
+// Candidate key of a node: its best remaining child (rank r at the next
+// position), as (rho bits, (255 - child depth) << 16 | (0xFFFF - node)) so
+// that a larger key wins under (rho desc, depth asc, parent index asc); 0 when
+// the node has no child left.
+__device__ __forceinline__ unsigned long long child_key(int node, float rho_node, int dep, int r,
+                                                       const float *s_tq, int K, int M, int N) {
+  const int d = dep + 1;
+  if (node >= N || d > K || r >= M) return 0ull;
+  const float rc = __fmul_rn(rho_node, s_tq[(d - 1) * M + r]);
+  return ((unsigned long long)__float_as_uint(rc) << 32) |
+         (unsigned long long)(((unsigned)(255 - d) << 16) | (unsigned)(0xFFFF - node));
+}
+
+// One warp per sequence.  Every inserted node owns one candidate key in
+// shared memory; per step each lane reduces the keys of its nodes, two warp
+// max-reductions pick the winner, and lane 0 alone inserts it: the new node's
+// state and both changed candidate keys are written with plain shared-memory
+// stores, so a step is one short dependent chain.  Outputs are written at the
+// end, coalesced.
 __global__ void __launch_bounds__(kExpandThreads)
 expand_kernel(const int32_t *__restrict__ top_tok, const float *__restrict__ top_q,
               const int32_t *__restrict__ root_token, int K, int M, int N,
               int32_t *__restrict__ parent, int32_t *__restrict__ tokens,
               int32_t *__restrict__ depth, float *__restrict__ rho, double *__restrict__ ahat) {
   extern __shared__ unsigned char smem_raw[];
-  float *s_tq = reinterpret_cast<float *>(smem_raw);            // [K][M]
+  float *s_tq = reinterpret_cast<float *>(smem_raw);                  // [K][M]
   int32_t *s_tt = reinterpret_cast<int32_t *>(s_tq + (size_t)K * M);  // [K][M]
+  __shared__ unsigned long long s_key[kMaxNodes];
   __shared__ float s_rho[kMaxNodes];
+  __shared__ int32_t s_dep[kMaxNodes], s_nch[kMaxNodes], s_par[kMaxNodes], s_tok[kMaxNodes];
 
   pdl_trigger();
   pdl_wait();
@@ -188,113 +197,64 @@ expand_kernel(const int32_t *__restrict__ top_tok, const float *__restrict__ top
     s_tq[x] = top_q[(size_t)b * K * M + x];
     s_tt[x] = top_tok[(size_t)b * K * M + x];
   }
+  for (int x = t; x < kMaxNodes; x += kExpandThreads) {
+    s_key[x] = 0ull;
+    s_rho[x] = 0.f;
+    s_dep[x] = 0;
+    s_nch[x] = 0;
+    s_par[x] = -1;
+    s_tok[x] = -1;
+  }
   __syncthreads();
   if (t >= 32) return;
   const int lane = t;
-  int32_t *par_b = parent + (size_t)b * N;
-  int32_t *tok_b = tokens + (size_t)b * N;
-  int32_t *dep_b = depth + (size_t)b * N;
-  float *rho_b = rho + (size_t)b * N;
-
-  float o_rho[kPerLane];
-  int o_dep[kPerLane], o_nch[kPerLane];
-  unsigned c_hi[kPerLane], c_lo[kPerLane];
-#pragma unroll
-  for (int j = 0; j < kPerLane; ++j) {
-    o_rho[j] = 0.f;
-    o_dep[j] = 0;
-    o_nch[j] = 0;
-    c_hi[j] = 0u;
-    c_lo[j] = 0u;
-  }
-
-  // candidate of owned slot j (node id = lane + 32 j): its best remaining child
-  auto refresh = [&](int j) {
-    const int node = lane + 32 * j;
-    const int d = o_dep[j] + 1;
-    const int r = o_nch[j];
-    if (node >= N || d > K || r >= M) {
-      c_hi[j] = 0u;
-      c_lo[j] = 0u;
-      return;
-    }
-    const float rc = __fmul_rn(o_rho[j], s_tq[(d - 1) * M + r]);
-    c_hi[j] = __float_as_uint(rc);
-    c_lo[j] = ((unsigned)(255 - d) << 16) | (unsigned)(0xFFFF - node);
-  };
-
+  double a_hat = 0.0;  // lane 0: sum of non-root rho in insertion order
   if (lane == 0) {
-    o_rho[0] = 1.f;
-    o_dep[0] = 0;
-    o_nch[0] = 0;
-    refresh(0);
-    par_b[0] = -1;
-    tok_b[0] = root_token[b];
-    dep_b[0] = 0;
-    rho_b[0] = 1.f;
     s_rho[0] = 1.f;
+    s_tok[0] = root_token[b];
+    s_key[0] = child_key(0, 1.f, 0, 0, s_tq, K, M, N);
   }
+  __syncwarp();
 
   int filled = N;
   for (int n = 1; n < N; ++n) {
-    unsigned bh = 0u, bl = 0u;
+    unsigned long long best = 0ull;
 #pragma unroll
-    for (int j = 0; j < kPerLane; ++j)
-      if (c_hi[j] > bh || (c_hi[j] == bh && c_lo[j] > bl)) {
-        bh = c_hi[j];
-        bl = c_lo[j];
-      }
+    for (int j = 0; j < kPerLane; ++j) {
+      const unsigned long long k = s_key[lane + 32 * j];
+      best = k > best ? k : best;
+    }
+    const unsigned bh = (unsigned)(best >> 32), bl = (unsigned)best;
     const unsigned H = __reduce_max_sync(0xffffffffu, bh);
     const unsigned Lo = __reduce_max_sync(0xffffffffu, bh == H ? bl : 0u);
     if (H == 0u && Lo == 0u) {  // no valid node left (host checks make this unreachable)
       filled = n;
       break;
     }
-    const int p = 0xFFFF - (int)(Lo & 0xFFFFu);
-    const int d = 255 - (int)((Lo >> 16) & 0xFFu);
-    const float rn = __uint_as_float(H);
-    int tok = 0;
-    if (lane == (p & 31)) {
-      const int jp = p >> 5;
-#pragma unroll
-      for (int j = 0; j < kPerLane; ++j)
-        if (j == jp) {
-          tok = s_tt[(d - 1) * M + o_nch[j]];
-          o_nch[j] += 1;
-          refresh(j);
-        }
-    }
-    tok = __shfl_sync(0xffffffffu, tok, p & 31);
-    if (lane == (n & 31)) {
-      const int jn = n >> 5;
-#pragma unroll
-      for (int j = 0; j < kPerLane; ++j)
-        if (j == jn) {
-          o_rho[j] = rn;
-          o_dep[j] = d;
-          o_nch[j] = 0;
-          refresh(j);
-        }
-      par_b[n] = p;
-      tok_b[n] = tok;
-      dep_b[n] = d;
-      rho_b[n] = rn;
+    if (lane == 0) {
+      const int p = 0xFFFF - (int)(Lo & 0xFFFFu);
+      const int d = 255 - (int)((Lo >> 16) & 0xFFu);
+      const float rn = __uint_as_float(H);
+      const int r = s_nch[p];
+      s_nch[p] = r + 1;
+      s_key[p] = child_key(p, s_rho[p], s_dep[p], r + 1, s_tq, K, M, N);
+      s_par[n] = p;
+      s_tok[n] = s_tt[(d - 1) * M + r];
+      s_dep[n] = d;
       s_rho[n] = rn;
+      s_key[n] = child_key(n, rn, d, 0, s_tq, K, M, N);
+      a_hat += (double)rn;
     }
+    __syncwarp();
   }
-  for (int n = filled + lane; n < N; n += 32) {
-    par_b[n] = -1;
-    tok_b[n] = -1;
-    dep_b[n] = 0;
-    rho_b[n] = 0.f;
-    s_rho[n] = 0.f;
+  for (int n = lane; n < N; n += 32) {
+    const bool ok = n < filled;
+    parent[(size_t)b * N + n] = ok ? s_par[n] : -1;
+    tokens[(size_t)b * N + n] = ok ? s_tok[n] : -1;
+    depth[(size_t)b * N + n] = ok ? s_dep[n] : 0;
+    rho[(size_t)b * N + n] = ok ? s_rho[n] : 0.f;
   }
-  __syncwarp();
-  if (lane == 0) {
-    double s = 0.0;
-    for (int n = 1; n < N; ++n) s += (double)s_rho[n];
-    ahat[b] = s;
-  }
+  if (lane == 0) ahat[b] = a_hat;
 }
 
 struct BestFirstPlan {
