@@ -923,14 +923,18 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
                 if (!((vis >> i) & 1u)) r[c2][i] = __float_as_uint(-INFINITY);
             }
           }
+          // the max with three-input max instructions: 8 chains of 8 values
           float mx[8];
 #pragma unroll
-          for (int a = 0; a < 8; ++a) mx[a] = __uint_as_float(r[0][a]);
-#pragma unroll
-          for (int i = 8; i < 64; ++i)
-            mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(r[i >> 5][i & 31]));
-          const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sc;
+          for (int a = 0; a < 8; ++a) {
+            const auto v = [&](int i) { return __uint_as_float(r[i >> 5][i & 31]); };
+            float m = fmax3(v(a), v(a + 8), v(a + 16));
+            m = fmax3(m, v(a + 24), v(a + 32));
+            m = fmax3(m, v(a + 40), v(a + 48));
+            mx[a] = fmaxf(m, v(a + 56));
+          }
+          const float mt = fmaxf(fmax3(mx[0], mx[1], mx[2]),
+                                 fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7])) * sc;
           const float m_new = fmaxf(m_use, mt);
           const bool upd = m_new > m_use + 8.f;  // first visible key, or the max grew by > 2^8
           const float alpha = upd ? exp2f(m_use - m_new) : 1.f;
@@ -945,22 +949,30 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
             m_use = m_new;
           }
           const float mb = m_use == -INFINITY ? 0.f : m_use;
-          float esum[2] = {0.f, 0.f}, rsum[2] = {0.f, 0.f};
+          // key pairs on packed fp32: one FMA for both arguments, one add for
+          // each of the two sums
+          const unsigned long long sc2 = f2_pack(sc, sc), nmb2 = f2_pack(-mb, -mb);
+          unsigned long long esum2 = f2_pack(0.f, 0.f), rsum2 = f2_pack(0.f, 0.f);
 #pragma unroll
           for (int c2 = 0; c2 < 2; ++c2) {
             uint32_t pk[16];  // P as bf16 pairs: column i holds keys 2i, 2i+1 of the chunk
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const float a = ex2_approx(fmaf(__uint_as_float(r[c2][2 * i]), sc, -mb));
-              const float c = ex2_approx(fmaf(__uint_as_float(r[c2][2 * i + 1]), sc, -mb));
+              const float2 x = f2_unpack(f2_fma(f2_pack(__uint_as_float(r[c2][2 * i]),
+                                                        __uint_as_float(r[c2][2 * i + 1])),
+                                                sc2, nmb2));
+              const float a = ex2_approx(x.x);
+              const float c = ex2_approx(x.y);
               pk[i] = pack_bf16(a, c);
-              esum[i & 1] += a + c;
-              rsum[i & 1] += pair_sum(pk[i]);
+              esum2 = f2_add(esum2, f2_pack(a, c));
+              rsum2 = f2_add(rsum2, f2_pack(__uint_as_float(pk[i] << 16),
+                                            __uint_as_float(pk[i] & 0xFFFF0000u)));
             }
             tmem_st16(tS + h * 32 + c2 * 16, pk);
           }
-          lt += rsum[0] + rsum[1];
-          lte += esum[0] + esum[1];
+          const float2 es = f2_unpack(esum2), rs = f2_unpack(rsum2);
+          lt += rs.x + rs.y;
+          lte += es.x + es.y;
         }
         l_sum += lt;
         l_ex += lte;
