@@ -74,6 +74,22 @@ def test_bastion_budget(tsd, N):
     compare(inp, g, o)
 
 
+def test_long_context_many_splits(tsd):
+    """Prefixes of 150k-200k keys: the split count reaches its largest values
+    (the merge takes its widest form), a GQA group of 16 heads fills 320 rows
+    (a full 256-row block plus a 64-row block that runs its two softmax groups
+    on alternate key tiles); sampled rows against the oracle."""
+    inp = gen.random_small(4242, B=2, N_max=20, Hq=16, Hkv=1, D=128, V=500, prefix_lo=150000,
+                           prefix_hi=200000, max_depth=5, ragged_nodes=False)
+    rng = np.random.default_rng(1)
+    sample = sorted({(b, int(rng.integers(inp.N_max)), int(rng.integers(inp.Hq)))
+                     for b in range(inp.B) for _ in range(40)})
+    g = run_gpu(tsd, inp)
+    o = run_oracle(inp, sample_attention=sample)
+    compare(inp, g, o, sample=sample)
+    assert g["status"] == 0
+
+
 SWEEP = [
     # B, N_max, Hq, Hkv, D, V, P range, depth
     (2, 1, 4, 4, 64, 100, (0, 40), 1),
