@@ -39,10 +39,13 @@ from .commit import commit_path
 from .best_first import best_first_tree, ranked_tokens
 from .rejection import modified_rejection_step, residual_distribution
 from .budget import verify_step_cost, calibrate, budget_select, cost_table
+from .stochastic import node_decision, tree_verify_stochastic, tree_verify_stochastic_all
 
 __all__ = [
     "ERR_RANGE", "ERR_CYCLE", "ERR_TOO_DEEP", "ERR_CLOSURE", "ERR_ROOT", "ERR_COUNT",
     "build_ancestors", "ancestor_chain", "bf16_to_f64", "tree_attention", "gather_sequence_kv",
     "verify_greedy", "commit_path", "best_first_tree", "ranked_tokens",
     "modified_rejection_step", "residual_distribution",
+    "verify_step_cost", "calibrate", "budget_select", "cost_table",
+    "node_decision", "tree_verify_stochastic", "tree_verify_stochastic_all",
 ]
