@@ -349,3 +349,82 @@ def random_small(seed: int, B: int, N_max: int, Hq: int, Hkv: int, D: int, V: in
     return VerifyInputs(name="random%d" % seed, B=B, N_max=N_max, Hq=Hq, Hkv=Hkv, D=D, V=V,
                         D_max=max_depth, parent=parent, n_nodes=n_nodes, prefix_len=prefix_len,
                         tokens=tokens, logits=logits, q=q, cache=cache, targets=targets)
+
+
+# Stochastic verification ---------------------------------------------------
+
+
+@dataclasses.dataclass
+class StochasticInputs:
+    B: int
+    N_max: int
+    V: int
+    D_max: int
+    parent: np.ndarray     # int32 [B][N_max]
+    n_nodes: np.ndarray    # int32 [B]
+    tokens: np.ndarray     # int32 [B][N_max]
+    logits: np.ndarray     # float32 [B][N_max][V]  target logits
+    q_draft: np.ndarray    # float32 [B][N_max][V]  draft probabilities
+    u_accept: np.ndarray   # float32 [B][N_max]     uniforms in [0, 1)
+    u_draw: np.ndarray     # float32 [B][N_max]
+    seed: int = 0
+
+
+def stochastic_inputs(seed: int, B: int, N_max: int, V: int, max_depth: int,
+                      parents: Optional[np.ndarray] = None, ragged_nodes: bool = False,
+                      logit_std: float = float(np.sqrt(2.0)), draft_noise: float = 1.0,
+                      relabel_ids: bool = True) -> StochasticInputs:
+    """Inputs for stochastic tree verification.
+
+    Target logits ~ N(0, logit_std^2) in fp32.  The draft row of node i is a
+    noisy copy of the target seen through the drafter: the normalised
+    exponential of (logits[i] + N(0, draft_noise^2)), formed in fp64 and
+    rounded once to fp32.  Each child's token is drawn from its parent's
+    draft row (independent draws, repeats allowed).  Uniforms are fp32 in
+    [0, 1).  ``parents`` [B][N_max] fixes the trees; otherwise random trees
+    of depth <= max_depth (ids relabelled, padding entries junk)."""
+    rng = np.random.default_rng(seed)
+    if ragged_nodes:
+        n_nodes = rng.integers(1, N_max, size=B, endpoint=True).astype(np.int32)
+    else:
+        n_nodes = np.full(B, N_max, dtype=np.int32)
+    if parents is not None:
+        parent = np.asarray(parents, dtype=np.int32).copy()
+    else:
+        parent = np.zeros((B, N_max), dtype=np.int32)
+        for b in range(B):
+            nb = int(n_nodes[b])
+            p = random_tree(rng, nb, max_depth)
+            if relabel_ids and nb > 2:
+                p = relabel(rng, p)
+            parent[b, :nb] = p
+            parent[b, nb:] = rng.integers(-5, 2 * N_max, size=N_max - nb)
+    logits = rng.standard_normal(size=(B, N_max, V), dtype=np.float32) * np.float32(logit_std)
+    q_draft = np.zeros((B, N_max, V), dtype=np.float32)
+    tokens = rng.integers(0, V, size=(B, N_max)).astype(np.int32)
+    for b in range(B):
+        nb = int(n_nodes[b])
+        for i in range(nb):
+            z = logits[b, i].astype(np.float64) + rng.standard_normal(V) * draft_noise
+            e = np.exp(z - z.max())
+            q64 = e / e.sum()
+            q_draft[b, i] = q64.astype(np.float32)
+            kids = np.nonzero(parent[b, :nb] == i)[0]
+            kids = kids[kids > 0]
+            if kids.size:
+                tokens[b, kids] = rng.choice(V, size=kids.size, p=q64)
+    u_accept = rng.random((B, N_max), dtype=np.float32)
+    u_draw = rng.random((B, N_max), dtype=np.float32)
+    return StochasticInputs(B=B, N_max=N_max, V=V, D_max=max_depth, parent=parent,
+                            n_nodes=n_nodes, tokens=tokens, logits=logits, q_draft=q_draft,
+                            u_accept=u_accept, u_draw=u_draw, seed=seed)
+
+
+def redraw_uniforms(inp: StochasticInputs, rng: np.random.Generator, accept_idx, draw_idx) -> None:
+    """In place: fresh uniforms at the given (b, node) index arrays."""
+    ab, ai = accept_idx
+    if len(ab):
+        inp.u_accept[ab, ai] = rng.random(len(ab), dtype=np.float32)
+    db, di = draw_idx
+    if len(db):
+        inp.u_draw[db, di] = rng.random(len(db), dtype=np.float32)

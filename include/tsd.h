@@ -237,6 +237,64 @@ int tsd_tree_verify_greedy_static(const float *logits, const int32_t *tokens,
                                   int32_t *bonus, tsd_stream_t stream);
 
 /*
+ * Stochastic verification ([Blog], classic speculative decoding: modified
+ * rejection sampling accepts a drafted token x ~ q with probability
+ * min(1, p(x)/q(x)) and on rejection draws from the normalised residual
+ * max(0, p - q), so the emitted token is distributed as the target p;
+ * [Blog] Medusa: every branch of the tree scored in one pass).
+ *
+ * Tree reading: the children of node i are independent draws from q_i (row i
+ * of q_draft), tried in increasing id order.  With p_i = softmax(logits[i])
+ * and r = p_i, child c (token x) is accepted iff
+ *   u_accept[b][c] * q_i(x) < r(x);
+ * on rejection r <- max(0, r - q_i) / sum(max(0, r - q_i)) (r <- q_i when
+ * that sum is 0) and the next child is tested.  When every child is rejected,
+ * or i is a leaf, node i draws draw[b][i] from r by inverse CDF in token
+ * order: the first token whose cumulative weight exceeds u_draw[b][i] times
+ * the total (rounding leaving none: the last token of positive weight).
+ * Children whose token lies outside [0, V) are skipped.  The walk starts at
+ * the root and follows next[] to the first node without an accepted child:
+ * accept_len = its depth, leaf = it, bonus = its draw, path[b][k] = safe id
+ * of the depth-k node of the walk, 0 beyond (the same layout as
+ * tsd_tree_verify_greedy, so tsd_kv_commit_path takes the result as is).
+ * Arithmetic is fp32 (max, sums, exponentials, residuals); each decision
+ * matches the exact one unless its uniform lies within rounding of the
+ * threshold.
+ *
+ * logits, q_draft  float [B][N_max][V]  target logits and draft
+ *                  probabilities (rows need not be normalised; non-negative,
+ *                  finite; logits finite or -inf)
+ * tokens, parent   int32 [B][N_max]; n_nodes int32 [B] or NULL
+ * err              int32 [B], REQUIRED: from tsd_tree_build_ancestors (the
+ *                  walk relies on its checks)
+ * u_accept, u_draw float [B][N_max], uniforms in [0, 1): u_accept[b][c] for
+ *                  the test of child c, u_draw[b][i] for a draw at node i
+ * next  int32 [B][N_max] out: accepted child of each node, or -1
+ * draw  int32 [B][N_max] out: the node's drawn token when next is -1, else -1
+ *       (padding rows and skipped sequences: -1 in both)
+ * accept_len, leaf, bonus int32 [B] out; path int32 [B][D_max+1] out.
+ *       A sequence with err != 0: accept_len 0, leaf -1, bonus -1, path 0.
+ * workspace  >= tsd_tree_verify_stochastic_workspace_bytes() bytes (one
+ *            ticket per sequence), ZERO-FILLED before first use; every call
+ *            leaves it zero-filled.  Calls sharing one must not overlap.
+ * No output (nor the workspace) may overlap an input: TSD_ERR_ARG.
+ * Limits: V <= 262144 (TSD_ERR_LIMIT).
+ * One launch: a cluster of up to 8 CTAs per node, each holding a slice of
+ * the node's rows in shared memory; the CTA that settles the sequence's last
+ * node walks the tree.
+ */
+size_t tsd_tree_verify_stochastic_workspace_bytes(int B, int N_max, int V);
+int tsd_tree_verify_stochastic(const float *logits, const float *q_draft, const int32_t *tokens,
+                               const int32_t *parent, const int32_t *n_nodes, const int32_t *err,
+                               const float *u_accept, const float *u_draw, int B, int N_max,
+                               int V, int D_max, int32_t *next, int32_t *draw,
+                               int32_t *accept_len, int32_t *leaf, int32_t *path, int32_t *bonus,
+                               void *workspace, size_t ws_bytes, tsd_stream_t stream);
+/* The launch shape tsd_tree_verify_stochastic picks on the current device:
+ * CTAs per node (cluster size) and floats of the row per CTA.  Host only. */
+int tsd_tree_verify_stochastic_plan(int B, int N_max, int V, int *cluster, int *slice);
+
+/*
  * a4. Commit of the accepted path with the prefix-sharing fast reorder
  *     ([EP-zh] 2.1: path-index commit reorders the cache along the accepted
  *     path and moves only the newly accepted segment, only when needed;

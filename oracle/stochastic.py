@@ -33,6 +33,8 @@ tree, where the pages are silent:
   at the first node with none.  accept_len = the number of accepted draft
   nodes (depth of the last node), leaf = that node, bonus = its draw,
   path[k] = safe id (real id + 1) of the depth-k node of the walk, 0 beyond.
+* A child whose token lies outside [0, V) is skipped: it is never accepted
+  and leaves the residual unchanged (the kernel cannot index such a token).
 * Every node is decided independently of whether the walk reaches it (the
   decisions use only the node's own row, children and uniforms), so
   ``next_child`` and ``draw`` are defined for all valid nodes.
@@ -85,7 +87,9 @@ def node_decision(logits_row, q_row, child_ids, child_tokens, u_accept, u_draw):
         u = float(u_accept[c])
         lhs, rhs = u * q[x], r[x]
         scale = max(lhs, rhs)
-        acc_margin = min(acc_margin, abs(lhs - rhs) / scale if scale > 0 else 0.0)
+        # both sides exactly zero (q(x) = 0 and r(x) underflowed): rejected
+        # whatever u is, so no uniform is near this decision
+        acc_margin = min(acc_margin, abs(lhs - rhs) / scale if scale > 0 else np.inf)
         if lhs < rhs:
             return int(c), -1, float(acc_margin), np.inf
         res = np.maximum(0.0, r - q)
@@ -121,7 +125,7 @@ def tree_verify_stochastic(logits, q, tokens, parent, n_nodes, err, d_max: int, 
         nb = n_max if n_nodes is None else int(n_nodes[b])
         par = [int(x) for x in parent[b][:nb]]
         for i in range(nb):
-            kids = [j for j in range(1, nb) if par[j] == i]
+            kids = [j for j in range(1, nb) if par[j] == i and 0 <= int(tokens[b][j]) < V]
             toks = [int(tokens[b][j]) for j in kids]
             c, t, am, dm = node_decision(logits[b, i], q[b, i], kids, toks, u_accept[b],
                                          u_draw[b][i])

@@ -251,3 +251,27 @@ def test_draw_boundaries():
     for u, t in ((0.0, 1), (0.2499, 1), (0.2501, 2), (0.4999, 2), (0.5001, 3), (ONE, 3)):
         c, tok, _, _ = node_decision(logits, q, [], [], np.zeros(1), u)
         assert c == -1 and tok == t
+
+
+def test_out_of_range_child_is_skipped():
+    """A child whose token lies outside [0, V) changes nothing: the result
+    equals that of the same tree without it."""
+    rng = np.random.default_rng(4)
+    V = 6
+    parent = np.array([[-1, 0, 0, 0, 1]])
+    logits = rng.normal(size=(1, 5, V))
+    q = rng.dirichlet(np.ones(V), size=(1, 5))
+    for bad in (-1, V, 10 ** 6):
+        for _ in range(20):
+            ua, ud = rng.random((1, 5)), rng.random((1, 5))
+            tokens = rng.integers(0, V, size=(1, 5))
+            tokens[0, 2] = bad
+            got = tree_verify_stochastic_all(logits, q, tokens, parent, None, 3, ua, ud)
+            # the same tree with node 2 moved under node 4 (never reached at the root)
+            par2 = parent.copy()
+            par2[0, 2] = 4
+            tok2 = tokens.copy()
+            tok2[0, 2] = 0
+            ref = tree_verify_stochastic_all(logits, q, tok2, par2, None, 3, ua, ud)
+            assert got[0][0, 0] == ref[0][0, 0] and got[1][0, 0] == ref[1][0, 0]
+            assert got[0][0, 0] != 2

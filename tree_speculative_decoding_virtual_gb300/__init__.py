@@ -45,6 +45,10 @@ SIGNATURES = {
     "tsd_tree_verify_static_capacity": (_SZ, []),
     "tsd_tree_verify_greedy_static": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P,
                                            _P, _P, _P, _P]),
+    "tsd_tree_verify_stochastic_workspace_bytes": (_SZ, [_I, _I, _I]),
+    "tsd_tree_verify_stochastic": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P,
+                                        _P, _P, _P, _P, _SZ, _P]),
+    "tsd_tree_verify_stochastic_plan": (_I, [_I, _I, _I, _P, _P]),
     "tsd_kv_commit_path": (_I, [_P, _P, _I, _I64, _P, _I, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I,
                                 _I, _P, _P, _P, _P]),
     "tsd_best_first_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
@@ -227,6 +231,53 @@ def tree_verify_greedy_static(logits, tokens, parent, anc, depth, mask, n_nodes,
         _ptr(bonus, torch.int32, "bonus"), _stream(stream))
     _check(rc, "tree_verify_greedy_static")
     return argmax, accept_len, leaf, path, bonus
+
+
+def tree_verify_stochastic_workspace_bytes(B: int, N_max: int, V: int) -> int:
+    return int(lib.tsd_tree_verify_stochastic_workspace_bytes(B, N_max, V))
+
+
+def tree_verify_stochastic(logits, q_draft, tokens, parent, n_nodes, err, u_accept, u_draw, D_max,
+                           next=None, draw=None, accept_len=None, leaf=None, path=None,
+                           bonus=None, workspace=None, stream=None):
+    """Modified rejection sampling over the tree.  logits, q_draft float32
+    [B][N_max][V]; u_accept, u_draw float32 [B][N_max] uniforms; err from
+    tree_build_ancestors (required).  Returns (next [B][N_max], draw
+    [B][N_max], accept_len [B], leaf [B], path [B][D_max+1], bonus [B]).  A
+    workspace passed in must be zero-filled before its first use."""
+    B, N_max, V = logits.shape
+    next = next if next is not None else _empty((B, N_max), torch.int32, logits)
+    draw = draw if draw is not None else _empty((B, N_max), torch.int32, logits)
+    accept_len = accept_len if accept_len is not None else _empty((B,), torch.int32, logits)
+    leaf = leaf if leaf is not None else _empty((B,), torch.int32, logits)
+    path = path if path is not None else _empty((B, D_max + 1), torch.int32, logits)
+    bonus = bonus if bonus is not None else _empty((B,), torch.int32, logits)
+    need = tree_verify_stochastic_workspace_bytes(B, N_max, V)
+    if workspace is None:
+        workspace = torch.zeros((max(need, 1),), dtype=torch.uint8, device=logits.device)
+    if tuple(q_draft.shape) != (B, N_max, V):
+        raise TsdError("q_draft must have the shape of logits")
+    rc = lib.tsd_tree_verify_stochastic(
+        _ptr(logits, torch.float32, "logits"), _ptr(q_draft, torch.float32, "q_draft"),
+        _ptr(tokens, torch.int32, "tokens"), _ptr(parent, torch.int32, "parent"),
+        _ptr(n_nodes, torch.int32, "n_nodes"), _ptr(err, torch.int32, "err"),
+        _ptr(u_accept, torch.float32, "u_accept"), _ptr(u_draw, torch.float32, "u_draw"),
+        B, N_max, V, D_max, _ptr(next, torch.int32, "next"), _ptr(draw, torch.int32, "draw"),
+        _ptr(accept_len, torch.int32, "accept_len"), _ptr(leaf, torch.int32, "leaf"),
+        _ptr(path, torch.int32, "path"), _ptr(bonus, torch.int32, "bonus"),
+        _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+    _check(rc, "tree_verify_stochastic")
+    return next, draw, accept_len, leaf, path, bonus
+
+
+def tree_verify_stochastic_plan(B: int, N_max: int, V: int):
+    """(CTAs per node, floats of the row per CTA) the call picks on the
+    current device."""
+    c, s = ctypes.c_int(0), ctypes.c_int(0)
+    _check(lib.tsd_tree_verify_stochastic_plan(B, N_max, V, ctypes.byref(c), ctypes.byref(s)),
+           "tree_verify_stochastic_plan")
+    return c.value, s.value
 
 
 # ---------------------------------------------------------------------------

@@ -19,8 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtsd.so")
 
-SOURCES = ["runtime.cu", "ancestors.cu", "attention.cu", "verify.cu", "commit.cu",
-           "best_first.cu", "budget.cu"]
+SOURCES = ["runtime.cu", "ancestors.cu", "attention.cu", "verify.cu", "verify_stochastic.cu",
+           "commit.cu", "best_first.cu", "budget.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

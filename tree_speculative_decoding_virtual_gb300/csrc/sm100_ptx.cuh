@@ -250,7 +250,6 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
 
-// 2^x with the hardware approximation (PTX ex2.approx.ftz.f32); ex2(-inf) = 0.
 // ---- packed fp32 pairs (two lanes of one 64-bit register pair) ----------------
 __device__ __forceinline__ unsigned long long f2_pack(float a, float b) {
   unsigned long long r;
@@ -279,10 +278,44 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }
+// 2^x with the hardware approximation (PTX ex2.approx.ftz.f32); ex2(-inf) = 0.
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
   return y;
+}
+
+// ---- thread-block clusters ---------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;\n" : "=r"(r));
+  return r;
+}
+// Cluster-wide barrier halves: every thread of every CTA of the cluster
+// arrives (release: its earlier shared-memory writes become visible to the
+// cluster) and then waits (acquire).  Warp-converged calls only.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+// 16-byte load from the shared memory of CTA `rank` of this cluster, at the
+// offset that `saddr` has in this CTA's own shared window.
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(saddr), "r"(rank));
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];\n"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(r)
+               : "memory");
+  return v;
 }
 
 // Byte offset of 16-byte chunk `c` (0..7) of row `r` inside a tile whose rows
