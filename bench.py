@@ -326,6 +326,12 @@ def gpu_arm(args, rank, world):
 
     B, N, Hq, Hkv, D, V, Dm = inp.B, inp.N_max, inp.Hq, inp.Hkv, inp.D, inp.V, inp.D_max
     c = inp.cache
+    stochastic = args.verify == "stochastic"
+    if stochastic:
+        q_draft_h, tok_h, ua_h, ud_h = gen.stochastic_for(inp)
+        inp.tokens = tok_h
+        q_draft, u_acc, u_drw = T(q_draft_h), T(ua_h), T(ud_h)
+        del q_draft_h
     parent, n_nodes, prefix = T(inp.parent), T(inp.n_nodes), T(inp.prefix_len)
     tokens, logits, q = T(inp.tokens), T(inp.logits), T(inp.q, torch.bfloat16)
     table = T(c.block_table)
@@ -342,7 +348,10 @@ def gpu_arm(args, rank, world):
     attn_ws = torch.empty((tsd.tree_attn_workspace_bytes(B, N, Hq, Hkv, D, max_slots),),
                           dtype=torch.uint8, device=dev)
     ver_ws = torch.zeros((tsd.tree_verify_workspace_bytes(B, N, V),), dtype=torch.uint8, device=dev)
+    st_ws = torch.zeros((tsd.tree_verify_stochastic_workspace_bytes(B, N, V),), dtype=torch.uint8,
+                        device=dev)
     am = torch.empty((B, N), **i32)
+    drw = torch.empty((B, N), **i32)
     A = torch.empty((B,), **i32)
     leaf = torch.empty((B,), **i32)
     path = torch.empty((B, Dm + 1), **i32)
@@ -360,8 +369,9 @@ def gpu_arm(args, rank, world):
         flush.zero_()
         flush_rd.sum()
 
+    verify_name = "tree_verify_stochastic" if stochastic else "tree_verify_greedy"
     names = (["best_first_tree_build"] if bastion else []) + [
-        "tree_build_ancestors", "tree_attn_fwd", "tree_verify_greedy", "kv_commit_path"]
+        "tree_build_ancestors", "tree_attn_fwd", verify_name, "kv_commit_path"]
     launches_per_step = (2 if bastion else 0) + 1 + 2 + 1 + 1
 
     calls = {}
@@ -376,6 +386,10 @@ def gpu_arm(args, rank, world):
     calls["tree_verify_greedy"] = lambda: tsd.tree_verify_greedy(
         logits, tokens, parent, anc, depth, mask, n_nodes, err, Dm, am, A, leaf, path, bonus,
         workspace=ver_ws)
+    if stochastic:
+        calls["tree_verify_stochastic"] = lambda: tsd.tree_verify_stochastic(
+            logits, q_draft, tokens, parent, n_nodes, err, u_acc, u_drw, Dm, am, drw, A, leaf,
+            path, bonus, workspace=st_ws)
     calls["kv_commit_path"] = lambda: tsd.kv_commit_path(
         kc, vc, table, prefix, n_nodes, A, path, err, N, Dm, new_len=new_len, moved=moved,
         status=status)
@@ -390,6 +404,25 @@ def gpu_arm(args, rank, world):
     torch.cuda.synchronize()
     moved_total = int(moved.sum().item())
     assert int(status.item()) == 0, "device status %d" % int(status.item())
+    rejected_rows = internal_rows = leaf_draws = 0
+    if stochastic:
+        # rows the method must read: the target row of every internal node
+        # (its children are decided on it), the draft row of each node that
+        # saw a rejection, and the target row of the walk's last node when it
+        # is a leaf (the bonus is drawn there); other leaves need nothing
+        nx = am.cpu().numpy()
+        leaf_h = leaf.cpu().numpy()
+        for b in range(B):
+            nb = int(inp.n_nodes[b])
+            for i in range(nb):
+                kids = [j for j in range(1, nb) if int(inp.parent[b, j]) == i
+                        and 0 <= int(inp.tokens[b, j]) < V]
+                if kids:
+                    internal_rows += 1
+                    if nx[b, i] != kids[0]:
+                        rejected_rows += 1
+                elif i == int(leaf_h[b]):
+                    leaf_draws += 1
 
     # CUDA graphs: the whole step, and each entry point on its own (timing
     # without host launch gaps; the kernels are the same launches)
@@ -471,11 +504,15 @@ def gpu_arm(args, rank, world):
     # ---- e2e: host buffers through the public API, copies inside the timing ----
     h_in = {"q": q, "logits": logits, "parent": parent, "tokens": tokens, "n_nodes": n_nodes,
             "prefix_len": prefix}
+    if stochastic:
+        h_in.update({"q_draft": q_draft, "u_accept": u_acc, "u_draw": u_drw})
     pinned = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in h_in.items()}
     for k, v in h_in.items():
         pinned[k].copy_(v.cpu())
     h_out_src = {"out": out, "argmax": am, "accept_len": A, "leaf": leaf, "path": path,
                  "bonus": bonus, "new_len": new_len}
+    if stochastic:
+        h_out_src["draw"] = drw
     h_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in h_out_src.items()}
     h2d = sum(v.numel() * v.element_size() for v in pinned.values())
     d2h = sum(v.numel() * v.element_size() for v in h_out.values())
@@ -501,8 +538,14 @@ def gpu_arm(args, rank, world):
         return None
     peak, peak_src, _ = load_peaks()
     abytes = algorithmic_bytes(inp, moved_total)
+    if stochastic:
+        # every valid node's target row, the draft rows of nodes that saw a
+        # rejection, and the per-node uniforms, tokens and parents
+        abytes["tree_verify_stochastic"] = (4 * V * (internal_rows + rejected_rows + leaf_draws)
+                                            + 4 * 4 * B * N)
+        del abytes["tree_verify_greedy"]
     step_bytes = sum(abytes.values())
-    dom = max(["tree_attn_fwd", "tree_verify_greedy"], key=lambda n: kernel_us[n])
+    dom = max(["tree_attn_fwd", verify_name], key=lambda n: kernel_us[n])
     achieved = abytes[dom] / (kernel_us[dom] * 1e-6) / 1e9
     attn_flops = attention_flops(inp)
     tc_peak, tc_src = load_tensor_peak()
@@ -531,9 +574,11 @@ def gpu_arm(args, rank, world):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16 (attention, fp32 accumulate); f32 (logits argmax); int32 (tree, paths)",
+        "dtype": "bf16 (attention, fp32 accumulate); f32 (%s); int32 (tree, paths)" % (
+            "rejection sampling" if stochastic else "logits argmax"),
         "data": "synthetic (seeded; shapes and distributions of the named workload)",
-        "config": {"workload": desc, "name": args.workload, "global_batch": B * world,
+        "config": {"workload": desc, "name": args.workload, "verify": args.verify,
+                   "global_batch": B * world,
                    "seq_len": max_slots, "parallelism": "replicas (dp%d)" % world,
                    "l2": "flushed between timed steps: 256 MiB write then 256 MiB read of another "
                          "buffer, outside the timed events (cold, clean L2)",
@@ -565,6 +610,10 @@ def gpu_arm(args, rank, world):
         "wall_s_timed_region": round(t_wall, 4),
         "kernel_sum_us": round(sum(kernel_us.values()), 3),
         "mean_accept_len": float(A.float().mean().item()),
+        "verify": (args.verify if not stochastic else
+                   {"mode": "stochastic", "internal_rows": internal_rows,
+                    "rows_with_rejection": rejected_rows, "leaf_draws": leaf_draws,
+                    "plan": tsd.tree_verify_stochastic_plan(B, N, V)}),
         "commit_layer_stacked": {
             "layers": n_layers, "us": round(stacked_us, 3),
             "algorithmic_bytes": abytes["kv_commit_path"] * n_layers,
@@ -772,6 +821,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="8b")
+    ap.add_argument("--verify", default="greedy", choices=["greedy", "stochastic"],
+                    help="a3: greedy (argmax) or stochastic (modified rejection sampling)")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--attn-kernel", default="tc", choices=["tc", "mma"],
@@ -792,7 +843,8 @@ def main(argv=None):
         import torch.distributed as dist
         dist.init_process_group("nccl")
     base = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.workload.startswith("bastion"):
+    if (rank == 0 and world == 1 and not args.no_cpu_baseline and args.verify == "greedy"
+            and not args.workload.startswith("bastion")):
         base = cpu_baseline(args.workload)
     res = (budget_arm if args.workload == "bastion-budget" else gpu_arm)(args, rank, world)
     if rank == 0:

@@ -428,3 +428,32 @@ def redraw_uniforms(inp: StochasticInputs, rng: np.random.Generator, accept_idx,
     db, di = draw_idx
     if len(db):
         inp.u_draw[db, di] = rng.random(len(db), dtype=np.float32)
+
+
+def stochastic_for(inp: VerifyInputs, seed: int = 0, draft_noise: float = 1.0):
+    """Draft rows, child tokens and uniforms for stochastic verification of
+    an existing verify workload (its trees and target logits): the draft row
+    of node i is the normalised exponential of (logits[i] + N(0,
+    draft_noise^2)) formed in fp64 and rounded to fp32; each child's token is
+    drawn from its parent's draft row; uniforms fp32 in [0, 1).  Returns
+    (q_draft [B][N][V], tokens [B][N], u_accept [B][N], u_draw [B][N])."""
+    rng = np.random.default_rng(1000 + seed)
+    B, N, V = inp.B, inp.N_max, inp.V
+    q_draft = np.zeros((B, N, V), dtype=np.float32)
+    tokens = inp.tokens.copy()
+    for b in range(B):
+        nb = int(inp.n_nodes[b])
+        for i in range(nb):
+            z = inp.logits[b, i].astype(np.float64) + rng.standard_normal(V) * draft_noise
+            e = np.exp(z - z.max())
+            q64 = e / e.sum()
+            q_draft[b, i] = q64.astype(np.float32)
+            kids = np.nonzero(inp.parent[b, :nb] == i)[0]
+            kids = kids[kids > 0]
+            if kids.size:
+                c = np.cumsum(q64)
+                tokens[b, kids] = np.minimum(np.searchsorted(c, rng.random(kids.size) * c[-1],
+                                                             side="right"), V - 1)
+    u_accept = rng.random((B, N), dtype=np.float32)
+    u_draw = rng.random((B, N), dtype=np.float32)
+    return q_draft, tokens, u_accept, u_draw

@@ -248,10 +248,11 @@ int tsd_tree_verify_greedy_static(const float *logits, const int32_t *tokens,
  * and r = p_i, child c (token x) is accepted iff
  *   u_accept[b][c] * q_i(x) < r(x);
  * on rejection r <- max(0, r - q_i) / sum(max(0, r - q_i)) (r <- q_i when
- * that sum is 0) and the next child is tested.  When every child is rejected,
- * or i is a leaf, node i draws draw[b][i] from r by inverse CDF in token
- * order: the first token whose cumulative weight exceeds u_draw[b][i] times
- * the total (rounding leaving none: the last token of positive weight).
+ * that sum is 0) and the next child is tested.  A node whose children are
+ * all rejected draws draw[b][i] from r by inverse CDF in token order: the
+ * first token whose cumulative weight exceeds u_draw[b][i] times the total
+ * (rounding leaving none: the last token of positive weight).  A walk that
+ * ends at a leaf draws the leaf's token the same way from p_leaf.
  * Children whose token lies outside [0, V) are skipped.  The walk starts at
  * the root and follows next[] to the first node without an accepted child:
  * accept_len = its depth, leaf = it, bonus = its draw, path[b][k] = safe id
@@ -270,18 +271,25 @@ int tsd_tree_verify_greedy_static(const float *logits, const int32_t *tokens,
  * u_accept, u_draw float [B][N_max], uniforms in [0, 1): u_accept[b][c] for
  *                  the test of child c, u_draw[b][i] for a draw at node i
  * next  int32 [B][N_max] out: accepted child of each node, or -1
- * draw  int32 [B][N_max] out: the node's drawn token when next is -1, else -1
- *       (padding rows and skipped sequences: -1 in both)
+ * draw  int32 [B][N_max] out: the drawn token of every node whose children
+ *       were all rejected and of the walk's last node; -1 elsewhere (other
+ *       leaves, nodes with an accepted child, padding, skipped sequences)
  * accept_len, leaf, bonus int32 [B] out; path int32 [B][D_max+1] out.
  *       A sequence with err != 0: accept_len 0, leaf -1, bonus -1, path 0.
- * workspace  >= tsd_tree_verify_stochastic_workspace_bytes() bytes (one
- *            ticket per sequence), ZERO-FILLED before first use; every call
- *            leaves it zero-filled.  Calls sharing one must not overlap.
- * No output (nor the workspace) may overlap an input: TSD_ERR_ARG.
+ * workspace  >= tsd_tree_verify_stochastic_workspace_bytes() bytes: one
+ *            ticket per sequence (the first 4*B bytes), ZERO-FILLED before
+ *            first use and left zero-filled by every call, then per-CTA
+ *            scratch that needs no initial contents.  Calls sharing one must
+ *            not overlap.
+ * status     int32 device word or NULL: TSD_STATUS_TIMEOUT if a bounded wait
+ *            for a row copy ran out (results then unspecified).
+ * No output (nor the workspace or status) may overlap an input: TSD_ERR_ARG.
  * Limits: V <= 262144 (TSD_ERR_LIMIT).
- * One launch: a cluster of up to 8 CTAs per node, each holding a slice of
- * the node's rows in shared memory; the CTA that settles the sequence's last
- * node walks the tree.
+ * One launch: a cluster of up to 8 CTAs per node.  An internal node holds
+ * its target row in shared memory, slice by slice, and decides its children;
+ * a leaf's CTAs record per-slice sums of its target row.  The CTA that
+ * finishes a sequence last walks the tree and, when the walk ends at a leaf,
+ * draws the bonus token from the one slice that holds it.
  */
 size_t tsd_tree_verify_stochastic_workspace_bytes(int B, int N_max, int V);
 int tsd_tree_verify_stochastic(const float *logits, const float *q_draft, const int32_t *tokens,
@@ -289,7 +297,8 @@ int tsd_tree_verify_stochastic(const float *logits, const float *q_draft, const 
                                const float *u_accept, const float *u_draw, int B, int N_max,
                                int V, int D_max, int32_t *next, int32_t *draw,
                                int32_t *accept_len, int32_t *leaf, int32_t *path, int32_t *bonus,
-                               void *workspace, size_t ws_bytes, tsd_stream_t stream);
+                               void *workspace, size_t ws_bytes, int32_t *status,
+                               tsd_stream_t stream);
 /* The launch shape tsd_tree_verify_stochastic picks on the current device:
  * CTAs per node (cluster size) and floats of the row per CTA.  Host only. */
 int tsd_tree_verify_stochastic_plan(int B, int N_max, int V, int *cluster, int *slice);

@@ -37,7 +37,10 @@ tree, where the pages are silent:
   and leaves the residual unchanged (the kernel cannot index such a token).
 * Every node is decided independently of whether the walk reaches it (the
   decisions use only the node's own row, children and uniforms), so
-  ``next_child`` and ``draw`` are defined for all valid nodes.
+  ``next_child`` is defined for all valid nodes, and so is ``draw`` for every
+  node whose children were all rejected.  A leaf draws only when it is the
+  walk's last node (its draw is then the bonus token); the other leaves'
+  draw entries are -1, since no token is ever taken from them.
 * A sequence with err != 0 is skipped: rows of next_child and draw -1,
   accept_len 0, leaf -1, path 0, bonus -1.  Padding rows are -1.
 
@@ -133,6 +136,11 @@ def tree_verify_stochastic(logits, q, tokens, parent, n_nodes, err, d_max: int, 
         walk = [0]
         while nxt[b, walk[-1]] >= 0:
             walk.append(int(nxt[b, walk[-1]]))
+        for i in range(nb):
+            leaf_node = not any(par[j] == i and 0 <= int(tokens[b][j]) < V for j in range(1, nb))
+            if leaf_node and i != walk[-1]:
+                drw[b, i] = -1
+                drw_m[b, i] = np.inf
         if len(walk) - 1 > d_max:
             raise ValueError("walk deeper than D_max on a tree that passed the checks")
         accept_len[b] = len(walk) - 1

@@ -238,7 +238,14 @@ def test_skipped_and_padding():
     nxt, drw, A, leaf, path, bonus = tree_verify_stochastic_all(
         logits, q, tokens, parent, n_nodes, 4, rng.random((2, n)), rng.random((2, n)))
     assert (nxt[0, 6:] == -1).all() and (drw[0, 6:] == -1).all()
-    assert ((nxt[0, :6] >= 0) ^ (drw[0, :6] >= 0)).all()
+    assert not ((nxt[0, :6] >= 0) & (drw[0, :6] >= 0)).any()
+    internal = [i for i in range(6) if any(parent[0, j] == i for j in range(1, 6))]
+    for i in range(6):
+        if i in internal or i == leaf[0]:
+            assert (nxt[0, i] >= 0) ^ (drw[0, i] >= 0)
+        else:
+            assert drw[0, i] == -1      # a leaf the walk does not reach draws nothing
+    assert bonus[0] == drw[0, leaf[0]] >= 0
     assert (nxt[1] == -1).all() and (drw[1] == -1).all()
     assert A[1] == 0 and leaf[1] == -1 and bonus[1] == -1 and (path[1] == 0).all()
 

@@ -47,7 +47,7 @@ SIGNATURES = {
                                            _P, _P, _P, _P]),
     "tsd_tree_verify_stochastic_workspace_bytes": (_SZ, [_I, _I, _I]),
     "tsd_tree_verify_stochastic": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P,
-                                        _P, _P, _P, _P, _SZ, _P]),
+                                        _P, _P, _P, _P, _SZ, _P, _P]),
     "tsd_tree_verify_stochastic_plan": (_I, [_I, _I, _I, _P, _P]),
     "tsd_kv_commit_path": (_I, [_P, _P, _I, _I64, _P, _I, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I,
                                 _I, _P, _P, _P, _P]),
@@ -239,12 +239,13 @@ def tree_verify_stochastic_workspace_bytes(B: int, N_max: int, V: int) -> int:
 
 def tree_verify_stochastic(logits, q_draft, tokens, parent, n_nodes, err, u_accept, u_draw, D_max,
                            next=None, draw=None, accept_len=None, leaf=None, path=None,
-                           bonus=None, workspace=None, stream=None):
+                           bonus=None, workspace=None, status=None, stream=None):
     """Modified rejection sampling over the tree.  logits, q_draft float32
     [B][N_max][V]; u_accept, u_draw float32 [B][N_max] uniforms; err from
     tree_build_ancestors (required).  Returns (next [B][N_max], draw
     [B][N_max], accept_len [B], leaf [B], path [B][D_max+1], bonus [B]).  A
-    workspace passed in must be zero-filled before its first use."""
+    workspace passed in must have its first 4*B bytes (the tickets) zeroed
+    before its first use; calls leave them zeroed."""
     B, N_max, V = logits.shape
     next = next if next is not None else _empty((B, N_max), torch.int32, logits)
     draw = draw if draw is not None else _empty((B, N_max), torch.int32, logits)
@@ -266,7 +267,7 @@ def tree_verify_stochastic(logits, q_draft, tokens, parent, n_nodes, err, u_acce
         _ptr(accept_len, torch.int32, "accept_len"), _ptr(leaf, torch.int32, "leaf"),
         _ptr(path, torch.int32, "path"), _ptr(bonus, torch.int32, "bonus"),
         _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
-        _stream(stream))
+        _ptr(status, torch.int32, "status"), _stream(stream))
     _check(rc, "tree_verify_stochastic")
     return next, draw, accept_len, leaf, path, bonus
 

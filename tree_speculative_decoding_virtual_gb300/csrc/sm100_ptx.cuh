@@ -109,6 +109,11 @@ __device__ __forceinline__ void bulk_load(uint32_t sdst, const void *gsrc, uint3
       "l"(gsrc), "r"(bytes), "r"(bar)
       : "memory");
 }
+// Bulk prefetch of [gsrc, gsrc + bytes) into L2 (16-byte aligned, bytes a
+// multiple of 16); nothing is written to shared memory and nothing waits.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *gsrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(gsrc), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void bulk_store(void *gdst, uint32_t ssrc, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(gdst),
                "r"(ssrc), "r"(bytes)
@@ -316,6 +321,16 @@ __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t saddr, uint32_t rank) {
                : "r"(r)
                : "memory");
   return v;
+}
+
+// 16-byte store into the shared memory of CTA `rank` of this cluster, at the
+// offset that `saddr` has in this CTA's own shared window.
+__device__ __forceinline__ void st_dsmem_f4(uint32_t saddr, uint32_t rank, float4 v) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(saddr), "r"(rank));
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(r), "f"(v.x), "f"(v.y),
+               "f"(v.z), "f"(v.w)
+               : "memory");
 }
 
 // Byte offset of 16-byte chunk `c` (0..7) of row `r` inside a tile whose rows
