@@ -421,7 +421,7 @@ struct Args {
   const float *logits, *qd;
   const int32_t *tokens, *parent, *n_nodes, *err;
   const float *u_accept, *u_draw;
-  int N_max, V, S, vec, bulk, prefetch, D_max;
+  int N_max, V, S, vec, bulk, D_max;
   uint64_t limit_ns;
   int32_t *next, *draw, *accept_len, *leaf, *path, *bonus;
   unsigned *counter;
@@ -594,12 +594,7 @@ __global__ void __launch_bounds__(kST, 3) verify_stochastic_kernel(const Args a)
     auto owner = [&](int j) { return j < nk ? s_ktok[j] / S : -1; };
 
     load_row_stats(sm, R4, lrow, cnt, S4, a.vec, bulk, a.limit_ns, 0);
-    if (t == 0) {
-      sm.mine.pub = owner(0) == c ? R[s_ktok[0] - lo] : 0.f;
-      // the draft row is read only after a rejection: have it in L2 by then
-      // (the first exchange's wait overlaps the fetch)
-      if (a.prefetch && cnt > 0) bulk_prefetch_l2(qrow, (uint32_t)cnt * 4u);
-    }
+    if (t == 0) sm.mine.pub = owner(0) == c ? R[s_ktok[0] - lo] : 0.f;
     bool level0 = true;
     exchange(sm, round++, true, C, owner(0));
     for (int j = 0; j < nk; ++j) {
@@ -818,9 +813,6 @@ TSD_API int tsd_tree_verify_stochastic(const float *logits, const float *q_draft
   a.S = p.S;
   a.vec = (V % 4 == 0) && aligned(logits, 16) && aligned(q_draft, 16);
   a.bulk = a.vec;  // bulk copies: 16-byte aligned rows and slices
-  // L2 prefetch of the internal nodes' draft rows when target and draft
-  // arrays together fit well inside L2 (129 MB); larger batches stream
-  a.prefetch = a.vec && 2.0 * (double)big <= 80.0 * 1024 * 1024;
   a.D_max = D_max;
   a.limit_ns = (uint64_t)option(TSD_OPT_WAIT_LIMIT_NS);
   a.next = next;
