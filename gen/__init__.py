@@ -318,9 +318,12 @@ def bastion_verify_inputs(parent: np.ndarray, tokens: np.ndarray, depth: np.ndar
 def random_small(seed: int, B: int, N_max: int, Hq: int, Hkv: int, D: int, V: int,
                  prefix_lo: int, prefix_hi: int, max_depth: int, p_match: float = 0.6,
                  ragged_nodes: bool = True, shuffle_blocks: bool = True,
-                 relabel_ids: bool = True, logit_std: float = 1.0) -> VerifyInputs:
+                 relabel_ids: bool = True, logit_std: float = 1.0,
+                 prefix_len: Optional[np.ndarray] = None) -> VerifyInputs:
     """Randomised small verify inputs for parity sweeps: ragged node counts
-    (padding rows), arbitrary parent order, shuffled pages."""
+    (padding rows), arbitrary parent order, shuffled pages.  ``prefix_len``,
+    when given, fixes the per-sequence prefix lengths instead of drawing them
+    from [prefix_lo, prefix_hi]."""
     rng = np.random.default_rng(seed)
     if ragged_nodes:
         n_nodes = rng.integers(1, N_max, size=B, endpoint=True).astype(np.int32)
@@ -335,7 +338,8 @@ def random_small(seed: int, B: int, N_max: int, Hq: int, Hkv: int, D: int, V: in
         parent[b, :nb] = p
         # padding entries hold junk that must be ignored
         parent[b, nb:] = rng.integers(-5, 2 * N_max, size=N_max - nb)
-    prefix_len = rng.integers(prefix_lo, prefix_hi, size=B, endpoint=True).astype(np.int32)
+    drawn = rng.integers(prefix_lo, prefix_hi, size=B, endpoint=True).astype(np.int32)
+    prefix_len = drawn if prefix_len is None else np.asarray(prefix_len, dtype=np.int32).copy()
     targets = rng.integers(0, V, size=(B, N_max)).astype(np.int32)
     tokens = np.zeros((B, N_max), dtype=np.int32)
     for b in range(B):

@@ -159,13 +159,17 @@ int tsd_tree_build_ancestors(const int32_t *parent, const int32_t *n_nodes, int 
  * n_nodes     int32 [B] or NULL
  * mask        uint32 [B][N_max][W]   from tsd_tree_build_ancestors
  * err         int32 [B] or NULL      sequences with err != 0 are skipped
- * max_slots   host upper bound on P_b + N_b over the batch; it sizes the
- *             split-KV grid.  A sequence exceeding it sets
- *             TSD_STATUS_BAD_LEN and is skipped.
+ * max_slots   host upper bound on P_b + N_b over the batch, at most 262144
+ *             (TSD_ERR_LIMIT beyond); it sizes the split-KV grid and the
+ *             workspace.  A sequence exceeding it sets TSD_STATUS_BAD_LEN
+ *             and is skipped.  For batches of up to 64 sequences the key
+ *             ranges are split on the device from the actual lengths, so a
+ *             loose bound costs workspace, not time.
  * out         bf16 [B][N_max][Hq][D]  out.  Skipped / padding rows are 0.
  * lse         float [B][N_max][Hq] or NULL  out.  Skipped rows -inf.
  * workspace   device scratch of ws_bytes >= tsd_tree_attn_workspace_bytes()
- *             (fp32 split-KV partials; no initial contents required).
+ *             (split-KV partials and the split plan; no initial contents
+ *             required).
  * status      int32 device word (see TSD_STATUS_*), may be NULL.
  */
 size_t tsd_tree_attn_workspace_bytes(int B, int N_max, int Hq, int Hkv, int D, int max_slots);

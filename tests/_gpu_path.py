@@ -28,9 +28,10 @@ def to_np(t, dtype=None):
     return a.view(dtype) if dtype is not None else a
 
 
-def run_gpu(tsd, inp, sample_attention=None, with_lse=True):
+def run_gpu(tsd, inp, sample_attention=None, with_lse=True, max_slots=None):
     """Whole hot path on the GPU; returns a dict of numpy arrays (cache after
-    commit included)."""
+    commit included).  ``max_slots`` is the host bound passed to the attention
+    (default: the exact largest prefix + nodes)."""
     c = inp.cache
     parent = dev_tensor(inp.parent)
     n_nodes = dev_tensor(inp.n_nodes)
@@ -40,7 +41,8 @@ def run_gpu(tsd, inp, sample_attention=None, with_lse=True):
     v = dev_tensor(c.v, torch.bfloat16)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     anc, depth, mask, err = tsd.tree_build_ancestors(parent, n_nodes, inp.D_max)
-    max_slots = int((inp.prefix_len + inp.n_nodes).max())
+    if max_slots is None:
+        max_slots = int((inp.prefix_len + inp.n_nodes).max())
     out, lse = tsd.tree_attn_fwd(dev_tensor(inp.q, torch.bfloat16), k, v, table, prefix, n_nodes,
                                  mask, err, max_slots, want_lse=with_lse, status=status)
     am, A, leaf, path, bonus = tsd.tree_verify_greedy(dev_tensor(inp.logits),

@@ -72,6 +72,9 @@ def test_host_argument_checks_without_gpu(lib_path):
     assert L.tsd_tree_build_ancestors(None, None, 0, 8, 4, None, None, None, None, None) == 0
     # head dim not supported
     assert L.tsd_tree_attn_workspace_bytes(1, 8, 4, 4, 96, 100) == 0
+    # key ranges longer than 32 splits of 64 key tiles of 128 keys
+    assert L.tsd_tree_attn_workspace_bytes(1, 8, 4, 4, 128, 262144) > 0
+    assert L.tsd_tree_attn_workspace_bytes(1, 8, 4, 4, 128, 262145) == 0
     # head dim not supported by the commit kernel
     assert L.tsd_kv_commit_path(None, None, 1, 0, None, 1, 1, None, None, None, None, None,
                                 1, 8, 4, 80, 4, None, None, None, None) == -2

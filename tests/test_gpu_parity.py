@@ -90,6 +90,37 @@ def test_long_context_many_splits(tsd):
     assert g["status"] == 0
 
 
+# Skewed prefix lengths: one long sequence among short ones (and an empty
+# prefix), so the device split plan cuts the long key ranges into many pieces
+# and the short ones into one or two.
+SKEWED_PREFIX = [20000, 150, 900, 40, 3000, 0, 7000, 260]
+
+
+@pytest.mark.parametrize("loose", [False, True])
+def test_ragged_split_plan(tsd, loose):
+    """Ragged batch through the device split plan, with the exact host bound
+    on prefix + nodes and with a loose one (4x): both must give the oracle's
+    result; the loose bound only changes the grid the plan may use."""
+    inp = gen.random_small(31337, B=8, N_max=24, Hq=16, Hkv=2, D=128, V=300, prefix_lo=0,
+                           prefix_hi=1, max_depth=6, prefix_len=np.array(SKEWED_PREFIX))
+    exact = int((inp.prefix_len + inp.n_nodes).max())
+    g = run_gpu(tsd, inp, max_slots=4 * exact if loose else exact)
+    o = run_oracle(inp)
+    compare(inp, g, o)
+    assert g["status"] == 0
+
+
+def test_large_batch_uniform_split(tsd):
+    """More sequences than the device plan takes (B = 70): the host's
+    uniform split and its three-dimensional grid."""
+    inp = gen.random_small(4711, B=70, N_max=6, Hq=4, Hkv=2, D=64, V=50, prefix_lo=0,
+                           prefix_hi=300, max_depth=3)
+    g = run_gpu(tsd, inp)
+    o = run_oracle(inp)
+    compare(inp, g, o)
+    assert g["status"] == 0
+
+
 SWEEP = [
     # B, N_max, Hq, Hkv, D, V, P range, depth
     (2, 1, 4, 4, 64, 100, (0, 40), 1),

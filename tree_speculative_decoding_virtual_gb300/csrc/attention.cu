@@ -26,6 +26,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <cmath>
 
 #include "sm100_ptx.cuh"
@@ -51,9 +52,16 @@ struct AttnParams {
   const int32_t *err;
   int N_max, Hq, Hkv, g, W, max_slots;
   float scale_log2;
-  int chunk, splits, row_tiles, rows_pad;
-  uint16_t *part_o;  // [B*Hkv][splits][rows_pad][D] fp16: the split's O / (l * c)
-  float4 *part_ml;   // [B*Hkv][splits][rows_pad]  (max in log2 units, sum l, scale c, 0)
+  int chunk, splits, row_tiles, rows_pad;  // the host's uniform split of the key range
+  // plan_mode 0/1: the uniform split; partials [B*Hkv][splits][rows_pad].
+  // plan_mode 2: the split is planned on the device from the actual lengths
+  // (tree_attn_plan_kernel); the grid is one block per work item (grid_items
+  // of them) and item k's partials are rows [k * kTcRows, (k + 1) * kTcRows).
+  int B, plan_mode, nsm, grid_items;
+  int4 *plan_out;    // plan_mode 2: per sequence (first item, splits, chunk in key tiles, row tiles)
+  int4 *plan_items;  // plan_mode 2: per block of the grid, its item (tree_attn_plan_kernel)
+  uint16_t *part_o;  // fp16 partial rows [..][D]: the split's O / (l * c)
+  float4 *part_ml;   // one per partial row: (max in log2 units, sum l, scale c, 0)
   uint16_t *out;
   float *lse;
   int32_t *status;
@@ -449,6 +457,33 @@ struct TcLayout {
   static constexpr uint32_t kTmemTile = 256;
 };
 
+// Device-side split plan (plan_mode 2), for batches of up to kPlanMaxSeq
+// sequences.  The work of (sequence b, kv head, row tile) is its key range of
+// t_b = ceil((P_b + N_b) / 128) tiles.  For a chunk bound C (in tiles) the
+// range is cut into n_b = ceil(t_b / C) pieces of ceil(t_b / n_b) tiles; each
+// piece is one work item (one block).  With one resident block per SM the
+// estimated time is waves x (longest piece + kPlanFixedTiles), waves =
+// ceil(items / SMs); the plan takes the C (1..64) of least estimate (ties:
+// the larger C), with items <= the grid and n_b <= kMaxSplits.  For a batch
+// of equal lengths this is the host's uniform split; for ragged lengths long
+// sequences get more pieces, so they no longer set the kernel's duration.
+// Items are numbered sequence by sequence, then kv head, split, row tile.
+constexpr int kPlanMaxSeq = 64;
+constexpr int kMaxSplits = 32;                               // pieces of one key range
+constexpr int kPlanMaxChunk = kTcMaxPages * kPage / kTcBN;   // 64 key tiles per item
+constexpr int kPlanFixedTiles = 4;                           // per-item set-up + partials
+constexpr int kPlanGroups = 5;                               // thread groups over the sequences
+constexpr int kPlanMinTiles = 16;  // uniform blocks shorter than this keep the uniform split
+static_assert(kPlanMaxChunk == 64, "the plan key keeps C in 6 bits");
+
+struct TcPlanShared {
+  int tiles[kPlanMaxSeq];  // t_b (0: sequence skipped)
+  int rtc[kPlanMaxSeq];    // row tiles that hold valid rows
+  int items[kPlanMaxChunk], longest[kPlanMaxChunk], most[kPlanMaxChunk];  // per C
+  unsigned best;  // (estimate << 6) | (64 - C), minimised (estimate clamped to 26 bits)
+  int mine, first;          // this block's sequence (-1: none) and its first item
+};
+
 struct TcShared {
   int32_t pages[kTcMaxPages];  // block ids of the split
   uint64_t k_full[kTcStages], k_empty[kTcStages], v_full[kTcStages], v_empty[kTcStages];
@@ -465,6 +500,137 @@ __device__ __forceinline__ bool tc_wait(uint64_t &bar, uint32_t parity, uint64_t
   if (mbar_wait(smem_addr(&bar), parity, limit)) return true;
   *abort = 1;
   return false;
+}
+
+// The device plan (see TcPlanShared), computed once per launch by one block
+// of kTcThreads threads before the split kernel.  It writes
+//   plan_seq[b]    (first item, splits n_b, chunk in key tiles, row tiles)
+//   plan_items[k]  for every block k of the split kernel's grid: (b, kv head,
+//                  rt | split << 5 | chunk << 11 | N_b << 18, P_b), or b = -1
+//                  when block k has no item
+// and reports sequences whose lengths do not fit (TSD_STATUS_BAD_LEN).
+__global__ void __launch_bounds__(kTcThreads) tree_attn_plan_kernel(const AttnParams p) {
+  __shared__ TcPlanShared ps;
+  __shared__ int s_P[kPlanMaxSeq], s_nb[kPlanMaxSeq], s_first[kPlanMaxSeq + 1];
+  pdl_trigger();
+  const int tid = threadIdx.x;
+  const int B = p.B;
+  for (int i = tid; i < kPlanMaxChunk; i += blockDim.x) {
+    ps.items[i] = 0;
+    ps.longest[i] = 0;
+    ps.most[i] = 0;
+  }
+  if (tid == 0) ps.best = ~0u;
+  pdl_wait();
+  if (tid < B) {
+    int P, nb;
+    const bool ok = seq_ok(p, tid, P, nb);
+    ps.tiles[tid] = ok ? (P + nb + kTcBN - 1) / kTcBN : 0;
+    ps.rtc[tid] = ok ? (nb * p.g + kTcRows - 1) / kTcRows : 0;
+    s_P[tid] = P;
+    s_nb[tid] = nb;
+    if (!ok && p.status) {
+      const int e = p.err ? p.err[tid] : 0;
+      const int nbb = p.n_nodes ? p.n_nodes[tid] : p.N_max;
+      if (e == 0 && nbb >= 1 && nbb <= p.N_max) atomicOr(p.status, TSD_STATUS_BAD_LEN);
+    }
+  }
+  __syncthreads();
+  // candidate C = 1 + (tid % 64); kPlanGroups groups of 64 threads share the sequences
+  if (tid < kPlanGroups * kPlanMaxChunk) {
+    const int ci = tid % kPlanMaxChunk;
+    const int C = ci + 1;
+    int items = 0, longest = 0, most = 0;
+    for (int s = tid / kPlanMaxChunk; s < B; s += kPlanGroups) {
+      const int t = ps.tiles[s];
+      if (t == 0) continue;
+      const int n = (t + C - 1) / C;
+      items += p.Hkv * ps.rtc[s] * n;
+      longest = max(longest, (t + n - 1) / n);
+      most = max(most, n);
+    }
+    if (items > 0) {
+      atomicAdd(&ps.items[ci], items);
+      atomicMax(&ps.longest[ci], longest);
+      atomicMax(&ps.most[ci], most);
+    }
+  }
+  __syncthreads();
+  if (tid < kPlanMaxChunk) {  // two full warps: one candidate per lane
+    const int items = ps.items[tid];
+    unsigned key = ~0u;
+    if (items > 0 && items <= p.grid_items && ps.most[tid] <= kMaxSplits) {
+      const long waves = (items + p.nsm - 1) / p.nsm;
+      const long est = min(waves * (long)(ps.longest[tid] + kPlanFixedTiles), (1L << 26) - 1);
+      key = ((unsigned)est << 6) | (unsigned)(kPlanMaxChunk - 1 - tid);
+    }
+    key = __reduce_min_sync(0xffffffffu, key);
+    if ((tid & 31) == 0) atomicMin(&ps.best, key);
+  }
+  __syncthreads();
+  // (no candidate: no sequence has work; every block gets b = -1)
+  const int C = ps.best == ~0u ? 0 : kPlanMaxChunk - (int)(ps.best & 63u);
+  if (tid < 32) {
+    // first item of each sequence: two sequences per lane (tid, tid + 32),
+    // exclusive scans over the lanes
+    int n[2], items[2], first[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int s = tid + 32 * h;
+      const int t = (s < B && C > 0) ? ps.tiles[s] : 0;
+      n[h] = t > 0 ? (t + C - 1) / C : 0;
+      items[h] = t > 0 ? p.Hkv * ps.rtc[s] * n[h] : 0;
+      int incl = items[h];
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (tid >= off) incl += y;
+      }
+      first[h] = incl - items[h];
+    }
+    const int half = __shfl_sync(0xffffffffu, first[0] + items[0], 31);
+    first[1] += half;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int s = tid + 32 * h;
+      if (s >= B) continue;
+      const int t = ps.tiles[s];
+      s_first[s] = first[h];
+      p.plan_out[s] = make_int4(first[h], n[h], n[h] > 0 ? (t + n[h] - 1) / n[h] : 0, ps.rtc[s]);
+    }
+  }
+  __syncthreads();
+  if (tid < 32) {
+    // total items: the last sequence's first item plus its items
+    if (tid == 0) {
+      int total = 0;
+      if (B > 0 && C > 0) {
+        const int s = B - 1, t = ps.tiles[s];
+        total = s_first[s] + (t > 0 ? p.Hkv * ps.rtc[s] * ((t + C - 1) / C) : 0);
+      }
+      s_first[kPlanMaxSeq] = total;
+    }
+  }
+  __syncthreads();
+  const int total = s_first[kPlanMaxSeq];
+  for (int k = tid; k < p.grid_items; k += blockDim.x) {
+    int4 e = make_int4(-1, 0, 0, 0);
+    if (k < total) {
+      int b = 0;  // the sequence whose items contain k (sequences without items are skipped)
+      for (int s = 1; s < B; ++s)
+        if (s_first[s] <= k && ps.tiles[s] > 0) b = s;
+      const int t = ps.tiles[b];
+      const int rtc = ps.rtc[b];
+      const int n = (t + C - 1) / C;
+      const int chunk = (t + n - 1) / n;
+      const int local = k - s_first[b];
+      const int rt = local % rtc;
+      const int split = (local / rtc) % n;
+      const int hkv = local / rtc / n;
+      e = make_int4(b, hkv, rt | (split << 5) | (chunk << 11) | (s_nb[b] << 18), s_P[b]);
+    }
+    p.plan_items[k] = e;
+  }
 }
 
 // Visibility of 32 consecutive key slots for one query row: bit i covers the
@@ -635,11 +801,18 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
   __shared__ TcShared sh;
 
   pdl_trigger();
-  const int rt = blockIdx.x;
-  const int split = blockIdx.y;
-  const int z = blockIdx.z;
-  const int b = z / p.Hkv;
-  const int hkv = z % p.Hkv;
+  // The work item: (row tile, split, sequence x kv head) from the grid for the
+  // uniform split; under the device plan the grid is one block per item and
+  // the item is known only once the plan kernel (the previous grid) has
+  // finished, so until then (b, hkv, rt, split) is the uniform split's guess,
+  // used for the prefetch.
+  const bool planned = p.plan_mode == 2;
+  const int item = blockIdx.x;
+  int rt = planned ? item % p.row_tiles : blockIdx.x;
+  int split = planned ? (item / p.row_tiles) % p.splits : blockIdx.y;
+  const int zg = planned ? item / (p.row_tiles * p.splits) : blockIdx.z;
+  int b = zg / p.Hkv;
+  int hkv = zg % p.Hkv;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -680,22 +853,41 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
 
-  attn_prefetch<D>(p, b, hkv, rt, split, warp, lane);
+  if (b < p.B) attn_prefetch<D>(p, b, hkv, rt, split, warp, lane);
   pdl_wait();
 
   int P = 0, nb = 0;
-  bool run = seq_ok(p, b, P, nb);
-  if (!run && rt == 0 && split == 0 && hkv == 0 && tid == 0 && p.status) {
-    const int e = p.err ? p.err[b] : 0;
-    const int nbb = p.n_nodes ? p.n_nodes[b] : p.N_max;
-    if (e == 0 && nbb >= 1 && nbb <= p.N_max) atomicOr(p.status, TSD_STATUS_BAD_LEN);
+  bool run;
+  int k_begin, k_end;
+  size_t item_row0;  // first partial row of this item
+  if (planned) {
+    const int4 e = __ldcg(&p.plan_items[item]);
+    run = e.x >= 0;
+    b = run ? e.x : 0;
+    hkv = e.y;
+    rt = e.z & 31;
+    split = (e.z >> 5) & 63;
+    const int chunk = ((e.z >> 11) & 127) * kTcBN;
+    nb = (e.z >> 18) & 511;
+    P = e.w;
+    k_begin = split * chunk;
+    k_end = min(P + nb, k_begin + chunk);
+    item_row0 = (size_t)item * kTcRows;
+  } else {
+    run = seq_ok(p, b, P, nb);
+    if (!run && rt == 0 && split == 0 && hkv == 0 && tid == 0 && p.status) {
+      const int e = p.err ? p.err[b] : 0;
+      const int nbb = p.n_nodes ? p.n_nodes[b] : p.N_max;
+      if (e == 0 && nbb >= 1 && nbb <= p.N_max) atomicOr(p.status, TSD_STATUS_BAD_LEN);
+    }
+    k_begin = split * p.chunk;
+    k_end = min(P + nb, k_begin + p.chunk);
+    item_row0 = ((size_t)zg * p.splits + split) * p.rows_pad + (size_t)rt * kTcRows;
   }
   const int rows_valid = nb * p.g;
   const int seq_len = P + nb;
-  const int k_begin = split * p.chunk;
   run = run && rt * kTcRows < rows_valid && k_begin < seq_len;
   const int ntile_rows = rt * kTcRows + kTcBM < rows_valid ? 2 : 1;  // row tiles with valid rows
-  const int k_end = min(seq_len, k_begin + p.chunk);
   const int ntiles = (k_end - k_begin + kTcBN - 1) / kTcBN;
   const int pg_first = k_begin / kPage;
   const int npg = run ? (k_end - 1) / kPage - pg_first + 1 : 0;  // <= kTcMaxPages (host check)
@@ -1050,14 +1242,13 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
           *reinterpret_cast<uint4 *>(srow + (((c * 4 + q8) ^ (rl & swz_mask)) << 4)) = v;
         }
       }
-      const size_t prow = ((size_t)z * p.splits + split) * p.rows_pad + rt * kTcRows + tr * kTcBM + rl;
+      const size_t prow = item_row0 + tr * kTcBM + rl;
       p.part_ml[prow] = make_float4(m_use, l_ex, cs, 0.f);
       fence_proxy_async_smem();
     }
     if (writer) asm volatile("bar.sync 1, %0;\n" ::"r"(nwr) : "memory");
     if (all_ok && warp == 2 && lane == 0) {
-      const size_t row0 = ((size_t)z * p.splits + split) * p.rows_pad + rt * kTcRows;
-      bulk_store(p.part_o + row0 * D, base + L::kStaging, (uint32_t)(nwr * D * 2));
+      bulk_store(p.part_o + item_row0 * D, base + L::kStaging, (uint32_t)(nwr * D * 2));
       bulk_wait_read();
     }
   }
@@ -1078,7 +1269,7 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
 // of split (l / (D/8)) + round * 32/(D/8).  Every load of every round is
 // issued before any is used, so the merge costs one memory round trip; lanes
 // holding the same chunk for different splits are then summed by shuffles.
-template <int D, int R>  // R: rounds of loads (R * 32 / (D/8) >= number of splits)
+template <int D, int R>  // R: rounds of loads per batch (R * 32 / (D/8) splits)
 __global__ void __launch_bounds__(256) tree_attn_combine_kernel(const AttnParams p, int B) {
   constexpr int kChunks = D / 8;            // 16-byte chunks of a partial row
   constexpr int kPerRound = 32 / kChunks;   // splits covered by one warp-wide load
@@ -1095,6 +1286,8 @@ __global__ void __launch_bounds__(256) tree_attn_combine_kernel(const AttnParams
   const int so = lane / kChunks;  // split offset within a round
   uint16_t *dst = p.out + (size_t)warp * D + c * 8;
 
+  // the device plan of sequence b, loaded beside its lengths (read only when b is valid)
+  const int4 plan = p.plan_mode == 2 ? __ldcg(&p.plan_out[b]) : make_int4(0, 0, 0, 0);
   int P, nb;
   const bool ok = seq_ok(p, b, P, nb) && node < nb;
   if (!ok) {
@@ -1104,21 +1297,37 @@ __global__ void __launch_bounds__(256) tree_attn_combine_kernel(const AttnParams
   }
   const int hkv = hq / p.g;
   const int row = node * p.g + (hq % p.g);
-  const size_t r0 = (size_t)(b * p.Hkv + hkv) * p.splits * p.rows_pad + row;
-  const int ns = (P + nb + p.chunk - 1) / p.chunk;  // <= R * kPerRound (host check)
-  // rows_pad is a multiple of 16, so every split's copy of this row has the
-  // same swizzle phase
-  const int pc = p.swizzled ? (c ^ (int)(r0 & (kChunks - 1))) : c;
-  const float4 ml = lane < ns ? __ldcg(&p.part_ml[r0 + (size_t)lane * p.rows_pad])
-                              : make_float4(-INFINITY, 0.f, 0.f, 0.f);
-  uint4 raw[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const int sp = r * kPerRound + so;
-    raw[r] = sp < ns ? __ldcg(reinterpret_cast<const uint4 *>(
-                           p.part_o + (r0 + (size_t)sp * p.rows_pad) * D + pc * 8))
-                     : make_uint4(0u, 0u, 0u, 0u);
+  // this row's partial for split 0, the distance between splits, their number
+  size_t r0, stride;
+  int ns;  // <= kMaxSplits
+  if (p.plan_mode == 2) {
+    const int4 pl = plan;  // (first item, splits, chunk, row tiles) of sequence b
+    r0 = ((size_t)pl.x + (size_t)hkv * pl.y * pl.w + row / kTcRows) * kTcRows + row % kTcRows;
+    stride = (size_t)pl.w * kTcRows;
+    ns = pl.y;
+  } else {
+    r0 = (size_t)(b * p.Hkv + hkv) * p.splits * p.rows_pad + row;
+    stride = p.rows_pad;
+    ns = (P + nb + p.chunk - 1) / p.chunk;
   }
+  // partial rows sit at multiples of 16 apart, so every split's copy of this
+  // row has the same swizzle phase
+  const int pc = p.swizzled ? (c ^ (int)(r0 & (kChunks - 1))) : c;
+  const float4 ml = lane < ns ? __ldcg(&p.part_ml[r0 + (size_t)lane * stride])
+                              : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+  // partials in batches of R rounds; every load of a batch is issued before
+  // any is used, the first batch before the weights are reduced
+  uint4 raw[R];
+  auto load_batch = [&](int s0) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int sp = s0 + r * kPerRound + so;
+      raw[r] = sp < ns ? __ldcg(reinterpret_cast<const uint4 *>(
+                             p.part_o + (r0 + (size_t)sp * stride) * D + pc * 8))
+                       : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  load_batch(0);
   float M = ml.x;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
@@ -1130,19 +1339,24 @@ __global__ void __launch_bounds__(256) tree_attn_combine_kernel(const AttnParams
   float acc[8];
 #pragma unroll
   for (int x = 0; x < 8; ++x) acc[x] = 0.f;
+  for (int s0 = 0;;) {  // ns is the same for the whole warp
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const int sp = r * kPerRound + so;
-    const float ws = __shfl_sync(0xffffffffu, w, sp & 31);
-    if (sp < ns) {
-      const uint32_t h[4] = {raw[r].x, raw[r].y, raw[r].z, raw[r].w};
+    for (int r = 0; r < R; ++r) {
+      const int sp = s0 + r * kPerRound + so;
+      const float ws = __shfl_sync(0xffffffffu, w, sp & 31);
+      if (sp < ns) {
+        const uint32_t h[4] = {raw[r].x, raw[r].y, raw[r].z, raw[r].w};
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h[k]));
-        acc[2 * k] += f.x * ws;
-        acc[2 * k + 1] += f.y * ws;
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h[k]));
+          acc[2 * k] += f.x * ws;
+          acc[2 * k + 1] += f.y * ws;
+        }
       }
     }
+    s0 += R * kPerRound;
+    if (s0 >= ns) break;
+    load_batch(s0);
   }
 #pragma unroll
   for (int off = kChunks; off < 32; off <<= 1)
@@ -1162,7 +1376,9 @@ cudaError_t launch_combine(const AttnParams &p, int B, cudaStream_t s) {
   constexpr int kPerRound = 32 / (D / 8);
   const long rows = (long)B * p.N_max * p.Hq;
   const dim3 grid((unsigned)((rows * 32 + 255) / 256));
-  const int rounds = (p.splits + kPerRound - 1) / kPerRound;
+  // one batch for the uniform split's count; under the device plan (counts
+  // known on the device only) batches of four rounds
+  const int rounds = p.plan_mode == 2 ? 4 : (p.splits + kPerRound - 1) / kPerRound;
   if (rounds <= 4) return launch(tree_attn_combine_kernel<D, 4>, grid, dim3(256), 0, s, p, B);
   if (rounds <= 8) return launch(tree_attn_combine_kernel<D, 8>, grid, dim3(256), 0, s, p, B);
   return launch(tree_attn_combine_kernel<D, 32 / kPerRound>, grid, dim3(256), 0, s, p, B);
@@ -1171,7 +1387,9 @@ cudaError_t launch_combine(const AttnParams &p, int B, cudaStream_t s) {
 struct AttnPlan {
   int impl;  // 0 tcgen05, 1 mma.sync
   int bm, bn, row_tiles, rows_pad, splits, chunk;
-  size_t o_bytes, ml_bytes;
+  int mode;          // plan_mode (AttnParams)
+  long grid_items;   // mode 2: blocks of the 1-D grid
+  size_t o_bytes, ml_bytes, plan_bytes;
 };
 
 AttnPlan plan_attn(int B, int N_max, int Hq, int Hkv, int D, int max_slots) {
@@ -1213,9 +1431,22 @@ AttnPlan plan_attn(int B, int N_max, int Hq, int Hkv, int D, int max_slots) {
   a.chunk = (int)chunk;
   a.splits = (int)((max_slots + chunk - 1) / chunk);
   if (a.splits < 1) a.splits = 1;
-  const size_t rows = (size_t)B * Hkv * a.splits * a.rows_pad;
+  const long items_u = units * a.splits;  // work items of the uniform split
+  // The device plan pays off only when lengths may differ (B > 1) and a
+  // uniform block would walk many tiles; it costs one small kernel.
+  a.mode = a.impl == 1 ? 0
+                       : (B > 1 && B <= kPlanMaxSeq && (a.chunk / a.bn) >= kPlanMinTiles ? 2 : 1);
+  a.grid_items = items_u;
+  size_t rows = (size_t)B * Hkv * a.splits * a.rows_pad;
+  if (a.mode == 2) {
+    // room for four waves of shorter pieces (at least the uniform split's
+    // blocks); blocks beyond the plan's items exit at once
+    a.grid_items = std::min(std::max(items_u, 4 * nsm), units * kMaxSplits);
+    rows = (size_t)a.grid_items * kTcRows;
+  }
   a.o_bytes = align_up(rows * D * sizeof(uint16_t), 256);
   a.ml_bytes = rows * sizeof(float4);
+  a.plan_bytes = a.mode == 2 ? ((size_t)B + (size_t)a.grid_items) * sizeof(int4) : 0;
   return a;
 }
 
@@ -1251,7 +1482,8 @@ bool make_cache_map(CUtensorMap *m, const uint16_t *cache, int num_blocks, int H
 
 template <int D>
 int launch_attn(AttnParams &p, const AttnPlan &a, int B, int num_blocks, cudaStream_t s) {
-  dim3 grid(p.row_tiles, p.splits, B * p.Hkv);
+  const dim3 grid = a.mode == 2 ? dim3((unsigned)a.grid_items)
+                                : dim3(p.row_tiles, p.splits, B * p.Hkv);
   if (a.impl == 0) {
     CUtensorMap k1, k8, v1, v8;
     if (!make_cache_map(&k1, p.k, num_blocks, p.Hkv, D, 1) ||
@@ -1260,6 +1492,8 @@ int launch_attn(AttnParams &p, const AttnPlan &a, int B, int num_blocks, cudaStr
         !make_cache_map(&v8, p.v, num_blocks, p.Hkv, D, kTcPagesPerTile))
       return TSD_ERR_CUDA;
     if (!set_smem((const void *)tree_attn_split_tc<D>, TcLayout<D>::kAlloc)) return TSD_ERR_CUDA;
+    if (a.mode == 2 && launch(tree_attn_plan_kernel, dim3(1), dim3(kTcThreads), 0, s, p) != cudaSuccess)
+      return TSD_ERR_CUDA;
     if (launch(tree_attn_split_tc<D>, grid, dim3(kTcThreads), TcLayout<D>::kAlloc, s, p, k1, k8, v1,
                v8) != cudaSuccess)
       return TSD_ERR_CUDA;
@@ -1282,6 +1516,8 @@ static int attn_check_dims(int B, int N_max, int Hq, int Hkv, int D, int max_slo
   if (N_max < 1 || N_max > tsd::kMaxNodes || (D != 64 && D != 128) || Hkv < 1 || Hq < Hkv ||
       Hq % Hkv != 0 || Hq / Hkv > 16 || B > 65535 || (long)B * Hkv > 65535)
     return TSD_ERR_LIMIT;
+  // a key range is cut into at most kMaxSplits pieces of at most kPlanMaxChunk tiles
+  if ((long)max_slots > (long)tsd::kMaxSplits * tsd::kPlanMaxChunk * tsd::kTcBN) return TSD_ERR_LIMIT;
   return TSD_OK;
 }
 
@@ -1289,7 +1525,7 @@ TSD_API size_t tsd_tree_attn_workspace_bytes(int B, int N_max, int Hq, int Hkv, 
                                              int max_slots) {
   if (attn_check_dims(B, N_max, Hq, Hkv, D, max_slots) != TSD_OK || B == 0) return 0;
   const tsd::AttnPlan a = tsd::plan_attn(B, N_max, Hq, Hkv, D, max_slots);
-  return a.o_bytes + a.ml_bytes;
+  return a.o_bytes + a.ml_bytes + a.plan_bytes;
 }
 
 TSD_API int tsd_tree_attn_fwd(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
@@ -1311,7 +1547,7 @@ TSD_API int tsd_tree_attn_fwd(const uint16_t *q, const uint16_t *k_cache, const 
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
     return TSD_ERR_ARG;
   const AttnPlan a = plan_attn(B, N_max, Hq, Hkv, D, max_slots);
-  if (!workspace || ws_bytes < a.o_bytes + a.ml_bytes || !aligned(workspace, 16))
+  if (!workspace || ws_bytes < a.o_bytes + a.ml_bytes + a.plan_bytes || !aligned(workspace, 16))
     return TSD_ERR_WORKSPACE;
   AttnParams p;
   p.q = q;
@@ -1337,6 +1573,14 @@ TSD_API int tsd_tree_attn_fwd(const uint16_t *q, const uint16_t *k_cache, const 
   p.rows_pad = a.rows_pad;
   p.part_o = static_cast<uint16_t *>(workspace);
   p.part_ml = reinterpret_cast<float4 *>(static_cast<char *>(workspace) + a.o_bytes);
+  p.plan_out = a.mode == 2 ? reinterpret_cast<int4 *>(static_cast<char *>(workspace) + a.o_bytes +
+                                                      a.ml_bytes)
+                           : nullptr;
+  p.plan_items = a.mode == 2 ? p.plan_out + B : nullptr;
+  p.B = B;
+  p.plan_mode = a.mode;
+  p.nsm = sm_count();
+  p.grid_items = (int)a.grid_items;
   p.out = out;
   p.lse = lse;
   p.status = status;
