@@ -467,7 +467,8 @@ struct TcLayout {
 // the larger C), with items <= the grid and n_b <= kMaxSplits.  For a batch
 // of equal lengths this is the host's uniform split; for ragged lengths long
 // sequences get more pieces, so they no longer set the kernel's duration.
-// Items are numbered sequence by sequence, then kv head, split, row tile.
+// Items are numbered by sequence (sequences with longer pieces first), then
+// kv head, split, row tile.
 constexpr int kPlanMaxSeq = 64;
 constexpr int kMaxSplits = 32;                               // pieces of one key range
 constexpr int kPlanMaxChunk = kTcMaxPages * kPage / kTcBN;   // 64 key tiles per item
@@ -512,6 +513,7 @@ __device__ __forceinline__ bool tc_wait(uint64_t &bar, uint32_t parity, uint64_t
 __global__ void __launch_bounds__(kTcThreads) tree_attn_plan_kernel(const AttnParams p) {
   __shared__ TcPlanShared ps;
   __shared__ int s_P[kPlanMaxSeq], s_nb[kPlanMaxSeq], s_first[kPlanMaxSeq + 1];
+  __shared__ int s_chunk[kPlanMaxSeq], s_items[kPlanMaxSeq], s_n[kPlanMaxSeq], s_order[kPlanMaxSeq];
   pdl_trigger();
   const int tid = threadIdx.x;
   const int B = p.B;
@@ -570,55 +572,50 @@ __global__ void __launch_bounds__(kTcThreads) tree_attn_plan_kernel(const AttnPa
   __syncthreads();
   // (no candidate: no sequence has work; every block gets b = -1)
   const int C = ps.best == ~0u ? 0 : kPlanMaxChunk - (int)(ps.best & 63u);
-  if (tid < 32) {
-    // first item of each sequence: two sequences per lane (tid, tid + 32),
-    // exclusive scans over the lanes
-    int n[2], items[2], first[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int s = tid + 32 * h;
-      const int t = (s < B && C > 0) ? ps.tiles[s] : 0;
-      n[h] = t > 0 ? (t + C - 1) / C : 0;
-      items[h] = t > 0 ? p.Hkv * ps.rtc[s] * n[h] : 0;
-      int incl = items[h];
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, off);
-        if (tid >= off) incl += y;
-      }
-      first[h] = incl - items[h];
-    }
-    const int half = __shfl_sync(0xffffffffu, first[0] + items[0], 31);
-    first[1] += half;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int s = tid + 32 * h;
-      if (s >= B) continue;
-      const int t = ps.tiles[s];
-      s_first[s] = first[h];
-      p.plan_out[s] = make_int4(first[h], n[h], n[h] > 0 ? (t + n[h] - 1) / n[h] : 0, ps.rtc[s]);
-    }
+  // Items are numbered sequence by sequence, the sequences taken in order of
+  // decreasing piece length (ties: increasing b), so the blocks dispatched
+  // first get the longest pieces and the short ones fill in behind them; a
+  // batch of equal lengths keeps the order b = 0, 1, ...
+  if (tid < B) {
+    const int t = C > 0 ? ps.tiles[tid] : 0;
+    const int n = t > 0 ? (t + C - 1) / C : 0;
+    s_chunk[tid] = n > 0 ? (t + n - 1) / n : 0;
+    s_items[tid] = n > 0 ? p.Hkv * ps.rtc[tid] * n : 0;
+    s_n[tid] = n;
   }
   __syncthreads();
-  if (tid < 32) {
-    // total items: the last sequence's first item plus its items
-    if (tid == 0) {
-      int total = 0;
-      if (B > 0 && C > 0) {
-        const int s = B - 1, t = ps.tiles[s];
-        total = s_first[s] + (t > 0 ? p.Hkv * ps.rtc[s] * ((t + C - 1) / C) : 0);
-      }
-      s_first[kPlanMaxSeq] = total;
-    }
+  if (tid < B) {
+    const int c = s_chunk[tid];
+    int rank = 0;
+    for (int s = 0; s < B; ++s) rank += (s_chunk[s] > c || (s_chunk[s] == c && s < tid)) ? 1 : 0;
+    s_order[rank] = tid;
   }
+  __syncthreads();
+  if (tid < 32) {  // exclusive scan of the items in rank order, two ranks per lane
+    const int r0 = 2 * tid, r1 = 2 * tid + 1;
+    const int i0 = r0 < B ? s_items[s_order[r0]] : 0;
+    const int i1 = r1 < B ? s_items[s_order[r1]] : 0;
+    int incl = i0 + i1;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (tid >= off) incl += y;
+    }
+    const int f0 = incl - i0 - i1;
+    if (r0 < B) s_first[s_order[r0]] = f0;
+    if (r1 < B) s_first[s_order[r1]] = f0 + i0;
+    if (tid == 31) s_first[kPlanMaxSeq] = incl;
+  }
+  __syncthreads();
+  if (tid < B) p.plan_out[tid] = make_int4(s_first[tid], s_n[tid], s_chunk[tid], ps.rtc[tid]);
   __syncthreads();
   const int total = s_first[kPlanMaxSeq];
   for (int k = tid; k < p.grid_items; k += blockDim.x) {
     int4 e = make_int4(-1, 0, 0, 0);
     if (k < total) {
-      int b = 0;  // the sequence whose items contain k (sequences without items are skipped)
-      for (int s = 1; s < B; ++s)
-        if (s_first[s] <= k && ps.tiles[s] > 0) b = s;
+      int b = -1;  // the sequence whose items contain k: the largest first item <= k
+      for (int s = 0; s < B; ++s)
+        if (ps.tiles[s] > 0 && s_first[s] <= k && (b < 0 || s_first[s] > s_first[b])) b = s;
       const int t = ps.tiles[b];
       const int rtc = ps.rtc[b];
       const int n = (t + C - 1) / C;
