@@ -40,6 +40,8 @@ from .best_first import best_first_tree, ranked_tokens
 from .rejection import modified_rejection_step, residual_distribution
 from .budget import verify_step_cost, calibrate, budget_select, cost_table
 from .stochastic import node_decision, tree_verify_stochastic, tree_verify_stochastic_all
+from .dynamic_tree import (dynamic_tree, expand_level, new_pool, pool_base, pool_size,
+                           rerank as dynamic_tree_rerank)
 
 __all__ = [
     "ERR_RANGE", "ERR_CYCLE", "ERR_TOO_DEEP", "ERR_CLOSURE", "ERR_ROOT", "ERR_COUNT",
@@ -48,4 +50,5 @@ __all__ = [
     "modified_rejection_step", "residual_distribution",
     "verify_step_cost", "calibrate", "budget_select", "cost_table",
     "node_decision", "tree_verify_stochastic", "tree_verify_stochastic_all",
+    "dynamic_tree", "expand_level", "new_pool", "pool_base", "pool_size", "dynamic_tree_rerank",
 ]
