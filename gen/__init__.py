@@ -285,6 +285,21 @@ def bastion_marginals(seed: Optional[int] = None):
     return q, root
 
 
+def dynamic_draft_rows(seed: int, b: int, pool_ids, V: int, temp: float = 1.0) -> np.ndarray:
+    """Stand-in for a drafter's per-node output in dynamic-tree construction:
+    the row of node (b, pool id) is softmax(z / temp), z ~ N(0,1) drawn from
+    a generator seeded by (seed, b, pool id), so every node has its own row and
+    the same node always gets the same row.  Softmax in fp64, rounded once to
+    fp32.  Returns float32 [len(pool_ids)][V]."""
+    rows = np.empty((len(pool_ids), V), dtype=np.float32)
+    for r, pid in enumerate(pool_ids):
+        rng = np.random.default_rng([seed, b, int(pid)])
+        z = rng.standard_normal(V) / temp
+        e = np.exp(z - z.max())
+        rows[r] = (e / e.sum()).astype(np.float32)
+    return rows
+
+
 def bastion_verify_inputs(parent: np.ndarray, tokens: np.ndarray, depth: np.ndarray,
                           draft_top1: np.ndarray, seed: Optional[int] = None) -> VerifyInputs:
     """Verify-layer inputs for a built budgeted tree.

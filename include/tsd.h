@@ -356,6 +356,53 @@ int tsd_best_first_tree_build(const float *q, const int32_t *root_token, int B, 
                               double *ahat, void *workspace, size_t ws_bytes, tsd_stream_t stream);
 
 /*
+ * Dynamic draft trees ([Blog] EAGLE-2 section: the tree grows deep where the
+ * drafter is confident and wide where it is uncertain; the page gives no
+ * algorithm.  Reading: node confidence is [BASTION]'s path score, an fp32
+ * product of draft probabilities along the path; expansion is level by level
+ * with a frontier of the k best nodes; the N-node tree keeps the N-1 best).
+ *
+ * Pool (caller-owned, per sequence M_max entries): pool_parent, pool_token,
+ * pool_depth int32 [B][M_max], pool_score float [B][M_max].  The root is pool
+ * id 0 (parent -1, depth 0, score 1); level 1 holds ids 1..k; level l >= 2
+ * holds 1 + k + (l-2) k^2 + f k + j for frontier slot f and token rank j.
+ *
+ * tsd_dynamic_tree_expand: one level.  Each of the F frontier nodes (F = 1 at
+ * level 1 -- the root, whose entry this call writes from root_token[b] --
+ * and F = k after) takes its k best tokens from its draft row q[b][f] (token
+ * rank: q desc, lower id first on ties) as children with score
+ * fl32(score(parent) * q); next_frontier[b] = the level's k best nodes by
+ * (score desc, pool id asc).
+ *   q             float [B][F][V], the drafter's distribution at each
+ *                 frontier node, in frontier order (values in [0, 1]);
+ *   root_token    int32 [B] (level 1 only, else ignored, may be NULL);
+ *   frontier      int32 [B][F] pool ids (level >= 2; NULL at level 1): the
+ *                 previous call's next_frontier;
+ *   next_frontier int32 [B][k] out, must not be `frontier`.
+ * Limits: 1 <= k <= 32, V >= k, the level's ids below M_max <= 8192, B <= 65535
+ * (TSD_ERR_LIMIT); F other than 1 / k: TSD_ERR_ARG.  A frontier id outside
+ * [0, M_max) gives children with parent -1 and score 0.
+ * workspace >= tsd_dynamic_tree_workspace_bytes(B, F, k) (no initial contents).
+ *
+ * tsd_dynamic_tree_rerank: the root and the N-1 best of pool ids 1..M-1 by
+ * (score desc, depth asc, pool id asc), in that order, into parent (re-indexed
+ * to output positions; -1 for the root), tokens, depth int32 [B][N] and score
+ * float [B][N].  A child never outscores its parent (q <= 1) and ranks after it,
+ * so parents are kept and come first: the output is an a1-ready parent array.
+ * Limits: 1 <= N <= 256, N <= M <= M_max <= 8192.
+ */
+size_t tsd_dynamic_tree_workspace_bytes(int B, int F, int k);
+int tsd_dynamic_tree_expand(const float *q, const int32_t *root_token, int B, int F, int V, int k,
+                            int level, const int32_t *frontier, int32_t *pool_parent,
+                            int32_t *pool_token, int32_t *pool_depth, float *pool_score, int M_max,
+                            int32_t *next_frontier, void *workspace, size_t ws_bytes,
+                            tsd_stream_t stream);
+int tsd_dynamic_tree_rerank(const int32_t *pool_parent, const int32_t *pool_token,
+                            const int32_t *pool_depth, const float *pool_score, int B, int M,
+                            int M_max, int N, int32_t *parent, int32_t *tokens, int32_t *depth,
+                            float *score, tsd_stream_t stream);
+
+/*
  * Tree budget ([BASTION] Methodology 3, hardware-aware online budget
  * controller): T_verify(N) from a roofline model of bandwidth and compute,
  * calibrated with measured step times; the tree grows until

@@ -53,6 +53,10 @@ SIGNATURES = {
                                 _I, _P, _P, _P, _P]),
     "tsd_best_first_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "tsd_best_first_tree_build": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "tsd_dynamic_tree_workspace_bytes": (_SZ, [_I, _I, _I]),
+    "tsd_dynamic_tree_expand": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P,
+                                     _SZ, _P]),
+    "tsd_dynamic_tree_rerank": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "tsd_verify_step_cost": (_I, [_I, _I, _I, _I, _P, _I, _I, _I, _D, _D, _P, _P, _P]),
     "tsd_budget_calibrate": (_I, [_P, _P, _I, _P, _P]),
     "tsd_budget_select": (_I, [_P, _I, _I, _P, _F, _P, _P, _P]),
@@ -341,6 +345,79 @@ def best_first_tree_build(q, root_token, N, parent=None, tokens=None, depth=None
         workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "best_first_tree_build")
     return parent, tokens, depth, rho, ahat
+
+
+# ---------------------------------------------------------------------------
+# dynamic draft trees
+# ---------------------------------------------------------------------------
+
+
+def dynamic_tree_pool_base(level: int, k: int) -> int:
+    """First pool id of an expansion level (level >= 1)."""
+    return 1 if level == 1 else 1 + k + (level - 2) * k * k
+
+
+def dynamic_tree_pool_size(levels: int, k: int) -> int:
+    """Pool ids used by `levels` levels, root included."""
+    if levels == 0:
+        return 1
+    return dynamic_tree_pool_base(levels, k) + (k if levels == 1 else k * k)
+
+
+def dynamic_tree_new_pool(B: int, M_max: int, device):
+    """Pool arrays (parent, token, depth int32, score float32), [B][M_max]."""
+    i32 = dict(dtype=torch.int32, device=device)
+    return (torch.empty((B, M_max), **i32), torch.empty((B, M_max), **i32),
+            torch.empty((B, M_max), **i32), torch.empty((B, M_max), dtype=torch.float32,
+                                                         device=device))
+
+
+def dynamic_tree_workspace_bytes(B: int, F: int, k: int) -> int:
+    return int(lib.tsd_dynamic_tree_workspace_bytes(B, F, k))
+
+
+def dynamic_tree_expand(q, k, level, pool, root_token=None, frontier=None, next_frontier=None,
+                        workspace=None, stream=None):
+    """One expansion level.  q float32 [B][F][V]: the draft rows of the F
+    frontier nodes (F = 1 at level 1: the root).  pool: the four [B][M_max]
+    arrays (updated).  Returns the next frontier, int32 [B][k]."""
+    B, F, V = q.shape
+    par, tok, dep, sco = pool
+    M_max = par.shape[1]
+    next_frontier = next_frontier if next_frontier is not None else _empty((B, k), torch.int32, q)
+    need = dynamic_tree_workspace_bytes(B, F, k)
+    if workspace is None:
+        workspace = _empty((max(need, 1),), torch.uint8, q)
+    rc = lib.tsd_dynamic_tree_expand(
+        _ptr(q, torch.float32, "q"),
+        _ptr(root_token, torch.int32, "root_token") if root_token is not None else None,
+        B, F, V, k, level,
+        _ptr(frontier, torch.int32, "frontier") if frontier is not None else None,
+        _ptr(par, torch.int32, "pool_parent"), _ptr(tok, torch.int32, "pool_token"),
+        _ptr(dep, torch.int32, "pool_depth"), _ptr(sco, torch.float32, "pool_score"), M_max,
+        _ptr(next_frontier, torch.int32, "next_frontier"), _ptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "dynamic_tree_expand")
+    return next_frontier
+
+
+def dynamic_tree_rerank(pool, M, N, parent=None, tokens=None, depth=None, score=None,
+                        stream=None):
+    """The N-node draft tree from pool ids 0..M-1.  Returns (parent, tokens,
+    depth int32 [B][N], score float32 [B][N])."""
+    par, tok, dep, sco = pool
+    B, M_max = par.shape
+    parent = parent if parent is not None else _empty((B, N), torch.int32, par)
+    tokens = tokens if tokens is not None else _empty((B, N), torch.int32, par)
+    depth = depth if depth is not None else _empty((B, N), torch.int32, par)
+    score = score if score is not None else _empty((B, N), torch.float32, par)
+    rc = lib.tsd_dynamic_tree_rerank(
+        _ptr(par, torch.int32, "pool_parent"), _ptr(tok, torch.int32, "pool_token"),
+        _ptr(dep, torch.int32, "pool_depth"), _ptr(sco, torch.float32, "pool_score"), B, M, M_max,
+        N, _ptr(parent, torch.int32, "parent"), _ptr(tokens, torch.int32, "tokens"),
+        _ptr(depth, torch.int32, "depth"), _ptr(score, torch.float32, "score"), _stream(stream))
+    _check(rc, "dynamic_tree_rerank")
+    return parent, tokens, depth, score
 
 
 # ---------------------------------------------------------------------------

@@ -19,6 +19,16 @@
 // warp max-reductions (rho bits, then (depth, parent) as a tie key) over
 // candidate keys held in shared memory.
 
+//
+// Dynamic draft trees ("Speculative Decoding Hierarquico: Medusa, EAGLE-2 e
+// Multi-Token Prediction", EAGLE-2 section: deep where the drafter is
+// confident, wide where it is not), built level by level with the path score
+// above as node confidence: each frontier node's top-k tokens (topk_kernel on
+// its draft row) become its children; one block per sequence scores them,
+// writes them to the node pool and keeps the level's k best as the next
+// frontier (bitonic sort in shared memory); the rerank kernel keeps the N-1
+// best pool nodes, in rank order, with parents re-indexed.
+
 #include "tsd_common.cuh"
 
 namespace tsd {
@@ -281,8 +291,211 @@ long long valid_nodes(int K, int V) {
   return total;
 }
 
+// ---------------------------------------------------------------------------
+// Dynamic draft trees.  Pool layout per sequence: root at 0; level 1 at 1..k;
+// level l >= 2 at 1 + k + (l-2) k^2 + f k + j (frontier slot f, token rank j).
+
+constexpr int kDynMaxK = 32;         // tokens per expanded node, frontier width
+constexpr int kDynMaxPool = 8192;    // pool ids per sequence (rerank sorts them in shared memory)
+constexpr int kDynThreads = 1024;
+
+__host__ __device__ inline long dyn_base(int level, int k) {
+  return level == 1 ? 1L : 1L + k + (long)(level - 2) * k * k;
+}
+
+// Bitonic sort of n (a power of two, <= 2 * blockDim.x * ...) keys in shared
+// memory, descending; every thread of the block calls it.
+__device__ void bitonic_desc(unsigned long long *keys, int n) {
+  for (int size = 2; size <= n; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int l = i ^ stride;
+        if (l > i) {
+          const unsigned long long a = keys[i], c = keys[l];
+          const bool up = (i & size) == 0;
+          if (up ? (a < c) : (a > c)) {
+            keys[i] = c;
+            keys[l] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// One block per sequence: the F * k children of one level.  Child c = f k + j
+// of frontier node frontier[f] takes token top_tok[f][j] with score
+// fl32(score(parent) * top_q[f][j]); the next frontier is the k best children
+// by (score desc, pool id asc).
+__global__ void __launch_bounds__(kDynThreads)
+dyn_expand_kernel(const int32_t *__restrict__ top_tok, const float *__restrict__ top_q,
+                  const int32_t *__restrict__ root_token, const int32_t *__restrict__ frontier,
+                  int F, int k, int level, int M_max, int32_t *__restrict__ pool_parent,
+                  int32_t *__restrict__ pool_token, int32_t *__restrict__ pool_depth,
+                  float *__restrict__ pool_score, int32_t *__restrict__ next_frontier) {
+  __shared__ unsigned long long s_key[kDynMaxK * kDynMaxK];
+  __shared__ float s_pscore[kDynMaxK];
+  __shared__ int32_t s_parent[kDynMaxK];
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.x, t = threadIdx.x;
+  const size_t pb = (size_t)b * M_max;
+  if (level == 1 && t == 0) {
+    pool_parent[pb] = -1;
+    pool_token[pb] = root_token[b];
+    pool_depth[pb] = 0;
+    pool_score[pb] = 1.f;
+  }
+  if (t < F) {
+    // a frontier id outside the pool (not one a previous level wrote) gives
+    // children with parent -1 and score 0, which a1 then rejects
+    int par = level == 1 ? 0 : frontier[(size_t)b * F + t];
+    const bool ok = par >= 0 && par < M_max;
+    par = ok ? par : -1;
+    s_parent[t] = par;
+    s_pscore[t] = level == 1 ? 1.f : (ok ? pool_score[pb + par] : 0.f);
+  }
+  const int n = F * k;
+  int n2 = 1;
+  while (n2 < n) n2 <<= 1;
+  __syncthreads();
+  const long base = dyn_base(level, k);
+  for (int c = t; c < n2; c += blockDim.x) {
+    unsigned long long key = 0ull;
+    if (c < n) {
+      const int f = c / k;
+      const size_t src = ((size_t)b * F + f) * k + (c - f * k);
+      const float sc = __fmul_rn(s_pscore[f], top_q[src]);
+      const long pid = base + c;
+      pool_parent[pb + pid] = s_parent[f];
+      pool_token[pb + pid] = top_tok[src];
+      pool_depth[pb + pid] = level;
+      pool_score[pb + pid] = sc;
+      key = ((unsigned long long)order_key(sc) << 32) | (unsigned long long)(0xFFFFFFFFu - (unsigned)pid);
+    }
+    s_key[c] = key;
+  }
+  __syncthreads();
+  bitonic_desc(s_key, n2);
+  if (t < k) next_frontier[(size_t)b * k + t] = (int32_t)(0xFFFFFFFFu - (unsigned)(s_key[t] & 0xFFFFFFFFull));
+}
+
+// One block per sequence: the root and the N-1 best of pool ids 1..M-1 by
+// (score desc, depth asc, pool id asc), in that order; parents re-indexed to
+// output positions (-1 for the root, and for a node whose parent was not kept,
+// which draft probabilities <= 1 rule out).
+__global__ void __launch_bounds__(kDynThreads)
+dyn_rerank_kernel(const int32_t *__restrict__ pool_parent, const int32_t *__restrict__ pool_token,
+                  const int32_t *__restrict__ pool_depth, const float *__restrict__ pool_score,
+                  int M, int M_max, int N, int32_t *__restrict__ parent,
+                  int32_t *__restrict__ tokens, int32_t *__restrict__ depth,
+                  float *__restrict__ score) {
+  extern __shared__ unsigned long long s_keys[];  // [n2], then int32 map [M]
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.x, t = threadIdx.x;
+  const size_t pb = (size_t)b * M_max;
+  const int n = M - 1;
+  int n2 = 1;
+  while (n2 < n) n2 <<= 1;
+  int32_t *s_map = reinterpret_cast<int32_t *>(s_keys + n2);
+  for (int i = t; i < n2; i += blockDim.x) {
+    unsigned long long key = 0ull;
+    if (i < n) {
+      const int pid = i + 1;
+      const unsigned dk = 31u - (unsigned)min(max(pool_depth[pb + pid], 0), 31);
+      key = ((unsigned long long)order_key(pool_score[pb + pid]) << 32) |
+            (unsigned long long)((dk << 27) | (0x7FFFFFFu - (unsigned)pid));
+    }
+    s_keys[i] = key;
+  }
+  for (int i = t; i < M; i += blockDim.x) s_map[i] = -1;
+  __syncthreads();
+  bitonic_desc(s_keys, n2);
+  const size_t ob = (size_t)b * N;
+  if (t == 0) s_map[0] = 0;
+  for (int r = t; r < N - 1; r += blockDim.x)
+    s_map[0x7FFFFFF - (int)(s_keys[r] & 0x7FFFFFFull)] = r + 1;
+  __syncthreads();
+  for (int r = t; r < N; r += blockDim.x) {
+    const int pid = r == 0 ? 0 : 0x7FFFFFF - (int)(s_keys[r - 1] & 0x7FFFFFFull);
+    const int pp = pool_parent[pb + pid];
+    parent[ob + r] = (r == 0 || pp < 0 || pp >= M) ? -1 : s_map[pp];
+    tokens[ob + r] = pool_token[pb + pid];
+    depth[ob + r] = pool_depth[pb + pid];
+    score[ob + r] = pool_score[pb + pid];
+  }
+}
+
+size_t dyn_rerank_smem(int M) {
+  int n2 = 1;
+  while (n2 < M - 1) n2 <<= 1;
+  return (size_t)n2 * sizeof(unsigned long long) + (size_t)M * sizeof(int32_t);
+}
+
 }  // namespace
 }  // namespace tsd
+
+TSD_API size_t tsd_dynamic_tree_workspace_bytes(int B, int F, int k) {
+  if (B <= 0 || F <= 0 || k <= 0 || F > tsd::kDynMaxK || k > tsd::kDynMaxK) return 0;
+  return tsd::align_up((size_t)B * F * k * sizeof(int32_t), 256) + (size_t)B * F * k * sizeof(float);
+}
+
+TSD_API int tsd_dynamic_tree_expand(const float *q, const int32_t *root_token, int B, int F, int V,
+                                    int k, int level, const int32_t *frontier,
+                                    int32_t *pool_parent, int32_t *pool_token, int32_t *pool_depth,
+                                    float *pool_score, int M_max, int32_t *next_frontier,
+                                    void *workspace, size_t ws_bytes, tsd_stream_t stream) {
+  using namespace tsd;
+  if (B < 0) return TSD_ERR_ARG;
+  if (k < 1 || k > kDynMaxK || level < 1 || V < k || B > 65535 || M_max < 1 ||
+      M_max > kDynMaxPool)
+    return TSD_ERR_LIMIT;
+  if (F != (level == 1 ? 1 : k)) return TSD_ERR_ARG;
+  if (dyn_base(level, k) + (long)F * k > (long)M_max) return TSD_ERR_LIMIT;
+  if (B == 0) return TSD_OK;
+  if (!q || !pool_parent || !pool_token || !pool_depth || !pool_score || !next_frontier)
+    return TSD_ERR_ARG;
+  if (level == 1 ? !root_token : !frontier) return TSD_ERR_ARG;
+  if (frontier && frontier == next_frontier) return TSD_ERR_ARG;
+  const size_t tok_bytes = align_up((size_t)B * F * k * sizeof(int32_t), 256);
+  if (!workspace || ws_bytes < tok_bytes + (size_t)B * F * k * sizeof(float) ||
+      !aligned(workspace, 16))
+    return TSD_ERR_WORKSPACE;
+  int32_t *top_tok = static_cast<int32_t *>(workspace);
+  float *top_q = reinterpret_cast<float *>(static_cast<char *>(workspace) + tok_bytes);
+  cudaStream_t s = as_cuda(stream);
+  if (launch(topk_kernel, dim3(F, B), dim3(kTopThreads), 0, s, q, F, V, k, top_tok, top_q) !=
+      cudaSuccess)
+    return TSD_ERR_CUDA;
+  if (launch(dyn_expand_kernel, dim3(B), dim3(kDynThreads), 0, s, top_tok, top_q, root_token,
+             frontier, F, k, level, M_max, pool_parent, pool_token, pool_depth, pool_score,
+             next_frontier) != cudaSuccess)
+    return TSD_ERR_CUDA;
+  return TSD_OK;
+}
+
+TSD_API int tsd_dynamic_tree_rerank(const int32_t *pool_parent, const int32_t *pool_token,
+                                    const int32_t *pool_depth, const float *pool_score, int B,
+                                    int M, int M_max, int N, int32_t *parent, int32_t *tokens,
+                                    int32_t *depth, float *score, tsd_stream_t stream) {
+  using namespace tsd;
+  if (B < 0) return TSD_ERR_ARG;
+  if (N < 1 || N > kMaxNodes || M < N || M > M_max || M_max > kDynMaxPool || B > 65535)
+    return TSD_ERR_LIMIT;
+  if (B == 0) return TSD_OK;
+  if (!pool_parent || !pool_token || !pool_depth || !pool_score || !parent || !tokens || !depth ||
+      !score)
+    return TSD_ERR_ARG;
+  const size_t smem = dyn_rerank_smem(M);
+  if (!set_smem((const void *)dyn_rerank_kernel, dyn_rerank_smem(kDynMaxPool))) return TSD_ERR_CUDA;
+  if (launch(dyn_rerank_kernel, dim3(B), dim3(kDynThreads), smem, as_cuda(stream), pool_parent,
+             pool_token, pool_depth, pool_score, M, M_max, N, parent, tokens, depth, score) !=
+      cudaSuccess)
+    return TSD_ERR_CUDA;
+  return TSD_OK;
+}
 
 TSD_API size_t tsd_best_first_workspace_bytes(int B, int K, int V, int N) {
   if (B <= 0 || K <= 0 || V <= 0 || N <= 0) return 0;
