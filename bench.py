@@ -60,6 +60,12 @@ def workload_inputs(name):
         return ("bastion", N, q, root), ("BASTION-style budgeted tree: B=8, K=16, V=32000 "
                                          "marginals, best-first budget N=%d, verify on Hq=32, "
                                          "Hkv=8, D=128, prefix 2048" % N)
+    if name == "dynamic":
+        c = gen.DYNAMIC
+        return ("dynamic", c), ("EAGLE-2-style dynamic draft tree: B=%d, V=%d, top-%d expansion "
+                                "over %d levels (drafter rows resident), rerank to N=%d, verify "
+                                "on Hq=32, Hkv=8, D=128, prefix 2048"
+                                % (c["B"], c["V"], c["k"], c["levels"], c["N"]))
     return gen.verify_workload(name), DESCRIPTIONS[name]
 
 
@@ -300,7 +306,8 @@ def gpu_arm(args, rank, world):
     stream = torch.cuda.current_stream()
 
     w, desc = workload_inputs(args.workload)
-    bastion = isinstance(w, tuple)
+    bastion = isinstance(w, tuple) and w[0] == "bastion"
+    dynamic = isinstance(w, tuple) and w[0] == "dynamic"
 
     def T(a, dtype=None):
         t = torch.from_numpy(np.ascontiguousarray(a))
@@ -321,6 +328,34 @@ def gpu_arm(args, rank, world):
         par_h, tok_h, dep_h = [x.cpu().numpy() for x in bf_out]
         top1 = np.argmax(q_marg, axis=-1)  # input synthesis only: plants target choices
         inp = gen.bastion_verify_inputs(par_h, tok_h, dep_h, top1)
+    elif dynamic:
+        # The drafter's rows for every level's frontier are generated once on
+        # the host (seeded per node) and kept in HBM; the timed step runs the
+        # level-by-level expansion on them, the rerank, and a1-a4 on the tree.
+        dc = w[1]
+        dB, dV, dk, dL, dN = dc["B"], dc["V"], dc["k"], dc["levels"], dc["N"]
+        dM = tsd.dynamic_tree_pool_size(dL, dk)
+        d_pool = tsd.dynamic_tree_new_pool(dB, dM, dev)
+        d_root = T(np.random.default_rng(dc["seed"]).integers(0, dV, size=dB).astype(np.int32))
+        d_fr = [None] + [torch.empty((dB, dk), dtype=torch.int32, device=dev) for _ in range(dL)]
+        d_ws = torch.empty(tsd.dynamic_tree_workspace_bytes(dB, dk, dk), dtype=torch.uint8,
+                           device=dev)
+        d_rows = []
+        fr_h = np.zeros((dB, 1), dtype=np.int32)
+        for level in range(1, dL + 1):
+            rows = np.stack([gen.dynamic_draft_rows(dc["seed"], b, fr_h[b], dV, dc["temp"])
+                             for b in range(dB)])
+            d_rows.append(T(rows))
+            tsd.dynamic_tree_expand(d_rows[-1], dk, level, d_pool, root_token=d_root,
+                                    frontier=d_fr[level - 1], next_frontier=d_fr[level],
+                                    workspace=d_ws)
+            fr_h = d_fr[level].cpu().numpy()
+        d_tree = [torch.empty((dB, dN), dtype=torch.int32, device=dev) for _ in range(3)]
+        d_score = torch.empty((dB, dN), dtype=torch.float32, device=dev)
+        tsd.dynamic_tree_rerank(d_pool, dM, dN, *d_tree, d_score)
+        torch.cuda.synchronize()
+        par_h, tok_h, dep_h = [x.cpu().numpy() for x in d_tree]
+        inp = gen.dynamic_verify_inputs(par_h, tok_h, dep_h)
     else:
         inp = w
 
@@ -334,6 +369,8 @@ def gpu_arm(args, rank, world):
         del q_draft_h
     parent, n_nodes, prefix = T(inp.parent), T(inp.n_nodes), T(inp.prefix_len)
     tokens, logits, q = T(inp.tokens), T(inp.logits), T(inp.q, torch.bfloat16)
+    if dynamic:  # a1-a4 read the tree the rerank writes every step
+        parent, tokens = d_tree[0], d_tree[1]
     table = T(c.block_table)
     kc, vc = T(c.k, torch.bfloat16), T(c.v, torch.bfloat16)
     max_slots = int((inp.prefix_len + inp.n_nodes).max())
@@ -370,14 +407,25 @@ def gpu_arm(args, rank, world):
         flush_rd.sum()
 
     verify_name = "tree_verify_stochastic" if stochastic else "tree_verify_greedy"
-    names = (["best_first_tree_build"] if bastion else []) + [
-        "tree_build_ancestors", "tree_attn_fwd", verify_name, "kv_commit_path"]
-    launches_per_step = (2 if bastion else 0) + 1 + 2 + 1 + 1
+    names = ((["best_first_tree_build"] if bastion else [])
+             + (["dynamic_tree_expand", "dynamic_tree_rerank"] if dynamic else [])
+             + ["tree_build_ancestors", "tree_attn_fwd", verify_name, "kv_commit_path"])
+    launches_per_step = ((2 if bastion else 0) + (2 * dL + 1 if dynamic else 0) + 1
+                         + tsd.tree_attn_launches(B, N, Hq, Hkv, D, max_slots) + 1 + 1)
 
     calls = {}
     if bastion:
         calls["best_first_tree_build"] = lambda: tsd.best_first_tree_build(
             qd, rootd, N_b, *bf_out, rho, ahat, workspace=bf_ws)
+    if dynamic:
+        def expand_all():
+            for level in range(1, dL + 1):
+                tsd.dynamic_tree_expand(d_rows[level - 1], dk, level, d_pool, root_token=d_root,
+                                        frontier=d_fr[level - 1], next_frontier=d_fr[level],
+                                        workspace=d_ws)
+        calls["dynamic_tree_expand"] = expand_all
+        calls["dynamic_tree_rerank"] = lambda: tsd.dynamic_tree_rerank(
+            d_pool, dM, dN, *d_tree, d_score)
     calls["tree_build_ancestors"] = lambda: tsd.tree_build_ancestors(
         parent, n_nodes, Dm, anc, depth, mask, err)
     calls["tree_attn_fwd"] = lambda: tsd.tree_attn_fwd(
@@ -506,6 +554,9 @@ def gpu_arm(args, rank, world):
             "prefix_len": prefix}
     if stochastic:
         h_in.update({"q_draft": q_draft, "u_accept": u_acc, "u_draw": u_drw})
+    if dynamic:  # the drafter's rows are the inputs; the tree is built on the device
+        del h_in["parent"], h_in["tokens"]
+        h_in.update({"draft_rows_%d" % (i + 1): r for i, r in enumerate(d_rows)})
     pinned = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in h_in.items()}
     for k, v in h_in.items():
         pinned[k].copy_(v.cpu())
@@ -544,6 +595,9 @@ def gpu_arm(args, rank, world):
         abytes["tree_verify_stochastic"] = (4 * V * (internal_rows + rejected_rows + leaf_draws)
                                             + 4 * 4 * B * N)
         del abytes["tree_verify_greedy"]
+    if dynamic:
+        # each level reads its frontier's draft rows once
+        abytes["dynamic_tree_expand"] = sum(4 * r.numel() for r in d_rows)
     step_bytes = sum(abytes.values())
     dom = max(["tree_attn_fwd", verify_name], key=lambda n: kernel_us[n])
     achieved = abytes[dom] / (kernel_us[dom] * 1e-6) / 1e9
@@ -844,7 +898,7 @@ def main(argv=None):
         dist.init_process_group("nccl")
     base = None
     if (rank == 0 and world == 1 and not args.no_cpu_baseline and args.verify == "greedy"
-            and not args.workload.startswith("bastion")):
+            and not args.workload.startswith("bastion") and args.workload != "dynamic"):
         base = cpu_baseline(args.workload)
     res = (budget_arm if args.workload == "bastion-budget" else gpu_arm)(args, rank, world)
     if rank == 0:
@@ -860,7 +914,8 @@ def reference_arm(args, world):
     """The oracle, as it stands, on the host cores: each step is a bounded
     sample of the workload (attention on a sample of rows, the rest in full),
     scaled to full-step units."""
-    name = args.workload if not args.workload.startswith("bastion") else "8b"
+    name = args.workload if not (args.workload.startswith("bastion")
+                                 or args.workload == "dynamic") else "8b"
     threads = os.cpu_count() or 1
     frac = oracle_sample_fraction(name)
     # size the run to a few minutes at most: measure one sampled step first

@@ -330,6 +330,40 @@ def bastion_verify_inputs(parent: np.ndarray, tokens: np.ndarray, depth: np.ndar
                         logits=logits, q=q, cache=cache, targets=targets)
 
 
+DYNAMIC = dict(B=8, V=32000, k=10, levels=6, N=64, temp=1.0, seed=5)
+
+
+def dynamic_verify_inputs(parent: np.ndarray, tokens: np.ndarray, depth: np.ndarray,
+                          seed: Optional[int] = None) -> VerifyInputs:
+    """Verify-layer inputs (the 8B shape with prefix 2048, V = 32000) for a
+    dynamic draft tree [B][N] in rank order.  The planted target of node i is,
+    with probability 0.6, the token of its first child in the tree (a node's
+    kept children are its best-ranked tokens, so the first is the drafter's
+    top choice there); otherwise, and for leaves, a uniform token."""
+    c = BASTION
+    B, N = parent.shape
+    rng = np.random.default_rng((DYNAMIC["seed"] if seed is None else seed) * 1000 + N)
+    targets = rng.integers(0, c["V"], size=(B, N)).astype(np.int32)
+    coin = rng.random((B, N))
+    for b in range(B):
+        first_child = {}
+        for i in range(1, N):
+            first_child.setdefault(int(parent[b, i]), i)
+        for i in range(N):
+            if i in first_child and coin[b, i] < c["p_match"]:
+                targets[b, i] = tokens[b, first_child[i]]
+    logits = rng.standard_normal(size=(B, N, c["V"]), dtype=np.float32) * np.float32(np.sqrt(2.0))
+    plant_targets(logits, targets)
+    q = normal_bf16(rng, (B, N, c["Hq"], c["D"]))
+    prefix_len = np.full(B, c["prefix"], dtype=np.int32)
+    n_nodes = np.full(B, N, dtype=np.int32)
+    cache = paged_cache(rng, prefix_len, n_nodes, c["Hkv"], c["D"], shuffle=False)
+    return VerifyInputs(name="dynamic%d" % N, B=B, N_max=N, Hq=c["Hq"], Hkv=c["Hkv"], D=c["D"],
+                        V=c["V"], D_max=max(1, int(depth.max())), parent=parent.astype(np.int32),
+                        n_nodes=n_nodes, prefix_len=prefix_len, tokens=tokens.astype(np.int32),
+                        logits=logits, q=q, cache=cache, targets=targets)
+
+
 def random_small(seed: int, B: int, N_max: int, Hq: int, Hkv: int, D: int, V: int,
                  prefix_lo: int, prefix_hi: int, max_depth: int, p_match: float = 0.6,
                  ragged_nodes: bool = True, shuffle_blocks: bool = True,

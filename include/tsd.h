@@ -173,6 +173,10 @@ int tsd_tree_build_ancestors(const int32_t *parent, const int32_t *n_nodes, int 
  * status      int32 device word (see TSD_STATUS_*), may be NULL.
  */
 size_t tsd_tree_attn_workspace_bytes(int B, int N_max, int Hq, int Hkv, int D, int max_slots);
+/* Kernels one tsd_tree_attn_fwd call launches for these sizes on the current
+ * device (2: split + merge; 3 with the device-side split plan); 0 for sizes
+ * it rejects.  Host only. */
+int tsd_tree_attn_launches(int B, int N_max, int Hq, int Hkv, int D, int max_slots);
 int tsd_tree_attn_fwd(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                       const int32_t *block_table, int max_blocks, int num_blocks,
                       const int32_t *prefix_len, const int32_t *n_nodes, const uint32_t *mask,

@@ -37,6 +37,7 @@ SIGNATURES = {
     "tsd_get_option": (_I64, [_I]),
     "tsd_tree_build_ancestors": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "tsd_tree_attn_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "tsd_tree_attn_launches": (_I, [_I, _I, _I, _I, _I, _I]),
     "tsd_tree_attn_fwd": (_I, [_P, _P, _P, _P, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F,
                                _P, _P, _P, _SZ, _P, _P]),
     "tsd_tree_verify_workspace_bytes": (_SZ, [_I, _I, _I]),
@@ -140,6 +141,11 @@ def tree_build_ancestors(parent, n_nodes, D_max, anc=None, depth=None, mask=None
 
 def tree_attn_workspace_bytes(B, N_max, Hq, Hkv, D, max_slots) -> int:
     return int(lib.tsd_tree_attn_workspace_bytes(B, N_max, Hq, Hkv, D, max_slots))
+
+
+def tree_attn_launches(B, N_max, Hq, Hkv, D, max_slots) -> int:
+    """Kernels one tree_attn_fwd call launches for these sizes."""
+    return int(lib.tsd_tree_attn_launches(B, N_max, Hq, Hkv, D, max_slots))
 
 
 def tree_attn_fwd(q, k_cache, v_cache, block_table, prefix_len, n_nodes, mask, err, max_slots,

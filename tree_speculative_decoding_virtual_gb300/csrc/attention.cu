@@ -1525,6 +1525,12 @@ TSD_API size_t tsd_tree_attn_workspace_bytes(int B, int N_max, int Hq, int Hkv, 
   return a.o_bytes + a.ml_bytes + a.plan_bytes;
 }
 
+TSD_API int tsd_tree_attn_launches(int B, int N_max, int Hq, int Hkv, int D, int max_slots) {
+  if (attn_check_dims(B, N_max, Hq, Hkv, D, max_slots) != TSD_OK || B == 0) return 0;
+  const tsd::AttnPlan a = tsd::plan_attn(B, N_max, Hq, Hkv, D, max_slots);
+  return a.mode == 2 ? 3 : 2;
+}
+
 TSD_API int tsd_tree_attn_fwd(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                               const int32_t *block_table, int max_blocks, int num_blocks,
                               const int32_t *prefix_len, const int32_t *n_nodes,
