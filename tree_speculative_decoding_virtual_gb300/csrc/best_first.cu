@@ -7,11 +7,12 @@
 // adds the valid node with the largest rho.
 //
 // Kernel 1 (one block per (position, sequence)): the M = min(N-1, V) best
-// tokens of the position, ranked by (q desc, token id asc).  A 4-pass 8-bit
-// radix select finds the M-th largest key; the selection is gathered with
-// coalesced reads (its order does not matter) and bitonic-sorted in shared
-// memory by (q desc, index asc); ties at the threshold beyond the budget are
-// resolved in index order.
+// tokens of the position, ranked by (q desc, token id asc).  A threshold
+// filter (topk_filter_kernel: the M-th best of the threads' best keys bounds
+// the row's M-th best from below; a second pass keeps the keys above it; a
+// bitonic sort ranks them), with a 4-pass 8-bit radix select as the fallback
+// (radix_topk_block: the M-th largest key, a coalesced gather, a bitonic sort,
+// ties at the threshold beyond the budget resolved in index order).
 // Kernel 2 (one block per sequence, one warp expanding): every inserted node
 // owns exactly one candidate, its best not-yet-inserted child (the next
 // rank at the next position); the child ranks of a node are consumed in
@@ -44,25 +45,22 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__global__ void __launch_bounds__(kTopThreads)
-topk_kernel(const float *__restrict__ q, int K, int V, int M, int32_t *__restrict__ top_tok,
-            float *__restrict__ top_q) {
+// The ranked top M (<= 256) of one row by radix select, for a block of at
+// least 256 threads; writes tok_out[0..M) and q_out[0..M).
+__device__ void radix_topk_block(const float *__restrict__ row, int V, int M,
+                                 int32_t *__restrict__ tok_out, float *__restrict__ q_out) {
   __shared__ unsigned hist[256];
   __shared__ unsigned s_prefix, s_remaining, s_eq_total;
   __shared__ unsigned s_ngt, s_neq;
   __shared__ unsigned long long s_sel[256];
-
-  pdl_trigger();
-  pdl_wait();
-  const int k = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
-  const float *row = q + ((size_t)b * K + k) * (size_t)V;
+  const int t = threadIdx.x, nthr = blockDim.x;
 
   // radix select: the M-th largest key T and how many keys equal to T to take
   unsigned prefix = 0u, pmask = 0u, remaining = (unsigned)M;
   for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int x = t; x < 256; x += kTopThreads) hist[x] = 0u;
+    for (int x = t; x < 256; x += nthr) hist[x] = 0u;
     __syncthreads();
-    for (int x = t; x < V; x += kTopThreads) {
+    for (int x = t; x < V; x += nthr) {
       const uint32_t key = order_key(__ldg(row + x));
       if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & 0xFFu], 1u);
     }
@@ -109,7 +107,7 @@ topk_kernel(const float *__restrict__ q, int K, int V, int M, int32_t *__restric
 
   // gather: keys > T (and every key == T when all are taken) land in any
   // order, the sort below orders them
-  for (int x = t; x < 256; x += kTopThreads) s_sel[x] = 0ull;
+  for (int x = t; x < 256; x += nthr) s_sel[x] = 0ull;
   if (t == 0) {
     s_ngt = 0u;
     s_neq = 0u;
@@ -124,7 +122,7 @@ topk_kernel(const float *__restrict__ q, int K, int V, int M, int32_t *__restric
       s_sel[cnt_gt + atomicAdd(&s_neq, 1u)] = packed;
     }
   };
-  for (int x = t; x < V; x += kTopThreads) take(order_key(__ldg(row + x)), x);
+  for (int x = t; x < V; x += nthr) take(order_key(__ldg(row + x)), x);
   if (!all_eq && warp == 0) {
     // ties at T beyond the budget: the lowest indices win, so warp 0 walks the
     // row in index order, 32 elements at a time
@@ -159,12 +157,24 @@ topk_kernel(const float *__restrict__ q, int K, int V, int M, int32_t *__restric
       __syncthreads();
     }
   }
-  for (int r = t; r < M; r += kTopThreads) {
+  for (int r = t; r < M; r += nthr) {
     const int idx = (int)(0xFFFFFFFFu - (unsigned)(s_sel[r] & 0xFFFFFFFFull));
-    top_tok[((size_t)b * K + k) * M + r] = idx;
-    top_q[((size_t)b * K + k) * M + r] = __ldg(row + idx);
+    tok_out[r] = idx;
+    q_out[r] = __ldg(row + idx);
   }
 }
+
+__global__ void __launch_bounds__(kTopThreads)
+topk_kernel(const float *__restrict__ q, int K, int V, int M, int32_t *__restrict__ top_tok,
+            float *__restrict__ top_q) {
+  pdl_trigger();
+  pdl_wait();
+  const int k = blockIdx.x, b = blockIdx.y;
+  const size_t o = ((size_t)b * K + k) * M;
+  radix_topk_block(q + ((size_t)b * K + k) * (size_t)V, V, M, top_tok + o, top_q + o);
+}
+
+
 
 constexpr int kExpandThreads = 256;
 constexpr int kPerLane = kMaxNodes / 32;  // candidate slots one lane scans
@@ -428,6 +438,110 @@ dyn_rerank_kernel(const int32_t *__restrict__ pool_parent, const int32_t *__rest
   }
 }
 
+// Ranked top M of every row by a threshold filter (M < kFiltThreads).
+// Pass 1: every thread's best key over its elements; the M-th best of those
+// per-thread bests, tau, is a lower bound of the row's M-th best key (the M
+// best per-thread bests are M distinct elements), so the top M all have keys
+// >= tau.  Pass 2 (the row is now in L1/L2) collects the keys >= tau, usually
+// little more than M of them, and a bitonic sort ranks them.  Keys are
+// (order_key(q) << 32 | ~index), distinct, larger is better: the ranking
+// (q desc, token id asc).  More than kFiltCap candidates (not seen with real
+// distributions) falls back to the radix select in the same block.
+constexpr int kFiltThreads = 512;
+constexpr int kFiltCap = 2048;
+
+__global__ void __launch_bounds__(kFiltThreads)
+topk_filter_kernel(const float *__restrict__ q, int K, int V, int M, int32_t *__restrict__ top_tok,
+                   float *__restrict__ top_q) {
+  __shared__ unsigned long long s_best[kFiltThreads];
+  __shared__ unsigned long long s_cand[kFiltCap];
+  __shared__ unsigned s_count;
+  pdl_trigger();
+  pdl_wait();
+  const int k = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
+  const float *row = q + ((size_t)b * K + k) * (size_t)V;
+  const size_t o = ((size_t)b * K + k) * M;
+  auto key2 = [](float v, int x) {
+    return ((unsigned long long)order_key(v) << 32) | (unsigned long long)(0xFFFFFFFFu - (unsigned)x);
+  };
+  // rows of a multiple of 4 floats are read as float4 (16-byte aligned: the
+  // caller's q is); others element by element
+  const bool vec = (V & 3) == 0 && ((reinterpret_cast<uintptr_t>(row) & 15) == 0);
+  const float4 *row4 = reinterpret_cast<const float4 *>(row);
+  const int V4 = V >> 2;
+  unsigned long long best = 0ull;
+  if (vec) {
+#pragma unroll 8
+    for (int x4 = t; x4 < V4; x4 += kFiltThreads) {
+      const float4 v = __ldg(row4 + x4);
+      const int x = 4 * x4;
+      unsigned long long k0 = key2(v.x, x), k1 = key2(v.y, x + 1), k2 = key2(v.z, x + 2),
+                         k3 = key2(v.w, x + 3);
+      k0 = k1 > k0 ? k1 : k0;
+      k2 = k3 > k2 ? k3 : k2;
+      k0 = k2 > k0 ? k2 : k0;
+      best = k0 > best ? k0 : best;
+    }
+  } else {
+#pragma unroll 8
+    for (int x = t; x < V; x += kFiltThreads) {
+      const unsigned long long key = key2(__ldg(row + x), x);
+      best = key > best ? key : best;
+    }
+  }
+  s_best[t] = best;
+  if (t == 0) s_count = 0u;
+  __syncthreads();
+  bitonic_desc(s_best, kFiltThreads);
+  const unsigned long long tau = s_best[M - 1];
+  auto offer = [&](unsigned long long key) {
+    if (key >= tau) {
+      const unsigned i = atomicAdd(&s_count, 1u);
+      if (i < (unsigned)kFiltCap) s_cand[i] = key;
+    }
+  };
+  if (vec) {
+#pragma unroll 4
+    for (int x4 = t; x4 < V4; x4 += kFiltThreads) {
+      const float4 v = __ldg(row4 + x4);
+      const int x = 4 * x4;
+      offer(key2(v.x, x));
+      offer(key2(v.y, x + 1));
+      offer(key2(v.z, x + 2));
+      offer(key2(v.w, x + 3));
+    }
+  } else {
+#pragma unroll 4
+    for (int x = t; x < V; x += kFiltThreads) offer(key2(__ldg(row + x), x));
+  }
+  __syncthreads();
+  const int n = (int)s_count;
+  if (n > kFiltCap) {  // block-uniform
+    radix_topk_block(row, V, M, top_tok + o, top_q + o);
+    return;
+  }
+  int n2 = 1;
+  while (n2 < n) n2 <<= 1;
+  for (int i = n + t; i < n2; i += kFiltThreads) s_cand[i] = 0ull;
+  __syncthreads();
+  bitonic_desc(s_cand, n2);
+  for (int r = t; r < M; r += kFiltThreads) {
+    const int idx = (int)(0xFFFFFFFFu - (unsigned)(s_cand[r] & 0xFFFFFFFFull));
+    top_tok[o + r] = idx;
+    top_q[o + r] = __ldg(row + idx);
+  }
+}
+
+// Ranked top M of every row of q [B][K][V]: the threshold filter, or the
+// radix select for M >= kFiltThreads.
+cudaError_t launch_topk(const float *q, int K, int B, int V, int M, int32_t *top_tok, float *top_q,
+                        cudaStream_t s) {
+  if (M < kFiltThreads)
+    return launch(topk_filter_kernel, dim3(K, B), dim3(kFiltThreads), 0, s, q, K, V, M, top_tok,
+                  top_q);
+  return launch(topk_kernel, dim3(K, B), dim3(kTopThreads), 0, s, q, K, V, M, top_tok, top_q);
+}
+
 size_t dyn_rerank_smem(int M) {
   int n2 = 1;
   while (n2 < M - 1) n2 <<= 1;
@@ -466,9 +580,7 @@ TSD_API int tsd_dynamic_tree_expand(const float *q, const int32_t *root_token, i
   int32_t *top_tok = static_cast<int32_t *>(workspace);
   float *top_q = reinterpret_cast<float *>(static_cast<char *>(workspace) + tok_bytes);
   cudaStream_t s = as_cuda(stream);
-  if (launch(topk_kernel, dim3(F, B), dim3(kTopThreads), 0, s, q, F, V, k, top_tok, top_q) !=
-      cudaSuccess)
-    return TSD_ERR_CUDA;
+  if (launch_topk(q, F, B, V, k, top_tok, top_q, s) != cudaSuccess) return TSD_ERR_CUDA;
   if (launch(dyn_expand_kernel, dim3(B), dim3(kDynThreads), 0, s, top_tok, top_q, root_token,
              frontier, F, k, level, M_max, pool_parent, pool_token, pool_depth, pool_score,
              next_frontier) != cudaSuccess)
@@ -520,11 +632,7 @@ TSD_API int tsd_best_first_tree_build(const float *q, const int32_t *root_token,
   int32_t *top_tok = static_cast<int32_t *>(workspace);
   float *top_q = reinterpret_cast<float *>(static_cast<char *>(workspace) + p.tok_bytes);
   cudaStream_t s = as_cuda(stream);
-  if (p.M > 0) {
-    if (launch(topk_kernel, dim3(K, B), dim3(kTopThreads), 0, s, q, K, V, p.M, top_tok, top_q) !=
-        cudaSuccess)
-      return TSD_ERR_CUDA;
-  }
+  if (p.M > 0 && launch_topk(q, K, B, V, p.M, top_tok, top_q, s) != cudaSuccess) return TSD_ERR_CUDA;
   const size_t smem = (size_t)K * (p.M > 0 ? p.M : 0) * (sizeof(float) + sizeof(int32_t));
   if (smem > 48 * 1024) {
     if (cudaFuncSetAttribute(expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
