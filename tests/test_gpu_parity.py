@@ -110,6 +110,37 @@ def test_ragged_split_plan(tsd, loose):
     assert g["status"] == 0
 
 
+def test_split_plan_edges(tsd):
+    """Device split plan at its limits: 64 sequences (the most it plans), with
+    ragged node counts, one empty prefix, one sequence far longer than the
+    rest, and malformed trees whose sequences the plan must leave out (their
+    rows zero) while the others are still split and merged correctly."""
+    rng = np.random.default_rng(64)
+    prefix = rng.integers(1, 400, size=64)
+    prefix[7] = 0
+    prefix[40] = 12000
+    inp = gen.random_small(6464, B=64, N_max=12, Hq=8, Hkv=2, D=128, V=200, prefix_lo=0,
+                           prefix_hi=1, max_depth=5, prefix_len=prefix)
+    for b in (3, 41):  # a self-loop and a second root: the ancestors kernel flags both
+        nb = int(inp.n_nodes[b])
+        if nb > 1:
+            inp.parent[b, nb - 1] = nb - 1 if b == 3 else -1
+    g = run_gpu(tsd, inp)
+    o = run_oracle(inp)
+    assert (o["err"][[3, 41]] != 0).any()
+    compare(inp, g, o)
+    assert g["status"] == 0
+
+
+def test_attention_launch_count(tsd):
+    """The launch count the library reports: split + merge, plus the plan
+    kernel for ragged-capable batches with long blocks."""
+    assert tsd.tree_attn_launches(1, 63, 32, 8, 128, 4159) == 2
+    assert tsd.tree_attn_launches(16, 31, 32, 8, 128, 8078) == 3
+    assert tsd.tree_attn_launches(70, 6, 4, 2, 64, 300) == 2
+    assert tsd.tree_attn_launches(1, 63, 32, 8, 96, 4159) == 0
+
+
 def test_large_batch_uniform_split(tsd):
     """More sequences than the device plan takes (B = 70): the host's
     uniform split and its three-dimensional grid."""
