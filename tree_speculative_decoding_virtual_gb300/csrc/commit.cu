@@ -19,6 +19,11 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kMaxMoves = kMaxDepth;  // k = 1..A, A <= D_max <= 32
 
+// Block id of slot page `i` of sequence b.
+__device__ __forceinline__ int trow_entry(const int32_t *block_table, int b, int max_blocks, int i) {
+  return block_table[(size_t)b * max_blocks + i];
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads)
 commit_kernel(uint16_t *__restrict__ k_cache, uint16_t *__restrict__ v_cache,
@@ -43,50 +48,63 @@ commit_kernel(uint16_t *__restrict__ k_cache, uint16_t *__restrict__ v_cache,
   const int t = threadIdx.x;
   const int cols = D_max + 1;
 
-  const int P = prefix_len[b];
-  const int nb = n_nodes ? n_nodes[b] : N_max;
-  const int eb = err ? err[b] : 0;
-  const int A = accept_len[b];
-  const int32_t *trow = block_table + (size_t)b * max_blocks;
-
-  if (t == 0) {
-    int ok = 1, bad = 0, n = 0;
+  // Planning by warp 0, one lane per path entry k = lane + 1 (k <= A <= D_max
+  // <= 32): every load of a round is independent, so the plan costs three
+  // dependent rounds (lengths and path, block ids, then the copy) rather than
+  // two per entry.  The error reported is the first failing entry's, in k
+  // order, as a sequential walk would find it.
+  if (t < 32) {
+    const int lane = t;
+    const int P = prefix_len[b];
+    const int nb = n_nodes ? n_nodes[b] : N_max;
+    const int eb = err ? err[b] : 0;
+    const int A = accept_len[b];
+    const int p0 = path[(size_t)b * cols];
+    const int k = lane + 1;
+    const int pk = k <= D_max ? path[(size_t)b * cols + k] : 0;
+    int ok = 1, bad = 0;
     if (eb != 0) {
       ok = 0;
     } else if (P < 0 || nb < 1 || nb > N_max || (long)P + nb > (long)max_blocks * kPage) {
       ok = 0;
       bad = TSD_STATUS_BAD_LEN;
-    } else if (A < 0 || A > D_max || A > nb - 1 || path[(size_t)b * cols] != 1) {
+    } else if (A < 0 || A > D_max || A > nb - 1 || p0 != 1) {
       ok = 0;
       bad = TSD_STATUS_BAD_PATH;
-    } else {
-      for (int k = 1; k <= A; ++k) {
-        const int node = path[(size_t)b * cols + k] - 1;
-        if (node < 0 || node >= nb) {
-          ok = 0;
-          bad = TSD_STATUS_BAD_PATH;
-          break;
-        }
-        if (node != k) {
-          const int src = P + node, dst = P + k;
-          const int ps = trow[src / kPage], pd = trow[dst / kPage];
-          if (ps < 0 || ps >= num_blocks || pd < 0 || pd >= num_blocks) {
-            ok = 0;
-            bad = TSD_STATUS_BAD_PAGE;
-            break;
-          }
-          s_src[n] = ((long long)ps * Hkv + h) * kPage + src % kPage;
-          s_dst[n] = ((long long)pd * Hkv + h) * kPage + dst % kPage;
-          ++n;
-        }
-      }
     }
-    if (!ok) n = 0;
-    s_n = n;
-    if (bad && status) atomicOr(status, bad);
-    if (h == 0 && layer == 0) {
-      new_len[b] = ok ? P + A + 1 : P;
-      if (moved) moved[b] = n;
+    // per entry (uniform branch above: ok is the same in every lane)
+    const bool mine = ok && k <= A;
+    const int node = pk - 1;
+    const bool bad_path = mine && (node < 0 || node >= nb);
+    const bool move = mine && !bad_path && node != k;
+    int ps = 0, pd = 0;
+    if (move) {
+      ps = trow_entry(block_table, b, max_blocks, (P + node) / kPage);
+      pd = trow_entry(block_table, b, max_blocks, (P + k) / kPage);
+    }
+    const bool bad_page = move && (ps < 0 || ps >= num_blocks || pd < 0 || pd >= num_blocks);
+    const unsigned fails = __ballot_sync(0xffffffffu, bad_path || bad_page);
+    if (ok && fails) {
+      const int first = __ffs(fails) - 1;  // the lowest failing k
+      const int kind = __shfl_sync(0xffffffffu, bad_path ? 1 : 2, first);
+      ok = 0;
+      bad = kind == 1 ? TSD_STATUS_BAD_PATH : TSD_STATUS_BAD_PAGE;
+    }
+    const unsigned moves = __ballot_sync(0xffffffffu, move);
+    const int n = ok ? __popc(moves) : 0;
+    if (ok && move) {
+      const int slot = __popc(moves & ((1u << lane) - 1u));
+      const int src = P + node, dst = P + k;
+      s_src[slot] = ((long long)ps * Hkv + h) * kPage + src % kPage;
+      s_dst[slot] = ((long long)pd * Hkv + h) * kPage + dst % kPage;
+    }
+    if (lane == 0) {
+      s_n = n;
+      if (bad && status) atomicOr(status, bad);
+      if (h == 0 && layer == 0) {
+        new_len[b] = ok ? P + A + 1 : P;
+        if (moved) moved[b] = n;
+      }
     }
   }
   __syncthreads();
