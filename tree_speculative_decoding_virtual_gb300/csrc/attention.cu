@@ -58,6 +58,7 @@ struct AttnParams {
   // (tree_attn_plan_kernel); the grid is one block per work item (grid_items
   // of them) and item k's partials are rows [k * kTcRows, (k + 1) * kTcRows).
   int B, plan_mode, nsm, grid_items;
+  int rpb;           // query rows per block: 256 (two row tiles) or 128 (one)
   int4 *plan_out;    // plan_mode 2: per sequence (first item, splits, chunk in key tiles, row tiles)
   int4 *plan_items;  // plan_mode 2: per block of the grid, its item (tree_attn_plan_kernel)
   uint16_t *part_o;  // fp16 partial rows [..][D]: the split's O / (l * c)
@@ -475,6 +476,7 @@ constexpr int kPlanMaxChunk = kTcMaxPages * kPage / kTcBN;   // 64 key tiles per
 constexpr int kPlanFixedTiles = 4;                           // per-item set-up + partials
 constexpr int kPlanGroups = 5;                               // thread groups over the sequences
 constexpr int kPlanMinTiles = 16;  // uniform blocks shorter than this keep the uniform split
+constexpr int kSmallBlockTiles = 4;  // 256-row blocks of at most this many key tiles: use 128 rows
 static_assert(kPlanMaxChunk == 64, "the plan key keeps C in 6 bits");
 
 struct TcPlanShared {
@@ -528,7 +530,7 @@ __global__ void __launch_bounds__(kTcThreads) tree_attn_plan_kernel(const AttnPa
     int P, nb;
     const bool ok = seq_ok(p, tid, P, nb);
     ps.tiles[tid] = ok ? (P + nb + kTcBN - 1) / kTcBN : 0;
-    ps.rtc[tid] = ok ? (nb * p.g + kTcRows - 1) / kTcRows : 0;
+    ps.rtc[tid] = ok ? (nb * p.g + p.rpb - 1) / p.rpb : 0;
     s_P[tid] = P;
     s_nb[tid] = nb;
     if (!ok && p.status) {
@@ -688,8 +690,8 @@ __device__ __forceinline__ void attn_prefetch(const AttnParams &p, int b, int hk
           reinterpret_cast<const char *>(cache + ((size_t)page * p.Hkv + hkv) * kPage * D);
       for (int off = lane * 128; off < kPage * D * 2; off += 32 * 128) prefetch_l2(blk + off);
     }
-  } else if (warp < 10) {
-    const int row = rt * kTcRows + ((warp - 2) >> 2) * kTcBM + (warp & 3) * 32 + lane;
+  } else if (warp < 10 && ((warp - 2) >> 2) * kTcBM < p.rpb) {
+    const int row = rt * p.rpb + ((warp - 2) >> 2) * kTcBM + (warp & 3) * 32 + lane;
     if (row < nb * p.g) {
       const char *q = reinterpret_cast<const char *>(
           p.q + (((size_t)b * p.N_max + row / p.g) * p.Hq + hkv * p.g + row % p.g) * D);
@@ -879,12 +881,13 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
     }
     k_begin = split * p.chunk;
     k_end = min(P + nb, k_begin + p.chunk);
-    item_row0 = ((size_t)zg * p.splits + split) * p.rows_pad + (size_t)rt * kTcRows;
+    item_row0 = ((size_t)zg * p.splits + split) * p.rows_pad + (size_t)rt * p.rpb;
   }
   const int rows_valid = nb * p.g;
   const int seq_len = P + nb;
-  run = run && rt * kTcRows < rows_valid && k_begin < seq_len;
-  const int ntile_rows = rt * kTcRows + kTcBM < rows_valid ? 2 : 1;  // row tiles with valid rows
+  run = run && rt * p.rpb < rows_valid && k_begin < seq_len;
+  // row tiles with valid rows
+  const int ntile_rows = p.rpb == kTcRows && rt * kTcRows + kTcBM < rows_valid ? 2 : 1;
   const int ntiles = (k_end - k_begin + kTcBN - 1) / kTcBN;
   const int pg_first = k_begin / kPage;
   const int npg = run ? (k_end - 1) / kPage - pg_first + 1 : 0;  // <= kTcMaxPages (host check)
@@ -1002,7 +1005,7 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
     const int tr = kv2 ? 0 : t;                       // row tile of this group
     const int quarter = warp & 3;                     // TMEM lanes 32*quarter .. +31
     const int rl = quarter * 32 + lane;               // row within the row tile
-    const int row = rt * kTcRows + tr * kTcBM + rl;
+    const int row = rt * p.rpb + tr * kTcBM + rl;
     const bool active = kv2 || t < ntile_rows;
     const bool rvalid = row < rows_valid;
     const int node = rvalid ? row / p.g : 0;
@@ -1067,7 +1070,7 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
 #pragma unroll
       for (int i = 0; i < 32 / kRowsPer; ++i) {
         const int r_in = quarter * 32 + i * kRowsPer + lane / kCh;  // row within the tile
-        const int grow = rt * kTcRows + tr * kTcBM + r_in;
+        const int grow = rt * p.rpb + tr * kTcBM + r_in;
         const int gr = grow < rows_valid ? grow : 0;
         const uint16_t *src =
             p.q + (((size_t)b * p.N_max + gr / p.g) * p.Hq + hkv * p.g + gr % p.g) * D + ch * 8;
@@ -1299,7 +1302,7 @@ __global__ void __launch_bounds__(256) tree_attn_combine_kernel(const AttnParams
   int ns;  // <= kMaxSplits
   if (p.plan_mode == 2) {
     const int4 pl = plan;  // (first item, splits, chunk, row tiles) of sequence b
-    r0 = ((size_t)pl.x + (size_t)hkv * pl.y * pl.w + row / kTcRows) * kTcRows + row % kTcRows;
+    r0 = ((size_t)pl.x + (size_t)hkv * pl.y * pl.w + row / p.rpb) * kTcRows + row % p.rpb;
     stride = (size_t)pl.w * kTcRows;
     ns = pl.y;
   } else {
@@ -1392,34 +1395,54 @@ struct AttnPlan {
 AttnPlan plan_attn(int B, int N_max, int Hq, int Hkv, int D, int max_slots) {
   AttnPlan a;
   a.impl = (int)option(TSD_OPT_ATTN_KERNEL);
-  a.bm = a.impl == 0 ? kTcRows : kBM;
   a.bn = a.impl == 0 ? kTcBN : kBN;
   const int g = Hq / Hkv;
-  a.row_tiles = (N_max * g + a.bm - 1) / a.bm;
-  a.rows_pad = a.row_tiles * a.bm;
-  const long units = (long)B * Hkv * a.row_tiles;
   const long nsm = sm_count();
   const long max_tiles = (max_slots + a.bn - 1) / a.bn;
-  long best_s = 1;
-  if (a.impl == 0) {
-    // one resident block per SM: estimated time = waves x (tiles per block +
-    // a fixed cost of about four 128-key tiles for the prologue and partials)
+  // the uniform split for blocks of bm rows: one resident block per SM,
+  // estimated time = waves x (tiles per block + a fixed cost of about four
+  // 128-key tiles for the prologue and partials)
+  auto split_for = [&](int bm, long &per) {
+    const long units = (long)B * Hkv * ((N_max * g + bm - 1) / bm);
+    long best_s = 1;
     double best_t = 1e30;
     for (long s = 1; s <= max_tiles && s <= 32; ++s) {
       const long waves = (units * s + nsm - 1) / nsm;
-      const long per = (max_tiles + s - 1) / s;
-      const double t = (double)waves * (double)(per + 4);
+      const long pr = (max_tiles + s - 1) / s;
+      const double t = (double)waves * (double)(pr + 4);
       if (t < best_t - 1e-9) {
         best_t = t;
         best_s = s;
+        per = pr;
       }
     }
+    return best_s;
+  };
+  long best_s = 1;
+  if (a.impl == 0) {
+    // Blocks of 256 rows (two row tiles share every K/V tile) unless that
+    // leaves each block only a few key tiles: then the work is latency-bound
+    // and 128-row blocks, whose two softmax groups take alternate key tiles,
+    // spread it over twice the blocks (the row tiles' blocks run side by side,
+    // so L2 serves their shared K/V).
+    long per = 0;
+    a.bm = kTcRows;
+    best_s = split_for(a.bm, per);
+    if (per <= kSmallBlockTiles && N_max * g > kTcBM) {
+      a.bm = kTcBM;
+      best_s = split_for(a.bm, per);
+    }
   } else {
+    a.bm = kBM;
+    const long units = (long)B * Hkv * ((N_max * g + a.bm - 1) / a.bm);
     const long target = 2L * nsm;
     best_s = (target + units - 1) / units;
     if (best_s > max_tiles) best_s = max_tiles;
     if (best_s < 1) best_s = 1;
   }
+  a.row_tiles = (N_max * g + a.bm - 1) / a.bm;
+  a.rows_pad = a.row_tiles * a.bm;
+  const long units = (long)B * Hkv * a.row_tiles;
   long chunk = (max_slots + best_s - 1) / best_s;
   chunk = (chunk + a.bn - 1) / a.bn * a.bn;
   if (a.impl == 0 && chunk > (long)kTcMaxPages * kPage) chunk = (long)kTcMaxPages * kPage;
@@ -1574,6 +1597,7 @@ TSD_API int tsd_tree_attn_fwd(const uint16_t *q, const uint16_t *k_cache, const 
   p.splits = a.splits;
   p.row_tiles = a.row_tiles;
   p.rows_pad = a.rows_pad;
+  p.rpb = a.bm;
   p.part_o = static_cast<uint16_t *>(workspace);
   p.part_ml = reinterpret_cast<float4 *>(static_cast<char *>(workspace) + a.o_bytes);
   p.plan_out = a.mode == 2 ? reinterpret_cast<int4 *>(static_cast<char *>(workspace) + a.o_bytes +
