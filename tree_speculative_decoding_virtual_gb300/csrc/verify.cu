@@ -201,6 +201,7 @@ verify_greedy_kernel(const float *__restrict__ logits, const int32_t *__restrict
 
   // ---- phase 2: acceptance search for sequence b (one node per thread) ----
   __shared__ int s_am[kMaxNodes];
+  __shared__ int s_par[kMaxNodes];
   __shared__ uint32_t s_match[kMaxNodes / 32];
   __shared__ int s_key[kThreads / 32];
 
@@ -223,7 +224,10 @@ verify_greedy_kernel(const float *__restrict__ logits, const int32_t *__restrict
     row_key[(size_t)b * N_max + t] = 0ull;  // zero again for the next call
     am = my_key ? (int)(0xFFFFFFFFu - (uint32_t)(my_key & 0xFFFFFFFFull)) : -1;
   }
-  if (t < kMaxNodes) s_am[t] = am;
+  if (t < kMaxNodes) {
+    s_am[t] = am;
+    s_par[t] = (seq_ok && t < nb) ? my_parent : -1;
+  }
   if (t < N_max) argmax_out[(size_t)b * N_max + t] = am;
   __syncthreads();
   // matched(i): root, or token equals the target's choice at the parent
@@ -260,8 +264,17 @@ verify_greedy_kernel(const float *__restrict__ logits, const int32_t *__restrict
   if (seq_ok && key >= 0) {
     const int A = key >> 16;
     const int leaf = 0xFFFF - (key & 0xFFFF);
-    for (int k = t; k < cols; k += kThreads)
-      path[(size_t)b * cols + k] = k <= A ? anc[((size_t)b * (N_max + 1) + leaf + 1) * cols + k] : 0;
+    if (t == 0) {
+      // path[k] = safe id of the leaf's depth-k ancestor (its ancestor-table
+      // row), walked up the parents already in shared memory: the accepted
+      // leaf's chain is valid and A = its depth, so no global round trip
+      int a = leaf;
+      for (int k = A; k >= 0; --k) {
+        path[(size_t)b * cols + k] = a + 1;
+        a = a >= 0 && a < kMaxNodes ? s_par[a] : -1;
+      }
+    }
+    for (int k = A + 1 + t; k < cols; k += kThreads) path[(size_t)b * cols + k] = 0;
     if (t == 0) {
       accept_len[b] = A;
       leaf_out[b] = leaf;
