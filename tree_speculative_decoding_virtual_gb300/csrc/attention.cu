@@ -615,9 +615,17 @@ __global__ void __launch_bounds__(kTcThreads) tree_attn_plan_kernel(const AttnPa
   for (int k = tid; k < p.grid_items; k += blockDim.x) {
     int4 e = make_int4(-1, 0, 0, 0);
     if (k < total) {
-      int b = -1;  // the sequence whose items contain k: the largest first item <= k
-      for (int s = 0; s < B; ++s)
-        if (ps.tiles[s] > 0 && s_first[s] <= k && (b < 0 || s_first[s] > s_first[b])) b = s;
+      // the sequence whose items contain k: first items grow with the rank,
+      // so it is the last rank whose first item is <= k (sequences without
+      // items rank last, their first item being the total, so the search
+      // never stops on one)
+      int lo = 0, hi = B - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_first[s_order[mid]] <= k) lo = mid; else hi = mid - 1;
+      }
+      while (lo > 0 && ps.tiles[s_order[lo]] == 0) --lo;
+      const int b = s_order[lo];
       const int t = ps.tiles[b];
       const int rtc = ps.rtc[b];
       const int n = (t + C - 1) / C;
