@@ -194,7 +194,9 @@ int tsd_tree_attn_fwd(const uint16_t *q, const uint16_t *k_cache, const uint16_t
  * accepted; node i is accepted iff its parent is and tokens[b][i] ==
  * argmax[b][parent(i)].  leaf = deepest accepted node (lowest id on ties);
  * accept_len = depth(leaf); path[b][k] = anc[b][leaf+1][k] for k <= accept_len,
- * 0 beyond; bonus = argmax[b][leaf].
+ * 0 beyond (the kernel walks the leaf's parents, which gives the same row of
+ * a table built by tsd_tree_build_ancestors from the same parent array);
+ * bonus = argmax[b][leaf].
  *
  * logits  float [B][N_max][V]; tokens, parent int32 [B][N_max];
  * anc, depth, mask, err  from tsd_tree_build_ancestors; n_nodes int32 [B] or NULL.
