@@ -132,6 +132,26 @@ def test_split_plan_edges(tsd):
     assert g["status"] == 0
 
 
+@pytest.mark.parametrize("D,N,Hq,Hkv", [(64, 30, 32, 8), (128, 32, 32, 8), (128, 9, 8, 8)])
+def test_two_blocks_per_sm_path(tsd, D, N, Hq, Hkv):
+    """Ragged batches with long key ranges whose kv heads each have at most
+    128 query rows run the two-blocks-per-SM kernel (64-key tiles,
+    double-buffered S): head dims 64 and 128, exactly 128 rows, tree tails
+    that end mid-tile, shuffled blocks; attention on a sample of rows."""
+    rng = np.random.default_rng(D + N)
+    prefix = rng.integers(2500, 9000, size=16)
+    inp = gen.random_small(700 + N, B=16, N_max=N, Hq=Hq, Hkv=Hkv, D=D, V=120, prefix_lo=0,
+                           prefix_hi=1, max_depth=6, prefix_len=prefix)
+    assert tsd.tree_attn_launches(16, N, Hq, Hkv, D, int((inp.prefix_len + inp.n_nodes).max())) == 3
+    sample = sorted({(b, int(rng.integers(inp.n_nodes[b])), int(rng.integers(Hq)))
+                     for b in range(16) for _ in range(12)}
+                    | {(3, i, h) for i in range(int(inp.n_nodes[3])) for h in range(Hq)})
+    g = run_gpu(tsd, inp)
+    o = run_oracle(inp, sample_attention=sample)
+    compare(inp, g, o, sample=sample)
+    assert g["status"] == 0
+
+
 def test_attention_launch_count(tsd):
     """The launch count the library reports: split + merge, plus the plan
     kernel for ragged-capable batches with long blocks."""

@@ -1271,6 +1271,461 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
   }
 }
 
+// ===========================================================================
+// Two blocks per SM, for launches whose blocks all hold one 128-row tile.  A
+// block of six warps with 64-key tiles needs 96 KB of shared memory, 256
+// tensor-memory columns and 192 threads of at most 168 registers, so two fit
+// on an SM: while one sets up, waits for its first tile or writes its
+// partials, the other streams.  One chain per block, over a double-buffered S:
+//   warp 0:    lane 0 loads K tiles, lane 1 V tiles (TMA into 2-stage rings
+//              of 64 keys; one 4-block box per 64-column half when the tile's
+//              blocks are consecutive, else one box per block)
+//   warp 1:    owns the tensor memory; lane 0 issues every MMA
+//   warps 2-5: softmax, one TMEM lane (= one query row) per thread
+// Per 64-key tile j: S_j = Q K_j^T into S buffer j & 1 (M=128, N=64); P_j as
+// bf16 over that buffer's first 32 columns; O += P_j V_j.  Issue order S_0,
+// S_1, P_0 V_0, S_2, P_1 V_1, S_3, ...: S_{j+2} reuses the buffer P_j V_j
+// reads (the tensor pipe runs in issue order), and while the softmax works on
+// S_j the tensor core computes S_{j+1} and P_{j-1} V_{j-1}.  So a P V may still
+// be running when the next tile's softmax raises the running max; the rescale
+// of O that the lazy max rule then needs first waits for it (pv_done).
+// Partials, waits, time-outs and teardown are as in tree_attn_split_tc.
+// ===========================================================================
+constexpr int kDualThreads = 192;
+constexpr int kDualBN = 64;                             // keys per tile
+constexpr int kDualPagesPerTile = kDualBN / kPage;      // 4
+constexpr uint32_t kDualTmemCols = 256;
+
+template <int D>
+struct DualLayout {
+  static constexpr int kHalves = D / 64;                 // 128-byte column blocks of a row
+  static constexpr uint32_t kQHalf = kTcBM * 128;
+  static constexpr uint32_t kQTile = kTcBM * D * 2;
+  static constexpr uint32_t kKVHalf = kDualBN * 128;
+  static constexpr uint32_t kTile = kDualBN * D * 2;
+  static constexpr uint32_t kQ = 0;
+  static constexpr uint32_t kK = kQTile;
+  static constexpr uint32_t kV = kK + 2 * kTile;
+  static constexpr uint32_t kBytes = kV + 2 * kTile;
+  static constexpr uint32_t kAlloc = kBytes + 1024;      // + alignment slack
+  static constexpr uint32_t kStaging = kK;               // the epilogue reuses the K ring
+  static_assert(2 * kTile >= kTcBM * D * 2, "epilogue staging fits the K ring");
+  static constexpr uint32_t kTmemS = 0;                  // S buffer s at s * kDualBN
+  static constexpr uint32_t kTmemO = 2 * kDualBN;
+  static_assert(kTmemO + D <= kDualTmemCols, "S buffers and O fit the allocation");
+};
+
+struct DualShared {
+  int32_t pages[kTcMaxPages];
+  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2];
+  uint64_t pv_done, o_final, q_full, drain, never;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int D>
+__device__ __forceinline__ void dual_load_tiles(const CUtensorMap *m1, const CUtensorMap *m4,
+                                                uint64_t *full, uint64_t *empty, uint32_t ring,
+                                                const int32_t *pages, int npg, int ntiles,
+                                                int hkv, uint64_t lim, volatile int *abort) {
+  using namespace sm100;
+  using L = DualLayout<D>;
+  int last_issued[2] = {-1, -1};
+  for (int j = 0; j < ntiles && !*abort; ++j) {
+    const int st = j & 1;
+    if (j >= 2 && !tc_wait(empty[st], ((j >> 1) - 1) & 1, lim, abort)) break;
+    const int g0 = j * kDualPagesPerTile;
+    int pg[kDualPagesPerTile];
+    bool run = true;
+#pragma unroll
+    for (int g = 0; g < kDualPagesPerTile; ++g) {
+      pg[g] = pages[min(g0 + g, npg - 1)];
+      run = run && pg[g] == pg[0] + g;
+    }
+    const uint32_t bar = smem_addr(&full[st]);
+    mbar_arrive_expect_tx(bar, L::kTile);
+#pragma unroll
+    for (int h = 0; h < L::kHalves; ++h) {
+      const uint32_t dst = ring + st * L::kTile + h * L::kKVHalf;
+      if (run) {
+        tma_load_4d(dst, m4, h * 64, 0, hkv, pg[0], bar);
+      } else {
+#pragma unroll
+        for (int g = 0; g < kDualPagesPerTile; ++g)
+          tma_load_4d(dst + g * kPage * 128, m1, h * 64, 0, hkv, pg[g], bar);
+      }
+    }
+    last_issued[st] = j;
+  }
+#pragma unroll
+  for (int st = 0; st < 2; ++st)
+    if (last_issued[st] >= 0)
+      mbar_wait(smem_addr(&full[st]), (last_issued[st] >> 1) & 1, kDrainLimitNs);
+}
+
+// S = Q K^T (M=128, N=64) for the K tile at kt into the TMEM S buffer ts,
+// then a commit to s_bar.
+template <int D>
+__device__ __noinline__ void dual_issue_s(uint32_t ts, uint32_t qt, uint32_t kt, uint32_t s_bar) {
+  using namespace sm100;
+  using L = DualLayout<D>;
+  constexpr uint32_t idS = idesc_bf16_f32(kTcBM, kDualBN, false, false);
+  tc_fence_after();
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk)
+    umma_bf16(ts, smem_desc_sw128(qt + (kk >> 2) * L::kQHalf + (kk & 3) * 32, 16, 1024),
+              smem_desc_sw128(kt + (kk >> 2) * L::kKVHalf + (kk & 3) * 32, 16, 1024), idS, kk > 0);
+  umma_commit(s_bar);
+}
+
+// O += P V (K = 64 keys; P read from the TMEM S buffer tp), then commits.
+template <int D>
+__device__ __noinline__ void dual_issue_pv(uint32_t to, uint32_t tp, uint32_t vt, bool accum,
+                                           uint32_t bar1, uint32_t bar2) {
+  using namespace sm100;
+  using L = DualLayout<D>;
+  constexpr uint32_t idPV = idesc_bf16_f32(kTcBM, D, false, true);
+  tc_fence_after();
+#pragma unroll
+  for (int kk = 0; kk < kDualBN / 16; ++kk)
+    umma_bf16_ta(to, tp + kk * 8, smem_desc_sw128(vt + kk * 16 * 128, L::kKVHalf, 1024), idPV,
+                 (accum || kk > 0) ? 1u : 0u);
+  if (bar1) umma_commit(bar1);
+  if (bar2) umma_commit(bar2);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kDualThreads, 2)
+tree_attn_split_dual(const AttnParams p, const __grid_constant__ CUtensorMap map_k1,
+                     const __grid_constant__ CUtensorMap map_k4,
+                     const __grid_constant__ CUtensorMap map_v1,
+                     const __grid_constant__ CUtensorMap map_v4) {
+  using namespace sm100;
+  using L = DualLayout<D>;
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ DualShared sh;
+
+  pdl_trigger();
+  // the work item, as in tree_attn_split_tc (the uniform split's guess until
+  // the plan may be read)
+  const bool planned = p.plan_mode == 2;
+  const int item = blockIdx.x;
+  int rt = planned ? item % p.row_tiles : blockIdx.x;
+  int split = planned ? (item / p.row_tiles) % p.splits : blockIdx.y;
+  const int zg = planned ? item / (p.row_tiles * p.splits) : blockIdx.z;
+  int b = zg / p.Hkv;
+  int hkv = zg % p.Hkv;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  unsigned char *gbase = smem_raw + (base - raw);
+  volatile int *abort = &sh.abort;
+  const uint64_t lim = p.wait_limit_ns;
+
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_addr(&sh.k_full[i]), 1);
+      mbar_init(smem_addr(&sh.k_empty[i]), 1);
+      mbar_init(smem_addr(&sh.v_full[i]), 1);
+      mbar_init(smem_addr(&sh.v_empty[i]), 1);
+      mbar_init(smem_addr(&sh.s_full[i]), 1);
+      mbar_init(smem_addr(&sh.p_full[i]), 4);
+    }
+    mbar_init(smem_addr(&sh.pv_done), 1);
+    mbar_init(smem_addr(&sh.o_final), 1);
+    mbar_init(smem_addr(&sh.q_full), 4);
+    mbar_init(smem_addr(&sh.drain), 1);
+    mbar_init(smem_addr(&sh.never), 1);
+    sh.abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&map_k1);
+    tma_prefetch_desc(&map_k4);
+    tma_prefetch_desc(&map_v1);
+    tma_prefetch_desc(&map_v4);
+  }
+  if (warp == 1) tmem_alloc(smem_addr(&sh.tmem_base), kDualTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_base;
+
+  if (b < p.B) attn_prefetch<D>(p, b, hkv, rt, split, warp, lane);
+  pdl_wait();
+
+  int P = 0, nb = 0;
+  bool run;
+  int k_begin, k_end;
+  size_t item_row0;
+  if (planned) {
+    const int4 e = __ldcg(&p.plan_items[item]);
+    run = e.x >= 0;
+    b = run ? e.x : 0;
+    hkv = e.y;
+    rt = e.z & 31;
+    split = (e.z >> 5) & 63;
+    const int chunk = ((e.z >> 11) & 127) * kTcBN;
+    nb = (e.z >> 18) & 511;
+    P = e.w;
+    k_begin = split * chunk;
+    k_end = min(P + nb, k_begin + chunk);
+    item_row0 = (size_t)item * kTcRows;
+  } else {
+    run = seq_ok(p, b, P, nb);
+    if (!run && rt == 0 && split == 0 && hkv == 0 && tid == 0 && p.status) {
+      const int e = p.err ? p.err[b] : 0;
+      const int nbb = p.n_nodes ? p.n_nodes[b] : p.N_max;
+      if (e == 0 && nbb >= 1 && nbb <= p.N_max) atomicOr(p.status, TSD_STATUS_BAD_LEN);
+    }
+    k_begin = split * p.chunk;
+    k_end = min(P + nb, k_begin + p.chunk);
+    item_row0 = ((size_t)zg * p.splits + split) * p.rows_pad + (size_t)rt * p.rpb;
+  }
+  const int rows_valid = nb * p.g;
+  run = run && rt * p.rpb < rows_valid && k_begin < P + nb;
+  const int ntiles = (k_end - k_begin + kDualBN - 1) / kDualBN;
+  const int pg_first = k_begin / kPage;
+  const int npg = run ? (k_end - 1) / kPage - pg_first + 1 : 0;  // <= kTcMaxPages
+
+  if (!run) {
+    // nothing to do for this block
+  } else if (warp == 0) {
+    // --------------------------- loaders (TMA) ---------------------------
+    const int32_t *trow = p.table + (size_t)b * p.max_blocks;
+    bool bad = false;
+    for (int i = lane; i < npg; i += 32) {
+      int page = __ldg(trow + pg_first + i);
+      if (page < 0 || page >= p.num_blocks) {
+        bad = true;
+        page = 0;
+      }
+      sh.pages[i] = page;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0 && p.status) atomicOr(p.status, TSD_STATUS_BAD_PAGE);
+    __syncwarp();
+    if (lane == 0)
+      dual_load_tiles<D>(&map_k1, &map_k4, sh.k_full, sh.k_empty, base + L::kK, sh.pages, npg,
+                         ntiles, hkv, lim, abort);
+    else if (lane == 1)
+      dual_load_tiles<D>(&map_v1, &map_v4, sh.v_full, sh.v_empty, base + L::kV, sh.pages, npg,
+                         ntiles, hkv, lim, abort);
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer ------------------------------
+    if (lane == 0) {
+      auto issue_s = [&](int j) {  // K_j has landed; S buffer j & 1 is free
+        dual_issue_s<D>(tmem + L::kTmemS + (j & 1) * kDualBN, base + L::kQ,
+                        base + L::kK + (j & 1) * L::kTile, smem_addr(&sh.s_full[j & 1]));
+        umma_commit(smem_addr(&sh.k_empty[j & 1]));
+      };
+      bool ok = !p.test_stall || tc_wait(sh.never, 0, lim, abort);
+      ok = ok && tc_wait(sh.q_full, 0, lim, abort);
+      for (int j = 0; ok && j < 2 && j < ntiles; ++j) {
+        ok = tc_wait(sh.k_full[j], 0, lim, abort);
+        if (ok) issue_s(j);
+      }
+      for (int j = 0; ok && j < ntiles; ++j) {
+        const int st = j & 1;
+        ok = !*abort && tc_wait(sh.p_full[st], (j >> 1) & 1, lim, abort);
+        ok = ok && tc_wait(sh.v_full[st], (j >> 1) & 1, lim, abort);
+        if (!ok) break;
+        dual_issue_pv<D>(tmem + L::kTmemO, tmem + L::kTmemS + st * kDualBN,
+                         base + L::kV + st * L::kTile, j > 0, smem_addr(&sh.pv_done),
+                         j == ntiles - 1 ? smem_addr(&sh.o_final) : 0u);
+        umma_commit(smem_addr(&sh.v_empty[st]));
+        if (j + 2 < ntiles) {
+          ok = tc_wait(sh.k_full[st], ((j + 2) >> 1) & 1, lim, abort);
+          if (ok) issue_s(j + 2);
+        }
+      }
+      // drain: every MMA issued above has completed
+      umma_commit(smem_addr(&sh.drain));
+      mbar_wait(smem_addr(&sh.drain), 0, kDrainLimitNs);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------ softmax ------------------------------
+    const int quarter = warp & 3;                      // TMEM lanes 32*quarter .. +31
+    const int rl = quarter * 32 + lane;                // row within the tile
+    const int row = rt * p.rpb + rl;
+    const bool rvalid = row < rows_valid;
+    const int node = rvalid ? row / p.g : 0;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t *mrow = p.mask + ((size_t)b * p.N_max + node) * p.W;
+    const uint32_t tO = tmem + L::kTmemO + lane_off;
+    auto warp_wait = [&](uint64_t &bar, uint32_t parity) -> bool {
+      const bool got = !*abort && tc_wait(bar, parity, lim, abort);
+      return __all_sync(0xffffffffu, got);
+    };
+    {
+      // Q rows -> shared memory (128-byte swizzle), as in tree_attn_split_tc
+      const uint32_t qt = base + L::kQ;
+      constexpr int kCh = D / 8;
+      constexpr int kRowsPer = 32 / kCh;
+      const int ch = lane % kCh;
+#pragma unroll
+      for (int i = 0; i < 32 / kRowsPer; ++i) {
+        const int r_in = quarter * 32 + i * kRowsPer + lane / kCh;
+        const int grow = rt * p.rpb + r_in;
+        const int gr = grow < rows_valid ? grow : 0;
+        const uint16_t *src =
+            p.q + (((size_t)b * p.N_max + gr / p.g) * p.Hq + hkv * p.g + gr % p.g) * D + ch * 8;
+        cp_async_16(qt + (ch >> 3) * L::kQHalf + sw128_offset(r_in, ch & 7), src);
+      }
+      cp_async_wait_all();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&sh.q_full));
+    }
+    float m_use = -INFINITY, l_sum = 0.f, l_ex = 0.f;
+    bool ok = true;
+    const float sc = p.scale_log2;
+    for (int j = 0; j < ntiles; ++j) {
+      const int st = j & 1;
+      if (!warp_wait(sh.s_full[st], (j >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tS = tmem + L::kTmemS + st * kDualBN + lane_off;
+      const int ts = k_begin + j * kDualBN;
+      const bool full = (ts + kDualBN <= P) && (ts + kDualBN <= k_end);
+      uint32_t r[2][32];
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) tmem_ld32(tS + c2 * 32, r[c2]);
+      tmem_wait_ld();
+      if (!full) {
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const int k0 = ts + c2 * 32;
+          const uint32_t vis = visible_bits(mrow, p.W, k0 - P, k_end - k0, rvalid);
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (!((vis >> i) & 1u)) r[c2][i] = __float_as_uint(-INFINITY);
+        }
+      }
+      float mx[8];
+#pragma unroll
+      for (int a = 0; a < 8; ++a) {
+        const auto v = [&](int i) { return __uint_as_float(r[i >> 5][i & 31]); };
+        float m = fmax3(v(a), v(a + 8), v(a + 16));
+        m = fmax3(m, v(a + 24), v(a + 32));
+        m = fmax3(m, v(a + 40), v(a + 48));
+        mx[a] = fmaxf(m, v(a + 56));
+      }
+      const float mt = fmaxf(fmax3(mx[0], mx[1], mx[2]),
+                             fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7])) * sc;
+      const float m_new = fmaxf(m_use, mt);
+      const bool upd = m_new > m_use + 8.f;  // first visible key, or the max grew by > 2^8
+      const float alpha = upd ? exp2f(m_use - m_new) : 1.f;
+      if (__any_sync(0xffffffffu, upd) && j > 0) {
+        // O holds P V of tiles before j - 1; the one of tile j - 1 may still run
+        if (!warp_wait(sh.pv_done, (j - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + c * 32, o);
+        }
+      }
+      if (upd) {
+        l_sum *= alpha;
+        l_ex *= alpha;
+        m_use = m_new;
+      }
+      const float mb = m_use == -INFINITY ? 0.f : m_use;
+      const unsigned long long sc2 = f2_pack(sc, sc), nmb2 = f2_pack(-mb, -mb);
+      unsigned long long esum2 = f2_pack(0.f, 0.f), rsum2 = f2_pack(0.f, 0.f);
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) {
+        uint32_t pk[16];  // P as bf16 pairs: column i holds keys 2i, 2i+1 of the chunk
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 x = f2_unpack(f2_fma(f2_pack(__uint_as_float(r[c2][2 * i]),
+                                                    __uint_as_float(r[c2][2 * i + 1])),
+                                            sc2, nmb2));
+          const float a = ex2_approx(x.x);
+          const float c = ex2_approx(x.y);
+          pk[i] = pack_bf16(a, c);
+          esum2 = f2_add(esum2, f2_pack(a, c));
+          rsum2 = f2_add(rsum2, f2_pack(__uint_as_float(pk[i] << 16),
+                                        __uint_as_float(pk[i] & 0xFFFF0000u)));
+        }
+        tmem_st16(tS + c2 * 16, pk);
+      }
+      const float2 es = f2_unpack(esum2), rs = f2_unpack(rsum2);
+      l_sum += rs.x + rs.y;
+      l_ex += es.x + es.y;
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&sh.p_full[st]));
+    }
+    if (ok) ok = warp_wait(sh.o_final, 0);  // the last P V
+
+    // ---- epilogue: O / (l c) in fp16 through shared memory, (m, l, c) per row ----
+    asm volatile("bar.sync 1, 128;\n" ::: "memory");
+    const bool all_ok = __all_sync(0xffffffffu, ok && !*abort);
+    if (all_ok) {
+      tc_fence_after();
+      float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+      float amax = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + c * 32, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(__uint_as_float(o[i])));
+      }
+      const float cs = pow2_above(amax * inv);
+      inv /= cs;
+      const int swz_mask = D / 8 - 1;
+      unsigned char *srow = gbase + L::kStaging + (size_t)rl * D * 2;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + c * 32, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {
+          uint4 v;
+          v.x = pack_f16(__uint_as_float(o[q8 * 8 + 0]) * inv, __uint_as_float(o[q8 * 8 + 1]) * inv);
+          v.y = pack_f16(__uint_as_float(o[q8 * 8 + 2]) * inv, __uint_as_float(o[q8 * 8 + 3]) * inv);
+          v.z = pack_f16(__uint_as_float(o[q8 * 8 + 4]) * inv, __uint_as_float(o[q8 * 8 + 5]) * inv);
+          v.w = pack_f16(__uint_as_float(o[q8 * 8 + 6]) * inv, __uint_as_float(o[q8 * 8 + 7]) * inv);
+          *reinterpret_cast<uint4 *>(srow + (((c * 4 + q8) ^ (rl & swz_mask)) << 4)) = v;
+        }
+      }
+      p.part_ml[item_row0 + rl] = make_float4(m_use, l_ex, cs, 0.f);
+      fence_proxy_async_smem();
+    }
+    asm volatile("bar.sync 1, 128;\n" ::: "memory");
+    if (all_ok && warp == 2 && lane == 0) {
+      bulk_store(p.part_o + item_row0 * D, base + L::kStaging, (uint32_t)(kTcBM * D * 2));
+      bulk_wait_read();
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (*abort && tid == 0 && p.status) atomicOr(p.status, TSD_STATUS_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kDualTmemCols);
+  }
+}
+
 // One warp per output row (b, node, q head): merge the splits.  Lane s reads
 // split s's (max, sum, scale).  A split's partial row is D/8 16-byte chunks,
 // so one warp-wide load covers 32/(D/8) splits: lane l reads chunk l % (D/8)
@@ -1396,6 +1851,7 @@ struct AttnPlan {
   int impl;  // 0 tcgen05, 1 mma.sync
   int bm, bn, row_tiles, rows_pad, splits, chunk;
   int mode;          // plan_mode (AttnParams)
+  bool dual;         // tree_attn_split_dual (two blocks per SM) instead of tree_attn_split_tc
   long grid_items;   // mode 2: blocks of the 1-D grid
   size_t o_bytes, ml_bytes, plan_bytes;
 };
@@ -1465,11 +1921,14 @@ AttnPlan plan_attn(int B, int N_max, int Hq, int Hkv, int D, int max_slots) {
   a.mode = a.impl == 1 ? 0
                        : (B > 1 && B <= kPlanMaxSeq && (a.chunk / a.bn) >= kPlanMinTiles ? 2 : 1);
   a.grid_items = items_u;
+  // Planned launches whose blocks all hold one 128-row tile run two blocks
+  // per SM (the plan then counts two block slots per SM).
+  a.dual = a.mode == 2 && N_max * g <= kTcBM;
   size_t rows = (size_t)B * Hkv * a.splits * a.rows_pad;
   if (a.mode == 2) {
-    // room for four waves of shorter pieces (at least the uniform split's
-    // blocks); blocks beyond the plan's items exit at once
-    a.grid_items = std::min(std::max(items_u, 4 * nsm), units * kMaxSplits);
+    // room for four waves of shorter pieces per block slot (at least the
+    // uniform split's blocks); blocks beyond the plan's items exit at once
+    a.grid_items = std::min(std::max(items_u, (a.dual ? 8 : 4) * nsm), units * kMaxSplits);
     rows = (size_t)a.grid_items * kTcRows;
   }
   a.o_bytes = align_up(rows * D * sizeof(uint16_t), 256);
@@ -1519,9 +1978,22 @@ int launch_attn(AttnParams &p, const AttnPlan &a, int B, int num_blocks, cudaStr
         !make_cache_map(&v1, p.v, num_blocks, p.Hkv, D, 1) ||
         !make_cache_map(&v8, p.v, num_blocks, p.Hkv, D, kTcPagesPerTile))
       return TSD_ERR_CUDA;
-    if (!set_smem((const void *)tree_attn_split_tc<D>, TcLayout<D>::kAlloc)) return TSD_ERR_CUDA;
     if (a.mode == 2 && launch(tree_attn_plan_kernel, dim3(1), dim3(kTcThreads), 0, s, p) != cudaSuccess)
       return TSD_ERR_CUDA;
+    if (a.dual) {
+      CUtensorMap k4, v4;
+      if (!make_cache_map(&k4, p.k, num_blocks, p.Hkv, D, kDualPagesPerTile) ||
+          !make_cache_map(&v4, p.v, num_blocks, p.Hkv, D, kDualPagesPerTile))
+        return TSD_ERR_CUDA;
+      if (!set_smem((const void *)tree_attn_split_dual<D>, DualLayout<D>::kAlloc)) return TSD_ERR_CUDA;
+      if (launch(tree_attn_split_dual<D>, grid, dim3(kDualThreads), DualLayout<D>::kAlloc, s, p, k1,
+                 k4, v1, v4) != cudaSuccess)
+        return TSD_ERR_CUDA;
+      if (cudaGetLastError() != cudaSuccess) return TSD_ERR_CUDA;
+      if (launch_combine<D>(p, B, s) != cudaSuccess) return TSD_ERR_CUDA;
+      return TSD_OK;
+    }
+    if (!set_smem((const void *)tree_attn_split_tc<D>, TcLayout<D>::kAlloc)) return TSD_ERR_CUDA;
     if (launch(tree_attn_split_tc<D>, grid, dim3(kTcThreads), TcLayout<D>::kAlloc, s, p, k1, k8, v1,
                v8) != cudaSuccess)
       return TSD_ERR_CUDA;
@@ -1614,7 +2086,7 @@ TSD_API int tsd_tree_attn_fwd(const uint16_t *q, const uint16_t *k_cache, const 
   p.plan_items = a.mode == 2 ? p.plan_out + B : nullptr;
   p.B = B;
   p.plan_mode = a.mode;
-  p.nsm = sm_count();
+  p.nsm = sm_count() * (a.dual ? 2 : 1);  // block slots the plan spreads items over
   p.grid_items = (int)a.grid_items;
   p.out = out;
   p.lse = lse;
