@@ -1866,12 +1866,12 @@ AttnPlan plan_attn(int B, int N_max, int Hq, int Hkv, int D, int max_slots) {
   // the uniform split for blocks of bm rows: one resident block per SM,
   // estimated time = waves x (tiles per block + a fixed cost of about four
   // 128-key tiles for the prologue and partials)
-  auto split_for = [&](int bm, long &per) {
+  auto split_for = [&](int bm, long slots, long &per) {
     const long units = (long)B * Hkv * ((N_max * g + bm - 1) / bm);
     long best_s = 1;
     double best_t = 1e30;
     for (long s = 1; s <= max_tiles && s <= 32; ++s) {
-      const long waves = (units * s + nsm - 1) / nsm;
+      const long waves = (units * s + slots - 1) / slots;
       const long pr = (max_tiles + s - 1) / s;
       const double t = (double)waves * (double)(pr + 4);
       if (t < best_t - 1e-9) {
@@ -1891,11 +1891,14 @@ AttnPlan plan_attn(int B, int N_max, int Hq, int Hkv, int D, int max_slots) {
     // so L2 serves their shared K/V).
     long per = 0;
     a.bm = kTcRows;
-    best_s = split_for(a.bm, per);
+    best_s = split_for(a.bm, nsm, per);
     if (per <= kSmallBlockTiles && N_max * g > kTcBM) {
       a.bm = kTcBM;
-      best_s = split_for(a.bm, per);
+      best_s = split_for(a.bm, nsm, per);
     }
+    // Blocks that all hold one 128-row tile run the two-blocks-per-SM kernel:
+    // two block slots per SM.
+    if (a.bm == kTcBM || N_max * g <= kTcBM) best_s = split_for(a.bm, 2 * nsm, per);
   } else {
     a.bm = kBM;
     const long units = (long)B * Hkv * ((N_max * g + a.bm - 1) / a.bm);
@@ -1923,7 +1926,7 @@ AttnPlan plan_attn(int B, int N_max, int Hq, int Hkv, int D, int max_slots) {
   a.grid_items = items_u;
   // Planned launches whose blocks all hold one 128-row tile run two blocks
   // per SM (the plan then counts two block slots per SM).
-  a.dual = a.mode == 2 && N_max * g <= kTcBM;
+  a.dual = a.impl == 0 && (a.bm == kTcBM || N_max * g <= kTcBM);
   size_t rows = (size_t)B * Hkv * a.splits * a.rows_pad;
   if (a.mode == 2) {
     // room for four waves of shorter pieces per block slot (at least the
