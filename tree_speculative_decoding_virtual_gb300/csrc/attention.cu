@@ -476,7 +476,7 @@ constexpr int kPlanMaxChunk = kTcMaxPages * kPage / kTcBN;   // 64 key tiles per
 constexpr int kPlanFixedTiles = 4;                           // per-item set-up + partials
 constexpr int kPlanGroups = 5;                               // thread groups over the sequences
 constexpr int kPlanMinTiles = 16;  // uniform blocks shorter than this keep the uniform split
-constexpr int kSmallBlockTiles = 4;  // 256-row blocks of at most this many key tiles: use 128 rows
+constexpr int kSmallBlockTiles = 31;  // 256-row blocks of at most this many key tiles: use 128 rows
 static_assert(kPlanMaxChunk == 64, "the plan key keeps C in 6 bits");
 
 struct TcPlanShared {
@@ -1884,11 +1884,12 @@ AttnPlan plan_attn(int B, int N_max, int Hq, int Hkv, int D, int max_slots) {
   };
   long best_s = 1;
   if (a.impl == 0) {
-    // Blocks of 256 rows (two row tiles share every K/V tile) unless that
-    // leaves each block only a few key tiles: then the work is latency-bound
-    // and 128-row blocks, whose two softmax groups take alternate key tiles,
-    // spread it over twice the blocks (the row tiles' blocks run side by side,
-    // so L2 serves their shared K/V).
+    // 128-row blocks (the two-blocks-per-SM kernel; the blocks of one kv
+    // head's row tiles run side by side, so L2 serves their shared K/V) unless
+    // 256-row blocks would each walk 32 or more key tiles: such long,
+    // tensor-bound blocks gain from two row tiles sharing every K/V tile
+    // (measured: the 70B shape, 128 rows 0.4% slower; 8B, budgeted and
+    // dynamic-tree layers 2-7% faster with 128 rows).
     long per = 0;
     a.bm = kTcRows;
     best_s = split_for(a.bm, nsm, per);
