@@ -763,15 +763,14 @@ __device__ __noinline__ void tc_issue_s(uint32_t tmem, uint32_t base, int q, int
   using namespace sm100;
   using L = TcLayout<D>;
   constexpr uint32_t idS = idesc_bf16_f32(kTcBM, kTcBN, false, false);
+  const uint64_t qd = smem_desc_sw128(base + L::kQ + q * L::kQTile, 16, 1024);
+  const uint64_t kd = smem_desc_sw128(base + L::kK + st * L::kTile, 16, 1024);
   tc_fence_after();
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     umma_bf16(tmem + t * L::kTmemTile + L::kTmemS,
-              smem_desc_sw128(base + L::kQ + q * L::kQTile + (kk >> 2) * L::kQHalf + (kk & 3) * 32,
-                              16, 1024),
-              smem_desc_sw128(base + L::kK + st * L::kTile + (kk >> 2) * L::kKVHalf + (kk & 3) * 32,
-                              16, 1024),
-              idS, kk > 0);
+              desc_add(qd, (kk >> 2) * L::kQHalf + (kk & 3) * 32),
+              desc_add(kd, (kk >> 2) * L::kKVHalf + (kk & 3) * 32), idS, kk > 0);
   }
   umma_commit(s_full);
 }
@@ -784,12 +783,12 @@ __device__ __noinline__ void tc_issue_pv(uint32_t tmem, uint32_t base, int t, in
   using namespace sm100;
   using L = TcLayout<D>;
   constexpr uint32_t idPV = idesc_bf16_f32(kTcBM, D, false, true);
+  const uint64_t vd = smem_desc_sw128(base + L::kV + st * L::kTile, L::kKVHalf, 1024);
   tc_fence_after();
 #pragma unroll
   for (int kk = 0; kk < kTcBN / 16; ++kk) {
     umma_bf16_ta(tmem + t * L::kTmemTile + L::kTmemO, tmem + t * L::kTmemTile + L::kTmemS + kk * 8,
-                 smem_desc_sw128(base + L::kV + st * L::kTile + kk * 16 * 128, L::kKVHalf, 1024),
-                 idPV, (accum || kk > 0) ? 1u : 0u);
+                 desc_add(vd, kk * 16 * 128), idPV, (accum || kk > 0) ? 1u : 0u);
   }
   if (final_bar) umma_commit(final_bar);
 }
@@ -1152,7 +1151,8 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
           // key pairs on packed fp32: one FMA for both arguments, one add for
           // each of the two sums
           const unsigned long long sc2 = f2_pack(sc, sc), nmb2 = f2_pack(-mb, -mb);
-          unsigned long long esum2 = f2_pack(0.f, 0.f), rsum2 = f2_pack(0.f, 0.f);
+          unsigned long long esum2 = f2_pack(0.f, 0.f);
+          float ra[2] = {0.f, 0.f}, rc[2] = {0.f, 0.f};  // rounded P: even / odd keys
 #pragma unroll
           for (int c2 = 0; c2 < 2; ++c2) {
             uint32_t pk[16];  // P as bf16 pairs: column i holds keys 2i, 2i+1 of the chunk
@@ -1165,13 +1165,12 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
               const float c = ex2_approx(x.y);
               pk[i] = pack_bf16(a, c);
               esum2 = f2_add(esum2, f2_pack(a, c));
-              rsum2 = f2_add(rsum2, f2_pack(__uint_as_float(pk[i] << 16),
-                                            __uint_as_float(pk[i] & 0xFFFF0000u)));
+              add_bf16x2(ra[i & 1], rc[i & 1], pk[i]);
             }
             tmem_st16(tS + h * 32 + c2 * 16, pk);
           }
-          const float2 es = f2_unpack(esum2), rs = f2_unpack(rsum2);
-          lt += rs.x + rs.y;
+          const float2 es = f2_unpack(esum2);
+          lt += (ra[0] + ra[1]) + (rc[0] + rc[1]);
           lte += es.x + es.y;
         }
         l_sum += lt;
@@ -1370,11 +1369,12 @@ __device__ __noinline__ void dual_issue_s(uint32_t ts, uint32_t qt, uint32_t kt,
   using namespace sm100;
   using L = DualLayout<D>;
   constexpr uint32_t idS = idesc_bf16_f32(kTcBM, kDualBN, false, false);
+  const uint64_t qd = smem_desc_sw128(qt, 16, 1024), kd = smem_desc_sw128(kt, 16, 1024);
   tc_fence_after();
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk)
-    umma_bf16(ts, smem_desc_sw128(qt + (kk >> 2) * L::kQHalf + (kk & 3) * 32, 16, 1024),
-              smem_desc_sw128(kt + (kk >> 2) * L::kKVHalf + (kk & 3) * 32, 16, 1024), idS, kk > 0);
+    umma_bf16(ts, desc_add(qd, (kk >> 2) * L::kQHalf + (kk & 3) * 32),
+              desc_add(kd, (kk >> 2) * L::kKVHalf + (kk & 3) * 32), idS, kk > 0);
   umma_commit(s_bar);
 }
 
@@ -1385,11 +1385,11 @@ __device__ __noinline__ void dual_issue_pv(uint32_t to, uint32_t tp, uint32_t vt
   using namespace sm100;
   using L = DualLayout<D>;
   constexpr uint32_t idPV = idesc_bf16_f32(kTcBM, D, false, true);
+  const uint64_t vd = smem_desc_sw128(vt, L::kKVHalf, 1024);
   tc_fence_after();
 #pragma unroll
   for (int kk = 0; kk < kDualBN / 16; ++kk)
-    umma_bf16_ta(to, tp + kk * 8, smem_desc_sw128(vt + kk * 16 * 128, L::kKVHalf, 1024), idPV,
-                 (accum || kk > 0) ? 1u : 0u);
+    umma_bf16_ta(to, tp + kk * 8, desc_add(vd, kk * 16 * 128), idPV, (accum || kk > 0) ? 1u : 0u);
   if (bar1) umma_commit(bar1);
   if (bar2) umma_commit(bar2);
 }
@@ -1644,7 +1644,8 @@ tree_attn_split_dual(const AttnParams p, const __grid_constant__ CUtensorMap map
       }
       const float mb = m_use == -INFINITY ? 0.f : m_use;
       const unsigned long long sc2 = f2_pack(sc, sc), nmb2 = f2_pack(-mb, -mb);
-      unsigned long long esum2 = f2_pack(0.f, 0.f), rsum2 = f2_pack(0.f, 0.f);
+      unsigned long long esum2 = f2_pack(0.f, 0.f);
+      float ra[2] = {0.f, 0.f}, rc[2] = {0.f, 0.f};  // rounded P: even / odd keys
 #pragma unroll
       for (int c2 = 0; c2 < 2; ++c2) {
         uint32_t pk[16];  // P as bf16 pairs: column i holds keys 2i, 2i+1 of the chunk
@@ -1657,13 +1658,12 @@ tree_attn_split_dual(const AttnParams p, const __grid_constant__ CUtensorMap map
           const float c = ex2_approx(x.y);
           pk[i] = pack_bf16(a, c);
           esum2 = f2_add(esum2, f2_pack(a, c));
-          rsum2 = f2_add(rsum2, f2_pack(__uint_as_float(pk[i] << 16),
-                                        __uint_as_float(pk[i] & 0xFFFF0000u)));
+          add_bf16x2(ra[i & 1], rc[i & 1], pk[i]);
         }
         tmem_st16(tS + c2 * 16, pk);
       }
-      const float2 es = f2_unpack(esum2), rs = f2_unpack(rsum2);
-      l_sum += rs.x + rs.y;
+      const float2 es = f2_unpack(esum2);
+      l_sum += (ra[0] + ra[1]) + (rc[0] + rc[1]);
       l_ex += es.x + es.y;
       tmem_wait_st();
       tc_fence_before();

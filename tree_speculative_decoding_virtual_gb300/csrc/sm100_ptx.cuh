@@ -178,6 +178,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   d |= (uint64_t)2u << 61;
   return d;
 }
+// The descriptor of the matrix `off_bytes` (a multiple of 16) past the one
+// `d` describes.  The start-address field holds address / 16 in 14 bits and
+// every shared-memory address of a block is below 256 KB, so the sum never
+// carries out of the field.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t off_bytes) {
+  return d + (uint64_t)(off_bytes >> 4);
+}
 // Instruction descriptor for kind::f16 with bf16 A/B and an fp32 accumulator.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major,
                                                       bool b_mn_major) {
@@ -276,6 +283,15 @@ __device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsig
   unsigned long long r;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
+}
+// acc_lo += the low bf16 of w and acc_hi += the high one: each is widened to
+// fp32 exactly and added with round-to-nearest (PTX mixed-precision add), so
+// no shift or mask is needed to unpack the pair.
+__device__ __forceinline__ void add_bf16x2(float &acc_lo, float &acc_hi, uint32_t w) {
+  asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n add.rn.f32.bf16 %0, lo, %0;\n"
+      " add.rn.f32.bf16 %1, hi, %1;\n}\n"
+      : "+f"(acc_lo), "+f"(acc_hi)
+      : "r"(w));
 }
 // max of three floats in one instruction
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
