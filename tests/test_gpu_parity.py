@@ -54,6 +54,40 @@ def test_workload_70b_sampled(tsd):
     assert g["status"] == 0
 
 
+def _plant_jump(inp, b, node, h, scale, slots):
+    """Set the keys at `slots` of sequence b (in the kv head of q-head h) to
+    `scale` times the query of (node, h): with |q|^2 ~ D their scores exceed
+    the other keys' by about 16 * scale in log2 units."""
+    c = inp.cache
+    hkv = h // (inp.Hq // inp.Hkv)
+    qf = (inp.q[b, node, h].astype(np.uint32) << 16).view(np.float32)
+    kbits = gen.bf16_bits(qf * np.float32(scale))
+    for s in slots:
+        c.k[c.block_table[b, s // gen.PAGE], hkv, s % gen.PAGE] = kbits
+
+
+@pytest.mark.parametrize("workload,scale", [("8b", 2.0), ("8b", 16.0), ("70b", 5.0)])
+def test_scores_far_above_the_first_tile(tsd, workload, scale):
+    """Keys late in a split's range that score far above its first tile (by
+    about 30, 260 and 80 in log2 units): the kernels weigh P against the first
+    tile's max while a tile sums to at most 2^64 and otherwise take the max
+    again and rescale; the planted rows and their neighbours match the oracle
+    (the 8B shape runs the two-blocks-per-SM kernel, the 70B shape 256-row
+    blocks)."""
+    inp = gen.verify_workload(workload)
+    P0 = int(inp.prefix_len[0])
+    slots = [P0 // 3, P0 // 2 + 37, (2 * P0) // 3 + 70, P0 - 5]
+    for h in (0, inp.Hq // inp.Hkv):  # a q-head of each of the first two kv heads
+        _plant_jump(inp, 0, 0, h, scale, slots)
+    sample = {(0, i, h) for i in range(min(inp.N_max, 8)) for h in range(inp.Hq)}
+    sample |= {(b, 0, 0) for b in range(inp.B)}
+    sample = sorted(sample)
+    g = run_gpu(tsd, inp)
+    o = run_oracle(inp, sample_attention=sample)
+    compare(inp, g, o, sample=sample)
+    assert g["status"] == 0
+
+
 @pytest.mark.parametrize("N", [16, 32, 64, 128, 256])
 def test_bastion_budget(tsd, N):
     import torch

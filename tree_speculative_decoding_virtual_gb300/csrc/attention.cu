@@ -1122,53 +1122,72 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
                 if (!((vis >> i) & 1u)) r[c2][i] = __float_as_uint(-INFINITY);
             }
           }
-          // the max with three-input max instructions: 8 chains of 8 values
-          float mx[8];
+          // Once every row of the warp has a reference max (m_use finite), P is
+          // taken against it with no max pass; a tile sum above 2^64 (a score
+          // more than 64 above the reference, or a non-finite one) sends the warp
+          // back through the exact path, which takes the max, moves the
+          // reference under the lazy rule and rescales.  P stays within 2^64 of
+          // the reference either way, far from fp32 overflow in every sum.
+          bool exact = !__all_sync(0xffffffffu, m_use != -INFINITY);
+          uint32_t pk[2][16];  // P as bf16 pairs: column i holds keys 2i, 2i+1 of a chunk
+          unsigned long long esum2;
+          float ra[2], rc[2];  // rounded P: even / odd keys
+#pragma unroll 1
+          for (;;) {
+            if (exact) {
+              // the max with three-input max instructions: 8 chains of 8 values
+              float mx[8];
 #pragma unroll
-          for (int a = 0; a < 8; ++a) {
-            const auto v = [&](int i) { return __uint_as_float(r[i >> 5][i & 31]); };
-            float m = fmax3(v(a), v(a + 8), v(a + 16));
-            m = fmax3(m, v(a + 24), v(a + 32));
-            m = fmax3(m, v(a + 40), v(a + 48));
-            mx[a] = fmaxf(m, v(a + 56));
-          }
-          const float mt = fmaxf(fmax3(mx[0], mx[1], mx[2]),
-                                 fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7])) * sc;
-          const float m_new = fmaxf(m_use, mt);
-          const bool upd = m_new > m_use + 8.f;  // first visible key, or the max grew by > 2^8
-          const float alpha = upd ? exp2f(m_use - m_new) : 1.f;
-          if (__any_sync(0xffffffffu, upd) && (u > 0 || h > 0)) {
-            const float s0 = rescale(alpha, u > 0, h > 0);
-            if (h > 0) lt = s0;  // the first half's P as rounded again
-          }
-          if (upd) {
-            l_sum *= alpha;
-            l_ex *= alpha;
-            lte *= alpha;  // (zero in the first half)
-            m_use = m_new;
-          }
-          const float mb = m_use == -INFINITY ? 0.f : m_use;
-          // key pairs on packed fp32: one FMA for both arguments, one add for
-          // each of the two sums
-          const unsigned long long sc2 = f2_pack(sc, sc), nmb2 = f2_pack(-mb, -mb);
-          unsigned long long esum2 = f2_pack(0.f, 0.f);
-          float ra[2] = {0.f, 0.f}, rc[2] = {0.f, 0.f};  // rounded P: even / odd keys
-#pragma unroll
-          for (int c2 = 0; c2 < 2; ++c2) {
-            uint32_t pk[16];  // P as bf16 pairs: column i holds keys 2i, 2i+1 of the chunk
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float2 x = f2_unpack(f2_fma(f2_pack(__uint_as_float(r[c2][2 * i]),
-                                                        __uint_as_float(r[c2][2 * i + 1])),
-                                                sc2, nmb2));
-              const float a = ex2_approx(x.x);
-              const float c = ex2_approx(x.y);
-              pk[i] = pack_bf16(a, c);
-              esum2 = f2_add(esum2, f2_pack(a, c));
-              add_bf16x2(ra[i & 1], rc[i & 1], pk[i]);
+              for (int a = 0; a < 8; ++a) {
+                const auto v = [&](int i) { return __uint_as_float(r[i >> 5][i & 31]); };
+                float m = fmax3(v(a), v(a + 8), v(a + 16));
+                m = fmax3(m, v(a + 24), v(a + 32));
+                m = fmax3(m, v(a + 40), v(a + 48));
+                mx[a] = fmaxf(m, v(a + 56));
+              }
+              const float mt = fmaxf(fmax3(mx[0], mx[1], mx[2]),
+                                     fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7])) * sc;
+              const float m_new = fmaxf(m_use, mt);
+              const bool upd = m_new > m_use + 8.f;  // first visible key, or the max grew by > 2^8
+              const float alpha = upd ? exp2f(m_use - m_new) : 1.f;
+              if (__any_sync(0xffffffffu, upd) && (u > 0 || h > 0)) {
+                const float s0 = rescale(alpha, u > 0, h > 0);
+                if (h > 0) lt = s0;  // the first half's P as rounded again
+              }
+              if (upd) {
+                l_sum *= alpha;
+                l_ex *= alpha;
+                lte *= alpha;  // (zero in the first half)
+                m_use = m_new;
+              }
             }
-            tmem_st16(tS + h * 32 + c2 * 16, pk);
+            const float mb = m_use == -INFINITY ? 0.f : m_use;
+            // key pairs on packed fp32: one FMA for both arguments, one add for
+            // the fp32 sum
+            const unsigned long long sc2 = f2_pack(sc, sc), nmb2 = f2_pack(-mb, -mb);
+            esum2 = f2_pack(0.f, 0.f);
+            ra[0] = ra[1] = rc[0] = rc[1] = 0.f;
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float2 x = f2_unpack(f2_fma(f2_pack(__uint_as_float(r[c2][2 * i]),
+                                                          __uint_as_float(r[c2][2 * i + 1])),
+                                                  sc2, nmb2));
+                const float a = ex2_approx(x.x);
+                const float c = ex2_approx(x.y);
+                pk[c2][i] = pack_bf16(a, c);
+                esum2 = f2_add(esum2, f2_pack(a, c));
+                add_bf16x2(ra[i & 1], rc[i & 1], pk[c2][i]);
+              }
+            }
+            if (exact) break;
+            const float2 e = f2_unpack(esum2);
+            exact = __any_sync(0xffffffffu, !(e.x + e.y <= 0x1p64f));
+            if (!exact) break;
           }
+#pragma unroll
+          for (int c2 = 0; c2 < 2; ++c2) tmem_st16(tS + h * 32 + c2 * 16, pk[c2]);
           const float2 es = f2_unpack(esum2);
           lt += (ra[0] + ra[1]) + (rc[0] + rc[1]);
           lte += es.x + es.y;
@@ -1606,62 +1625,82 @@ tree_attn_split_dual(const AttnParams p, const __grid_constant__ CUtensorMap map
             if (!((vis >> i) & 1u)) r[c2][i] = __float_as_uint(-INFINITY);
         }
       }
-      float mx[8];
-#pragma unroll
-      for (int a = 0; a < 8; ++a) {
-        const auto v = [&](int i) { return __uint_as_float(r[i >> 5][i & 31]); };
-        float m = fmax3(v(a), v(a + 8), v(a + 16));
-        m = fmax3(m, v(a + 24), v(a + 32));
-        m = fmax3(m, v(a + 40), v(a + 48));
-        mx[a] = fmaxf(m, v(a + 56));
-      }
-      const float mt = fmaxf(fmax3(mx[0], mx[1], mx[2]),
-                             fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7])) * sc;
-      const float m_new = fmaxf(m_use, mt);
-      const bool upd = m_new > m_use + 8.f;  // first visible key, or the max grew by > 2^8
-      const float alpha = upd ? exp2f(m_use - m_new) : 1.f;
-      if (__any_sync(0xffffffffu, upd) && j > 0) {
-        // O holds P V of tiles before j - 1; the one of tile j - 1 may still run
-        if (!warp_wait(sh.pv_done, (j - 1) & 1)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+      // P against the reference max once every row of the warp has one; the
+      // exact path (max, lazy rule, rescale) otherwise or when a tile sum
+      // exceeds 2^64, as in tree_attn_split_tc
+      bool exact = !__all_sync(0xffffffffu, m_use != -INFINITY), failed = false;
+      uint32_t pk[2][16];  // P as bf16 pairs: column i holds keys 2i, 2i+1 of a chunk
+      unsigned long long esum2;
+      float ra[2], rc[2];  // rounded P: even / odd keys
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + c * 32, o);
-          tmem_wait_ld();
+      for (;;) {
+        if (exact) {
+          float mx[8];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(tO + c * 32, o);
+          for (int a = 0; a < 8; ++a) {
+            const auto v = [&](int i) { return __uint_as_float(r[i >> 5][i & 31]); };
+            float m = fmax3(v(a), v(a + 8), v(a + 16));
+            m = fmax3(m, v(a + 24), v(a + 32));
+            m = fmax3(m, v(a + 40), v(a + 48));
+            mx[a] = fmaxf(m, v(a + 56));
+          }
+          const float mt = fmaxf(fmax3(mx[0], mx[1], mx[2]),
+                                 fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7])) * sc;
+          const float m_new = fmaxf(m_use, mt);
+          const bool upd = m_new > m_use + 8.f;  // first visible key, or the max grew by > 2^8
+          const float alpha = upd ? exp2f(m_use - m_new) : 1.f;
+          if (__any_sync(0xffffffffu, upd) && j > 0) {
+            // O holds P V of tiles before j - 1; the one of tile j - 1 may still run
+            if (!warp_wait(sh.pv_done, (j - 1) & 1)) {
+              failed = true;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(tO + c * 32, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st32(tO + c * 32, o);
+            }
+          }
+          if (upd) {
+            l_sum *= alpha;
+            l_ex *= alpha;
+            m_use = m_new;
+          }
         }
-      }
-      if (upd) {
-        l_sum *= alpha;
-        l_ex *= alpha;
-        m_use = m_new;
-      }
-      const float mb = m_use == -INFINITY ? 0.f : m_use;
-      const unsigned long long sc2 = f2_pack(sc, sc), nmb2 = f2_pack(-mb, -mb);
-      unsigned long long esum2 = f2_pack(0.f, 0.f);
-      float ra[2] = {0.f, 0.f}, rc[2] = {0.f, 0.f};  // rounded P: even / odd keys
+        const float mb = m_use == -INFINITY ? 0.f : m_use;
+        const unsigned long long sc2 = f2_pack(sc, sc), nmb2 = f2_pack(-mb, -mb);
+        esum2 = f2_pack(0.f, 0.f);
+        ra[0] = ra[1] = rc[0] = rc[1] = 0.f;
 #pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
-        uint32_t pk[16];  // P as bf16 pairs: column i holds keys 2i, 2i+1 of the chunk
+        for (int c2 = 0; c2 < 2; ++c2) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 x = f2_unpack(f2_fma(f2_pack(__uint_as_float(r[c2][2 * i]),
-                                                    __uint_as_float(r[c2][2 * i + 1])),
-                                            sc2, nmb2));
-          const float a = ex2_approx(x.x);
-          const float c = ex2_approx(x.y);
-          pk[i] = pack_bf16(a, c);
-          esum2 = f2_add(esum2, f2_pack(a, c));
-          add_bf16x2(ra[i & 1], rc[i & 1], pk[i]);
+          for (int i = 0; i < 16; ++i) {
+            const float2 x = f2_unpack(f2_fma(f2_pack(__uint_as_float(r[c2][2 * i]),
+                                                      __uint_as_float(r[c2][2 * i + 1])),
+                                              sc2, nmb2));
+            const float a = ex2_approx(x.x);
+            const float c = ex2_approx(x.y);
+            pk[c2][i] = pack_bf16(a, c);
+            esum2 = f2_add(esum2, f2_pack(a, c));
+            add_bf16x2(ra[i & 1], rc[i & 1], pk[c2][i]);
+          }
         }
-        tmem_st16(tS + c2 * 16, pk);
+        if (exact) break;
+        const float2 e = f2_unpack(esum2);
+        exact = __any_sync(0xffffffffu, !(e.x + e.y <= 0x1p64f));
+        if (!exact) break;
       }
+      if (failed) {
+        ok = false;
+        break;
+      }
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) tmem_st16(tS + c2 * 16, pk[c2]);
       const float2 es = f2_unpack(esum2);
       l_sum += (ra[0] + ra[1]) + (rc[0] + rc[1]);
       l_ex += es.x + es.y;
