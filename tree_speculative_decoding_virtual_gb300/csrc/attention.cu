@@ -62,7 +62,7 @@ struct AttnParams {
   int4 *plan_out;    // plan_mode 2: per sequence (first item, splits, chunk in key tiles, row tiles)
   int4 *plan_items;  // plan_mode 2: per block of the grid, its item (tree_attn_plan_kernel)
   uint16_t *part_o;  // fp16 partial rows [..][D]: the split's O / (l * c)
-  float4 *part_ml;   // one per partial row: (max in log2 units, sum l, scale c, 0)
+  float4 *part_ml;   // one per partial row: (reference max in log2 units, sum l, scale c, 0)
   uint16_t *out;
   float *lse;
   int32_t *status;
@@ -411,12 +411,17 @@ tree_attn_split_kernel(const AttnParams p) {
 // tile runs while the other's MMAs execute.  S_{t,j+1} is issued right
 // behind P_tj V_j and MMAs complete in issue order, so when the softmax sees
 // S_tj complete, every earlier MMA of the row tile has completed too: O may
-// be rescaled and S_tj overwritten by P_tj with no further wait.  The
-// running max is raised lazily: O and the row sum are rescaled (in TMEM)
-// only when a max exceeds the one in use by more than 2^8, so P never
-// exceeds 256 and the result is the same softmax.  A tile's row is handled
-// in two 64-key halves; if the second half raises the max, the first half's
-// P (already in TMEM) is rescaled too.
+// be rescaled and S_tj overwritten by P_tj with no further wait.  P is taken
+// against a reference max m per row, raised lazily: the tile's max is
+// computed only while the row has no reference yet or when P would sum above
+// 2^64 (a score more than 64 above m), and then O and the row sums are
+// rescaled (in TMEM) only if that max exceeds m by more than 2^8.  Every sum
+// stays far from fp32 overflow and P keeps its relative precision, so the
+// result is the same softmax.  A tile's row is handled in two 64-key halves;
+// if the second half raises m, the first half's P (already in TMEM) is
+// rescaled too.  (The tile max is ALU work that the MMA-issuing warp, which
+// shares an SM sub-partition with a softmax warp of each group, would wait
+// behind.)
 // K and V tiles are read straight from the paged cache by TMA (4-D view
 // [block][kv head][slot][D], 128-byte swizzle): when the eight 16-slot
 // blocks of a tile are consecutive one box fetches them, otherwise one box
@@ -1305,8 +1310,8 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
 // S_1, P_0 V_0, S_2, P_1 V_1, S_3, ...: S_{j+2} reuses the buffer P_j V_j
 // reads (the tensor pipe runs in issue order), and while the softmax works on
 // S_j the tensor core computes S_{j+1} and P_{j-1} V_{j-1}.  So a P V may still
-// be running when the next tile's softmax raises the running max; the rescale
-// of O that the lazy max rule then needs first waits for it (pv_done).
+// be running when the next tile's softmax raises the reference max; the
+// rescale of O that the lazy rule then needs first waits for it (pv_done).
 // Partials, waits, time-outs and teardown are as in tree_attn_split_tc.
 // ===========================================================================
 constexpr int kDualThreads = 192;
