@@ -38,7 +38,7 @@ from .verify import verify_greedy
 from .commit import commit_path
 from .best_first import best_first_tree, ranked_tokens
 from .rejection import modified_rejection_step, residual_distribution
-from .budget import verify_step_cost, calibrate, budget_select, cost_table
+from .budget import verify_step_cost, calibrate, speedup_curve, budget_select, cost_table
 from .stochastic import node_decision, tree_verify_stochastic, tree_verify_stochastic_all
 from .dynamic_tree import (dynamic_tree, expand_level, new_pool, pool_base, pool_size,
                            rerank as dynamic_tree_rerank)
@@ -48,7 +48,7 @@ __all__ = [
     "build_ancestors", "ancestor_chain", "bf16_to_f64", "tree_attention", "gather_sequence_kv",
     "verify_greedy", "commit_path", "best_first_tree", "ranked_tokens",
     "modified_rejection_step", "residual_distribution",
-    "verify_step_cost", "calibrate", "budget_select", "cost_table",
+    "verify_step_cost", "calibrate", "speedup_curve", "budget_select", "cost_table",
     "node_decision", "tree_verify_stochastic", "tree_verify_stochastic_all",
     "dynamic_tree", "expand_level", "new_pool", "pool_base", "pool_size", "dynamic_tree_rerank",
 ]

@@ -22,10 +22,10 @@ Readings taken where the page is silent:
   inserted (best-first insertion order), accumulated in fp64 in that order.
 * "Starts to decrease": the chosen N is the largest n such that
   S(1) <= S(2) <= ... <= S(n) (equal values do not stop the growth); when S
-  never decreases, the whole budget.  The choice is taken in fp32: A_hat is
-  an fp32 running sum in insertion order, and S(n) < S(n-1) is tested as
-  A_hat(n) * C(n-1) < A_hat(n-1) * C(n) (L_AR > 0 cancels), each product
-  rounded to fp32; S at the chosen n is (A_hat * L_AR) / C, in fp32.
+  never decreases, the whole budget.  S(n) is the page's quotient written
+  out in fp64: A_hat(n) is the fp64 sum of the non-root path scores (as
+  stored) in insertion order, S(n) = A_hat(n) * L_AR / C(n) with the step
+  costs as given; s_opt is S at the chosen n.
 """
 
 from __future__ import annotations
@@ -67,28 +67,38 @@ def calibrate(t_roof, t_meas):
     return alpha, beta
 
 
+def speedup_curve(rho_row, cost, l_ar):
+    """S(n) = A_hat(n) * L_AR / C(n) for n = 1..N_max, in fp64.  rho_row:
+    [N_max] path scores in insertion order (rho_row[0] is the root, which
+    A_hat leaves out); cost: [N_max + 1], cost[n] = C(n) > 0."""
+    L = float(l_ar)
+    S, a = [], 0.0
+    for n in range(1, len(rho_row) + 1):
+        if n >= 2:
+            a += float(rho_row[n - 1])
+        S.append(a * L / float(cost[n]))
+    return np.array(S, dtype=np.float64)
+
+
 def budget_select(rho, cost, l_ar):
     """rho: [B][N_max] path scores in insertion order (rho[b][0] is the root);
-    cost: [N_max + 1] with cost[n] = C(n) > 0 for n = 1..N_max; l_ar: L_AR.
-    Returns (n_opt int32 [B], s_opt float32 [B])."""
-    f32 = np.float32
-    rho = np.asarray(rho, dtype=f32)
-    cost = np.asarray(cost, dtype=f32)
-    l_ar = f32(l_ar)
+    cost: [N_max + 1] with cost[n] = C(n) > 0 for n = 1..N_max; l_ar: L_AR > 0.
+    Returns (n_opt int32 [B], s_opt float64 [B]): the last n before S first
+    decreases, and S there."""
+    rho = np.asarray(rho)
+    cost = np.asarray(cost)
     B, n_max = rho.shape
+    if not float(l_ar) > 0.0 or not np.all(cost[1:n_max + 1] > 0):
+        raise ValueError("L_AR and every step cost must be positive")
     n_opt = np.zeros(B, dtype=np.int32)
-    s_opt = np.zeros(B, dtype=f32)
+    s_opt = np.zeros(B, dtype=np.float64)
     for b in range(B):
-        a_prev, c_prev = f32(0.0), cost[1]
-        best = 1
-        for n in range(2, n_max + 1):
-            a = f32(a_prev + rho[b, n - 1])
-            c = cost[n]
-            if f32(a * c_prev) < f32(a_prev * c):  # S(n) < S(n - 1)
-                break
-            a_prev, c_prev, best = a, c, n
-        n_opt[b] = best
-        s_opt[b] = f32(f32(a_prev * l_ar) / c_prev)
+        S = speedup_curve(rho[b], cost, l_ar)
+        n = 1
+        while n < n_max and not S[n] < S[n - 1]:
+            n += 1
+        n_opt[b] = n
+        s_opt[b] = S[n - 1]
     return n_opt, s_opt
 
 
@@ -104,4 +114,4 @@ def cost_table(alpha, beta, t_draft, t_roof_of_n, n_max):
     return c
 
 
-__all__ = ["verify_step_cost", "calibrate", "budget_select", "cost_table"]
+__all__ = ["verify_step_cost", "calibrate", "speedup_curve", "budget_select", "cost_table"]

@@ -1,8 +1,12 @@
 """GPU parity of the tree budget ([BASTION] Methodology 3) against the oracle:
 the library's host-side cost model and calibration, and the device-side
-choice of the tree size from best-first path scores (bit-exact: both sides
-take every step in fp32 in the same order).  Then the chosen sizes drive the
-verify step on the truncated trees."""
+choice of the tree size from best-first path scores.  The kernel takes the
+choice in fp32 (a running sum of the path scores, a cross-multiplied
+comparison), the oracle is the page's quotient in fp64; both read the same
+fp32 cost table.  The chosen size must be the oracle's wherever every
+comparison that decides it is further from a tie than the kernel's rounding
+can move it, and S there must agree within that rounding.  Then the chosen
+sizes drive the verify step on the truncated trees."""
 
 import numpy as np
 import pytest
@@ -48,11 +52,41 @@ def test_calibrate_matches_oracle(tsd):
 
 
 def _cost(n_max, seed):
-    # C(n) = T_draft + alpha * t_roof(n) + beta on the BASTION verify shape
+    # C(n) = T_draft + alpha * t_roof(n) + beta on the BASTION verify shape,
+    # rounded to fp32 (the table the kernel reads; the oracle reads the same
+    # values)
     c = gen.BASTION
     t_roof = lambda n: oracle.verify_step_cost(c["B"], 32, 8, 128, [2048] * c["B"], c["V"],
                                                min(16, max(n - 1, 0)), n, 6757.2, 1888.4)[2]
-    return oracle.cost_table(1.3, 11.0 + seed, 20.0, t_roof, n_max)
+    return oracle.cost_table(1.3, 11.0 + seed, 20.0, t_roof, n_max).astype(np.float32)
+
+
+U32 = 2.0 ** -24  # unit roundoff of fp32
+
+
+def _fp32_margin(n_max):
+    """Relative error bound of the kernel's two sides of S(n) < S(n-1): an
+    fp32 running sum of at most n_max - 1 positive terms, then one product."""
+    return 2.0 * (n_max + 2) * U32
+
+
+def _check_choice(rho, cost, l_ar, n_gpu, s_gpu):
+    """Exact n where every deciding comparison clears the fp32 margin; S at
+    the choice within the kernel's rounding.  Returns the rows checked."""
+    n_ref, s_ref = oracle.budget_select(rho, cost.astype(np.float64), l_ar)
+    n_max = rho.shape[1]
+    checked = 0
+    for b in range(rho.shape[0]):
+        S = oracle.speedup_curve(rho[b], cost.astype(np.float64), l_ar)
+        top = min(int(n_ref[b]) + 1, n_max)
+        gaps = [abs(S[n - 1] - S[n - 2]) / S[n - 2] for n in range(2, top + 1) if S[n - 2] > 0]
+        if gaps and min(gaps) <= _fp32_margin(n_max):
+            continue  # a near-tie: either side of it is a correct fp32 choice
+        assert int(n_gpu[b]) == int(n_ref[b]), (b, int(n_gpu[b]), int(n_ref[b]))
+        bound = (int(n_ref[b]) + 2) * U32 * abs(s_ref[b])
+        assert abs(float(s_gpu[b]) - s_ref[b]) <= bound, (b, float(s_gpu[b]), s_ref[b])
+        checked += 1
+    return checked
 
 
 @pytest.mark.parametrize("n_max", [16, 64, 256])
@@ -62,37 +96,41 @@ def test_select_on_best_first_scores(tsd, n_max):
     q, root = gen.bastion_marginals()
     parent, tokens, depth, rho, ahat = tsd.best_first_tree_build(dev_tensor(q), dev_tensor(root),
                                                                  n_max)
-    cost = _cost(n_max, 0)
-    for l_ar in (5.0, 40.0, 400.0):
-        n_opt, s_opt = tsd.budget_select(rho, torch.from_numpy(cost.astype(np.float32)).cuda(), l_ar)
-        torch.cuda.synchronize()
-        r_n, r_s = oracle.budget_select(to_np(rho), cost, l_ar)
-        assert np.array_equal(to_np(n_opt), r_n)
-        assert np.array_equal(to_np(s_opt), r_s)
+    checked = 0
+    for seed in range(3):
+        cost = _cost(n_max, 7.0 * seed)
+        for l_ar in (5.0, 40.0, 400.0):
+            n_opt, s_opt = tsd.budget_select(rho, torch.from_numpy(cost).cuda(), l_ar)
+            torch.cuda.synchronize()
+            checked += _check_choice(to_np(rho), cost, l_ar, to_np(n_opt), to_np(s_opt))
+    assert checked >= 0.9 * 9 * q.shape[0], checked
 
 
 def test_select_random_scores_and_edges(tsd):
     import torch
     from _gpu_path import to_np
     rng = np.random.default_rng(5)
+    checked = total = 0
     for _ in range(20):
         B, n_max = int(rng.integers(1, 300)), int(rng.integers(1, 257))  # B up to 65535 allowed
         rho = np.sort(rng.random((B, n_max)).astype(np.float32), axis=1)[:, ::-1].copy()
         rho[:, 0] = 1.0
         rho[:, n_max // 2:] *= np.float32(rng.random())  # a drop, so some choices stop early
         cost = np.concatenate([[1.0], np.cumsum(rng.uniform(0.1, 5.0, size=n_max)) + 10.0])
+        cost = cost.astype(np.float32)
         l_ar = float(rng.uniform(1, 100))
-        n_opt, s_opt = tsd.budget_select(torch.from_numpy(rho).cuda(),
-                                         torch.from_numpy(cost.astype(np.float32)).cuda(), l_ar)
+        n_opt, s_opt = tsd.budget_select(torch.from_numpy(rho).cuda(), torch.from_numpy(cost).cuda(),
+                                         l_ar)
         torch.cuda.synchronize()
-        r_n, r_s = oracle.budget_select(rho, cost, l_ar)
-        assert np.array_equal(to_np(n_opt), r_n) and np.array_equal(to_np(s_opt), r_s)
+        checked += _check_choice(rho, cost, l_ar, to_np(n_opt), to_np(s_opt))
+        total += B
+    assert checked >= 0.9 * total, (checked, total)
     # host-side argument checks: nothing is launched
     rho_d = torch.from_numpy(rho).cuda()
     with pytest.raises(tsd.TsdError):
-        tsd.budget_select(rho_d, torch.from_numpy(cost.astype(np.float32)).cuda(), -1.0)
+        tsd.budget_select(rho_d, torch.from_numpy(cost).cuda(), -1.0)
     with pytest.raises(tsd.TsdError):
-        tsd.budget_select(rho_d, torch.from_numpy(cost[:2].astype(np.float32)).cuda(), 1.0)
+        tsd.budget_select(rho_d, torch.from_numpy(cost[:2]).cuda(), 1.0)
 
 
 def test_chosen_sizes_drive_the_verify_step(tsd):
@@ -106,7 +144,7 @@ def test_chosen_sizes_drive_the_verify_step(tsd):
     parent, tokens, depth, rho, ahat = tsd.best_first_tree_build(dev_tensor(q), dev_tensor(root),
                                                                  n_max)
     cost = _cost(n_max, 0)
-    n_opt, _ = tsd.budget_select(rho, torch.from_numpy(cost.astype(np.float32)).cuda(), 60.0)
+    n_opt, _ = tsd.budget_select(rho, torch.from_numpy(cost).cuda(), 60.0)
     torch.cuda.synchronize()
     n_opt = to_np(n_opt)
     assert (n_opt >= 1).all() and (n_opt <= n_max).all()

@@ -83,12 +83,24 @@ def _first_local_max_exact(rho_row, cost, l_ar):
     return n, S[n - 1]
 
 
+def _deciding_gap(rho_row, cost, l_ar, n_opt):
+    """Smallest relative gap |S(n) - S(n-1)| / S(n-1) among the comparisons
+    that decide n_opt (n = 2 .. n_opt + 1), in exact rationals."""
+    S = []
+    for n in range(1, len(rho_row) + 1):
+        a = sum((Fraction(float(r)) for r in rho_row[1:n]), Fraction(0))
+        S.append(a * Fraction(float(l_ar)) / Fraction(float(cost[n])))
+    gaps = [abs(S[n - 1] - S[n - 2]) / S[n - 2] for n in range(2, min(n_opt + 1, len(S)) + 1)
+            if S[n - 2] > 0]
+    return float(min(gaps)) if gaps else float("inf")
+
+
 def test_budget_select_matches_exact_brute_force():
     rng = np.random.default_rng(11)
     for _ in range(200):
         n_max = int(rng.integers(1, 40))
-        # dyadic values with few significant bits: every sum and product the
-        # choice forms is exact in fp32, so it must match exact arithmetic
+        # dyadic values with few significant bits: every sum and quotient's
+        # comparison is exact, so the fp64 choice must match exact arithmetic
         rho = np.sort(rng.integers(0, 64, size=n_max) / 64.0)[::-1].astype(np.float32)
         rho[0] = 1.0
         cost = np.concatenate([[1.0], rng.integers(8, 512, size=n_max).astype(np.float64)])
@@ -97,7 +109,47 @@ def test_budget_select_matches_exact_brute_force():
         n_opt, s_opt = budget.budget_select(rho[None, :], cost, l_ar)
         n_ref, s_ref = _first_local_max_exact(rho, cost, l_ar)
         assert int(n_opt[0]) == n_ref
-        assert s_opt[0] == pytest.approx(float(s_ref), rel=1e-6)
+        assert s_opt[0] == pytest.approx(float(s_ref), rel=1e-12)
+
+
+def test_budget_select_non_dyadic_matches_exact_brute_force():
+    """Path scores that are products of draft probabilities (fp32, full
+    significands), costs from an affine roofline model with a non-integer
+    slope and offset, a non-integer L_AR: the choice equals the exact-rational
+    one whenever the deciding comparisons are not within fp64 rounding of a
+    tie (such draws are redrawn; they are rare)."""
+    rng = np.random.default_rng(23)
+    checked = 0
+    while checked < 300:
+        n_max = int(rng.integers(2, 80))
+        q = rng.dirichlet(np.full(6, 0.7), size=n_max).max(axis=1)
+        rho = np.empty(n_max, dtype=np.float32)
+        rho[0] = 1.0
+        for i in range(1, n_max):  # each node's score: its parent's times a probability
+            rho[i] = np.float32(rho[int(rng.integers(0, i))] * np.float32(q[i]))
+        rho[1:] = np.sort(rho[1:])[::-1]  # best-first insertion order
+        t_roof = np.cumsum(rng.uniform(0.05, 3.0, size=n_max)) + rng.uniform(5.0, 50.0)
+        cost = np.concatenate([[1.0], rng.uniform(1.0, 40.0) + rng.uniform(0.8, 4.0) * t_roof])
+        l_ar = float(rng.uniform(0.3, 90.0))
+        n_ref, s_ref = _first_local_max_exact(rho, cost, l_ar)
+        if _deciding_gap(rho, cost, l_ar, n_ref) < 1e-12:
+            continue
+        n_opt, s_opt = budget.budget_select(rho[None, :], cost, l_ar)
+        assert int(n_opt[0]) == n_ref
+        assert s_opt[0] == pytest.approx(float(s_ref), rel=1e-12)
+        checked += 1
+
+
+def test_speedup_curve_against_exact_rationals():
+    rng = np.random.default_rng(4)
+    rho = np.concatenate([[1.0], rng.random(30)]).astype(np.float32)
+    cost = np.concatenate([[1.0], 3.0 + np.cumsum(rng.random(31))])
+    S = budget.speedup_curve(rho, cost, 7.25)
+    for n in range(1, 32):
+        exact = sum((Fraction(float(r)) for r in rho[1:n]), Fraction(0)) * Fraction(7.25) \
+            / Fraction(float(cost[n]))
+        assert S[n - 1] == pytest.approx(float(exact), rel=1e-13)
+    assert S[0] == 0.0  # the root alone accepts nothing beyond the autoregressive token
 
 
 def test_budget_select_closed_forms():
@@ -114,5 +166,13 @@ def test_budget_select_closed_forms():
         r[0, 0] = 1.0
         r[0, 1:m] = 0.5
         assert budget.budget_select(r, cost, 3.0)[0][0] == m
+    # equal values do not stop the growth: scores that vanish after node m
+    # under a flat cost keep S constant from m on, so the whole budget is used
+    flat = np.full(n_max + 1, 12.5)
+    for m in (2, 9):
+        r = np.zeros((1, n_max), dtype=np.float32)
+        r[0, 0] = 1.0
+        r[0, 1:m] = 0.3
+        assert budget.budget_select(r, flat, 3.0)[0][0] == n_max
     # a single node: nothing to choose
     assert budget.budget_select(np.ones((2, 1), np.float32), np.array([1.0, 1.0]), 1.0)[0].tolist() == [1, 1]
