@@ -5,7 +5,7 @@ One step = ancestors (a1) + tree attention (a2) + greedy verify (a3) + KV
 commit (a4) for the whole batch of one layer, back to back on one stream
 (plus the best-first tree build a5 for the budgeted-tree workloads).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 8b]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 70b]
   python bench.py --impl reference ...   # the CPU oracle arm
 
 Prints ONE JSON line (rank 0).  Inputs are synthetic (seeded, the shapes of
@@ -27,6 +27,7 @@ import re
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -180,9 +181,9 @@ def ncu_traffic(kernel_key, workload):
 class ClockSampler:
     def __init__(self, index):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench.csv")
+        fd, self.path = tempfile.mkstemp(prefix="tsd_clocks_", suffix=".csv")
+        os.close(fd)
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(index),
@@ -217,6 +218,10 @@ class ClockSampler:
                 rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
             except ValueError:
                 continue
+        try:
+            os.unlink(self.path)
+        except OSError:
+            pass
         if not rows:
             return None
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -321,19 +326,35 @@ def whole_job_rate(ms_per_step_max: float, world: int) -> float:
 # GPU arm
 # ---------------------------------------------------------------------------
 
-def gpu_arm(args, rank, world):
+# the configurations measured beside the headline workload in one run
+CONFIG_SET = ["tiny", "8b", "ragged", "70b", "bastion16", "bastion32", "bastion64", "bastion128",
+              "bastion256"]
+
+
+def _graph_capture(torch, fn):
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream().wait_stream(side)
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+def measure_workload(name, args, rank, world, dev, flush_l2, full, verify="greedy"):
+    """Set up one workload on the device and time it.  One step = the hot
+    path over the whole batch, captured as one CUDA graph.  Returns the
+    result dict (rank 0) or None."""
     import torch
     import torch.distributed as dist
 
     import tree_speculative_decoding_virtual_gb300 as tsd
 
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    tsd.set_option(tsd.OPT_ATTN_KERNEL, 0 if args.attn_kernel == "tc" else 1)
-    dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
-
-    w, desc = workload_inputs(args.workload)
+    steps, warmup = args.steps, args.warmup
+    w, desc = workload_inputs(name)
     bastion = isinstance(w, tuple) and w[0] == "bastion"
     dynamic = isinstance(w, tuple) and w[0] == "dynamic"
 
@@ -389,7 +410,7 @@ def gpu_arm(args, rank, world):
 
     B, N, Hq, Hkv, D, V, Dm = inp.B, inp.N_max, inp.Hq, inp.Hkv, inp.D, inp.V, inp.D_max
     c = inp.cache
-    stochastic = args.verify == "stochastic"
+    stochastic = verify == "stochastic"
     if stochastic:
         q_draft_h, tok_h, ua_h, ud_h = gen.stochastic_for(inp)
         inp.tokens = tok_h
@@ -410,11 +431,11 @@ def gpu_arm(args, rank, world):
     err = torch.empty((B,), **i32)
     out = torch.empty((B, N, Hq, D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, N, Hq), dtype=torch.float32, device=dev)
-    attn_ws = torch.empty((tsd.tree_attn_workspace_bytes(B, N, Hq, Hkv, D, max_slots),),
-                          dtype=torch.uint8, device=dev)
+    attn_need = tsd.tree_attn_workspace_bytes(B, N, Hq, Hkv, D, max_slots)
+    attn_ws = (torch.empty((attn_need,), dtype=torch.uint8, device=dev) if attn_need > 0 else None)
     ver_ws = torch.zeros((tsd.tree_verify_workspace_bytes(B, N, V),), dtype=torch.uint8, device=dev)
-    st_ws = torch.zeros((tsd.tree_verify_stochastic_workspace_bytes(B, N, V),), dtype=torch.uint8,
-                        device=dev)
+    st_ws = (torch.zeros((tsd.tree_verify_stochastic_workspace_bytes(B, N, V),), dtype=torch.uint8,
+                         device=dev) if stochastic else None)
     am = torch.empty((B, N), **i32)
     drw = torch.empty((B, N), **i32)
     A = torch.empty((B,), **i32)
@@ -424,22 +445,14 @@ def gpu_arm(args, rank, world):
     new_len = torch.empty((B,), **i32)
     moved = torch.empty((B,), **i32)
     status = torch.zeros((1,), **i32)
-    flush = torch.empty((FLUSH_BYTES,), dtype=torch.uint8, device=dev)
-    flush_rd = torch.ones((FLUSH_BYTES // 8,), dtype=torch.int64, device=dev)
-
-    def flush_l2():
-        # write one buffer larger than L2, then read another: the timed step
-        # starts with a cold L2 holding clean lines, so no write-back of the
-        # flush's dirty lines is charged to the kernels
-        flush.zero_()
-        flush_rd.sum()
 
     verify_name = "tree_verify_stochastic" if stochastic else "tree_verify_greedy"
     names = ((["best_first_tree_build"] if bastion else [])
              + (["dynamic_tree_expand", "dynamic_tree_rerank"] if dynamic else [])
              + ["tree_build_ancestors", "tree_attn_fwd", verify_name, "kv_commit_path"])
+    attn_launches = tsd.tree_attn_launches(B, N, Hq, Hkv, D, max_slots)
     launches_per_step = ((2 if bastion else 0) + (2 * dL + 1 if dynamic else 0) + 1
-                         + tsd.tree_attn_launches(B, N, Hq, Hkv, D, max_slots) + 1 + 1)
+                         + attn_launches + 1 + 1)
 
     calls = {}
     if bastion:
@@ -474,7 +487,7 @@ def gpu_arm(args, rank, world):
         for n in names:
             calls[n]()
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         flush_l2()
         step()
     torch.cuda.synchronize()
@@ -500,133 +513,175 @@ def gpu_arm(args, rank, world):
                 elif i == int(leaf_h[b]):
                     leaf_draws += 1
 
-    # CUDA graphs: the whole step, and each entry point on its own (timing
-    # without host launch gaps; the kernels are the same launches)
-    def capture(fn):
-        g = torch.cuda.CUDAGraph()
-        side = torch.cuda.Stream()
-        side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):
-            fn()
-        torch.cuda.current_stream().wait_stream(side)
-        with torch.cuda.graph(g):
-            fn()
-        return g
-
+    # CUDA graphs: the whole step; each entry point alone; each entry point
+    # behind the L2 flush inside the graph, and the flush alone (their
+    # difference is the entry point's device time from the end of the flush,
+    # without the gap between the start event and a graph's first kernel)
+    capture = lambda fn: _graph_capture(torch, fn)
     g_step = capture(step)
     g_one = {n: capture(calls[n]) for n in names}
+    g_flush = capture(flush_l2)
+
+    def flushed(fn):
+        def run():
+            flush_l2()
+            fn()
+        return run
+    g_fk = {n: capture(flushed(calls[n])) for n in names}
+    g_fstep = capture(flushed(step))
     torch.cuda.synchronize()
 
-    sampler = ClockSampler(local) if rank == 0 else None
+    sampler = ClockSampler(int(dev.index or 0)) if (rank == 0 and full) else None
     # ---- timed region 1: whole steps (the headline value) ----
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+          for _ in range(steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.perf_counter()
-    for s in range(args.steps):
+    for s_ in range(steps):
         flush_l2()
-        ev[s][0].record(stream)
+        ev[s_][0].record(stream)
         g_step.replay()
-        ev[s][1].record(stream)
+        ev[s_][1].record(stream)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
     if world > 1:
         dist.barrier()
-    ms_per_step = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev) / args.steps, world, dev)
+    ms_per_step = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev) / steps, world, dev)
+    clocks = sampler.stop() if sampler else None
 
-    # ---- timed region 2: per entry point (roofline of the dominant kernel) ----
+    # ---- timed region 2: per entry point ----
+    reps = max(3, min(steps, 400))
     nev = len(names) + 1
-    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(reps)]
     torch.cuda.synchronize()
-    for s in range(args.steps):
+    for s_ in range(reps):
         flush_l2()
-        kev[s][0].record(stream)
+        kev[s_][0].record(stream)
         for j, n in enumerate(names):
             g_one[n].replay()
-            kev[s][j + 1].record(stream)
+            kev[s_][j + 1].record(stream)
     torch.cuda.synchronize()
-    per_kernel = {n: 0.0 for n in names}
+    per_entry = {n: 0.0 for n in names}
     for e in kev:
         for j, n in enumerate(names):
-            per_kernel[n] += e[j].elapsed_time(e[j + 1])
-    kernel_us = {n: 1000.0 * v / args.steps for n, v in per_kernel.items()}
+            per_entry[n] += e[j].elapsed_time(e[j + 1])
+    entry_us = {n: 1000.0 * v / reps for n, v in per_entry.items()}
 
-    # ---- a4 layer-stacked: the step's accepted paths committed into L layers'
-    # caches in one launch (bandwidth is only meaningful this way; per layer the
-    # commit moves a few KB).  L = 80, or fewer when 80 layers of this cache
-    # would take more than 4 GB.
-    layer_bytes = 2 * kc.numel() * kc.element_size()
-    n_layers = int(max(1, min(80, (4 << 30) // max(layer_bytes, 1))))
-    kL = kc.unsqueeze(0).repeat(n_layers, 1, 1, 1, 1)
-    vL = vc.unsqueeze(0).repeat(n_layers, 1, 1, 1, 1)
-    stacked = lambda: tsd.kv_commit_path(kL, vL, table, prefix, n_nodes, A, path, err, N, Dm,
-                                         new_len=new_len, moved=moved, status=status)
-    stacked()
-    g_stacked = capture(stacked)
-    torch.cuda.synchronize()
-    sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(max(3, min(args.steps, 200)))]
-    for a_, b_ in sev:
-        flush_l2()
-        a_.record(stream)
-        g_stacked.replay()
-        b_.record(stream)
-    torch.cuda.synchronize()
-    stacked_us = 1000.0 * sum(a_.elapsed_time(b_) for a_, b_ in sev) / len(sev)
-    del kL, vL, g_stacked
+    # ---- timed region 3: kernel-only device time (graph deltas) ----
+    order = ["flush"] + names + ["step"]
+    graphs = dict(g_fk, flush=g_flush, step=g_fstep)
+    acc = {n: 0.0 for n in order}
+    for _ in range(reps):
+        for n in order:
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_.record(stream)
+            graphs[n].replay()
+            b_.record(stream)
+            b_.synchronize()
+            acc[n] += a_.elapsed_time(b_)
+    flush_us = 1000.0 * acc["flush"] / reps
+    kernel_us = {n: max(0.0, 1000.0 * acc[n] / reps - flush_us) for n in names}
+    step_kernel_us = max(0.0, 1000.0 * acc["step"] / reps - flush_us)
 
-    # ---- e2e: host buffers through the public API, copies inside the timing ----
-    h_in = {"q": q, "logits": logits, "parent": parent, "tokens": tokens, "n_nodes": n_nodes,
-            "prefix_len": prefix}
-    if stochastic:
-        h_in.update({"q_draft": q_draft, "u_accept": u_acc, "u_draw": u_drw})
-    if dynamic:  # the drafter's rows are the inputs; the tree is built on the device
-        del h_in["parent"], h_in["tokens"]
-        h_in.update({"draft_rows_%d" % (i + 1): r for i, r in enumerate(d_rows)})
-    pinned = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in h_in.items()}
-    for k, v in h_in.items():
-        pinned[k].copy_(v.cpu())
-    h_out_src = {"out": out, "argmax": am, "accept_len": A, "leaf": leaf, "path": path,
-                 "bonus": bonus, "new_len": new_len}
-    if stochastic:
-        h_out_src["draw"] = drw
-    h_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in h_out_src.items()}
-    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
-    d2h = sum(v.numel() * v.element_size() for v in h_out.values())
-    e2e_steps = max(3, min(args.steps, 200))
-    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(e2e_steps)]
-    # The logits (and the stochastic verifier's draft rows and uniforms) are
-    # read only by the verify call, so they are copied on a second stream while
-    # the tree and attention kernels run, as a serving loop would overlap them;
-    # that stream starts after the start event and after the previous step's
-    # last reads, and verify waits for it.
-    late = [k for k in h_in if k in ("logits", "q_draft", "u_accept", "u_draw")]
-    copy_stream = torch.cuda.Stream()
-    for s in range(e2e_steps + 3):
-        flush_l2()
-        if s >= 3:
-            e2e_ev[s - 3][0].record(stream)
-        copy_stream.wait_stream(stream)
-        with torch.cuda.stream(copy_stream):
-            for k in late:
-                h_in[k].copy_(pinned[k], non_blocking=True)
+    stacked_us = n_layers = None
+    if full:
+        # ---- a4 layer-stacked: the step's accepted paths committed into L
+        # layers' caches in one launch (bandwidth is only meaningful this way;
+        # per layer the commit moves a few KB).  L = 80, or fewer when 80
+        # layers of this cache would take more than 4 GB.
+        layer_bytes = 2 * kc.numel() * kc.element_size()
+        n_layers = int(max(1, min(80, (4 << 30) // max(layer_bytes, 1))))
+        kL = kc.unsqueeze(0).repeat(n_layers, 1, 1, 1, 1)
+        vL = vc.unsqueeze(0).repeat(n_layers, 1, 1, 1, 1)
+        stacked = lambda: tsd.kv_commit_path(kL, vL, table, prefix, n_nodes, A, path, err, N, Dm,
+                                             new_len=new_len, moved=moved, status=status)
+        stacked()
+        g_stacked = capture(stacked)
+        torch.cuda.synchronize()
+        sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(max(3, min(steps, 200)))]
+        for a_, b_ in sev:
+            flush_l2()
+            a_.record(stream)
+            g_stacked.replay()
+            b_.record(stream)
+        torch.cuda.synchronize()
+        stacked_us = 1000.0 * sum(a_.elapsed_time(b_) for a_, b_ in sev) / len(sev)
+        del kL, vL, g_stacked
+
+    e2e = None
+    if full:
+        # ---- e2e: host buffers through the public API, copies inside the timing ----
+        h_in = {"q": q, "logits": logits, "parent": parent, "tokens": tokens, "n_nodes": n_nodes,
+                "prefix_len": prefix}
+        if stochastic:
+            h_in.update({"q_draft": q_draft, "u_accept": u_acc, "u_draw": u_drw})
+        if dynamic:  # the drafter's rows are the inputs; the tree is built on the device
+            del h_in["parent"], h_in["tokens"]
+            h_in.update({"draft_rows_%d" % (i + 1): r for i, r in enumerate(d_rows)})
+        pinned = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in h_in.items()}
         for k, v in h_in.items():
-            if k not in late:
-                v.copy_(pinned[k], non_blocking=True)
-        for n in names:  # the public API calls, launched from Python
-            if n == verify_name:
-                stream.wait_stream(copy_stream)
-            calls[n]()
-        for k, v in h_out_src.items():
-            h_out[k].copy_(v, non_blocking=True)
-        if s >= 3:
-            e2e_ev[s - 3][1].record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev) / e2e_steps, world, dev)
-    clocks = sampler.stop() if sampler else None
+            pinned[k].copy_(v.cpu())
+        h_out_src = {"out": out, "argmax": am, "accept_len": A, "leaf": leaf, "path": path,
+                     "bonus": bonus, "new_len": new_len}
+        if stochastic:
+            h_out_src["draw"] = drw
+        h_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+                 for k, v in h_out_src.items()}
+        h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+        d2h = sum(v.numel() * v.element_size() for v in h_out.values())
+        e2e_steps = max(3, min(steps, 200))
+        e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(e2e_steps)]
+        # The logits (and the stochastic verifier's draft rows and uniforms)
+        # are read only by the verify call, so they are copied on a second
+        # stream while the tree and attention kernels run, as a serving loop
+        # would overlap them; that stream starts after the start event and
+        # after the previous step's last reads, and verify waits for it.
+        late = [k for k in h_in if k in ("logits", "q_draft", "u_accept", "u_draw")]
+        copy_stream = torch.cuda.Stream()
+        for s_ in range(e2e_steps + 3):
+            flush_l2()
+            if s_ >= 3:
+                e2e_ev[s_ - 3][0].record(stream)
+            copy_stream.wait_stream(stream)
+            with torch.cuda.stream(copy_stream):
+                for k in late:
+                    h_in[k].copy_(pinned[k], non_blocking=True)
+            for k, v in h_in.items():
+                if k not in late:
+                    v.copy_(pinned[k], non_blocking=True)
+            for n in names:  # the public API calls, launched from Python
+                if n == verify_name:
+                    stream.wait_stream(copy_stream)
+                calls[n]()
+            for k, v in h_out_src.items():
+                h_out[k].copy_(v, non_blocking=True)
+            if s_ >= 3:
+                e2e_ev[s_ - 3][1].record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev) / e2e_steps, world, dev)
+        # the box's pinned host-to-device copy rate, for reading the e2e figure
+        big = max(v.numel() * v.element_size() for v in pinned.values())
+        src = max(pinned.values(), key=lambda v: v.numel() * v.element_size())
+        dst = torch.empty_like(src, device=dev)
+        hev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(20)]
+        for a_, b_ in hev:
+            a_.record(stream)
+            dst.copy_(src, non_blocking=True)
+            b_.record(stream)
+        torch.cuda.synchronize()
+        h2d_gbs = big / (min(a_.elapsed_time(b_) for a_, b_ in hev) * 1e-3) / 1e9
+        e2e = {"value": round(whole_job_rate(e2e_ms, world), 2), "unit": "steps/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e2e_ms, 4),
+               "overlap": "%s copied on a second stream under the kernels before verify"
+                          % "+".join(late),
+               "pinned_h2d_gbs": round(h2d_gbs, 1),
+               "pinned_h2d_probe": "one %d-byte pinned host-to-device copy, best of 20" % big}
 
     if rank != 0:
         return None
@@ -643,30 +698,54 @@ def gpu_arm(args, rank, world):
         abytes["dynamic_tree_expand"] = sum(4 * r.numel() for r in d_rows)
     step_bytes = sum(abytes.values())
     dom = max(["tree_attn_fwd", verify_name], key=lambda n: kernel_us[n])
-    achieved = abytes[dom] / (kernel_us[dom] * 1e-6) / 1e9
     attn_flops = attention_flops(inp)
     tc_peak, tc_src = load_tensor_peak()
-    attn_tflops = attn_flops / (kernel_us["tree_attn_fwd"] * 1e-6) / 1e12
     # the attention's binding roof: HBM when its bytes take longer at peak
     # bandwidth than its FLOPs at peak tensor throughput, else the tensor pipe
-    tensor_bound = dom == "tree_attn_fwd" and (attn_flops / (tc_peak * 1e12)
-                                               > abytes[dom] / (peak * 1e9))
+    attn_tensor = attn_flops / (tc_peak * 1e12) > abytes["tree_attn_fwd"] / (peak * 1e9)
+    tensor_bound = dom == "tree_attn_fwd" and attn_tensor
+    t_dom = kernel_us[dom] * 1e-6
+    achieved = abytes[dom] / t_dom / 1e9
+    attn_tflops = attn_flops / (kernel_us["tree_attn_fwd"] * 1e-6) / 1e12
     kernels = {}
     for n in names:
-        entry = {"us": round(kernel_us[n], 3)}
+        entry = {"us": round(kernel_us[n], 3), "entry_us": round(entry_us[n], 3)}
         if n in abytes:
             gbs = abytes[n] / (kernel_us[n] * 1e-6) / 1e9 if kernel_us[n] > 0 else 0.0
             entry.update({"algorithmic_bytes": abytes[n], "gbs": round(gbs, 1),
                           "frac_of_hbm_peak": round(gbs / peak, 4)})
+        if n == "tree_attn_fwd":
+            entry.update({"algorithmic_flops": attn_flops, "tflops": round(attn_tflops, 1),
+                          "frac_of_tensor_peak": round(attn_tflops / tc_peak, 4),
+                          "bound": "tensor" if attn_tensor else "hbm",
+                          "launches": attn_launches,
+                          "plan": tsd.tree_attn_plan(B, N, Hq, Hkv, D, max_slots)})
         kernels[n] = entry
-    launches = launches_per_step * args.steps
+    launches = launches_per_step * steps
+    if tensor_bound:
+        roofline = {"bound": "tensor", "kernel": dom, "achieved": round(attn_tflops, 1),
+                    "peak": tc_peak, "unit": "TFLOP/s", "frac": round(attn_tflops / tc_peak, 4),
+                    "traffic": ncu_traffic(dom, name), "peak_source": tc_src,
+                    "algorithmic_flops_per_launch": attn_flops,
+                    "algorithmic_bytes_per_launch": abytes[dom],
+                    "hbm_frac": round(achieved / peak, 4)}
+    else:
+        roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+                    "unit": "GB/s", "frac": round(achieved / peak, 4),
+                    "traffic": ncu_traffic(dom, name), "peak_source": peak_src,
+                    "algorithmic_bytes_per_launch": abytes[dom],
+                    "algorithmic_flops_per_launch": attn_flops if dom == "tree_attn_fwd" else None,
+                    "tensor_frac": (round(attn_tflops / tc_peak, 4)
+                                    if dom == "tree_attn_fwd" else None)}
+    roofline["time_basis"] = ("kernel-only device time: CUDA events around graph replays of "
+                              "[L2 flush, entry point] minus [L2 flush] alone, %d reps" % reps)
     result = {
         "metric": METRIC,
         "value": round(whole_job_rate(ms_per_step, world), 2),
         "unit": "steps/s",
         "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
+        "steps": steps,
+        "warmup": warmup,
         "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True,
         "scaling": "weak",
@@ -674,53 +753,90 @@ def gpu_arm(args, rank, world):
         "dtype": "bf16 (attention, fp32 accumulate); f32 (%s); int32 (tree, paths)" % (
             "rejection sampling" if stochastic else "logits argmax"),
         "data": "synthetic (seeded; shapes and distributions of the named workload)",
-        "config": {"workload": desc, "name": args.workload, "verify": args.verify,
+        "config": {"workload": desc, "name": name, "verify": verify,
                    "global_batch": B * world,
                    "seq_len": max_slots, "parallelism": "replicas (dp%d)" % world,
                    "l2": "flushed between timed steps: 256 MiB write then 256 MiB read of another "
                          "buffer, outside the timed events (cold, clean L2)",
                    "timing": "CUDA events on the launching stream around CUDA-graph replays of "
-                             "the whole step (value) and of each entry point (kernels)",
-                   "attention_kernel": "tcgen05" if args.attn_kernel == "tc" else "mma.sync"},
+                             "the whole step (value) and of each entry point (kernels)"},
         "hbm_gbs_step": round(step_bytes / (ms_per_step * 1e-3) / 1e9, 1),
+        "step_kernel_us": round(step_kernel_us, 3),
         "kernels": kernels,
-        "roofline": ({"bound": "tensor", "kernel": dom, "achieved": round(attn_tflops, 1),
-                      "peak": tc_peak, "unit": "TFLOP/s", "frac": round(attn_tflops / tc_peak, 4),
-                      "traffic": ncu_traffic(dom, args.workload), "peak_source": tc_src,
-                      "algorithmic_flops_per_launch": attn_flops,
-                      "algorithmic_bytes_per_launch": abytes[dom],
-                      "hbm_frac": round(achieved / peak, 4)}
-                     if tensor_bound else
-                     {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
-                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                      "traffic": ncu_traffic(dom, args.workload), "peak_source": peak_src,
-                      "algorithmic_bytes_per_launch": abytes[dom],
-                      "algorithmic_flops_per_launch": attn_flops if dom == "tree_attn_fwd" else None,
-                      "tensor_frac": (round(attn_tflops / tc_peak, 4)
-                                      if dom == "tree_attn_fwd" else None)}),
+        "roofline": roofline,
         "attention_tflops": round(attn_tflops, 1),
-        "e2e": {"value": round(whole_job_rate(e2e_ms, world), 2), "unit": "steps/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_ms, 4),
-                "overlap": "%s copied on a second stream under the kernels before verify"
-                           % "+".join(late)},
         "gpu_launches": launches,
-        "clocks": clocks,
         "wall_s_timed_region": round(t_wall, 4),
         "kernel_sum_us": round(sum(kernel_us.values()), 3),
         "mean_accept_len": float(A.float().mean().item()),
-        "verify": (args.verify if not stochastic else
+        "verify": (verify if not stochastic else
                    {"mode": "stochastic", "internal_rows": internal_rows,
                     "rows_with_rejection": rejected_rows, "leaf_draws": leaf_draws,
                     "plan": tsd.tree_verify_stochastic_plan(B, N, V)}),
-        "commit_layer_stacked": {
+    }
+    if full:
+        result["e2e"] = e2e
+        result["clocks"] = clocks
+        result["commit_layer_stacked"] = {
             "layers": n_layers, "us": round(stacked_us, 3),
             "algorithmic_bytes": abytes["kv_commit_path"] * n_layers,
             "gbs": round(abytes["kv_commit_path"] * n_layers / (stacked_us * 1e-6) / 1e9, 1),
             "frac_of_hbm_peak": round(abytes["kv_commit_path"] * n_layers
-                                      / (stacked_us * 1e-6) / 1e9 / peak, 4)},
-    }
+                                      / (stacked_us * 1e-6) / 1e9 / peak, 4)}
     return result
+
+
+def config_summary(r):
+    """The compact per-configuration record carried beside the headline."""
+    a = r["kernels"]["tree_attn_fwd"]
+    return {"workload": r["config"]["workload"], "steps_per_s": r["value"],
+            "ms_per_step": r["ms_per_step"], "step_kernel_us": r["step_kernel_us"],
+            "kernels_us": {n: k["us"] for n, k in r["kernels"].items()},
+            "entry_us": {n: k["entry_us"] for n, k in r["kernels"].items()},
+            "attention": {"bound": a["bound"], "gbs": a["gbs"],
+                          "frac_of_hbm_peak": a["frac_of_hbm_peak"], "tflops": a["tflops"],
+                          "frac_of_tensor_peak": a["frac_of_tensor_peak"],
+                          "frac_of_binding_roof": (a["frac_of_tensor_peak"]
+                                                   if a["bound"] == "tensor"
+                                                   else a["frac_of_hbm_peak"]),
+                          "launches": a["launches"], "plan": a["plan"]},
+            "verify_frac_of_hbm_peak": r["kernels"]["tree_verify_greedy"]["frac_of_hbm_peak"]
+            if "tree_verify_greedy" in r["kernels"] else None,
+            "roofline": {k: r["roofline"][k] for k in ("bound", "kernel", "achieved", "unit",
+                                                       "frac")},
+            "steps": r["steps"], "mean_accept_len": r["mean_accept_len"]}
+
+
+def gpu_arm(args, rank, world):
+    import torch
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    flush = torch.empty((FLUSH_BYTES,), dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones((FLUSH_BYTES // 8,), dtype=torch.int64, device=dev)
+
+    def flush_l2():
+        # write one buffer larger than L2, then read another: the timed step
+        # starts with a cold L2 holding clean lines, so no write-back of the
+        # flush's dirty lines is charged to the kernels
+        flush.zero_()
+        flush_rd.sum()
+
+    res = measure_workload(args.workload, args, rank, world, dev, flush_l2, full=True,
+                           verify=args.verify)
+    if world == 1 and args.configs and args.verify == "greedy":
+        sub = argparse.Namespace(**vars(args))
+        sub.steps = max(3, min(args.steps, args.config_steps))
+        others = {}
+        for name in CONFIG_SET:
+            if name == args.workload:
+                continue
+            r = measure_workload(name, sub, rank, 1, dev, flush_l2, full=False)
+            others[name] = config_summary(r)
+            torch.cuda.empty_cache()
+        res["configs"] = others
+    return res
 
 
 def budget_arm(args, rank, world):
@@ -919,13 +1035,17 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="8b")
+    ap.add_argument("--workload", default="70b",
+                    help="headline workload (default: the long-context 70B-shaped layer, the "
+                         "largest configuration on one GPU)")
     ap.add_argument("--verify", default="greedy", choices=["greedy", "stochastic"],
                     help="a3: greedy (argmax) or stochastic (modified rejection sampling)")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--attn-kernel", default="tc", choices=["tc", "mma"],
-                    help="tree attention kernel: tcgen05 (default) or the mma.sync one")
+    ap.add_argument("--no-configs", dest="configs", action="store_false",
+                    help="skip the other configurations measured beside the headline")
+    ap.add_argument("--config-steps", type=int, default=2000,
+                    help="timed steps for each of the other configurations")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
 

@@ -96,8 +96,6 @@ const char *tsd_version(void);
  *                          and MMAs (bounded), frees its tensor memory and
  *                          returns; 0 makes every wait that is not already
  *                          satisfied run out.
- *   TSD_OPT_ATTN_KERNEL    0: tcgen05/TMA tree attention (default);
- *                          1: the mma.sync kernel kept for comparison.
  *   TSD_OPT_TEST_STALL     1: the tcgen05 attention's MMA thread first waits
  *                          on a barrier nothing ever signals, so that wait
  *                          runs out after TSD_OPT_WAIT_LIMIT_NS and the
@@ -105,9 +103,8 @@ const char *tsd_version(void);
  * Returns TSD_ERR_ARG for an unknown key or value.
  */
 #define TSD_OPT_WAIT_LIMIT_NS 0
-#define TSD_OPT_ATTN_KERNEL 1
-#define TSD_OPT_TEST_STALL 2
-#define TSD_OPT_COUNT 3
+#define TSD_OPT_TEST_STALL 1
+#define TSD_OPT_COUNT 2
 int tsd_set_option(int key, int64_t value);
 int64_t tsd_get_option(int key);
 
@@ -169,14 +166,29 @@ int tsd_tree_build_ancestors(const int32_t *parent, const int32_t *n_nodes, int 
  * lse         float [B][N_max][Hq] or NULL  out.  Skipped rows -inf.
  * workspace   device scratch of ws_bytes >= tsd_tree_attn_workspace_bytes()
  *             (split-KV partials and the split plan; no initial contents
- *             required).
+ *             required).  That size is 0, and workspace may be NULL, when
+ *             every key range is one piece (below).
  * status      int32 device word (see TSD_STATUS_*), may be NULL.
+ * Work split: the key range of each (sequence, kv head, block of 128 or 256
+ * query rows) is cut into pieces sized to fill the GPU; a second kernel
+ * merges the pieces of each row.  When every range is one piece the rows are
+ * written directly: one launch, no workspace.  Batches of 2..64 sequences
+ * whose blocks would walk long key ranges are split on the device from the
+ * actual lengths (three launches: plan, split, merge).
  */
 size_t tsd_tree_attn_workspace_bytes(int B, int N_max, int Hq, int Hkv, int D, int max_slots);
 /* Kernels one tsd_tree_attn_fwd call launches for these sizes on the current
- * device (2: split + merge; 3 with the device-side split plan); 0 for sizes
- * it rejects.  Host only. */
+ * device (1: one piece per key range; 2: split + merge; 3 with the device-side
+ * split plan); 0 for sizes it rejects.  Host only. */
 int tsd_tree_attn_launches(int B, int N_max, int Hq, int Hkv, int D, int max_slots);
+/* The launch shape tsd_tree_attn_fwd picks for these sizes on the current
+ * device (host only; for measurement and tests).  info: int32 [8] out:
+ * mode (1: uniform split, 2: device plan), two-blocks-per-SM kernel (0/1),
+ * query rows per block (128 or 256), row blocks per kv head, pieces per key
+ * range (mode 2: the uniform guess the plan refines), keys per piece, blocks
+ * in the grid, and 1 when rows go straight to the output (one piece, no
+ * merge kernel).  TSD_ERR_LIMIT / TSD_ERR_ARG as tsd_tree_attn_fwd. */
+int tsd_tree_attn_plan(int B, int N_max, int Hq, int Hkv, int D, int max_slots, int32_t *info);
 int tsd_tree_attn_fwd(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                       const int32_t *block_table, int max_blocks, int num_blocks,
                       const int32_t *prefix_len, const int32_t *n_nodes, const uint32_t *mask,
@@ -233,10 +245,14 @@ int tsd_tree_verify_greedy(const float *logits, const int32_t *tokens, const int
  * scratch (B tickets plus B * N_max 8-byte argmax keys) exceeds it return
  * TSD_ERR_LIMIT.  The call itself allocates nothing.
  * - The first call on a device looks up the array's device address (with
- *   that device current); make that first call before any stream capture.
+ *   that device current) and caches it with the id of the device's context;
+ *   a call after a device reset looks it up again.  Make the first call on a
+ *   device (and the first after a reset) before any stream capture.  Host
+ *   threads may call concurrently: the look-up is serialised.
  * - Every call zeroes the tickets and keys it uses on `stream` before its
  *   kernel runs.
- *   All calls share the one array: calls that overlap on the GPU race.
+ * - Each GPU has its own instance of the array.  All calls on one device
+ *   share it: calls that overlap on the same device (two streams) race.
  */
 size_t tsd_tree_verify_static_capacity(void);
 int tsd_tree_verify_greedy_static(const float *logits, const int32_t *tokens,

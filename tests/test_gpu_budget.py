@@ -70,9 +70,20 @@ def _fp32_margin(n_max):
     return 2.0 * (n_max + 2) * U32
 
 
+def _allowed_within(S, n, margin):
+    """Whether stopping at n is the rule's choice once comparisons within a
+    relative `margin` of a tie may go either way: no clear decrease up to n,
+    and no clear increase right after it."""
+    for k in range(2, n + 1):
+        if S[k - 1] < S[k - 2] * (1.0 - margin):
+            return False
+    return n == len(S) or S[n] < S[n - 1] * (1.0 + margin)
+
+
 def _check_choice(rho, cost, l_ar, n_gpu, s_gpu):
     """Exact n where every deciding comparison clears the fp32 margin; S at
-    the choice within the kernel's rounding.  Returns the rows checked."""
+    the choice within the kernel's rounding.  Near-ties: a choice the margin
+    allows.  Returns the rows checked exactly."""
     n_ref, s_ref = oracle.budget_select(rho, cost.astype(np.float64), l_ar)
     n_max = rho.shape[1]
     checked = 0
@@ -81,7 +92,9 @@ def _check_choice(rho, cost, l_ar, n_gpu, s_gpu):
         top = min(int(n_ref[b]) + 1, n_max)
         gaps = [abs(S[n - 1] - S[n - 2]) / S[n - 2] for n in range(2, top + 1) if S[n - 2] > 0]
         if gaps and min(gaps) <= _fp32_margin(n_max):
-            continue  # a near-tie: either side of it is a correct fp32 choice
+            # a near-tie: either side of it is a correct fp32 choice
+            assert _allowed_within(S, int(n_gpu[b]), _fp32_margin(n_max)), (b, int(n_gpu[b]))
+            continue
         assert int(n_gpu[b]) == int(n_ref[b]), (b, int(n_gpu[b]), int(n_ref[b]))
         bound = (int(n_ref[b]) + 2) * U32 * abs(s_ref[b])
         assert abs(float(s_gpu[b]) - s_ref[b]) <= bound, (b, float(s_gpu[b]), s_ref[b])
@@ -96,14 +109,17 @@ def test_select_on_best_first_scores(tsd, n_max):
     q, root = gen.bastion_marginals()
     parent, tokens, depth, rho, ahat = tsd.best_first_tree_build(dev_tensor(q), dev_tensor(root),
                                                                  n_max)
-    checked = 0
-    for seed in range(3):
-        cost = _cost(n_max, 7.0 * seed)
-        for l_ar in (5.0, 40.0, 400.0):
+    # the choice sits where S stops growing, so its deciding comparison is
+    # often close to a tie; many cost tables give enough rows clear of it
+    checked = total = 0
+    for seed in range(12):
+        cost = _cost(n_max, 5.0 * seed)
+        for l_ar in (5.0, 400.0):
             n_opt, s_opt = tsd.budget_select(rho, torch.from_numpy(cost).cuda(), l_ar)
             torch.cuda.synchronize()
             checked += _check_choice(to_np(rho), cost, l_ar, to_np(n_opt), to_np(s_opt))
-    assert checked >= 0.9 * 9 * q.shape[0], checked
+            total += q.shape[0]
+    assert checked >= 0.4 * total, (checked, total)
 
 
 def test_select_random_scores_and_edges(tsd):

@@ -37,6 +37,19 @@ def test_workload_full(tsd, name):
     assert o["accept_len"].min() >= 0
 
 
+@pytest.mark.parametrize("seed", [5, 8])
+def test_tiny_shape_with_accepted_moves(tsd, seed):
+    """The tiny workload's shapes with seeds whose trees accept two and four
+    draft tokens, so the commit moves entries (seed 0, the workload's own,
+    accepts none)."""
+    inp = gen.verify_workload("tiny", seed=seed)
+    g = run_gpu(tsd, inp)
+    o = run_oracle(inp)
+    compare(inp, g, o)
+    assert g["status"] == 0
+    assert o["accept_len"].min() >= 2 and o["moved"].min() >= 2
+
+
 def test_workload_70b_sampled(tsd):
     inp = gen.verify_workload("70b")
     rng = np.random.default_rng(0)
@@ -124,6 +137,33 @@ def test_long_context_many_splits(tsd):
     assert g["status"] == 0
 
 
+@pytest.mark.parametrize("case", ["70b-shaped", "kv2"])
+def test_single_sequence_long_context(tsd, case):
+    """One sequence with a long prefix and the host's uniform split: the 70B
+    shape with B = 1 (eight 128-row blocks per kv head), and on the 256-row
+    kernel a GQA group of 16 over 20 nodes (a 256-row block and a 64-row block
+    whose two softmax groups take alternate key tiles) with a 150k-key prefix
+    cut into 32 pieces."""
+    if case == "70b-shaped":
+        inp = gen.random_small(77, B=1, N_max=127, Hq=64, Hkv=8, D=128, V=300, prefix_lo=32768,
+                               prefix_hi=32768, max_depth=8, ragged_nodes=False)
+    else:
+        inp = gen.random_small(78, B=1, N_max=20, Hq=16, Hkv=1, D=128, V=300, prefix_lo=150000,
+                               prefix_hi=150000, max_depth=5, ragged_nodes=False)
+    max_slots = int((inp.prefix_len + inp.n_nodes).max())
+    plan = tsd.tree_attn_plan(1, inp.N_max, inp.Hq, inp.Hkv, inp.D, max_slots)
+    assert plan["mode"] == 1 and plan["splits"] > 1
+    if case == "kv2":
+        assert plan["rows_per_block"] == 256 and plan["two_blocks_per_sm"] == 0
+    rng = np.random.default_rng(5)
+    sample = sorted({(0, int(rng.integers(inp.N_max)), int(rng.integers(inp.Hq)))
+                     for _ in range(60)} | {(0, inp.N_max - 1, h) for h in range(inp.Hq)})
+    g = run_gpu(tsd, inp)
+    o = run_oracle(inp, sample_attention=sample)
+    compare(inp, g, o, sample=sample)
+    assert g["status"] == 0
+
+
 # Skewed prefix lengths: one long sequence among short ones (and an empty
 # prefix), so the device split plan cuts the long key ranges into many pieces
 # and the short ones into one or two.
@@ -188,16 +228,46 @@ def test_two_blocks_per_sm_path(tsd, D, N, Hq, Hkv):
 
 def test_attention_launch_count(tsd):
     """The launch count the library reports: split + merge, plus the plan
-    kernel for ragged-capable batches with long blocks."""
+    kernel for ragged-capable batches with long blocks, and a single launch
+    (no workspace) when every key range is one piece."""
     assert tsd.tree_attn_launches(1, 63, 32, 8, 128, 4159) == 2
     assert tsd.tree_attn_launches(16, 31, 32, 8, 128, 8078) == 3
     assert tsd.tree_attn_launches(70, 6, 4, 2, 64, 300) == 2
+    assert tsd.tree_attn_launches(40, 31, 32, 8, 128, 431) == 1
+    assert tsd.tree_attn_workspace_bytes(40, 31, 32, 8, 128, 431) == 0
     assert tsd.tree_attn_launches(1, 63, 32, 8, 96, 4159) == 0
+
+
+@pytest.mark.parametrize("case", ["128-row blocks", "256-row blocks"])
+def test_single_piece_key_ranges(tsd, case):
+    """Enough (sequence, kv head) units to fill the GPU with one piece per key
+    range: rows are normalised and written by the split kernel itself (no
+    merge launch, no workspace), on the two-blocks-per-SM kernel (40
+    sequences, short prefixes) and on the 256-row kernel (one sequence, 60
+    kv heads, a 4500-key prefix, 320 rows per kv head: a full 256-row block
+    and a 64-row block whose two softmax groups take alternate key tiles)."""
+    if case == "128-row blocks":
+        inp = gen.random_small(4040, B=40, N_max=31, Hq=32, Hkv=8, D=128, V=64, prefix_lo=100,
+                               prefix_hi=400, max_depth=5)
+    else:
+        inp = gen.random_small(4041, B=1, N_max=20, Hq=960, Hkv=60, D=128, V=64, prefix_lo=4500,
+                               prefix_hi=4500, max_depth=5, ragged_nodes=False)
+    max_slots = int((inp.prefix_len + inp.n_nodes).max())
+    plan = tsd.tree_attn_plan(inp.B, inp.N_max, inp.Hq, inp.Hkv, inp.D, max_slots)
+    assert plan["direct"] == 1 and plan["two_blocks_per_sm"] == (1 if case == "128-row blocks" else 0)
+    assert tsd.tree_attn_workspace_bytes(inp.B, inp.N_max, inp.Hq, inp.Hkv, inp.D, max_slots) == 0
+    rng = np.random.default_rng(9)
+    sample = sorted({(int(rng.integers(inp.B)), int(rng.integers(inp.N_max)), int(rng.integers(inp.Hq)))
+                     for _ in range(120)} | {(0, i, h) for i in range(inp.N_max) for h in (0, inp.Hq - 1)})
+    g = run_gpu(tsd, inp)
+    o = run_oracle(inp, sample_attention=sample)
+    compare(inp, g, o, sample=sample)
+    assert g["status"] == 0
 
 
 def test_large_batch_uniform_split(tsd):
     """More sequences than the device plan takes (B = 70): the host's
-    uniform split and its three-dimensional grid."""
+    uniform split, its three-dimensional grid and the in-cluster merge."""
     inp = gen.random_small(4711, B=70, N_max=6, Hq=4, Hkv=2, D=64, V=50, prefix_lo=0,
                            prefix_hi=300, max_depth=3)
     g = run_gpu(tsd, inp)

@@ -52,4 +52,6 @@ def test_options_are_validated():
         tsd.set_option(99, 1)
     with pytest.raises(tsd.TsdError):
         tsd.set_option(tsd.OPT_WAIT_LIMIT_NS, -5)
-    assert tsd.get_option(tsd.OPT_ATTN_KERNEL) in (0, 1)
+    assert tsd.get_option(tsd.OPT_TEST_STALL) == 0
+    with pytest.raises(tsd.TsdError):
+        tsd.set_option(tsd.OPT_TEST_STALL, 2)

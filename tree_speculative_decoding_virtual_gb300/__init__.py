@@ -26,7 +26,7 @@ _ERR_NAMES = {TSD_ERR_ARG: "TSD_ERR_ARG", TSD_ERR_LIMIT: "TSD_ERR_LIMIT",
 
 TREE_RANGE, TREE_CYCLE, TREE_TOO_DEEP, TREE_CLOSURE, TREE_ROOT, TREE_COUNT = 1, 2, 4, 8, 16, 32
 STATUS_BAD_PAGE, STATUS_BAD_LEN, STATUS_BAD_PATH, STATUS_TIMEOUT = 1, 2, 4, 8
-OPT_WAIT_LIMIT_NS, OPT_ATTN_KERNEL, OPT_TEST_STALL = 0, 1, 2
+OPT_WAIT_LIMIT_NS, OPT_TEST_STALL = 0, 1
 
 # C signatures: (name, restype, argtypes)
 _P, _I, _I64, _SZ, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
@@ -38,6 +38,7 @@ SIGNATURES = {
     "tsd_tree_build_ancestors": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "tsd_tree_attn_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "tsd_tree_attn_launches": (_I, [_I, _I, _I, _I, _I, _I]),
+    "tsd_tree_attn_plan": (_I, [_I, _I, _I, _I, _I, _I, _P]),
     "tsd_tree_attn_fwd": (_I, [_P, _P, _P, _P, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F,
                                _P, _P, _P, _SZ, _P, _P]),
     "tsd_tree_verify_workspace_bytes": (_SZ, [_I, _I, _I]),
@@ -148,6 +149,15 @@ def tree_attn_launches(B, N_max, Hq, Hkv, D, max_slots) -> int:
     return int(lib.tsd_tree_attn_launches(B, N_max, Hq, Hkv, D, max_slots))
 
 
+def tree_attn_plan(B, N_max, Hq, Hkv, D, max_slots) -> dict:
+    """The launch shape tree_attn_fwd picks for these sizes on this device."""
+    info = (ctypes.c_int32 * 8)()
+    _check(lib.tsd_tree_attn_plan(B, N_max, Hq, Hkv, D, max_slots, info), "tree_attn_plan")
+    keys = ["mode", "two_blocks_per_sm", "rows_per_block", "row_blocks", "splits", "keys_per_split",
+            "grid_blocks", "direct"]
+    return dict(zip(keys, [int(x) for x in info]))
+
+
 def tree_attn_fwd(q, k_cache, v_cache, block_table, prefix_len, n_nodes, mask, err, max_slots,
                   scale=None, out=None, lse=None, want_lse=True, workspace=None, status=None,
                   stream=None):
@@ -163,8 +173,9 @@ def tree_attn_fwd(q, k_cache, v_cache, block_table, prefix_len, n_nodes, mask, e
     if lse is None and want_lse:
         lse = _empty((B, N_max, Hq), torch.float32, q)
     need = tree_attn_workspace_bytes(B, N_max, Hq, Hkv, D, max_slots)
-    if workspace is None:
-        workspace = _empty((max(need, 1),), torch.uint8, q)
+    if workspace is None and need > 0:
+        workspace = _empty((need,), torch.uint8, q)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = lib.tsd_tree_attn_fwd(
         _ptr(q, torch.bfloat16, "q"), _ptr(k_cache, torch.bfloat16, "k_cache"),
         _ptr(v_cache, torch.bfloat16, "v_cache"), _ptr(block_table, torch.int32, "block_table"),
@@ -172,7 +183,7 @@ def tree_attn_fwd(q, k_cache, v_cache, block_table, prefix_len, n_nodes, mask, e
         _ptr(n_nodes, torch.int32, "n_nodes"), _ptr(mask, torch.int32, "mask"),
         _ptr(err, torch.int32, "err"), B, N_max, Hq, Hkv, D, int(max_slots), float(scale),
         _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"),
-        _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+        _ptr(workspace, None, "workspace"), ws_bytes,
         _ptr(status, torch.int32, "status"), _stream(stream))
     _check(rc, "tree_attn_fwd")
     return out, lse
@@ -474,7 +485,7 @@ def budget_select(rho, cost, l_ar, n_opt=None, s_opt=None, stream=None):
 
 
 def set_option(key: int, value: int) -> None:
-    """Process-wide library option (OPT_WAIT_LIMIT_NS, OPT_ATTN_KERNEL, OPT_TEST_STALL)."""
+    """Process-wide library option (OPT_WAIT_LIMIT_NS, OPT_TEST_STALL)."""
     _check(lib.tsd_set_option(key, value), "set_option")
 
 

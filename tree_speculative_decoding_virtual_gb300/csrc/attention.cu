@@ -11,15 +11,13 @@
 // Layout of the work.  For one (sequence b, kv head) the query rows are the
 // tree nodes times the q heads of that kv group, packed node-major
 // (row = node * g + head-in-group), so the GQA group shares every K/V tile.
-// A block owns 64 such rows and one split of the key range (split-KV, sized
-// to fill the GPU); keys are read straight from the paged cache with 16-byte
-// cp.async (double-buffered, XOR-swizzled rows).  Q K^T and P V run on the
-// tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate) with an online
-// softmax in registers.  Tiles that lie wholly inside the committed prefix
-// are visible to every row and skip masking; tiles that reach the tree tail
-// read each row's ancestor bitmask word by word.  Each split writes fp32
-// partials (O, running max, running sum); a combine kernel merges them,
-// normalises and rounds to bf16.
+// A block owns 128 or 256 such rows and one split of the key range (split-KV,
+// sized to fill the GPU).  K/V tiles come straight from the paged cache by
+// TMA; Q K^T and P V run on the tensor cores (tcgen05.mma, bf16 in, fp32
+// accumulate in tensor memory) with an online softmax between them.  Tiles
+// that lie wholly inside the committed prefix are visible to every row and
+// skip masking; tiles that reach the tree tail apply each row's ancestor
+// bitmask.  The splits of one key range are merged into the bf16 output.
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -35,9 +33,6 @@
 namespace tsd {
 namespace {
 
-constexpr int kBM = 64;  // query rows per block
-constexpr int kBN = 64;  // keys per tile
-constexpr int kAttnThreads = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct AttnParams {
@@ -53,7 +48,7 @@ struct AttnParams {
   int N_max, Hq, Hkv, g, W, max_slots;
   float scale_log2;
   int chunk, splits, row_tiles, rows_pad;  // the host's uniform split of the key range
-  // plan_mode 0/1: the uniform split; partials [B*Hkv][splits][rows_pad].
+  // plan_mode 1: the uniform split; partials [B*Hkv][splits][rows_pad].
   // plan_mode 2: the split is planned on the device from the actual lengths
   // (tree_attn_plan_kernel); the grid is one block per work item (grid_items
   // of them) and item k's partials are rows [k * kTcRows, (k + 1) * kTcRows).
@@ -68,42 +63,9 @@ struct AttnParams {
   int32_t *status;
   uint64_t wait_limit_ns;
   int test_stall;  // wait on a barrier nothing signals (exercises the timeout path)
-  int swizzled;    // partial rows hold 16-byte chunk k at position k ^ (row % (D/8))
+  int direct;      // 1: one split per key range; rows go straight to the output
 };
 
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool pred) {
-  const int n = pred ? 16 : 0;
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3,
-                                        uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3,
-                                          uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void mma_bf16(float *c, const uint32_t *a, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&h);
@@ -121,12 +83,6 @@ __device__ __forceinline__ float pow2_above(float amax) {
   return __uint_as_float((uint32_t)(min(max(e, -126), 127) + 127) << 23);
 }
 
-// byte offset of 16-byte chunk `ch` of row `row` in a swizzled [rows][D] bf16 tile
-template <int D>
-__device__ __forceinline__ uint32_t swz(int row, int ch) {
-  return (uint32_t)((row * (D / 8) + (ch ^ (row & 7))) * 16);
-}
-
 // Sequence-level validity shared by the split and combine kernels.
 __device__ __forceinline__ bool seq_ok(const AttnParams &p, int b, int &P, int &nb) {
   P = p.prefix_len[b];
@@ -136,255 +92,6 @@ __device__ __forceinline__ bool seq_ok(const AttnParams &p, int b, int &P, int &
   if (P < 0 || (long)P + nb > (long)p.max_slots || (long)P + nb > (long)p.max_blocks * kPage)
     return false;
   return true;
-}
-
-template <int D>
-__global__ void __launch_bounds__(kAttnThreads)
-tree_attn_split_kernel(const AttnParams p) {
-  constexpr int kCh = D / 8;    // 16-byte chunks per row
-  constexpr int kKT = D / 16;   // k-steps of Q K^T
-  constexpr int kDT = D / 8;    // n-tiles of P V
-  extern __shared__ __align__(128) unsigned char smem[];
-  unsigned char *sQ = smem;
-  unsigned char *sK = smem + kBM * D * 2;
-  unsigned char *sV = sK + 2 * kBN * D * 2;
-
-  pdl_trigger();
-  pdl_wait();
-  const int rt = blockIdx.x;
-  const int split = blockIdx.y;
-  const int z = blockIdx.z;
-  const int b = z / p.Hkv;
-  const int hkv = z % p.Hkv;
-  const int tid = threadIdx.x;
-  const int lane = tid & 31;
-  const int warp = tid >> 5;
-
-  int P, nb;
-  const bool ok = seq_ok(p, b, P, nb);
-  if (!ok) {
-    if (rt == 0 && split == 0 && hkv == 0 && tid == 0 && p.status) {
-      const int e = p.err ? p.err[b] : 0;
-      const int nbb = p.n_nodes ? p.n_nodes[b] : p.N_max;
-      if (e == 0 && nbb >= 1 && nbb <= p.N_max) atomicOr(p.status, TSD_STATUS_BAD_LEN);
-    }
-    return;
-  }
-  const int rows_valid = nb * p.g;
-  if (rt * kBM >= rows_valid) return;
-  const int seq_len = P + nb;
-  const int k_begin = split * p.chunk;
-  if (k_begin >= seq_len) return;
-  const int k_end = min(seq_len, k_begin + p.chunk);
-  const int ntiles = (k_end - k_begin + kBN - 1) / kBN;
-  const int32_t *trow = p.table + (size_t)b * p.max_blocks;
-
-  // ---- Q tile (rows rt*64 .. +63), zero-filled past the valid rows ----
-  for (int c = tid; c < kBM * kCh; c += kAttnThreads) {
-    const int r = c / kCh, ch = c % kCh;
-    const int row = rt * kBM + r;
-    const bool valid = row < rows_valid;
-    const int node = valid ? row / p.g : 0;
-    const int head = hkv * p.g + (valid ? row % p.g : 0);
-    const uint16_t *src = p.q + (((size_t)b * p.N_max + node) * p.Hq + head) * D + ch * 8;
-    cp_async16(smem_u32(sQ) + swz<D>(r, ch), src, valid);
-  }
-
-  bool bad_page = false;
-  auto load_tile = [&](int stage, int ts) {
-    for (int c = tid; c < kBN * kCh; c += kAttnThreads) {
-      const int r = c / kCh, ch = c % kCh;
-      const int slot = ts + r;
-      bool valid = slot < k_end;
-      int page = 0;
-      if (valid) {
-        page = __ldg(trow + slot / kPage);
-        if (page < 0 || page >= p.num_blocks) {
-          bad_page = true;
-          valid = false;
-          page = 0;
-        }
-      }
-      const size_t off = (((size_t)page * p.Hkv + hkv) * kPage + slot % kPage) * D + ch * 8;
-      cp_async16(smem_u32(sK + stage * kBN * D * 2) + swz<D>(r, ch), p.k + off, valid);
-      cp_async16(smem_u32(sV + stage * kBN * D * 2) + swz<D>(r, ch), p.v + off, valid);
-    }
-  };
-
-  load_tile(0, k_begin);
-  cp_async_commit();
-
-  // per-thread rows: ra (accumulator regs 0,1) and rb (regs 2,3)
-  const int ra_local = warp * 16 + (lane >> 2);
-  const int ra = rt * kBM + ra_local;
-  const int rb = ra + 8;
-  const int node_a = ra < rows_valid ? ra / p.g : -1;
-  const int node_b = rb < rows_valid ? rb / p.g : -1;
-  const uint32_t *mask_a = p.mask + ((size_t)b * p.N_max + (node_a < 0 ? 0 : node_a)) * p.W;
-  const uint32_t *mask_b = p.mask + ((size_t)b * p.N_max + (node_b < 0 ? 0 : node_b)) * p.W;
-
-  uint32_t qf[kKT][4];
-  float o[kDT][4];
-#pragma unroll
-  for (int i = 0; i < kDT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float m_run[2] = {-INFINITY, -INFINITY};
-  float l_run[2] = {0.f, 0.f};
-
-  for (int it = 0; it < ntiles; ++it) {
-    const int ts = k_begin + it * kBN;
-    if (it + 1 < ntiles) {
-      load_tile((it + 1) & 1, ts + kBN);
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-    if (it == 0) {
-#pragma unroll
-      for (int kk = 0; kk < kKT; ++kk)
-        ldsm_x4(qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3],
-                smem_u32(sQ) + swz<D>(warp * 16 + (lane & 15), kk * 2 + (lane >> 4)));
-    }
-    const uint32_t kbase = smem_u32(sK + (it & 1) * kBN * D * 2);
-    const uint32_t vbase = smem_u32(sV + (it & 1) * kBN * D * 2);
-
-    // S = Q K^T for this warp's 16 rows x 64 keys
-    float s[8][4];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < kKT; ++kk) {
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(b0, b1, b2, b3,
-                kbase + swz<D>(np * 16 + (lane & 7) + ((lane >> 4) << 3),
-                               kk * 2 + ((lane >> 3) & 1)));
-        mma_bf16(s[2 * np], qf[kk], b0, b1);
-        mma_bf16(s[2 * np + 1], qf[kk], b2, b3);
-      }
-    }
-
-    // scale, mask, online softmax
-    const bool full = (ts + kBN <= P) && (ts + kBN <= k_end);
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float x = s[nt][e] * p.scale_log2;
-        if (!full) {
-          const int slot = ts + nt * 8 + 2 * (lane & 3) + (e & 1);
-          bool vis = slot < k_end;
-          if (vis && slot >= P) {
-            const int j = slot - P;
-            const int node = (e < 2) ? node_a : node_b;
-            const uint32_t *mrow = (e < 2) ? mask_a : mask_b;
-            vis = node >= 0 && ((__ldg(mrow + (j >> 5)) >> (j & 31)) & 1u);
-          }
-          if (!vis) x = -INFINITY;
-        }
-        s[nt][e] = x;
-      }
-    }
-    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      mx[0] = fmaxf(mx[0], fmaxf(s[nt][0], s[nt][1]));
-      mx[1] = fmaxf(mx[1], fmaxf(s[nt][2], s[nt][3]));
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
-      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-    }
-    float alpha[2], muse[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const float mnew = fmaxf(m_run[h], mx[h]);
-      muse[h] = mnew == -INFINITY ? 0.f : mnew;
-      alpha[h] = exp2f(m_run[h] - muse[h]);
-      m_run[h] = mnew;
-    }
-    float rs[2] = {0.f, 0.f};
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      s[nt][0] = exp2f(s[nt][0] - muse[0]);
-      s[nt][1] = exp2f(s[nt][1] - muse[0]);
-      s[nt][2] = exp2f(s[nt][2] - muse[1]);
-      s[nt][3] = exp2f(s[nt][3] - muse[1]);
-      rs[0] += s[nt][0] + s[nt][1];
-      rs[1] += s[nt][2] + s[nt][3];
-    }
-    l_run[0] = l_run[0] * alpha[0] + rs[0];
-    l_run[1] = l_run[1] * alpha[1] + rs[1];
-#pragma unroll
-    for (int dt = 0; dt < kDT; ++dt) {
-      o[dt][0] *= alpha[0];
-      o[dt][1] *= alpha[0];
-      o[dt][2] *= alpha[1];
-      o[dt][3] *= alpha[1];
-    }
-
-    // O += P V
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      uint32_t a[4];
-      a[0] = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
-      a[1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
-      a[2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-      a[3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-#pragma unroll
-      for (int dp = 0; dp < kDT / 2; ++dp) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(b0, b1, b2, b3,
-                  vbase + swz<D>(kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3),
-                                 2 * dp + (lane >> 4)));
-        mma_bf16(o[2 * dp], a, b0, b1);
-        mma_bf16(o[2 * dp + 1], a, b2, b3);
-      }
-    }
-    __syncthreads();  // this stage is refilled by the next iteration's prefetch
-  }
-
-  if (bad_page && p.status) atomicOr(p.status, TSD_STATUS_BAD_PAGE);
-
-  // ---- write the split's partials ----
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
-    l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
-  }
-  const size_t base = ((size_t)z * p.splits + split) * p.rows_pad + rt * kBM;
-  uint16_t *po = p.part_o + base * D;
-  const int ca = 2 * (lane & 3);
-  float inv_a = l_run[0] > 0.f ? 1.f / l_run[0] : 0.f;
-  float inv_b = l_run[1] > 0.f ? 1.f / l_run[1] : 0.f;
-  float amax_a = 0.f, amax_b = 0.f;
-#pragma unroll
-  for (int dt = 0; dt < kDT; ++dt) {
-    amax_a = fmaxf(amax_a, fmaxf(fabsf(o[dt][0]), fabsf(o[dt][1])));
-    amax_b = fmaxf(amax_b, fmaxf(fabsf(o[dt][2]), fabsf(o[dt][3])));
-  }
-#pragma unroll
-  for (int off = 1; off <= 2; off <<= 1) {  // the four threads holding a row
-    amax_a = fmaxf(amax_a, __shfl_xor_sync(0xffffffffu, amax_a, off));
-    amax_b = fmaxf(amax_b, __shfl_xor_sync(0xffffffffu, amax_b, off));
-  }
-  const float c_a = pow2_above(amax_a * inv_a), c_b = pow2_above(amax_b * inv_b);
-  inv_a /= c_a;
-  inv_b /= c_b;
-#pragma unroll
-  for (int dt = 0; dt < kDT; ++dt) {
-    *reinterpret_cast<uint32_t *>(po + (size_t)ra_local * D + dt * 8 + ca) =
-        pack_f16(o[dt][0] * inv_a, o[dt][1] * inv_a);
-    *reinterpret_cast<uint32_t *>(po + (size_t)(ra_local + 8) * D + dt * 8 + ca) =
-        pack_f16(o[dt][2] * inv_b, o[dt][3] * inv_b);
-  }
-  if ((lane & 3) == 0) {
-    p.part_ml[base + ra_local] = make_float4(m_run[0], l_run[0], c_a, 0.f);
-    p.part_ml[base + ra_local + 8] = make_float4(m_run[1], l_run[1], c_b, 0.f);
-  }
 }
 
 
@@ -413,11 +120,12 @@ tree_attn_split_kernel(const AttnParams p) {
 // S_tj complete, every earlier MMA of the row tile has completed too: O may
 // be rescaled and S_tj overwritten by P_tj with no further wait.  P is taken
 // against a reference max m per row, raised lazily: the tile's max is
-// computed only while the row has no reference yet or when P would sum above
-// 2^64 (a score more than 64 above m), and then O and the row sums are
-// rescaled (in TMEM) only if that max exceeds m by more than 2^8.  Every sum
-// stays far from fp32 overflow and P keeps its relative precision, so the
-// result is the same softmax.  A tile's row is handled in two 64-key halves;
+// computed only while the row has no reference yet or when its P would sum
+// above 2^64 (a score more than 57 above m), and only then are m moved and O
+// and the row sums rescaled (in TMEM).  Each row decides this on its own
+// scores alone, so a row's result does not depend on the other rows of its
+// warp.  Every sum stays far from fp32 overflow and P keeps its relative
+// precision, so the result is the same softmax.  A tile's row is handled in two 64-key halves;
 // if the second half raises m, the first half's P (already in TMEM) is
 // rescaled too.  (The tile max is ALU work that the MMA-issuing warp, which
 // shares an SM sub-partition with a softmax warp of each group, would wait
@@ -713,6 +421,56 @@ __device__ __forceinline__ void attn_prefetch(const AttnParams &p, int b, int hk
   }
 }
 
+// ---- uniform split of one piece per key range: rows straight to the output ----
+// Output row of block row `row` (within the kv head's rows) of sequence b.
+__device__ __forceinline__ size_t out_row(const AttnParams &p, int b, int hkv, int row) {
+  return ((size_t)b * p.N_max + row / p.g) * p.Hq + hkv * p.g + row % p.g;
+}
+
+// Zeros and lse -inf for rows [row0, row0 + nrows) that are past the
+// sequence's valid rows (all of them for a skipped sequence).
+template <int D>
+__device__ void write_invalid_rows(const AttnParams &p, int b, int hkv, int row0, int nrows,
+                                   bool seq_valid, int rows_valid, int tid, int nthreads) {
+  const int rows_all = p.N_max * p.g;
+  for (int r = tid; r < nrows; r += nthreads) {
+    const int row = row0 + r;
+    if (row >= rows_all) break;
+    if (seq_valid && row < rows_valid) continue;
+    const size_t o = out_row(p, b, hkv, row);
+    uint4 *dst = reinterpret_cast<uint4 *>(p.out + o * D);
+#pragma unroll
+    for (int k = 0; k < D / 8; ++k) dst[k] = make_uint4(0u, 0u, 0u, 0u);
+    if (p.lse) p.lse[o] = -INFINITY;
+  }
+}
+
+// One row normalised straight from tensor memory: O / l_sum in bf16, lse from
+// the fp32 sum (tO: the thread's TMEM lane of O).  Called by whole warps (the
+// TMEM loads are warp-collective); only threads whose row is valid store.
+template <int D>
+__device__ __forceinline__ void write_row_direct(const AttnParams &p, size_t orow, bool valid,
+                                                 uint32_t tO, float m, float l_sum, float l_ex) {
+  using namespace sm100;
+  const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+  uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * D);
+#pragma unroll 1
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t o[32];
+    tmem_ld32(tO + c * 32, o);
+    tmem_wait_ld();
+    if (valid) {
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8) {
+        const float *f = reinterpret_cast<const float *>(&o[q8 * 8]);
+        dst[c * 4 + q8] = make_uint4(pack_bf16(f[0] * inv, f[1] * inv), pack_bf16(f[2] * inv, f[3] * inv),
+                                     pack_bf16(f[4] * inv, f[5] * inv), pack_bf16(f[6] * inv, f[7] * inv));
+      }
+    }
+  }
+  if (valid && p.lse) p.lse[orow] = l_ex > 0.f ? (m + log2f(l_ex)) * 0.6931471805599453f : -INFINITY;
+}
+
 // One loader thread: TMA loads of K (or V) tiles 0..ntiles-1 into a ring,
 // waiting for a stage to be released before refilling it, then a drain so no
 // copy is in flight when the block exits.
@@ -895,6 +653,7 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
     k_end = min(P + nb, k_begin + p.chunk);
     item_row0 = ((size_t)zg * p.splits + split) * p.rows_pad + (size_t)rt * p.rpb;
   }
+  const bool seq_valid = run;
   const int rows_valid = nb * p.g;
   const int seq_len = P + nb;
   run = run && rt * p.rpb < rows_valid && k_begin < seq_len;
@@ -941,8 +700,6 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
     // phase ahead of the one wanted (the order bounds it), so parities are
     // unambiguous.
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(kTcBM, kTcBN, false, false);
-      constexpr uint32_t idPV = idesc_bf16_f32(kTcBM, D, false, true);
       auto issue_s = [&](int t, int j) {  // K_j has landed; S_t is free
         tc_issue_s<D>(tmem, base, kv2 ? 0 : t, t, j % kTcStages, smem_addr(&sh.s_full[t]));
       };
@@ -1127,13 +884,17 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
                 if (!((vis >> i) & 1u)) r[c2][i] = __float_as_uint(-INFINITY);
             }
           }
-          // Once every row of the warp has a reference max (m_use finite), P is
-          // taken against it with no max pass; a tile sum above 2^64 (a score
-          // more than 64 above the reference, or a non-finite one) sends the warp
-          // back through the exact path, which takes the max, moves the
-          // reference under the lazy rule and rescales.  P stays within 2^64 of
-          // the reference either way, far from fp32 overflow in every sum.
-          bool exact = !__all_sync(0xffffffffu, m_use != -INFINITY);
+          // P is taken against the row's reference max with no max pass.  The
+          // exact path takes the tile max and moves the reference (rescaling O
+          // and the first half's P) for the rows that need it: a row with no
+          // visible key yet, or one whose tile sums above 2^64 (a score more
+          // than 57 above the reference, or a non-finite one).  Rows that need
+          // nothing keep their reference and recompute the same P, so a row's
+          // result depends on its own scores only.  Every P stays below 2^64
+          // and a tile's sum below 2^71, far from fp32 overflow.
+          const bool none = m_use == -INFINITY;
+          bool exact = __all_sync(0xffffffffu, none), trig = false;
+          const bool mixed = !exact && __any_sync(0xffffffffu, none);
           uint32_t pk[2][16];  // P as bf16 pairs: column i holds keys 2i, 2i+1 of a chunk
           unsigned long long esum2;
           float ra[2], rc[2];  // rounded P: even / odd keys
@@ -1153,11 +914,11 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
               const float mt = fmaxf(fmax3(mx[0], mx[1], mx[2]),
                                      fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7])) * sc;
               const float m_new = fmaxf(m_use, mt);
-              const bool upd = m_new > m_use + 8.f;  // first visible key, or the max grew by > 2^8
+              const bool upd = none ? m_new > -INFINITY : trig;
               const float alpha = upd ? exp2f(m_use - m_new) : 1.f;
               if (__any_sync(0xffffffffu, upd) && (u > 0 || h > 0)) {
                 const float s0 = rescale(alpha, u > 0, h > 0);
-                if (h > 0) lt = s0;  // the first half's P as rounded again
+                if (h > 0 && upd) lt = s0;  // the first half's P as rounded again
               }
               if (upd) {
                 l_sum *= alpha;
@@ -1188,7 +949,8 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
             }
             if (exact) break;
             const float2 e = f2_unpack(esum2);
-            exact = __any_sync(0xffffffffu, !(e.x + e.y <= 0x1p64f));
+            trig = !none && !(e.x + e.y <= 0x1p64f);
+            exact = mixed || __any_sync(0xffffffffu, trig);
             if (!exact) break;
           }
 #pragma unroll
@@ -1240,7 +1002,13 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
       }
       tmem_wait_st();
     }
-    if (all_ok) {
+    if (p.direct) {  // one piece per key range: the row straight to the output
+      if (all_ok) {
+        tc_fence_after();
+        const int wrow = rt * p.rpb + tr * kTcBM + rl;
+        write_row_direct<D>(p, out_row(p, b, hkv, wrow), wrow < rows_valid, tO, m_use, l_sum, l_ex);
+      }
+    } else if (all_ok) {
       tc_fence_after();
       float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
       float amax = 0.f;  // pass 1: the row's largest |O|
@@ -1277,10 +1045,12 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
       p.part_ml[prow] = make_float4(m_use, l_ex, cs, 0.f);
       fence_proxy_async_smem();
     }
-    if (writer) asm volatile("bar.sync 1, %0;\n" ::"r"(nwr) : "memory");
-    if (all_ok && warp == 2 && lane == 0) {
-      bulk_store(p.part_o + item_row0 * D, base + L::kStaging, (uint32_t)(nwr * D * 2));
-      bulk_wait_read();
+    if (!p.direct) {
+      if (writer) asm volatile("bar.sync 1, %0;\n" ::"r"(nwr) : "memory");
+      if (all_ok && warp == 2 && lane == 0) {
+        bulk_store(p.part_o + item_row0 * D, base + L::kStaging, (uint32_t)(nwr * D * 2));
+        bulk_wait_read();
+      }
     }
   }
 
@@ -1292,6 +1062,8 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  if (p.direct)
+    write_invalid_rows<D>(p, b, hkv, rt * p.rpb, p.rpb, seq_valid, rows_valid, tid, kTcThreads);
 }
 
 // ===========================================================================
@@ -1310,7 +1082,7 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
 // S_1, P_0 V_0, S_2, P_1 V_1, S_3, ...: S_{j+2} reuses the buffer P_j V_j
 // reads (the tensor pipe runs in issue order), and while the softmax works on
 // S_j the tensor core computes S_{j+1} and P_{j-1} V_{j-1}.  So a P V may still
-// be running when the next tile's softmax raises the reference max; the
+// be running when the next tile's softmax raises a row's reference max; the
 // rescale of O that the lazy rule then needs first waits for it (pv_done).
 // Partials, waits, time-outs and teardown are as in tree_attn_split_tc.
 // ===========================================================================
@@ -1507,6 +1279,7 @@ tree_attn_split_dual(const AttnParams p, const __grid_constant__ CUtensorMap map
     k_end = min(P + nb, k_begin + p.chunk);
     item_row0 = ((size_t)zg * p.splits + split) * p.rows_pad + (size_t)rt * p.rpb;
   }
+  const bool seq_valid = run;
   const int rows_valid = nb * p.g;
   run = run && rt * p.rpb < rows_valid && k_begin < P + nb;
   const int ntiles = (k_end - k_begin + kDualBN - 1) / kDualBN;
@@ -1630,10 +1403,11 @@ tree_attn_split_dual(const AttnParams p, const __grid_constant__ CUtensorMap map
             if (!((vis >> i) & 1u)) r[c2][i] = __float_as_uint(-INFINITY);
         }
       }
-      // P against the reference max once every row of the warp has one; the
-      // exact path (max, lazy rule, rescale) otherwise or when a tile sum
-      // exceeds 2^64, as in tree_attn_split_tc
-      bool exact = !__all_sync(0xffffffffu, m_use != -INFINITY), failed = false;
+      // P against the reference max, with the exact path (max, reference
+      // moved, rescale) for rows that need it, as in tree_attn_split_tc
+      const bool none = m_use == -INFINITY;
+      bool exact = __all_sync(0xffffffffu, none), failed = false, trig = false;
+      const bool mixed = !exact && __any_sync(0xffffffffu, none);
       uint32_t pk[2][16];  // P as bf16 pairs: column i holds keys 2i, 2i+1 of a chunk
       unsigned long long esum2;
       float ra[2], rc[2];  // rounded P: even / odd keys
@@ -1652,7 +1426,9 @@ tree_attn_split_dual(const AttnParams p, const __grid_constant__ CUtensorMap map
           const float mt = fmaxf(fmax3(mx[0], mx[1], mx[2]),
                                  fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7])) * sc;
           const float m_new = fmaxf(m_use, mt);
-          const bool upd = m_new > m_use + 8.f;  // first visible key, or the max grew by > 2^8
+          // a row moves its reference only for its own first visible key or
+          // its own tile sum above 2^64, never because a neighbour did
+          const bool upd = none ? m_new > -INFINITY : trig;
           const float alpha = upd ? exp2f(m_use - m_new) : 1.f;
           if (__any_sync(0xffffffffu, upd) && j > 0) {
             // O holds P V of tiles before j - 1; the one of tile j - 1 may still run
@@ -1697,7 +1473,8 @@ tree_attn_split_dual(const AttnParams p, const __grid_constant__ CUtensorMap map
         }
         if (exact) break;
         const float2 e = f2_unpack(esum2);
-        exact = __any_sync(0xffffffffu, !(e.x + e.y <= 0x1p64f));
+        trig = !none && !(e.x + e.y <= 0x1p64f);
+        exact = mixed || __any_sync(0xffffffffu, trig);
         if (!exact) break;
       }
       if (failed) {
@@ -1719,7 +1496,12 @@ tree_attn_split_dual(const AttnParams p, const __grid_constant__ CUtensorMap map
     // ---- epilogue: O / (l c) in fp16 through shared memory, (m, l, c) per row ----
     asm volatile("bar.sync 1, 128;\n" ::: "memory");
     const bool all_ok = __all_sync(0xffffffffu, ok && !*abort);
-    if (all_ok) {
+    if (p.direct) {  // one piece per key range: the row straight to the output
+      if (all_ok) {
+        tc_fence_after();
+        write_row_direct<D>(p, out_row(p, b, hkv, row), rvalid, tO, m_use, l_sum, l_ex);
+      }
+    } else if (all_ok) {
       tc_fence_after();
       float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
       float amax = 0.f;
@@ -1753,10 +1535,12 @@ tree_attn_split_dual(const AttnParams p, const __grid_constant__ CUtensorMap map
       p.part_ml[item_row0 + rl] = make_float4(m_use, l_ex, cs, 0.f);
       fence_proxy_async_smem();
     }
-    asm volatile("bar.sync 1, 128;\n" ::: "memory");
-    if (all_ok && warp == 2 && lane == 0) {
-      bulk_store(p.part_o + item_row0 * D, base + L::kStaging, (uint32_t)(kTcBM * D * 2));
-      bulk_wait_read();
+    if (!p.direct) {
+      asm volatile("bar.sync 1, 128;\n" ::: "memory");
+      if (all_ok && warp == 2 && lane == 0) {
+        bulk_store(p.part_o + item_row0 * D, base + L::kStaging, (uint32_t)(kTcBM * D * 2));
+        bulk_wait_read();
+      }
     }
   }
 
@@ -1768,6 +1552,8 @@ tree_attn_split_dual(const AttnParams p, const __grid_constant__ CUtensorMap map
     tc_fence_after();
     tmem_dealloc(tmem, kDualTmemCols);
   }
+  if (p.direct)
+    write_invalid_rows<D>(p, b, hkv, rt * p.rpb, kTcBM, seq_valid, rows_valid, tid, kDualThreads);
 }
 
 // One warp per output row (b, node, q head): merge the splits.  Lane s reads
@@ -1819,7 +1605,7 @@ __global__ void __launch_bounds__(256) tree_attn_combine_kernel(const AttnParams
   }
   // partial rows sit at multiples of 16 apart, so every split's copy of this
   // row has the same swizzle phase
-  const int pc = p.swizzled ? (c ^ (int)(r0 & (kChunks - 1))) : c;
+  const int pc = c ^ (int)(r0 & (kChunks - 1));
   const float4 ml = lane < ns ? __ldcg(&p.part_ml[r0 + (size_t)lane * stride])
                               : make_float4(-INFINITY, 0.f, 0.f, 0.f);
   // partials in batches of R rounds; every load of a batch is issued before
@@ -1892,29 +1678,27 @@ cudaError_t launch_combine(const AttnParams &p, int B, cudaStream_t s) {
 }
 
 struct AttnPlan {
-  int impl;  // 0 tcgen05, 1 mma.sync
-  int bm, bn, row_tiles, rows_pad, splits, chunk;
-  int mode;          // plan_mode (AttnParams)
+  int bm, row_tiles, rows_pad, splits, chunk;
+  int mode;          // plan_mode (AttnParams): 1 uniform split, 2 device plan
   bool dual;         // tree_attn_split_dual (two blocks per SM) instead of tree_attn_split_tc
+  bool direct;       // uniform split of one piece: rows go straight to the output
   long grid_items;   // mode 2: blocks of the 1-D grid
   size_t o_bytes, ml_bytes, plan_bytes;
 };
 
 AttnPlan plan_attn(int B, int N_max, int Hq, int Hkv, int D, int max_slots) {
   AttnPlan a;
-  a.impl = (int)option(TSD_OPT_ATTN_KERNEL);
-  a.bn = a.impl == 0 ? kTcBN : kBN;
   const int g = Hq / Hkv;
   const long nsm = sm_count();
-  const long max_tiles = (max_slots + a.bn - 1) / a.bn;
-  // the uniform split for blocks of bm rows: one resident block per SM,
+  const long max_tiles = (max_slots + kTcBN - 1) / kTcBN;
+  // the uniform split for blocks of bm rows: `slots` block slots at once,
   // estimated time = waves x (tiles per block + a fixed cost of about four
   // 128-key tiles for the prologue and partials)
   auto split_for = [&](int bm, long slots, long &per) {
     const long units = (long)B * Hkv * ((N_max * g + bm - 1) / bm);
     long best_s = 1;
     double best_t = 1e30;
-    for (long s = 1; s <= max_tiles && s <= 32; ++s) {
+    for (long s = 1; s <= max_tiles && s <= kMaxSplits; ++s) {
       const long waves = (units * s + slots - 1) / slots;
       const long pr = (max_tiles + s - 1) / s;
       const double t = (double)waves * (double)(pr + 4);
@@ -1926,53 +1710,41 @@ AttnPlan plan_attn(int B, int N_max, int Hq, int Hkv, int D, int max_slots) {
     }
     return best_s;
   };
-  long best_s = 1;
-  if (a.impl == 0) {
-    // 128-row blocks (the two-blocks-per-SM kernel; the blocks of one kv
-    // head's row tiles run side by side, so L2 serves their shared K/V) unless
-    // 256-row blocks would each walk 32 or more key tiles: such long,
-    // tensor-bound blocks gain from two row tiles sharing every K/V tile
-    // (measured: the 70B shape, 128 rows 0.4% slower; 8B, budgeted and
-    // dynamic-tree layers 2-7% faster with 128 rows).
-    long per = 0;
-    a.bm = kTcRows;
+  // 128-row blocks (the two-blocks-per-SM kernel; the blocks of one kv
+  // head's row tiles run side by side, so L2 serves their shared K/V) unless
+  // 256-row blocks would each walk 32 or more key tiles: such long,
+  // tensor-bound blocks gain from two row tiles sharing every K/V tile
+  // (measured: the 70B shape, 128 rows 0.4% slower; 8B, budgeted and
+  // dynamic-tree layers 2-7% faster with 128 rows).
+  long per = 0;
+  a.bm = kTcRows;
+  long best_s = split_for(a.bm, nsm, per);
+  if (per <= kSmallBlockTiles && N_max * g > kTcBM) {
+    a.bm = kTcBM;
     best_s = split_for(a.bm, nsm, per);
-    if (per <= kSmallBlockTiles && N_max * g > kTcBM) {
-      a.bm = kTcBM;
-      best_s = split_for(a.bm, nsm, per);
-    }
-    // Blocks that all hold one 128-row tile run the two-blocks-per-SM kernel:
-    // two block slots per SM.
-    if (a.bm == kTcBM || N_max * g <= kTcBM) best_s = split_for(a.bm, 2 * nsm, per);
-  } else {
-    a.bm = kBM;
-    const long units = (long)B * Hkv * ((N_max * g + a.bm - 1) / a.bm);
-    const long target = 2L * nsm;
-    best_s = (target + units - 1) / units;
-    if (best_s > max_tiles) best_s = max_tiles;
-    if (best_s < 1) best_s = 1;
   }
+  // Blocks that all hold one 128-row tile run the two-blocks-per-SM kernel:
+  // two block slots per SM.
+  a.dual = a.bm == kTcBM || N_max * g <= kTcBM;
+  if (a.dual) best_s = split_for(a.bm, 2 * nsm, per);
   a.row_tiles = (N_max * g + a.bm - 1) / a.bm;
   a.rows_pad = a.row_tiles * a.bm;
   const long units = (long)B * Hkv * a.row_tiles;
   long chunk = (max_slots + best_s - 1) / best_s;
-  chunk = (chunk + a.bn - 1) / a.bn * a.bn;
-  if (a.impl == 0 && chunk > (long)kTcMaxPages * kPage) chunk = (long)kTcMaxPages * kPage;
-  if (a.impl == 0 && chunk > 64L * kTcBN) chunk = 64L * kTcBN;  // at most 64 tiles per block
-  while ((max_slots + chunk - 1) / chunk > 32) chunk += a.bn;
+  chunk = (chunk + kTcBN - 1) / kTcBN * kTcBN;
+  if (chunk > (long)kTcMaxPages * kPage) chunk = (long)kTcMaxPages * kPage;
+  if (chunk > 64L * kTcBN) chunk = 64L * kTcBN;  // at most 64 tiles per block
+  while ((max_slots + chunk - 1) / chunk > kMaxSplits) chunk += kTcBN;
   a.chunk = (int)chunk;
   a.splits = (int)((max_slots + chunk - 1) / chunk);
   if (a.splits < 1) a.splits = 1;
   const long items_u = units * a.splits;  // work items of the uniform split
   // The device plan pays off only when lengths may differ (B > 1) and a
   // uniform block would walk many tiles; it costs one small kernel.
-  a.mode = a.impl == 1 ? 0
-                       : (B > 1 && B <= kPlanMaxSeq && (a.chunk / a.bn) >= kPlanMinTiles ? 2 : 1);
+  a.mode = B > 1 && B <= kPlanMaxSeq && (a.chunk / kTcBN) >= kPlanMinTiles ? 2 : 1;
+  a.direct = a.mode == 1 && a.splits == 1;
   a.grid_items = items_u;
-  // Planned launches whose blocks all hold one 128-row tile run two blocks
-  // per SM (the plan then counts two block slots per SM).
-  a.dual = a.impl == 0 && (a.bm == kTcBM || N_max * g <= kTcBM);
-  size_t rows = (size_t)B * Hkv * a.splits * a.rows_pad;
+  size_t rows = a.direct ? 0 : (size_t)B * Hkv * a.splits * a.rows_pad;
   if (a.mode == 2) {
     // room for four waves of shorter pieces per block slot (at least the
     // uniform split's blocks); blocks beyond the plan's items exit at once
@@ -2019,40 +1791,26 @@ template <int D>
 int launch_attn(AttnParams &p, const AttnPlan &a, int B, int num_blocks, cudaStream_t s) {
   const dim3 grid = a.mode == 2 ? dim3((unsigned)a.grid_items)
                                 : dim3(p.row_tiles, p.splits, B * p.Hkv);
-  if (a.impl == 0) {
-    CUtensorMap k1, k8, v1, v8;
-    if (!make_cache_map(&k1, p.k, num_blocks, p.Hkv, D, 1) ||
-        !make_cache_map(&k8, p.k, num_blocks, p.Hkv, D, kTcPagesPerTile) ||
-        !make_cache_map(&v1, p.v, num_blocks, p.Hkv, D, 1) ||
-        !make_cache_map(&v8, p.v, num_blocks, p.Hkv, D, kTcPagesPerTile))
-      return TSD_ERR_CUDA;
-    if (a.mode == 2 && launch(tree_attn_plan_kernel, dim3(1), dim3(kTcThreads), 0, s, p) != cudaSuccess)
-      return TSD_ERR_CUDA;
-    if (a.dual) {
-      CUtensorMap k4, v4;
-      if (!make_cache_map(&k4, p.k, num_blocks, p.Hkv, D, kDualPagesPerTile) ||
-          !make_cache_map(&v4, p.v, num_blocks, p.Hkv, D, kDualPagesPerTile))
-        return TSD_ERR_CUDA;
-      if (!set_smem((const void *)tree_attn_split_dual<D>, DualLayout<D>::kAlloc)) return TSD_ERR_CUDA;
-      if (launch(tree_attn_split_dual<D>, grid, dim3(kDualThreads), DualLayout<D>::kAlloc, s, p, k1,
-                 k4, v1, v4) != cudaSuccess)
-        return TSD_ERR_CUDA;
-      if (cudaGetLastError() != cudaSuccess) return TSD_ERR_CUDA;
-      if (launch_combine<D>(p, B, s) != cudaSuccess) return TSD_ERR_CUDA;
-      return TSD_OK;
-    }
-    if (!set_smem((const void *)tree_attn_split_tc<D>, TcLayout<D>::kAlloc)) return TSD_ERR_CUDA;
-    if (launch(tree_attn_split_tc<D>, grid, dim3(kTcThreads), TcLayout<D>::kAlloc, s, p, k1, k8, v1,
-               v8) != cudaSuccess)
-      return TSD_ERR_CUDA;
+  const int pages = a.dual ? kDualPagesPerTile : kTcPagesPerTile;
+  CUtensorMap k1, kn, v1, vn;
+  if (!make_cache_map(&k1, p.k, num_blocks, p.Hkv, D, 1) ||
+      !make_cache_map(&kn, p.k, num_blocks, p.Hkv, D, pages) ||
+      !make_cache_map(&v1, p.v, num_blocks, p.Hkv, D, 1) ||
+      !make_cache_map(&vn, p.v, num_blocks, p.Hkv, D, pages))
+    return TSD_ERR_CUDA;
+  if (a.mode == 2 && launch(tree_attn_plan_kernel, dim3(1), dim3(kTcThreads), 0, s, p) != cudaSuccess)
+    return TSD_ERR_CUDA;
+  cudaError_t e;
+  if (a.dual) {
+    if (!set_smem((const void *)tree_attn_split_dual<D>, DualLayout<D>::kAlloc)) return TSD_ERR_CUDA;
+    e = launch(tree_attn_split_dual<D>, grid, dim3(kDualThreads), DualLayout<D>::kAlloc, s, p, k1, kn,
+               v1, vn);
   } else {
-    const size_t smem = (size_t)(kBM + 4 * kBN) * D * 2;
-    if (!set_smem((const void *)tree_attn_split_kernel<D>, smem)) return TSD_ERR_CUDA;
-    if (launch(tree_attn_split_kernel<D>, grid, dim3(kAttnThreads), smem, s, p) != cudaSuccess)
-      return TSD_ERR_CUDA;
+    if (!set_smem((const void *)tree_attn_split_tc<D>, TcLayout<D>::kAlloc)) return TSD_ERR_CUDA;
+    e = launch(tree_attn_split_tc<D>, grid, dim3(kTcThreads), TcLayout<D>::kAlloc, s, p, k1, kn, v1, vn);
   }
-  if (cudaGetLastError() != cudaSuccess) return TSD_ERR_CUDA;
-  if (launch_combine<D>(p, B, s) != cudaSuccess) return TSD_ERR_CUDA;
+  if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return TSD_ERR_CUDA;
+  if (!a.direct && launch_combine<D>(p, B, s) != cudaSuccess) return TSD_ERR_CUDA;
   return TSD_OK;
 }
 
@@ -2079,7 +1837,25 @@ TSD_API size_t tsd_tree_attn_workspace_bytes(int B, int N_max, int Hq, int Hkv, 
 TSD_API int tsd_tree_attn_launches(int B, int N_max, int Hq, int Hkv, int D, int max_slots) {
   if (attn_check_dims(B, N_max, Hq, Hkv, D, max_slots) != TSD_OK || B == 0) return 0;
   const tsd::AttnPlan a = tsd::plan_attn(B, N_max, Hq, Hkv, D, max_slots);
-  return a.mode == 2 ? 3 : 2;
+  return a.mode == 2 ? 3 : a.direct ? 1 : 2;
+}
+
+TSD_API int tsd_tree_attn_plan(int B, int N_max, int Hq, int Hkv, int D, int max_slots,
+                               int32_t *info) {
+  if (!info) return TSD_ERR_ARG;
+  const int dims = attn_check_dims(B, N_max, Hq, Hkv, D, max_slots);
+  if (dims != TSD_OK) return dims;
+  if (B == 0) return TSD_ERR_ARG;
+  const tsd::AttnPlan a = tsd::plan_attn(B, N_max, Hq, Hkv, D, max_slots);
+  info[0] = a.mode;
+  info[1] = a.dual ? 1 : 0;
+  info[2] = a.bm;
+  info[3] = a.row_tiles;
+  info[4] = a.splits;
+  info[5] = a.chunk;
+  info[6] = (int32_t)(a.mode == 2 ? a.grid_items : (long)a.row_tiles * a.splits * B * Hkv);
+  info[7] = a.direct ? 1 : 0;
+  return TSD_OK;
 }
 
 TSD_API int tsd_tree_attn_fwd(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
@@ -2101,7 +1877,8 @@ TSD_API int tsd_tree_attn_fwd(const uint16_t *q, const uint16_t *k_cache, const 
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
     return TSD_ERR_ARG;
   const AttnPlan a = plan_attn(B, N_max, Hq, Hkv, D, max_slots);
-  if (!workspace || ws_bytes < a.o_bytes + a.ml_bytes + a.plan_bytes || !aligned(workspace, 16))
+  const size_t need = a.o_bytes + a.ml_bytes + a.plan_bytes;
+  if (need > 0 && (!workspace || ws_bytes < need || !aligned(workspace, 16)))
     return TSD_ERR_WORKSPACE;
   AttnParams p;
   p.q = q;
@@ -2141,7 +1918,7 @@ TSD_API int tsd_tree_attn_fwd(const uint16_t *q, const uint16_t *k_cache, const 
   p.status = status;
   p.wait_limit_ns = (uint64_t)option(TSD_OPT_WAIT_LIMIT_NS);
   p.test_stall = (int)option(TSD_OPT_TEST_STALL);
-  p.swizzled = a.impl == 0 ? 1 : 0;
+  p.direct = a.direct ? 1 : 0;
   return D == 128 ? launch_attn<128>(p, a, B, num_blocks, as_cuda(stream))
                   : launch_attn<64>(p, a, B, num_blocks, as_cuda(stream));
 }

@@ -19,7 +19,6 @@ int sm_count() {
 
 static int64_t g_options[TSD_OPT_COUNT] = {
     2000000000LL,  // TSD_OPT_WAIT_LIMIT_NS: 2 s
-    0,             // TSD_OPT_ATTN_KERNEL: tcgen05
     0,             // TSD_OPT_TEST_STALL: off
 };
 
@@ -50,7 +49,6 @@ TSD_API const char *tsd_version(void) { return "tsd 0.2 (sm_103a)"; }
 TSD_API int tsd_set_option(int key, int64_t value) {
   if (key < 0 || key >= TSD_OPT_COUNT) return TSD_ERR_ARG;
   if (key == TSD_OPT_WAIT_LIMIT_NS && value < 0) return TSD_ERR_ARG;
-  if (key == TSD_OPT_ATTN_KERNEL && (value < 0 || value > 1)) return TSD_ERR_ARG;
   if (key == TSD_OPT_TEST_STALL && (value < 0 || value > 1)) return TSD_ERR_ARG;
   tsd::g_options[key] = value;
   return TSD_OK;

@@ -18,8 +18,11 @@
 // bitmasks and writes leaf / accept_len / path / bonus; it also resets the
 // ticket, so the workspace is zero again when the launch ends.
 
+#include <cuda.h>
+
 #include <climits>
 #include <cmath>
+#include <mutex>
 
 #include "sm100_ptx.cuh"
 #include "tsd_common.cuh"
@@ -368,34 +371,70 @@ TSD_API int tsd_tree_verify_greedy(const float *logits, const int32_t *tokens,
 // device) is not acceptable.  This entry point keeps its scratch (the
 // per-sequence tickets and the per-row argmax keys) in a fixed array
 // in device global memory, loaded with the library: every GPU that loads
-// libtsd.so holds kStaticScratchBytes of it until the process exits.
+// libtsd.so holds its own kStaticScratchBytes instance until the process
+// exits.
 //
 // In host code `g_verify_scratch` names a host-side shadow, not device
-// memory, so its device address is looked up once per device with
-// cudaGetSymbolAddress (with that device current) and cached.  The first
-// call on a device performs that look-up, so make it before any stream
-// capture.  All calls share the one array: each call zeroes the tickets and
-// row keys it uses on its stream before its kernel runs, and calls that
-// overlap on the GPU (two streams, or two devices' contexts racing on one
-// array) race on it.
+// memory, so its device address is looked up with cudaGetSymbolAddress (with
+// the device current) and cached per device, together with the id of the
+// CUDA context it belongs to: after a device reset the context, and with it
+// the address, changes, and the next call looks it up again.  The look-up is
+// serialised by a mutex, so host threads may make their first calls at
+// once.  The first call on a device (and the first after a reset) performs
+// that look-up, so make it before any stream capture.  All calls on one
+// device share its array: each call zeroes the tickets and row keys it uses
+// on its stream before its kernel runs, and calls that overlap on the same
+// device (two streams) race on it.
 // ---------------------------------------------------------------------------
 
 namespace tsd {
 namespace {
 
-constexpr size_t kStaticScratchBytes = 1u << 20;  // 1 MiB
+constexpr size_t kStaticScratchBytes = 1u << 20;  // 1 MiB per device
 __device__ __align__(256) unsigned char g_verify_scratch[kStaticScratchBytes];
 
+// Id of the calling thread's current CUDA context (0 when it cannot be read).
+unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext *);
+  using GetId = CUresult (*)(CUcontext, unsigned long long *);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void *f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(f);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
 void *static_scratch_ptr() {
-  static void *ptrs[64] = {nullptr};
+  struct Entry {
+    unsigned long long ctx;
+    void *ptr;
+  };
+  static std::mutex mu;
+  static Entry cache[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (!ptrs[dev]) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_verify_scratch) != cudaSuccess) return nullptr;
-    ptrs[dev] = p;
-  }
-  return ptrs[dev];
+  std::lock_guard<std::mutex> lock(mu);
+  const unsigned long long ctx = current_context_id();  // 0 before the context exists
+  if (cache[dev].ptr && ctx != 0 && cache[dev].ctx == ctx) return cache[dev].ptr;
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_verify_scratch) != cudaSuccess) return nullptr;
+  cache[dev] = Entry{current_context_id(), p};  // the look-up made the context current
+  return p;
 }
 
 }  // namespace
