@@ -188,6 +188,51 @@ def paged_cache(rng: np.random.Generator, prefix_len: np.ndarray, n_nodes: np.nd
     return PagedCache(k=k, v=v, block_table=table, num_blocks=num_blocks, max_blocks=max_blocks)
 
 
+def grow_cache(rng: np.random.Generator, cache: PagedCache, prefix_len: np.ndarray,
+               n_nodes: np.ndarray, extra: int) -> PagedCache:
+    """A copy of `cache` whose block table also covers `extra` more slots per
+    sequence, past slot P_b + N_b: fresh blocks appended to the pool (N(0,1)
+    bf16, in shuffled order), the existing blocks and table entries kept."""
+    B = len(prefix_len)
+    have = [(int(prefix_len[b]) + int(n_nodes[b]) + PAGE - 1) // PAGE for b in range(B)]
+    need = [(int(prefix_len[b]) + int(n_nodes[b]) + extra + PAGE - 1) // PAGE for b in range(B)]
+    add = [need[b] - have[b] for b in range(B)]
+    num_blocks = cache.num_blocks + sum(add)
+    fresh = (cache.num_blocks + rng.permutation(sum(add))).astype(np.int32)
+    table = np.zeros((B, max(max(need), cache.max_blocks)), dtype=np.int32)
+    table[:, :cache.block_table.shape[1]] = cache.block_table
+    pos = 0
+    for b in range(B):
+        table[b, have[b]:need[b]] = fresh[pos:pos + add[b]]
+        pos += add[b]
+    hkv, d = cache.k.shape[1], cache.k.shape[3]
+    k = np.concatenate([cache.k, normal_bf16(rng, (sum(add), hkv, PAGE, d))])
+    v = np.concatenate([cache.v, normal_bf16(rng, (sum(add), hkv, PAGE, d))])
+    return PagedCache(k=k, v=v, block_table=table, num_blocks=num_blocks,
+                      max_blocks=table.shape[1])
+
+
+def next_step_tree(rng: np.random.Generator, B: int, N_max: int, Hq: int, Hkv: int, D: int,
+                   max_depth: int):
+    """The next verify step's draft trees for a two-step scenario: node counts,
+    parent arrays (random trees, arbitrary id order), queries, and the K/V rows
+    of every node ([B][N_max][Hkv][D] bf16 bits each; the caller writes them
+    wherever its commit left room)."""
+    n_nodes = rng.integers(1, N_max, size=B, endpoint=True).astype(np.int32)
+    parent = np.zeros((B, N_max), dtype=np.int32)
+    for b in range(B):
+        nb = int(n_nodes[b])
+        p = random_tree(rng, nb, max_depth)
+        if nb > 2:
+            p = relabel(rng, p)
+        parent[b, :nb] = p
+        parent[b, nb:] = -1
+    q = normal_bf16(rng, (B, N_max, Hq, D))
+    k_rows = normal_bf16(rng, (B, N_max, Hkv, D))
+    v_rows = normal_bf16(rng, (B, N_max, Hkv, D))
+    return n_nodes, parent, q, k_rows, v_rows
+
+
 # --------------------------------------------------------------------------
 # workloads
 # --------------------------------------------------------------------------

@@ -33,9 +33,9 @@ trees); none is "parity unpinned".
 
 from .tree import (ERR_RANGE, ERR_CYCLE, ERR_TOO_DEEP, ERR_CLOSURE, ERR_ROOT, ERR_COUNT,
                    build_ancestors, ancestor_chain)
-from .attention import bf16_to_f64, tree_attention, gather_sequence_kv
+from .attention import bf16_to_f64, tree_attention, gather_sequence_kv, physical_slots
 from .verify import verify_greedy
-from .commit import commit_path
+from .commit import commit_path, commit_remap
 from .best_first import best_first_tree, ranked_tokens
 from .rejection import modified_rejection_step, residual_distribution
 from .budget import verify_step_cost, calibrate, speedup_curve, budget_select, cost_table
@@ -46,7 +46,8 @@ from .dynamic_tree import (dynamic_tree, expand_level, new_pool, pool_base, pool
 __all__ = [
     "ERR_RANGE", "ERR_CYCLE", "ERR_TOO_DEEP", "ERR_CLOSURE", "ERR_ROOT", "ERR_COUNT",
     "build_ancestors", "ancestor_chain", "bf16_to_f64", "tree_attention", "gather_sequence_kv",
-    "verify_greedy", "commit_path", "best_first_tree", "ranked_tokens",
+    "verify_greedy", "commit_path", "commit_remap", "physical_slots", "best_first_tree",
+    "ranked_tokens",
     "modified_rejection_step", "residual_distribution",
     "verify_step_cost", "calibrate", "speedup_curve", "budget_select", "cost_table",
     "node_decision", "tree_verify_stochastic", "tree_verify_stochastic_all",

@@ -23,6 +23,12 @@ Readings taken where the pages are silent:
 The cache is paged: K, V are [num_blocks][Hkv][16][D] bf16 (as uint16 bits),
 token slot t of sequence b lives in block block_table[b][t // 16], row t % 16.
 All arithmetic is fp64 on the exact bf16 values.
+
+Reading through a deferred commit (tree_attention_remapped): logical slot
+s of the committed sequence is physical slot remap_src[b][s - remap_base[b]]
+for s in [remap_base[b], remap_base[b] + remap_len[b]), else slot s; the tree's
+node j is at physical slot tail_base[b] + j.  The keys a node sees, and their
+order, are those of the sequence the copy commit would have produced.
 """
 
 from __future__ import annotations
@@ -54,13 +60,25 @@ def gather_sequence_kv(cache: np.ndarray, block_table: np.ndarray, b: int, hkv: 
     return bf16_to_f64(np.concatenate(rows, axis=0))
 
 
+def gather_slots_kv(cache: np.ndarray, block_table: np.ndarray, b: int, hkv: int,
+                    slots) -> np.ndarray:
+    """fp64 [len(slots)][D] rows of one kv head of one sequence, at the given
+    physical slots, in that order."""
+    rows = [cache[int(block_table[b, s // PAGE]), hkv, s % PAGE, :] for s in slots]
+    if not rows:
+        return np.zeros((0, cache.shape[-1]), dtype=np.float64)
+    return bf16_to_f64(np.stack(rows, axis=0))
+
+
 def tree_attention(q, k_cache, v_cache, block_table, prefix_len, n_nodes, parent, err,
-                   scale: float, sample=None):
+                   scale: float, sample=None, remap=None):
     """Reference tree attention.
 
     q: uint16 [B][N_max][Hq][D]; k_cache, v_cache: uint16 [num_blocks][Hkv][16][D].
     parent: int [B][N_max]; err: int [B] (sequences with err != 0 are skipped).
     sample: optional iterable of (b, i, h) to compute; others stay 0 / -inf.
+    remap: optional (remap_src, remap_base, remap_len, tail_base) of a deferred
+    commit (see the module notes).
     Returns out fp64 [B][N_max][Hq][D], lse fp64 [B][N_max][Hq].
     """
     q = np.asarray(q)
@@ -93,8 +111,13 @@ def tree_attention(q, k_cache, v_cache, block_table, prefix_len, n_nodes, parent
             heads = [hkv * g + x for x in range(g)]
             if wanted is not None and not any(h in heads for (_, h) in wanted[b]):
                 continue
-            K = gather_sequence_kv(k_cache, block_table, b, hkv, P + nb)
-            V = gather_sequence_kv(v_cache, block_table, b, hkv, P + nb)
+            if remap is None:
+                K = gather_sequence_kv(k_cache, block_table, b, hkv, P + nb)
+                V = gather_sequence_kv(v_cache, block_table, b, hkv, P + nb)
+            else:
+                slots = physical_slots(remap, b, P, nb)
+                K = gather_slots_kv(k_cache, block_table, b, hkv, slots)
+                V = gather_slots_kv(v_cache, block_table, b, hkv, slots)
             for h in heads:
                 if wanted is not None:
                     nodes = sorted(i for (i, hh) in wanted[b] if hh == h and i < nb)
@@ -113,6 +136,20 @@ def tree_attention(q, k_cache, v_cache, block_table, prefix_len, n_nodes, parent
                 out[b, nodes, h, :] = (w @ V) / l
                 lse[b, nodes, h] = (m + np.log(l))[:, 0]
     return out, lse
+
+
+def physical_slots(remap, b: int, P: int, nb: int):
+    """Physical slot of every logical key of sequence b, in logical order: the
+    committed prefix [0, P) through the deferred commit's record, then the
+    tree's nb nodes from tail_base."""
+    remap_src, remap_base, remap_len, tail_base = remap
+    rb, rl = int(remap_base[b]), int(remap_len[b])
+    out = []
+    for s in range(P):
+        out.append(int(remap_src[b, s - rb]) if rb <= s < rb + rl else s)
+    T = int(tail_base[b])
+    out.extend(T + j for j in range(nb))
+    return out
 
 
 def tree_attention_all(q, k_cache, v_cache, block_table, prefix_len, n_nodes, parent, d_max,
