@@ -197,6 +197,31 @@ int tsd_tree_attn_fwd(const uint16_t *q, const uint16_t *k_cache, const uint16_t
                       int32_t *status, tsd_stream_t stream);
 
 /*
+ * a2 through a deferred commit (see tsd_kv_commit_remap): the same attention
+ * over the committed sequence of length P_b = prefix_len[b] and the tree,
+ * where
+ *   - logical slot s in [remap_base[b], remap_base[b] + remap_len[b]) is read
+ *     from physical slot remap_src[b * remap_stride + s - remap_base[b]];
+ *   - the tree's node j is read from physical slot tail_base[b] + j;
+ *   - every other slot is read where it is.
+ * Keys are visited in logical order, so the result is bit for bit the one
+ * tsd_tree_attn_fwd gives after the copy commit moved the same entries.
+ * remap_src/remap_base/remap_len: all NULL (no record) or all given, with
+ * 1 <= remap_stride <= 33 and each record inside [0, P_b) (else the sequence
+ * is skipped with TSD_STATUS_BAD_LEN); tail_base NULL: the tree at P_b.
+ * Recorded slots and the tree are fetched slot by slot, the rest of the key
+ * range with the usual block loads.  Other arguments as tsd_tree_attn_fwd.
+ */
+int tsd_tree_attn_fwd_remap(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                            const int32_t *block_table, int max_blocks, int num_blocks,
+                            const int32_t *prefix_len, const int32_t *n_nodes,
+                            const uint32_t *mask, const int32_t *err, int B, int N_max, int Hq,
+                            int Hkv, int D, int max_slots, float scale, const int32_t *remap_src,
+                            int remap_stride, const int32_t *remap_base, const int32_t *remap_len,
+                            const int32_t *tail_base, uint16_t *out, float *lse, void *workspace,
+                            size_t ws_bytes, int32_t *status, tsd_stream_t stream);
+
+/*
  * a3. Greedy verification ([Blog] Medusa: the target evaluates every branch
  *     in one parallel pass and the longest valid path is selected; [EP-zh]
  *     lay summary section 3).
@@ -354,6 +379,52 @@ int tsd_kv_commit_path(uint16_t *k_cache, uint16_t *v_cache, int num_layers, int
                        const int32_t *path, const int32_t *err, int B, int N_max, int Hkv, int D,
                        int D_max, int32_t *new_len, int32_t *moved, int32_t *status,
                        tsd_stream_t stream);
+
+/*
+ * a4 from a tree at its own base: as tsd_kv_commit_path, but real node i's
+ * K/V are at slot tail_base[b] + i (REQUIRED, int32 [B]); slot P_b + k
+ * receives the entry of slot tail_base[b] + path[b][k] - 1, the root too
+ * when the two bases differ.  This materialises a deferred commit's record
+ * (tail_base = the recorded tree's base).  tail_base[b] + n_nodes[b] must lie
+ * inside the sequence's table (else TSD_STATUS_BAD_LEN).
+ */
+int tsd_kv_commit_path_from(uint16_t *k_cache, uint16_t *v_cache, int num_layers,
+                            int64_t layer_stride, const int32_t *block_table, int max_blocks,
+                            int num_blocks, const int32_t *prefix_len, const int32_t *n_nodes,
+                            const int32_t *accept_len, const int32_t *path, const int32_t *err,
+                            const int32_t *tail_base, int B, int N_max, int Hkv, int D, int D_max,
+                            int32_t *new_len, int32_t *moved, int32_t *status,
+                            tsd_stream_t stream);
+
+/*
+ * Deferred commit ([EP-zh] 2.1: the fast reorder moves only the accepted
+ * segment, only when needed; its conclusion names commit efficiency as
+ * future work).  Nothing moves: the call records where each committed entry
+ * already is, and the next step's tsd_tree_attn_fwd_remap reads the committed
+ * sequence through the record, with the next tree placed after the current
+ * one so that no recorded entry is overwritten.  A later
+ * tsd_kv_commit_path_from with the same path and tree base moves the
+ * entries into place.
+ *
+ * prefix_len, n_nodes (or NULL), accept_len, path, err (or NULL): as
+ * tsd_kv_commit_path; tail_base int32 [B] or NULL: where this step's tree
+ * sits (NULL: at P_b).  Outputs, int32:
+ *   remap_src  [B][D_max+1]  tail_base + path[k] - 1 for k <= accept_len,
+ *                            -1 beyond (the physical slot of logical P_b + k)
+ *   remap_base [B] = P_b;  remap_len [B] = accept_len + 1;
+ *   new_len    [B] = P_b + accept_len + 1;
+ *   next_tail  [B] = tail_base + n_nodes (where the next tree's node 0 goes).
+ * A sequence with err != 0, or whose lengths or path fail the checks of
+ * tsd_kv_commit_path (TSD_STATUS_BAD_LEN / BAD_PATH in *status), records
+ * nothing: remap_len 0, new_len P_b, next_tail its tree base.
+ * One warp per sequence.
+ */
+int tsd_kv_commit_remap(const int32_t *prefix_len, const int32_t *n_nodes,
+                        const int32_t *accept_len, const int32_t *path, const int32_t *err,
+                        const int32_t *tail_base, int B, int N_max, int D_max,
+                        int32_t *remap_src, int32_t *remap_base, int32_t *remap_len,
+                        int32_t *new_len, int32_t *next_tail, int32_t *status,
+                        tsd_stream_t stream);
 
 /*
  * a5. Best-first budgeted tree construction ([BASTION] Methodology 1: path

@@ -41,6 +41,8 @@ SIGNATURES = {
     "tsd_tree_attn_plan": (_I, [_I, _I, _I, _I, _I, _I, _P]),
     "tsd_tree_attn_fwd": (_I, [_P, _P, _P, _P, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F,
                                _P, _P, _P, _SZ, _P, _P]),
+    "tsd_tree_attn_fwd_remap": (_I, [_P, _P, _P, _P, _I, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                     _F, _P, _I, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "tsd_tree_verify_workspace_bytes": (_SZ, [_I, _I, _I]),
     "tsd_tree_verify_greedy": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P,
                                     _P, _P, _SZ, _P]),
@@ -53,6 +55,9 @@ SIGNATURES = {
     "tsd_tree_verify_stochastic_plan": (_I, [_I, _I, _I, _P, _P]),
     "tsd_kv_commit_path": (_I, [_P, _P, _I, _I64, _P, _I, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I,
                                 _I, _P, _P, _P, _P]),
+    "tsd_kv_commit_path_from": (_I, [_P, _P, _I, _I64, _P, _I, _I, _P, _P, _P, _P, _P, _P, _I, _I,
+                                     _I, _I, _I, _P, _P, _P, _P]),
+    "tsd_kv_commit_remap": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
     "tsd_best_first_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "tsd_best_first_tree_build": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "tsd_dynamic_tree_workspace_bytes": (_SZ, [_I, _I, _I]),
@@ -160,10 +165,12 @@ def tree_attn_plan(B, N_max, Hq, Hkv, D, max_slots) -> dict:
 
 def tree_attn_fwd(q, k_cache, v_cache, block_table, prefix_len, n_nodes, mask, err, max_slots,
                   scale=None, out=None, lse=None, want_lse=True, workspace=None, status=None,
-                  stream=None):
+                  stream=None, remap=None):
     """q bf16 [B][N_max][Hq][D]; caches bf16 [num_blocks][Hkv][16][D];
-    block_table int32 [B][max_blocks].  Returns (out bf16 [B][N_max][Hq][D],
-    lse float32 [B][N_max][Hq] or None)."""
+    block_table int32 [B][max_blocks].  remap: None, or (remap_src [B][D_max+1],
+    remap_base [B], remap_len [B], tail_base [B]) from kv_commit_remap, to read
+    the committed sequence through a deferred commit.  Returns (out bf16
+    [B][N_max][Hq][D], lse float32 [B][N_max][Hq] or None)."""
     B, N_max, Hq, D = q.shape
     num_blocks, Hkv = k_cache.shape[0], k_cache.shape[1]
     max_blocks = block_table.shape[1]
@@ -176,6 +183,22 @@ def tree_attn_fwd(q, k_cache, v_cache, block_table, prefix_len, n_nodes, mask, e
     if workspace is None and need > 0:
         workspace = _empty((need,), torch.uint8, q)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if remap is not None:
+        src, rbase, rlen, tbase = remap
+        rc = lib.tsd_tree_attn_fwd_remap(
+            _ptr(q, torch.bfloat16, "q"), _ptr(k_cache, torch.bfloat16, "k_cache"),
+            _ptr(v_cache, torch.bfloat16, "v_cache"),
+            _ptr(block_table, torch.int32, "block_table"), max_blocks, num_blocks,
+            _ptr(prefix_len, torch.int32, "prefix_len"), _ptr(n_nodes, torch.int32, "n_nodes"),
+            _ptr(mask, torch.int32, "mask"), _ptr(err, torch.int32, "err"), B, N_max, Hq, Hkv, D,
+            int(max_slots), float(scale), _ptr(src, torch.int32, "remap_src"),
+            int(src.shape[1]) if src is not None else 0, _ptr(rbase, torch.int32, "remap_base"),
+            _ptr(rlen, torch.int32, "remap_len"), _ptr(tbase, torch.int32, "tail_base"),
+            _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"),
+            _ptr(workspace, None, "workspace"), ws_bytes, _ptr(status, torch.int32, "status"),
+            _stream(stream))
+        _check(rc, "tree_attn_fwd_remap")
+        return out, lse
     rc = lib.tsd_tree_attn_fwd(
         _ptr(q, torch.bfloat16, "q"), _ptr(k_cache, torch.bfloat16, "k_cache"),
         _ptr(v_cache, torch.bfloat16, "v_cache"), _ptr(block_table, torch.int32, "block_table"),
@@ -308,9 +331,10 @@ def tree_verify_stochastic_plan(B: int, N_max: int, V: int):
 
 def kv_commit_path(k_cache, v_cache, block_table, prefix_len, n_nodes, accept_len, path, err,
                    N_max, D_max, num_layers=1, new_len=None, moved=None, status=None,
-                   stream=None):
+                   stream=None, tail_base=None):
     """Caches bf16 [num_layers][num_blocks][Hkv][16][D] (or without the layer
-    axis).  Commits in place.  Returns (new_len [B], moved [B])."""
+    axis).  Commits in place; tail_base int32 [B]: the tree sits there instead
+    of right after the prefix.  Returns (new_len [B], moved [B])."""
     if k_cache.dim() == 5:
         num_layers = k_cache.shape[0]
         num_blocks, Hkv, _, D = k_cache.shape[1:]
@@ -321,6 +345,18 @@ def kv_commit_path(k_cache, v_cache, block_table, prefix_len, n_nodes, accept_le
     B, max_blocks = block_table.shape
     new_len = new_len if new_len is not None else _empty((B,), torch.int32, k_cache)
     moved = moved if moved is not None else _empty((B,), torch.int32, k_cache)
+    if tail_base is not None:
+        rc = lib.tsd_kv_commit_path_from(
+            _ptr(k_cache, torch.bfloat16, "k_cache"), _ptr(v_cache, torch.bfloat16, "v_cache"),
+            num_layers, layer_stride, _ptr(block_table, torch.int32, "block_table"), max_blocks,
+            num_blocks, _ptr(prefix_len, torch.int32, "prefix_len"),
+            _ptr(n_nodes, torch.int32, "n_nodes"), _ptr(accept_len, torch.int32, "accept_len"),
+            _ptr(path, torch.int32, "path"), _ptr(err, torch.int32, "err"),
+            _ptr(tail_base, torch.int32, "tail_base"), B, N_max, Hkv, D, D_max,
+            _ptr(new_len, torch.int32, "new_len"), _ptr(moved, torch.int32, "moved"),
+            _ptr(status, torch.int32, "status"), _stream(stream))
+        _check(rc, "kv_commit_path_from")
+        return new_len, moved
     rc = lib.tsd_kv_commit_path(
         _ptr(k_cache, torch.bfloat16, "k_cache"), _ptr(v_cache, torch.bfloat16, "v_cache"),
         num_layers, layer_stride, _ptr(block_table, torch.int32, "block_table"), max_blocks,
@@ -331,6 +367,26 @@ def kv_commit_path(k_cache, v_cache, block_table, prefix_len, n_nodes, accept_le
         _ptr(status, torch.int32, "status"), _stream(stream))
     _check(rc, "kv_commit_path")
     return new_len, moved
+
+
+def kv_commit_remap(prefix_len, n_nodes, accept_len, path, err, N_max, D_max, tail_base=None,
+                    status=None, stream=None):
+    """Deferred commit: records where each committed entry is, moves nothing.
+    Returns (remap_src [B][D_max+1], remap_base [B], remap_len [B], new_len [B],
+    next_tail [B]); pass (remap_src, remap_base, remap_len, next_tail) as
+    tree_attn_fwd(remap=...) in the next step, with the next tree's K/V
+    written from next_tail on."""
+    B = prefix_len.shape[0]
+    outs = [_empty((B, D_max + 1), torch.int32, prefix_len)] + [
+        _empty((B,), torch.int32, prefix_len) for _ in range(4)]
+    rc = lib.tsd_kv_commit_remap(
+        _ptr(prefix_len, torch.int32, "prefix_len"), _ptr(n_nodes, torch.int32, "n_nodes"),
+        _ptr(accept_len, torch.int32, "accept_len"), _ptr(path, torch.int32, "path"),
+        _ptr(err, torch.int32, "err"), _ptr(tail_base, torch.int32, "tail_base"), B, N_max, D_max,
+        *[_ptr(o, torch.int32, "out") for o in outs], _ptr(status, torch.int32, "status"),
+        _stream(stream))
+    _check(rc, "kv_commit_remap")
+    return tuple(outs)
 
 
 # ---------------------------------------------------------------------------

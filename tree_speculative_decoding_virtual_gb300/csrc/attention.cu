@@ -64,6 +64,12 @@ struct AttnParams {
   uint64_t wait_limit_ns;
   int test_stall;  // wait on a barrier nothing signals (exercises the timeout path)
   int direct;      // 1: one split per key range; rows go straight to the output
+  // Reading through a deferred commit (all null: the plain layout).  Logical
+  // slot s in [remap_base[b], remap_base[b] + remap_len[b]) of sequence b is
+  // physical slot remap_src[b * remap_stride + s - remap_base[b]]; the tree's
+  // node j is at physical slot tail_base[b] + j (null: P_b + j).
+  const int32_t *remap_src, *remap_base, *remap_len, *tail_base;
+  int remap_stride;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -91,6 +97,14 @@ __device__ __forceinline__ bool seq_ok(const AttnParams &p, int b, int &P, int &
   if (e != 0 || nb < 1 || nb > p.N_max) return false;
   if (P < 0 || (long)P + nb > (long)p.max_slots || (long)P + nb > (long)p.max_blocks * kPage)
     return false;
+  if (p.tail_base) {  // the tree at its own base must fit the sequence's table
+    const int T = p.tail_base[b];
+    if (T < 0 || (long)T + nb > (long)p.max_blocks * kPage) return false;
+  }
+  if (p.remap_len) {
+    const int rb = p.remap_base[b], rl = p.remap_len[b];
+    if (rl < 0 || rl > p.remap_stride || (rl > 0 && (rb < 0 || (long)rb + rl > (long)P))) return false;
+  }
   return true;
 }
 
@@ -471,6 +485,82 @@ __device__ __forceinline__ void write_row_direct(const AttnParams &p, size_t oro
   if (valid && p.lse) p.lse[orow] = l_ex > 0.f ? (m + log2f(l_ex)) * 0.6931471805599453f : -INFINITY;
 }
 
+// ---- reading through a deferred commit ----
+// Where the keys of one (sequence, kv head) live when a deferred commit's
+// record or a tree at its own base is in use.
+struct SlotMap {
+  const int32_t *trow;  // the sequence's block table row
+  const int32_t *rsrc;  // physical slots of logical [rb, rb + rl)
+  int rb, rl, P, tb;    // record, prefix length, tree base
+  int k_end;            // end of the block's key range
+  bool active;          // some logical slot is not at its own physical slot
+};
+
+__device__ __forceinline__ SlotMap slot_map(const AttnParams &p, int b, int P, int k_end) {
+  SlotMap m;
+  m.trow = p.table + (size_t)b * p.max_blocks;
+  m.rsrc = p.remap_src ? p.remap_src + (size_t)b * p.remap_stride : nullptr;
+  m.rb = p.remap_base ? p.remap_base[b] : 0;
+  m.rl = p.remap_len ? p.remap_len[b] : 0;
+  m.P = P;
+  m.tb = p.tail_base ? p.tail_base[b] : P;
+  m.k_end = k_end;
+  m.active = (m.rsrc && m.rl > 0) || m.tb != P;
+  return m;
+}
+
+// Whether logical key tile [ts, ts + bn) holds a slot that is not at its own
+// physical slot.
+__device__ __forceinline__ bool tile_moved(const SlotMap &m, int ts, int bn) {
+  if (!m.active) return false;
+  if (m.rl > 0 && ts < m.rb + m.rl && ts + bn > m.rb) return true;
+  return m.tb != m.P && ts + bn > m.P;
+}
+
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void *src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+
+// One key tile (bn slots) of K or V loaded slot by slot by the loader
+// thread, into the layout the TMA boxes produce (64-column halves of bn rows,
+// 128-byte swizzle), then a proxy fence and one arrival on `bar`.  Slots past
+// the key range and slots whose block id is out of range read as zeros (the
+// latter also set `bad`).
+template <int D, int BN>
+__device__ void load_tile_by_slot(const uint16_t *cache, const AttnParams &p, const SlotMap &m,
+                                  int hkv, int ts, uint32_t dst, uint32_t bar, bool &bad) {
+  using namespace sm100;
+  for (int r = 0; r < BN; ++r) {
+    const int s = ts + r;
+    int phys = s;
+    bool valid = s < m.k_end;
+    if (valid) {
+      if (s >= m.P) phys = m.tb + (s - m.P);
+      else if (m.rsrc && s >= m.rb && s < m.rb + m.rl) phys = __ldg(m.rsrc + (s - m.rb));
+    }
+    int page = 0;
+    if (valid) {
+      page = phys >= 0 && phys < p.max_blocks * kPage ? __ldg(m.trow + phys / kPage) : -1;
+      if (page < 0 || page >= p.num_blocks) {
+        bad = true;
+        valid = false;
+        page = 0;
+      }
+    }
+    const uint16_t *src = cache + (((size_t)page * p.Hkv + hkv) * kPage + (valid ? phys % kPage : 0)) * D;
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h)
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        cp_async16_zfill(dst + h * (BN * 128) + sw128_offset(r, c), src + h * 64 + c * 8, valid);
+  }
+  cp_async_wait_all();
+  fence_proxy_async_smem();  // the tensor core reads these rows through the async proxy
+  mbar_arrive(bar);
+}
+
 // One loader thread: TMA loads of K (or V) tiles 0..ntiles-1 into a ring,
 // waiting for a stage to be released before refilling it, then a drain so no
 // copy is in flight when the block exits.
@@ -478,7 +568,9 @@ template <int D>
 __device__ __forceinline__ void tc_load_tiles(const CUtensorMap *m1, const CUtensorMap *m8,
                                               uint64_t *full, uint64_t *empty, uint32_t ring,
                                               const int32_t *pages, int npg, int ntiles, int hkv,
-                                              uint64_t lim, volatile int *abort) {
+                                              uint64_t lim, volatile int *abort,
+                                              const uint16_t *cache, const AttnParams &p,
+                                              const SlotMap &sm, int k_begin, bool &bad) {
   using namespace sm100;
   using L = TcLayout<D>;
   int last_issued[kTcStages];
@@ -487,6 +579,12 @@ __device__ __forceinline__ void tc_load_tiles(const CUtensorMap *m1, const CUten
   for (int j = 0; j < ntiles && !*abort; ++j) {
     const int st = j % kTcStages;
     if (j >= kTcStages && !tc_wait(empty[st], ((j / kTcStages) - 1) & 1, lim, abort)) break;
+    if (tile_moved(sm, k_begin + j * kTcBN, kTcBN)) {
+      load_tile_by_slot<D, kTcBN>(cache, p, sm, hkv, k_begin + j * kTcBN, ring + st * L::kTile,
+                                  smem_addr(&full[st]), bad);
+      last_issued[st] = j;
+      continue;
+    }
     const int g0 = j * kTcPagesPerTile;
     int pg[kTcPagesPerTile];
     bool run = true;
@@ -685,12 +783,15 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
     }
     asm volatile("bar.sync 2, 64;\n" ::: "memory");  // block ids visible to both loaders
     if (lane == 0) {
+      const SlotMap sm = slot_map(p, b, P, k_end);
+      bool bad = false;
       if (warp == 0)
         tc_load_tiles<D>(&map_k1, &map_k8, sh.k_full, sh.k_empty, base + L::kK, sh.pages, npg,
-                         ntiles, hkv, lim, abort);
+                         ntiles, hkv, lim, abort, p.k, p, sm, k_begin, bad);
       else
         tc_load_tiles<D>(&map_v1, &map_v8, sh.v_full, sh.v_empty, base + L::kV, sh.pages, npg,
-                         ntiles, hkv, lim, abort);
+                         ntiles, hkv, lim, abort, p.v, p, sm, k_begin, bad);
+      if (bad && p.status) atomicOr(p.status, TSD_STATUS_BAD_PAGE);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -1122,13 +1223,21 @@ template <int D>
 __device__ __forceinline__ void dual_load_tiles(const CUtensorMap *m1, const CUtensorMap *m4,
                                                 uint64_t *full, uint64_t *empty, uint32_t ring,
                                                 const int32_t *pages, int npg, int ntiles,
-                                                int hkv, uint64_t lim, volatile int *abort) {
+                                                int hkv, uint64_t lim, volatile int *abort,
+                                                const uint16_t *cache, const AttnParams &p,
+                                                const SlotMap &sm, int k_begin, bool &bad) {
   using namespace sm100;
   using L = DualLayout<D>;
   int last_issued[2] = {-1, -1};
   for (int j = 0; j < ntiles && !*abort; ++j) {
     const int st = j & 1;
     if (j >= 2 && !tc_wait(empty[st], ((j >> 1) - 1) & 1, lim, abort)) break;
+    if (tile_moved(sm, k_begin + j * kDualBN, kDualBN)) {
+      load_tile_by_slot<D, kDualBN>(cache, p, sm, hkv, k_begin + j * kDualBN, ring + st * L::kTile,
+                                    smem_addr(&full[st]), bad);
+      last_issued[st] = j;
+      continue;
+    }
     const int g0 = j * kDualPagesPerTile;
     int pg[kDualPagesPerTile];
     bool run = true;
@@ -1302,12 +1411,17 @@ tree_attn_split_dual(const AttnParams p, const __grid_constant__ CUtensorMap map
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0 && p.status) atomicOr(p.status, TSD_STATUS_BAD_PAGE);
     __syncwarp();
-    if (lane == 0)
-      dual_load_tiles<D>(&map_k1, &map_k4, sh.k_full, sh.k_empty, base + L::kK, sh.pages, npg,
-                         ntiles, hkv, lim, abort);
-    else if (lane == 1)
-      dual_load_tiles<D>(&map_v1, &map_v4, sh.v_full, sh.v_empty, base + L::kV, sh.pages, npg,
-                         ntiles, hkv, lim, abort);
+    if (lane < 2) {
+      const SlotMap sm = slot_map(p, b, P, k_end);
+      bool bad_slot = false;
+      if (lane == 0)
+        dual_load_tiles<D>(&map_k1, &map_k4, sh.k_full, sh.k_empty, base + L::kK, sh.pages, npg,
+                           ntiles, hkv, lim, abort, p.k, p, sm, k_begin, bad_slot);
+      else
+        dual_load_tiles<D>(&map_v1, &map_v4, sh.v_full, sh.v_empty, base + L::kV, sh.pages, npg,
+                           ntiles, hkv, lim, abort, p.v, p, sm, k_begin, bad_slot);
+      if (bad_slot && p.status) atomicOr(p.status, TSD_STATUS_BAD_PAGE);
+    }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ------------------------------
@@ -1858,13 +1972,15 @@ TSD_API int tsd_tree_attn_plan(int B, int N_max, int Hq, int Hkv, int D, int max
   return TSD_OK;
 }
 
-TSD_API int tsd_tree_attn_fwd(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+static int attn_fwd_impl(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                               const int32_t *block_table, int max_blocks, int num_blocks,
                               const int32_t *prefix_len, const int32_t *n_nodes,
                               const uint32_t *mask, const int32_t *err, int B, int N_max, int Hq,
                               int Hkv, int D, int max_slots, float scale, uint16_t *out,
                               float *lse, void *workspace, size_t ws_bytes, int32_t *status,
-                              tsd_stream_t stream) {
+                              const int32_t *remap_src, int remap_stride,
+                              const int32_t *remap_base, const int32_t *remap_len,
+                              const int32_t *tail_base, tsd_stream_t stream) {
   using namespace tsd;
   const int dims = attn_check_dims(B, N_max, Hq, Hkv, D, max_slots);
   if (dims != TSD_OK) return dims;
@@ -1919,6 +2035,43 @@ TSD_API int tsd_tree_attn_fwd(const uint16_t *q, const uint16_t *k_cache, const 
   p.wait_limit_ns = (uint64_t)option(TSD_OPT_WAIT_LIMIT_NS);
   p.test_stall = (int)option(TSD_OPT_TEST_STALL);
   p.direct = a.direct ? 1 : 0;
+  p.remap_src = remap_src;
+  p.remap_base = remap_base;
+  p.remap_len = remap_len;
+  p.tail_base = tail_base;
+  p.remap_stride = remap_stride;
   return D == 128 ? launch_attn<128>(p, a, B, num_blocks, as_cuda(stream))
                   : launch_attn<64>(p, a, B, num_blocks, as_cuda(stream));
+}
+
+TSD_API int tsd_tree_attn_fwd(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                              const int32_t *block_table, int max_blocks, int num_blocks,
+                              const int32_t *prefix_len, const int32_t *n_nodes,
+                              const uint32_t *mask, const int32_t *err, int B, int N_max, int Hq,
+                              int Hkv, int D, int max_slots, float scale, uint16_t *out,
+                              float *lse, void *workspace, size_t ws_bytes, int32_t *status,
+                              tsd_stream_t stream) {
+  return attn_fwd_impl(q, k_cache, v_cache, block_table, max_blocks, num_blocks, prefix_len,
+                       n_nodes, mask, err, B, N_max, Hq, Hkv, D, max_slots, scale, out, lse,
+                       workspace, ws_bytes, status, nullptr, 0, nullptr, nullptr, nullptr, stream);
+}
+
+TSD_API int tsd_tree_attn_fwd_remap(const uint16_t *q, const uint16_t *k_cache,
+                                    const uint16_t *v_cache, const int32_t *block_table,
+                                    int max_blocks, int num_blocks, const int32_t *prefix_len,
+                                    const int32_t *n_nodes, const uint32_t *mask,
+                                    const int32_t *err, int B, int N_max, int Hq, int Hkv, int D,
+                                    int max_slots, float scale, const int32_t *remap_src,
+                                    int remap_stride, const int32_t *remap_base,
+                                    const int32_t *remap_len, const int32_t *tail_base,
+                                    uint16_t *out, float *lse, void *workspace, size_t ws_bytes,
+                                    int32_t *status, tsd_stream_t stream) {
+  const bool rec = remap_src || remap_base || remap_len;
+  if (rec && (!remap_src || !remap_base || !remap_len || remap_stride < 1 ||
+              remap_stride > tsd::kMaxDepth + 1))
+    return TSD_ERR_ARG;
+  return attn_fwd_impl(q, k_cache, v_cache, block_table, max_blocks, num_blocks, prefix_len,
+                       n_nodes, mask, err, B, N_max, Hq, Hkv, D, max_slots, scale, out, lse,
+                       workspace, ws_bytes, status, remap_src, remap_stride, remap_base, remap_len,
+                       tail_base, stream);
 }
