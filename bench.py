@@ -53,8 +53,10 @@ DESCRIPTIONS = {
 }
 
 
-def workload_inputs(name):
-    """Host arrays for a workload (numpy), and a description."""
+def workload_inputs(name, batch=None):
+    """Host arrays for a workload (numpy), and a description.  batch: keep the
+    first `batch` sequences only (the same shapes at a smaller size, for
+    profiling)."""
     if name.startswith("bastion"):
         N = int(name[len("bastion"):])
         q, root = gen.bastion_marginals()
@@ -67,7 +69,11 @@ def workload_inputs(name):
                                 "over %d levels (drafter rows resident), rerank to N=%d, verify "
                                 "on Hq=32, Hkv=8, D=128, prefix 2048"
                                 % (c["B"], c["V"], c["k"], c["levels"], c["N"]))
-    return gen.verify_workload(name), DESCRIPTIONS[name]
+    inp = gen.verify_workload(name)
+    if batch is not None and batch < inp.B:
+        return (gen.first_sequences(inp, batch),
+                DESCRIPTIONS[name] + " (first %d of %d sequences)" % (batch, inp.B))
+    return inp, DESCRIPTIONS[name]
 
 
 def algorithmic_bytes(inp, moved_total):
@@ -354,7 +360,7 @@ def measure_workload(name, args, rank, world, dev, flush_l2, full, verify="greed
 
     stream = torch.cuda.current_stream()
     steps, warmup = args.steps, args.warmup
-    w, desc = workload_inputs(name)
+    w, desc = workload_inputs(name, getattr(args, "batch", None))
     bastion = isinstance(w, tuple) and w[0] == "bastion"
     dynamic = isinstance(w, tuple) and w[0] == "dynamic"
 
@@ -828,6 +834,7 @@ def gpu_arm(args, rank, world):
     if world == 1 and args.configs and args.verify == "greedy":
         sub = argparse.Namespace(**vars(args))
         sub.steps = max(3, min(args.steps, args.config_steps))
+        sub.batch = None
         others = {}
         for name in CONFIG_SET:
             if name == args.workload:
@@ -1046,6 +1053,8 @@ def main(argv=None):
                     help="skip the other configurations measured beside the headline")
     ap.add_argument("--config-steps", type=int, default=2000,
                     help="timed steps for each of the other configurations")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="keep the first B sequences of the headline workload (profiling)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
 

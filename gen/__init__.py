@@ -310,6 +310,28 @@ def verify_workload(name: str, seed: Optional[int] = None, with_logits: bool = T
                         logits=logits, q=q, cache=cache, targets=targets)
 
 
+def first_sequences(inp: VerifyInputs, n: int) -> VerifyInputs:
+    """The first n sequences of a workload, with a pool holding only their
+    cache blocks (ids renumbered in increasing order, so a shuffled table stays
+    shuffled).  The same shapes at a smaller size, for profiling."""
+    n = max(1, min(n, inp.B))
+    table = inp.cache.block_table[:n]
+    need = [(int(inp.prefix_len[b]) + int(inp.n_nodes[b]) + PAGE - 1) // PAGE for b in range(n)]
+    used = np.unique(np.concatenate([table[b, :need[b]] for b in range(n)]))
+    remap = {int(x): i for i, x in enumerate(used)}
+    new_table = np.zeros_like(table)
+    for b in range(n):
+        new_table[b, :need[b]] = [remap[int(x)] for x in table[b, :need[b]]]
+    cache = PagedCache(k=inp.cache.k[used], v=inp.cache.v[used], block_table=new_table,
+                       num_blocks=len(used), max_blocks=new_table.shape[1])
+    logits = inp.logits[:n] if inp.logits.ndim == 3 else inp.logits
+    return VerifyInputs(name=inp.name, B=n, N_max=inp.N_max, Hq=inp.Hq, Hkv=inp.Hkv, D=inp.D,
+                        V=inp.V, D_max=inp.D_max, parent=inp.parent[:n].copy(),
+                        n_nodes=inp.n_nodes[:n].copy(), prefix_len=inp.prefix_len[:n].copy(),
+                        tokens=inp.tokens[:n].copy(), logits=np.ascontiguousarray(logits),
+                        q=inp.q[:n].copy(), cache=cache, targets=inp.targets[:n].copy())
+
+
 # BASTION-style budgeted trees -------------------------------------------------
 
 BASTION = dict(B=8, K=16, V=32000, Hq=32, Hkv=8, D=128, prefix=2048, p_match=0.6,
