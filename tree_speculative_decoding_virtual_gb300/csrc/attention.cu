@@ -119,8 +119,14 @@ __device__ __forceinline__ bool seq_ok(const AttnParams &p, int b, int &P, int &
 //              Q K^T that read it completed)
 //   warp 10:   lane 0 loads V tiles the same way (refilled once both P V
 //              that read a stage completed); a warp of its own, so K and V
-//              loads never wait on each other
-//   warp 1:    owns 512 TMEM columns; lane 0 issues every MMA
+//              loads never wait on each other.  With two row tiles the
+//              stages are released by row tile B's softmax group: S_Bj is
+//              committed after every MMA that reads K_j or V_{j-1}
+//   warp 1:    owns 512 TMEM columns; lane 0 issues every MMA and does
+//              nothing else (it paces the tensor core): with two row tiles
+//              its only waits are for P, since row tile A's softmax group
+//              checks that V_j and K_{j+1} have landed before it hands over
+//              P_Aj
 //   warps 2-5: softmax of row tile A, warps 6-9: of row tile B; one TMEM lane
 //              (= one query row) per thread
 // Per 128-key tile j and row tile t:
@@ -561,52 +567,93 @@ __device__ void load_tile_by_slot(const uint16_t *cache, const AttnParams &p, co
   mbar_arrive(bar);
 }
 
+// Tile j of K (or V) into stage j % kTcStages of the ring: TMA boxes, or slot
+// by slot where the tile holds a slot that is not at its own physical slot.
+template <int D>
+__device__ __forceinline__ void tc_load_tile(const CUtensorMap *m1, const CUtensorMap *m8,
+                                             uint64_t *full, uint32_t ring, const int32_t *pages,
+                                             int npg, int hkv, const uint16_t *cache,
+                                             const AttnParams &p, const SlotMap &sm, int k_begin,
+                                             bool &bad, int j) {
+  using namespace sm100;
+  using L = TcLayout<D>;
+  const int st = j % kTcStages;
+  if (tile_moved(sm, k_begin + j * kTcBN, kTcBN)) {
+    load_tile_by_slot<D, kTcBN>(cache, p, sm, hkv, k_begin + j * kTcBN, ring + st * L::kTile,
+                                smem_addr(&full[st]), bad);
+    return;
+  }
+  const int g0 = j * kTcPagesPerTile;
+  int pg[kTcPagesPerTile];
+  bool run = true;
+#pragma unroll
+  for (int g = 0; g < kTcPagesPerTile; ++g) {
+    pg[g] = pages[min(g0 + g, npg - 1)];
+    run = run && pg[g] == pg[0] + g;
+  }
+  const uint32_t bar = smem_addr(&full[st]);
+  mbar_arrive_expect_tx(bar, L::kTile);
+#pragma unroll
+  for (int h = 0; h < L::kHalves; ++h) {
+    const uint32_t dst = ring + st * L::kTile + h * L::kKVHalf;
+    if (run) {
+      tma_load_4d(dst, m8, h * 64, 0, hkv, pg[0], bar);
+    } else {
+#pragma unroll
+      for (int g = 0; g < kTcPagesPerTile; ++g)
+        tma_load_4d(dst + g * kPage * 128, m1, h * 64, 0, hkv, pg[g], bar);
+    }
+  }
+}
+
+// Arrival of a loader on the MMA thread's hand-off barrier for phase ph: the
+// loader's tile has landed and phase ph - 1 has completed (so the arrival
+// cannot count toward an earlier phase; phase ph cannot complete without it).
+__device__ __forceinline__ bool hand_over(uint64_t *hand, int ph, uint64_t &full, uint32_t parity,
+                                          uint64_t lim, volatile int *abort) {
+  using namespace sm100;
+  if (!tc_wait(full, parity, lim, abort)) return false;
+  if (ph > 0 && !tc_wait(*hand, (ph - 1) & 1, lim, abort)) return false;
+  mbar_arrive(smem_addr(hand));
+  return true;
+}
+
 // One loader thread: TMA loads of K (or V) tiles 0..ntiles-1 into a ring,
 // waiting for a stage to be released before refilling it, then a drain so no
-// copy is in flight when the block exits.
+// copy is in flight when the block exits.  With `hand`, the loader also tells
+// the MMA thread (through row tile A's P barrier, phase j) that the tile the
+// MMAs after P_Aj read has landed: V_j (lag 0) or K_{j+1} (lag 1; the last
+// phase, with no K tile after it, gets a plain arrival).
 template <int D>
 __device__ __forceinline__ void tc_load_tiles(const CUtensorMap *m1, const CUtensorMap *m8,
                                               uint64_t *full, uint64_t *empty, uint32_t ring,
                                               const int32_t *pages, int npg, int ntiles, int hkv,
                                               uint64_t lim, volatile int *abort,
                                               const uint16_t *cache, const AttnParams &p,
-                                              const SlotMap &sm, int k_begin, bool &bad) {
+                                              const SlotMap &sm, int k_begin, bool &bad,
+                                              uint64_t *hand, int lag) {
   using namespace sm100;
   using L = TcLayout<D>;
   int last_issued[kTcStages];
 #pragma unroll
   for (int i = 0; i < kTcStages; ++i) last_issued[i] = -1;
-  for (int j = 0; j < ntiles && !*abort; ++j) {
+  bool all = true;
+  for (int j = 0; j < ntiles; ++j) {
     const int st = j % kTcStages;
-    if (j >= kTcStages && !tc_wait(empty[st], ((j / kTcStages) - 1) & 1, lim, abort)) break;
-    if (tile_moved(sm, k_begin + j * kTcBN, kTcBN)) {
-      load_tile_by_slot<D, kTcBN>(cache, p, sm, hkv, k_begin + j * kTcBN, ring + st * L::kTile,
-                                  smem_addr(&full[st]), bad);
-      last_issued[st] = j;
-      continue;
+    if (*abort || (j >= kTcStages && !tc_wait(empty[st], ((j / kTcStages) - 1) & 1, lim, abort))) {
+      all = false;
+      break;
     }
-    const int g0 = j * kTcPagesPerTile;
-    int pg[kTcPagesPerTile];
-    bool run = true;
-#pragma unroll
-    for (int g = 0; g < kTcPagesPerTile; ++g) {
-      pg[g] = pages[min(g0 + g, npg - 1)];
-      run = run && pg[g] == pg[0] + g;
-    }
-    const uint32_t bar = smem_addr(&full[st]);
-    mbar_arrive_expect_tx(bar, L::kTile);
-#pragma unroll
-    for (int h = 0; h < L::kHalves; ++h) {
-      const uint32_t dst = ring + st * L::kTile + h * L::kKVHalf;
-      if (run) {
-        tma_load_4d(dst, m8, h * 64, 0, hkv, pg[0], bar);
-      } else {
-#pragma unroll
-        for (int g = 0; g < kTcPagesPerTile; ++g)
-          tma_load_4d(dst + g * kPage * 128, m1, h * 64, 0, hkv, pg[g], bar);
-      }
-    }
+    tc_load_tile<D>(m1, m8, full, ring, pages, npg, hkv, cache, p, sm, k_begin, bad, j);
     last_issued[st] = j;
+    if (hand && j >= lag && !hand_over(hand, j - lag, full[st], (j / kTcStages) & 1, lim, abort)) {
+      all = false;
+      break;
+    }
+  }
+  if (hand && lag == 1 && all && ntiles >= 1) {
+    const int ph = ntiles - 1;
+    if (ph == 0 || tc_wait(*hand, (ph - 1) & 1, lim, abort)) mbar_arrive(smem_addr(hand));
   }
   // drain: the last loads issued into each stage have landed
 #pragma unroll
@@ -616,24 +663,29 @@ __device__ __forceinline__ void tc_load_tiles(const CUtensorMap *m1, const CUten
 }
 
 // S_t = Q_q K^T for the K tile in stage st into the S columns of TMEM tile
-// t, then a commit to s_full.  Out of line: one copy of the code for every
-// call site.
+// t, then a commit to s_full.  With `peek` nonzero, the phase `parity` of
+// that barrier is tested (without waiting) while the last two MMAs are still
+// queued, so the test's latency is hidden behind them; returns the result.
+// Out of line: one copy of the code for every call site.
 template <int D>
-__device__ __noinline__ void tc_issue_s(uint32_t tmem, uint32_t base, int q, int t, int st,
-                                        uint32_t s_full) {
+__device__ __noinline__ bool tc_issue_s(uint32_t tmem, uint32_t base, int q, int t, int st,
+                                        uint32_t s_full, uint32_t peek, uint32_t parity) {
   using namespace sm100;
   using L = TcLayout<D>;
   constexpr uint32_t idS = idesc_bf16_f32(kTcBM, kTcBN, false, false);
   const uint64_t qd = smem_desc_sw128(base + L::kQ + q * L::kQTile, 16, 1024);
   const uint64_t kd = smem_desc_sw128(base + L::kK + st * L::kTile, 16, 1024);
   tc_fence_after();
+  bool ready = false;
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
+    if (kk == D / 16 - 2 && peek) ready = mbar_test(peek, parity);
     umma_bf16(tmem + t * L::kTmemTile + L::kTmemS,
               desc_add(qd, (kk >> 2) * L::kQHalf + (kk & 3) * 32),
               desc_add(kd, (kk >> 2) * L::kKVHalf + (kk & 3) * 32), idS, kk > 0);
   }
   umma_commit(s_full);
+  return ready;
 }
 
 // O_t += P_t V for the V tile in stage st (P read from tensor memory); a
@@ -701,7 +753,7 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(smem_addr(&sh.s_full[t]), 1);
-      mbar_init(smem_addr(&sh.p_full[t]), 4);
+      mbar_init(smem_addr(&sh.p_full[t]), t == 0 ? 6 : 4);
       mbar_init(smem_addr(&sh.o_final[t]), 1);
       mbar_init(smem_addr(&sh.q_full[t]), 4);
     }
@@ -720,7 +772,10 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
 
-  if (b < p.B) attn_prefetch<D>(p, b, hkv, rt, split, warp, lane);
+  // Blocks of the first wave warm L2 while the previous kernel finishes; a
+  // later block starts after that kernel has ended and loads at once.
+  const int lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+  if (b < p.B && lin < p.nsm) attn_prefetch<D>(p, b, hkv, rt, split, warp, lane);
   pdl_wait();
 
   int P = 0, nb = 0;
@@ -785,12 +840,13 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
     if (lane == 0) {
       const SlotMap sm = slot_map(p, b, P, k_end);
       bool bad = false;
+      uint64_t *hand = kv2 ? nullptr : &sh.p_full[0];
       if (warp == 0)
         tc_load_tiles<D>(&map_k1, &map_k8, sh.k_full, sh.k_empty, base + L::kK, sh.pages, npg,
-                         ntiles, hkv, lim, abort, p.k, p, sm, k_begin, bad);
+                         ntiles, hkv, lim, abort, p.k, p, sm, k_begin, bad, hand, 1);
       else
         tc_load_tiles<D>(&map_v1, &map_v8, sh.v_full, sh.v_empty, base + L::kV, sh.pages, npg,
-                         ntiles, hkv, lim, abort, p.v, p, sm, k_begin, bad);
+                         ntiles, hkv, lim, abort, p.v, p, sm, k_begin, bad, hand, 0);
       if (bad && p.status) atomicOr(p.status, TSD_STATUS_BAD_PAGE);
     }
     __syncwarp();
@@ -801,8 +857,11 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
     // phase ahead of the one wanted (the order bounds it), so parities are
     // unambiguous.
     if (lane == 0) {
-      auto issue_s = [&](int t, int j) {  // K_j has landed; S_t is free
-        tc_issue_s<D>(tmem, base, kv2 ? 0 : t, t, j % kTcStages, smem_addr(&sh.s_full[t]));
+      // K_j has landed; S_t is free.  Returns whether phase `parity` of `peek`
+      // (when nonzero) had completed by the end of the issue.
+      auto issue_s = [&](int t, int j, uint32_t peek = 0u, uint32_t parity = 0u) -> bool {
+        return tc_issue_s<D>(tmem, base, kv2 ? 0 : t, t, j % kTcStages, smem_addr(&sh.s_full[t]),
+                             peek, parity);
       };
       auto issue_pv = [&](int t, int j) {  // V_j has landed; P_tj is in TMEM
         const bool last = kv2 ? j + 2 >= ntiles : j == ntiles - 1;
@@ -838,30 +897,24 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
           }
         }
       } else {
-        // one chain per row tile; the two chains alternate on the tensor core
+        // one chain per row tile; the two chains alternate on the tensor core.
+        // This thread paces the tensor core, so it does nothing else: the K
+        // and V stages are released by the last row tile's softmax group, and
+        // a role that gave up is noticed through the bounded waits.
         ok = ok && tc_wait(sh.k_full[0], 0, lim, abort);
         for (int t = 0; ok && t < ntile_rows; ++t) {
           ok = tc_wait(sh.q_full[t], 0, lim, abort);
           if (ok) issue_s(t, 0);
         }
-        if (ok && ntiles == 1) umma_commit(smem_addr(&sh.k_empty[0]));
         for (int j = 0; ok && j < ntiles; ++j) {
           const bool next = j + 1 < ntiles;
           for (int t = 0; ok && t < ntile_rows; ++t) {
-            ok = !*abort && tc_wait(sh.p_full[t], j & 1, lim, abort);
-            if (ok && t == 0) ok = tc_wait(sh.v_full[j % kTcStages], (j / kTcStages) & 1, lim, abort);
+            // P_tj is in TMEM (and, for row tile A, V_j and K_{j+1} have landed)
+            ok = tc_wait(sh.p_full[t], j & 1, lim, abort);
             if (!ok) break;
             issue_pv(t, j);
-            if (next) {
-              if (t == 0)
-                ok = tc_wait(sh.k_full[(j + 1) % kTcStages], ((j + 1) / kTcStages) & 1, lim, abort);
-              if (ok) issue_s(t, j + 1);
-            }
+            if (next) issue_s(t, j + 1);
           }
-          if (!ok) break;
-          umma_commit(smem_addr(&sh.v_empty[j % kTcStages]));  // both P V of tile j
-          if (next) umma_commit(smem_addr(&sh.k_empty[(j + 1) % kTcStages]));  // both S of j+1
-          if (j == 0 && next) umma_commit(smem_addr(&sh.k_empty[0]));
         }
       }
       // drain: every MMA issued above has completed
@@ -961,6 +1014,13 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
         }
         // S_tj is complete, and with it every earlier MMA of this row tile
         tc_fence_after();
+        if (!kv2 && t == ntile_rows - 1 && warp == 2 + 4 * t && lane == 0) {
+          // S_tj was committed after every other MMA that reads K_j or V_{j-1}
+          // (a commit tracks all of the issuing thread's earlier MMAs): both
+          // stages can be refilled
+          mbar_arrive(smem_addr(&sh.k_empty[j % kTcStages]));
+          if (j > 0) mbar_arrive(smem_addr(&sh.v_empty[(j - 1) % kTcStages]));
+        }
         const int ts = k_begin + j * kTcBN;
         const bool full = (ts + kTcBN <= P) && (ts + kTcBN <= k_end);
         // Two row sums: l_sum adds P exactly as rounded to bf16 for the P V
@@ -1065,7 +1125,10 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&sh.p_full[t]));
+        // p_full[0] counts six arrivals: its four warps and, with two row
+        // tiles, the two loaders (V_j and K_{j+1} have landed); else warp 2
+        // stands in for the loaders
+        if (lane == 0) mbar_arrive_cnt(smem_addr(&sh.p_full[t]), kv2 && warp == 2 ? 3u : 1u);
       }
       if (ok) ok = warp_wait(sh.o_final[t], 0);  // this row tile's last P V
     }
@@ -1357,7 +1420,10 @@ tree_attn_split_dual(const AttnParams p, const __grid_constant__ CUtensorMap map
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
 
-  if (b < p.B) attn_prefetch<D>(p, b, hkv, rt, split, warp, lane);
+  // Blocks of the first wave warm L2 while the previous kernel finishes; a
+  // later block starts after that kernel has ended and loads at once.
+  const int lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+  if (b < p.B && lin < p.nsm) attn_prefetch<D>(p, b, hkv, rt, split, warp, lane);
   pdl_wait();
 
   int P = 0, nb = 0;
