@@ -662,6 +662,20 @@ __device__ __forceinline__ void tc_load_tiles(const CUtensorMap *m1, const CUten
       mbar_wait(smem_addr(&full[st]), (last_issued[st] / kTcStages) & 1, kDrainLimitNs);
 }
 
+// One S chain (K = D in D / 16 steps) from precomputed descriptors: one
+// block of MMA instructions for D = 128.
+template <int D>
+__device__ __forceinline__ void tc_s_chain(uint32_t d, const uint64_t (&a)[D / 16],
+                                           const uint64_t (&b)[D / 16], uint32_t idesc) {
+  using namespace sm100;
+  if constexpr (D == 128) {
+    umma8_ss(d, a, b, idesc, 0u);
+  } else {
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) umma_bf16(d, a[kk], b[kk], idesc, kk > 0);
+  }
+}
+
 // S_t = Q_q K^T for the K tile in stage st into the S columns of TMEM tile
 // t, then a commit to s_full.  With `peek` nonzero, the phase `parity` of
 // that barrier is tested (without waiting) while the last two MMAs are still
@@ -899,21 +913,63 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
       } else {
         // one chain per row tile; the two chains alternate on the tensor core.
         // This thread paces the tensor core, so it does nothing else: the K
-        // and V stages are released by the last row tile's softmax group, and
-        // a role that gave up is noticed through the bounded waits.
+        // and V stages are released by the last row tile's softmax group, a
+        // role that gave up is noticed through the bounded waits, and every
+        // MMA descriptor is computed once, here, so that issuing a group of
+        // MMAs is one block of MMA instructions.
+        constexpr uint32_t idS = idesc_bf16_f32(kTcBM, kTcBN, false, false);
+        constexpr uint32_t idPV = idesc_bf16_f32(kTcBM, D, false, true);
+        uint64_t qa[2][D / 16], kb[kTcStages][D / 16], vb[kTcStages][kTcBN / 16];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const uint64_t qd = smem_desc_sw128(base + L::kQ + i * L::kQTile, 16, 1024);
+          const uint64_t kd = smem_desc_sw128(base + L::kK + i * L::kTile, 16, 1024);
+          const uint64_t vd = smem_desc_sw128(base + L::kV + i * L::kTile, L::kKVHalf, 1024);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            qa[i][kk] = desc_add(qd, (kk >> 2) * L::kQHalf + (kk & 3) * 32);
+            kb[i][kk] = desc_add(kd, (kk >> 2) * L::kKVHalf + (kk & 3) * 32);
+          }
+#pragma unroll
+          for (int kk = 0; kk < kTcBN / 16; ++kk) vb[i][kk] = desc_add(vd, kk * 16 * 128);
+        }
+        // S_t = Q_t K^T from K stage st, then a commit to s_full[t] (the
+        // branches keep every array index a constant)
+        auto s_group = [&](int t, int st) {
+          const uint32_t d = tmem + t * L::kTmemTile + L::kTmemS;
+          tc_fence_after();
+          if (t == 0) {
+            if (st == 0) tc_s_chain<D>(d, qa[0], kb[0], idS);
+            else tc_s_chain<D>(d, qa[0], kb[1], idS);
+          } else {
+            if (st == 0) tc_s_chain<D>(d, qa[1], kb[0], idS);
+            else tc_s_chain<D>(d, qa[1], kb[1], idS);
+          }
+          umma_commit(smem_addr(&sh.s_full[t]));
+        };
+        // O_t += P_t V from V stage st (P read from tensor memory)
+        auto pv_group = [&](int t, int st, bool accum, bool last) {
+          const uint32_t d = tmem + t * L::kTmemTile + L::kTmemO;
+          const uint32_t a = tmem + t * L::kTmemTile + L::kTmemS;
+          tc_fence_after();
+          if (st == 0) umma8_ts(d, a, vb[0], idPV, accum ? 1u : 0u);
+          else umma8_ts(d, a, vb[1], idPV, accum ? 1u : 0u);
+          if (last) umma_commit(smem_addr(&sh.o_final[t]));
+        };
         ok = ok && tc_wait(sh.k_full[0], 0, lim, abort);
         for (int t = 0; ok && t < ntile_rows; ++t) {
           ok = tc_wait(sh.q_full[t], 0, lim, abort);
-          if (ok) issue_s(t, 0);
+          if (ok) s_group(t, 0);
         }
         for (int j = 0; ok && j < ntiles; ++j) {
           const bool next = j + 1 < ntiles;
+          const int st = j % kTcStages;
           for (int t = 0; ok && t < ntile_rows; ++t) {
             // P_tj is in TMEM (and, for row tile A, V_j and K_{j+1} have landed)
             ok = tc_wait(sh.p_full[t], j & 1, lim, abort);
             if (!ok) break;
-            issue_pv(t, j);
-            if (next) issue_s(t, j + 1);
+            pv_group(t, st, j > 0, !next);
+            if (next) s_group(t, st ^ 1);
           }
         }
       }

@@ -221,6 +221,47 @@ __device__ __forceinline__ void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, u
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Eight MMAs from one asm block (a K = 128 chain of K = 16 steps): D in
+// tensor memory, A and B from shared-memory descriptors a[i], b[i].  The first
+// step accumulates into D only when acc0 is nonzero, the others always.  One
+// block of instructions with its operands in registers keeps the issuing
+// thread's instruction count per MMA near one, which matters when the warps
+// sharing its SM sub-partition are busy.
+__device__ __forceinline__ void umma8_ss(uint32_t d, const uint64_t (&a)[8], const uint64_t (&b)[8],
+                                         uint32_t idesc, uint32_t acc0) {
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.b32 p, %18, 0;\n setp.ne.b32 q, 1, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %17, p;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %4, %17, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %6, %17, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %8, %17, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %10, %17, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %11, %12, %17, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %13, %14, %17, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %15, %16, %17, q;\n}\n" ::"r"(d),
+      "l"(a[0]), "l"(b[0]), "l"(a[1]), "l"(b[1]), "l"(a[2]), "l"(b[2]), "l"(a[3]), "l"(b[3]),
+      "l"(a[4]), "l"(b[4]), "l"(a[5]), "l"(b[5]), "l"(a[6]), "l"(b[6]), "l"(a[7]), "l"(b[7]),
+      "r"(idesc), "r"(acc0)
+      : "memory");
+}
+// The same with A read from tensor memory: step i reads columns a + 8 i.
+__device__ __forceinline__ void umma8_ts(uint32_t d, uint32_t a, const uint64_t (&b)[8],
+                                         uint32_t idesc, uint32_t acc0) {
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.b32 p, %18, 0;\n setp.ne.b32 q, 1, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %17, p;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %4, %17, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %6, %17, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %17, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %10, %17, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%11], %12, %17, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%13], %14, %17, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%15], %16, %17, q;\n}\n" ::"r"(d),
+      "r"(a), "l"(b[0]), "r"(a + 8), "l"(b[1]), "r"(a + 16), "l"(b[2]), "r"(a + 24), "l"(b[3]),
+      "r"(a + 32), "l"(b[4]), "r"(a + 40), "l"(b[5]), "r"(a + 48), "l"(b[6]), "r"(a + 56), "l"(b[7]),
+      "r"(idesc), "r"(acc0)
+      : "memory");
+}
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
