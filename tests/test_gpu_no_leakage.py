@@ -7,7 +7,7 @@ output and lse bit-identical, and the outputs of its ancestors and of every
 other sequence too; every node whose own slot was overwritten must change.
 
 Runs the three kernel layouts: the 8B shape (two blocks per SM, splits
-merged inside their cluster), the ragged batch (device split plan) and the
+merged by the merge kernel), the ragged batch (device split plan) and the
 70B shape (256-row blocks)."""
 
 import numpy as np

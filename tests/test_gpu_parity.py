@@ -229,10 +229,13 @@ def test_two_blocks_per_sm_path(tsd, D, N, Hq, Hkv):
 def test_attention_launch_count(tsd):
     """The launch count the library reports: split + merge, plus the plan
     kernel for ragged-capable batches with long blocks, and a single launch
-    (no workspace) when every key range is one piece."""
+    (no workspace) when every key range is one piece, which the host plan
+    also prefers when a second piece would save less than the merge costs
+    (70 sequences of 300 keys)."""
     assert tsd.tree_attn_launches(1, 63, 32, 8, 128, 4159) == 2
     assert tsd.tree_attn_launches(16, 31, 32, 8, 128, 8078) == 3
-    assert tsd.tree_attn_launches(70, 6, 4, 2, 64, 300) == 2
+    assert tsd.tree_attn_launches(70, 6, 4, 2, 64, 1300) == 2
+    assert tsd.tree_attn_launches(70, 6, 4, 2, 64, 300) == 1
     assert tsd.tree_attn_launches(40, 31, 32, 8, 128, 431) == 1
     assert tsd.tree_attn_workspace_bytes(40, 31, 32, 8, 128, 431) == 0
     assert tsd.tree_attn_launches(1, 63, 32, 8, 96, 4159) == 0
@@ -265,11 +268,16 @@ def test_single_piece_key_ranges(tsd, case):
     assert g["status"] == 0
 
 
-def test_large_batch_uniform_split(tsd):
+@pytest.mark.parametrize("prefix_hi,launches", [(300, 1), (1300, 2)])
+def test_large_batch_uniform_split(tsd, prefix_hi, launches):
     """More sequences than the device plan takes (B = 70): the host's
-    uniform split, its three-dimensional grid and the in-cluster merge."""
+    uniform split and its three-dimensional grid, with one piece per key
+    range (rows written by the split kernel) and with two pieces and the
+    merge kernel."""
     inp = gen.random_small(4711, B=70, N_max=6, Hq=4, Hkv=2, D=64, V=50, prefix_lo=0,
-                           prefix_hi=300, max_depth=3)
+                           prefix_hi=prefix_hi, max_depth=3)
+    max_slots = int((inp.prefix_len + inp.n_nodes).max())
+    assert tsd.tree_attn_launches(inp.B, inp.N_max, inp.Hq, inp.Hkv, inp.D, max_slots) == launches
     g = run_gpu(tsd, inp)
     o = run_oracle(inp)
     compare(inp, g, o)

@@ -89,12 +89,12 @@ __device__ __forceinline__ float pow2_above(float amax) {
   return __uint_as_float((uint32_t)(min(max(e, -126), 127) + 127) << 23);
 }
 
-// Sequence-level validity shared by the split and combine kernels.
-__device__ __forceinline__ bool seq_ok(const AttnParams &p, int b, int &P, int &nb) {
+// Sequence-level validity from the input lengths and records alone (no
+// error flag: that one comes from the ancestor pass).
+__device__ __forceinline__ bool seq_shape_ok(const AttnParams &p, int b, int &P, int &nb) {
   P = p.prefix_len[b];
   nb = p.n_nodes ? p.n_nodes[b] : p.N_max;
-  const int e = p.err ? p.err[b] : 0;
-  if (e != 0 || nb < 1 || nb > p.N_max) return false;
+  if (nb < 1 || nb > p.N_max) return false;
   if (P < 0 || (long)P + nb > (long)p.max_slots || (long)P + nb > (long)p.max_blocks * kPage)
     return false;
   if (p.tail_base) {  // the tree at its own base must fit the sequence's table
@@ -106,6 +106,12 @@ __device__ __forceinline__ bool seq_ok(const AttnParams &p, int b, int &P, int &
     if (rl < 0 || rl > p.remap_stride || (rl > 0 && (rb < 0 || (long)rb + rl > (long)P))) return false;
   }
   return true;
+}
+
+// Sequence-level validity shared by the split and combine kernels.
+__device__ __forceinline__ bool seq_ok(const AttnParams &p, int b, int &P, int &nb) {
+  const bool shape = seq_shape_ok(p, b, P, nb);
+  return shape && !(p.err && p.err[b] != 0);
 }
 
 
@@ -1476,11 +1482,26 @@ tree_attn_split_dual(const AttnParams p, const __grid_constant__ CUtensorMap map
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
 
-  // Blocks of the first wave warm L2 while the previous kernel finishes; a
-  // later block starts after that kernel has ended and loads at once.
-  const int lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
-  if (b < p.B && lin < p.nsm) attn_prefetch<D>(p, b, hkv, rt, split, warp, lane);
-  pdl_wait();
+  // With the uniform split the work item and everything the block reads up
+  // to the tree's mask (lengths, block ids, K, V, Q) are inputs, not results
+  // of the previous kernel on the stream (the ancestor pass, which releases
+  // this grid early): the block streams and computes before it waits for that
+  // kernel, and waits only before it reads the mask or the error flag and
+  // before its first global write.  Under the device plan the item is known
+  // only once the plan kernel (the previous grid) has finished; blocks of its
+  // first wave warm L2 meanwhile.
+  bool waited = planned;
+  if (planned) {
+    const int lin = blockIdx.x;
+    if (b < p.B && lin < p.nsm) attn_prefetch<D>(p, b, hkv, rt, split, warp, lane);
+    pdl_wait();
+  }
+  auto wait_prev = [&]() {
+    if (!waited) {
+      pdl_wait();
+      waited = true;
+    }
+  };
 
   int P = 0, nb = 0;
   bool run;
@@ -1500,17 +1521,12 @@ tree_attn_split_dual(const AttnParams p, const __grid_constant__ CUtensorMap map
     k_end = min(P + nb, k_begin + chunk);
     item_row0 = (size_t)item * kTcRows;
   } else {
-    run = seq_ok(p, b, P, nb);
-    if (!run && rt == 0 && split == 0 && hkv == 0 && tid == 0 && p.status) {
-      const int e = p.err ? p.err[b] : 0;
-      const int nbb = p.n_nodes ? p.n_nodes[b] : p.N_max;
-      if (e == 0 && nbb >= 1 && nbb <= p.N_max) atomicOr(p.status, TSD_STATUS_BAD_LEN);
-    }
+    run = seq_shape_ok(p, b, P, nb);  // the error flag is read after the wait
     k_begin = split * p.chunk;
     k_end = min(P + nb, k_begin + p.chunk);
     item_row0 = ((size_t)zg * p.splits + split) * p.rows_pad + (size_t)rt * p.rpb;
   }
-  const bool seq_valid = run;
+  const bool shape_ok = run;
   const int rows_valid = nb * p.g;
   run = run && rt * p.rpb < rows_valid && k_begin < P + nb;
   const int ntiles = (k_end - k_begin + kDualBN - 1) / kDualBN;
@@ -1630,6 +1646,7 @@ tree_attn_split_dual(const AttnParams p, const __grid_constant__ CUtensorMap map
       for (int c2 = 0; c2 < 2; ++c2) tmem_ld32(tS + c2 * 32, r[c2]);
       tmem_wait_ld();
       if (!full) {
+        wait_prev();  // the mask is the ancestor pass's output
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2) {
           const int k0 = ts + c2 * 32;
@@ -1730,10 +1747,13 @@ tree_attn_split_dual(const AttnParams p, const __grid_constant__ CUtensorMap map
     if (ok) ok = warp_wait(sh.o_final, 0);  // the last P V
 
     // ---- epilogue: O / (l c) in fp16 through shared memory, (m, l, c) per row ----
+    // (global writes only once the previous grid has finished: it may still
+    // read what an earlier call wrote here)
+    wait_prev();
     asm volatile("bar.sync 1, 128;\n" ::: "memory");
     const bool all_ok = __all_sync(0xffffffffu, ok && !*abort);
     if (p.direct) {  // one piece per key range: the row straight to the output
-      if (all_ok) {
+      if (all_ok && !(p.err && p.err[b] != 0)) {
         tc_fence_after();
         write_row_direct<D>(p, out_row(p, b, hkv, row), rvalid, tO, m_use, l_sum, l_ex);
       }
@@ -1783,6 +1803,13 @@ tree_attn_split_dual(const AttnParams p, const __grid_constant__ CUtensorMap map
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  wait_prev();
+  const bool seq_valid = shape_ok && !(p.err && p.err[b] != 0);
+  if (!planned && !shape_ok && rt == 0 && split == 0 && hkv == 0 && tid == 0 && p.status) {
+    const int e = p.err ? p.err[b] : 0;
+    const int nbb = p.n_nodes ? p.n_nodes[b] : p.N_max;
+    if (e == 0 && nbb >= 1 && nbb <= p.N_max) atomicOr(p.status, TSD_STATUS_BAD_LEN);
+  }
   if (*abort && tid == 0 && p.status) atomicOr(p.status, TSD_STATUS_TIMEOUT);
   if (warp == 1) {
     tc_fence_after();
@@ -1929,7 +1956,8 @@ AttnPlan plan_attn(int B, int N_max, int Hq, int Hkv, int D, int max_slots) {
   const long max_tiles = (max_slots + kTcBN - 1) / kTcBN;
   // the uniform split for blocks of bm rows: `slots` block slots at once,
   // estimated time = waves x (tiles per block + a fixed cost of about four
-  // 128-key tiles for the prologue and partials)
+  // 128-key tiles for the prologue and partials), plus about two tiles for
+  // the merge kernel when a key range has more than one piece
   auto split_for = [&](int bm, long slots, long &per) {
     const long units = (long)B * Hkv * ((N_max * g + bm - 1) / bm);
     long best_s = 1;
@@ -1937,7 +1965,7 @@ AttnPlan plan_attn(int B, int N_max, int Hq, int Hkv, int D, int max_slots) {
     for (long s = 1; s <= max_tiles && s <= kMaxSplits; ++s) {
       const long waves = (units * s + slots - 1) / slots;
       const long pr = (max_tiles + s - 1) / s;
-      const double t = (double)waves * (double)(pr + 4);
+      const double t = (double)waves * (double)(pr + 4) + (s > 1 ? 2.0 : 0.0);
       if (t < best_t - 1e-9) {
         best_t = t;
         best_s = s;

@@ -48,7 +48,8 @@ commit_kernel(uint16_t *__restrict__ k_cache, uint16_t *__restrict__ v_cache,
   __shared__ long long s_dst[kMaxMoves];
   __shared__ int s_n;
 
-  pdl_trigger();
+  // No early release of the next kernel: it may be an attention pass, which
+  // reads the cache before it waits for this grid.
   pdl_wait();
   const int h = blockIdx.x;
   const int b = blockIdx.y;
@@ -228,7 +229,8 @@ commit_remap_kernel(const int32_t *__restrict__ prefix_len, const int32_t *__res
                     int D_max, int32_t *__restrict__ remap_src, int32_t *__restrict__ remap_base,
                     int32_t *__restrict__ remap_len, int32_t *__restrict__ new_len,
                     int32_t *__restrict__ next_tail, int32_t *__restrict__ status) {
-  pdl_trigger();
+  // No early release of the next kernel: it may be an attention pass, which
+  // reads the record before it waits for this grid.
   pdl_wait();
   const int b = blockIdx.x, lane = threadIdx.x;
   const int cols = D_max + 1;
