@@ -755,6 +755,13 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  // Under the device plan the grid has room for more items than the plan
+  // may make; a block past the first wave starts once the plan kernel has
+  // finished, and one with no item leaves before any set-up.
+  if (planned && item >= p.nsm) {
+    pdl_wait();
+    if (__ldcg(&p.plan_items[item]).x < 0) return;
+  }
 
   // Set-up touches no global memory, so it runs while the previous kernel on
   // the stream finishes (programmatic launch); so does the L2 prefetch.
@@ -1392,37 +1399,6 @@ __device__ __forceinline__ void dual_load_tiles(const CUtensorMap *m1, const CUt
       mbar_wait(smem_addr(&full[st]), (last_issued[st] >> 1) & 1, kDrainLimitNs);
 }
 
-// S = Q K^T (M=128, N=64) for the K tile at kt into the TMEM S buffer ts,
-// then a commit to s_bar.
-template <int D>
-__device__ __noinline__ void dual_issue_s(uint32_t ts, uint32_t qt, uint32_t kt, uint32_t s_bar) {
-  using namespace sm100;
-  using L = DualLayout<D>;
-  constexpr uint32_t idS = idesc_bf16_f32(kTcBM, kDualBN, false, false);
-  const uint64_t qd = smem_desc_sw128(qt, 16, 1024), kd = smem_desc_sw128(kt, 16, 1024);
-  tc_fence_after();
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk)
-    umma_bf16(ts, desc_add(qd, (kk >> 2) * L::kQHalf + (kk & 3) * 32),
-              desc_add(kd, (kk >> 2) * L::kKVHalf + (kk & 3) * 32), idS, kk > 0);
-  umma_commit(s_bar);
-}
-
-// O += P V (K = 64 keys; P read from the TMEM S buffer tp), then commits.
-template <int D>
-__device__ __noinline__ void dual_issue_pv(uint32_t to, uint32_t tp, uint32_t vt, bool accum,
-                                           uint32_t bar1, uint32_t bar2) {
-  using namespace sm100;
-  using L = DualLayout<D>;
-  constexpr uint32_t idPV = idesc_bf16_f32(kTcBM, D, false, true);
-  const uint64_t vd = smem_desc_sw128(vt, L::kKVHalf, 1024);
-  tc_fence_after();
-#pragma unroll
-  for (int kk = 0; kk < kDualBN / 16; ++kk)
-    umma_bf16_ta(to, tp + kk * 8, desc_add(vd, kk * 16 * 128), idPV, (accum || kk > 0) ? 1u : 0u);
-  if (bar1) umma_commit(bar1);
-  if (bar2) umma_commit(bar2);
-}
 
 template <int D>
 __global__ void __launch_bounds__(kDualThreads, 2)
@@ -1448,6 +1424,13 @@ tree_attn_split_dual(const AttnParams p, const __grid_constant__ CUtensorMap map
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  // Under the device plan the grid has room for more items than the plan
+  // may make; a block past the first wave starts once the plan kernel has
+  // finished, and one with no item leaves before any set-up.
+  if (planned && item >= p.nsm) {
+    pdl_wait();
+    if (__ldcg(&p.plan_items[item]).x < 0) return;
+  }
 
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -1564,10 +1547,33 @@ tree_attn_split_dual(const AttnParams p, const __grid_constant__ CUtensorMap map
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ------------------------------
     if (lane == 0) {
+      // Every MMA descriptor is computed once, here, so that a group of MMAs
+      // is one block of MMA instructions (the issuing thread shares its SM
+      // sub-partition with busy softmax warps); the K stages are released by
+      // the softmax warps, which see each S complete.
+      constexpr uint32_t idS = idesc_bf16_f32(kTcBM, kDualBN, false, false);
+      constexpr uint32_t idPV = idesc_bf16_f32(kTcBM, D, false, true);
+      uint64_t qa[D / 16], kb[2][D / 16], vb[2][kDualBN / 16];
+      {
+        const uint64_t qd = smem_desc_sw128(base + L::kQ, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) qa[kk] = desc_add(qd, (kk >> 2) * L::kQHalf + (kk & 3) * 32);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const uint64_t kd = smem_desc_sw128(base + L::kK + i * L::kTile, 16, 1024);
+          const uint64_t vd = smem_desc_sw128(base + L::kV + i * L::kTile, L::kKVHalf, 1024);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) kb[i][kk] = desc_add(kd, (kk >> 2) * L::kKVHalf + (kk & 3) * 32);
+#pragma unroll
+          for (int kk = 0; kk < kDualBN / 16; ++kk) vb[i][kk] = desc_add(vd, kk * 16 * 128);
+        }
+      }
       auto issue_s = [&](int j) {  // K_j has landed; S buffer j & 1 is free
-        dual_issue_s<D>(tmem + L::kTmemS + (j & 1) * kDualBN, base + L::kQ,
-                        base + L::kK + (j & 1) * L::kTile, smem_addr(&sh.s_full[j & 1]));
-        umma_commit(smem_addr(&sh.k_empty[j & 1]));
+        const uint32_t d = tmem + L::kTmemS + (j & 1) * kDualBN;
+        tc_fence_after();
+        if (j & 1) tc_s_chain<D>(d, qa, kb[1], idS);
+        else tc_s_chain<D>(d, qa, kb[0], idS);
+        umma_commit(smem_addr(&sh.s_full[j & 1]));
       };
       bool ok = !p.test_stall || tc_wait(sh.never, 0, lim, abort);
       ok = ok && tc_wait(sh.q_full, 0, lim, abort);
@@ -1577,12 +1583,17 @@ tree_attn_split_dual(const AttnParams p, const __grid_constant__ CUtensorMap map
       }
       for (int j = 0; ok && j < ntiles; ++j) {
         const int st = j & 1;
-        ok = !*abort && tc_wait(sh.p_full[st], (j >> 1) & 1, lim, abort);
+        ok = tc_wait(sh.p_full[st], (j >> 1) & 1, lim, abort);
         ok = ok && tc_wait(sh.v_full[st], (j >> 1) & 1, lim, abort);
         if (!ok) break;
-        dual_issue_pv<D>(tmem + L::kTmemO, tmem + L::kTmemS + st * kDualBN,
-                         base + L::kV + st * L::kTile, j > 0, smem_addr(&sh.pv_done),
-                         j == ntiles - 1 ? smem_addr(&sh.o_final) : 0u);
+        {
+          const uint32_t d = tmem + L::kTmemO, a = tmem + L::kTmemS + st * kDualBN;
+          tc_fence_after();
+          if (st) umma4_ts(d, a, vb[1], idPV, j > 0 ? 1u : 0u);
+          else umma4_ts(d, a, vb[0], idPV, j > 0 ? 1u : 0u);
+          umma_commit(smem_addr(&sh.pv_done));
+          if (j == ntiles - 1) umma_commit(smem_addr(&sh.o_final));
+        }
         umma_commit(smem_addr(&sh.v_empty[st]));
         if (j + 2 < ntiles) {
           ok = tc_wait(sh.k_full[st], ((j + 2) >> 1) & 1, lim, abort);
@@ -1638,6 +1649,9 @@ tree_attn_split_dual(const AttnParams p, const __grid_constant__ CUtensorMap map
         break;
       }
       tc_fence_after();
+      // S_j was the last MMA to read K_j (the commit tracks it): the stage can
+      // be refilled
+      if (warp == 2 && lane == 0) mbar_arrive(smem_addr(&sh.k_empty[st]));
       const uint32_t tS = tmem + L::kTmemS + st * kDualBN + lane_off;
       const int ts = k_begin + j * kDualBN;
       const bool full = (ts + kDualBN <= P) && (ts + kDualBN <= k_end);

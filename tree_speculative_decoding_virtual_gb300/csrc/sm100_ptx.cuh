@@ -262,6 +262,19 @@ __device__ __forceinline__ void umma8_ts(uint32_t d, uint32_t a, const uint64_t 
       "r"(idesc), "r"(acc0)
       : "memory");
 }
+// Four steps of the same, A from tensor memory (a K = 64 chain).
+__device__ __forceinline__ void umma4_ts(uint32_t d, uint32_t a, const uint64_t (&b)[4],
+                                         uint32_t idesc, uint32_t acc0) {
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.b32 p, %10, 0;\n setp.ne.b32 q, 1, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %9, p;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %4, %9, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %6, %9, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %9, q;\n}\n" ::"r"(d),
+      "r"(a), "l"(b[0]), "r"(a + 8), "l"(b[1]), "r"(a + 16), "l"(b[2]), "r"(a + 24), "l"(b[3]),
+      "r"(idesc), "r"(acc0)
+      : "memory");
+}
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
