@@ -453,12 +453,17 @@ def measure_workload(name, args, rank, world, dev, flush_l2, full, verify="greed
     status = torch.zeros((1,), **i32)
 
     verify_name = "tree_verify_stochastic" if stochastic else "tree_verify_greedy"
-    names = ((["best_first_tree_build"] if bastion else [])
-             + (["dynamic_tree_expand", "dynamic_tree_rerank"] if dynamic else [])
-             + ["tree_build_ancestors", "tree_attn_fwd", verify_name, "kv_commit_path"])
+    fused_name = "tree_verify_greedy_commit"
+    head = ((["best_first_tree_build"] if bastion else [])
+            + (["dynamic_tree_expand", "dynamic_tree_rerank"] if dynamic else [])
+            + ["tree_build_ancestors", "tree_attn_fwd"])
+    # every entry point is timed on its own; the greedy step runs verification
+    # and commit as the one fused launch
+    names = head + [verify_name, "kv_commit_path"] + ([] if stochastic else [fused_name])
+    step_names = head + ([verify_name, "kv_commit_path"] if stochastic else [fused_name])
     attn_launches = tsd.tree_attn_launches(B, N, Hq, Hkv, D, max_slots)
     launches_per_step = ((2 if bastion else 0) + (2 * dL + 1 if dynamic else 0) + 1
-                         + attn_launches + 1 + 1)
+                         + attn_launches + (2 if stochastic or B == 1 else 1))
 
     calls = {}
     if bastion:
@@ -488,9 +493,13 @@ def measure_workload(name, args, rank, world, dev, flush_l2, full, verify="greed
     calls["kv_commit_path"] = lambda: tsd.kv_commit_path(
         kc, vc, table, prefix, n_nodes, A, path, err, N, Dm, new_len=new_len, moved=moved,
         status=status)
+    calls[fused_name] = lambda: tsd.tree_verify_greedy_commit(
+        logits, tokens, parent, anc, depth, mask, n_nodes, err, Dm, kc, vc, table, prefix,
+        argmax=am, accept_len=A, leaf=leaf, path=path, bonus=bonus, new_len=new_len, moved=moved,
+        status=status, workspace=ver_ws)
 
     def step():
-        for n in names:
+        for n in step_names:
             calls[n]()
 
     for _ in range(warmup):
@@ -659,8 +668,8 @@ def measure_workload(name, args, rank, world, dev, flush_l2, full, verify="greed
             for k, v in h_in.items():
                 if k not in late:
                     v.copy_(pinned[k], non_blocking=True)
-            for n in names:  # the public API calls, launched from Python
-                if n == verify_name:
+            for n in step_names:  # the public API calls, launched from Python
+                if n in (verify_name, fused_name):
                     stream.wait_stream(copy_stream)
                 calls[n]()
             for k, v in h_out_src.items():
@@ -702,6 +711,8 @@ def measure_workload(name, args, rank, world, dev, flush_l2, full, verify="greed
     if dynamic:
         # each level reads its frontier's draft rows once
         abytes["dynamic_tree_expand"] = sum(4 * r.numel() for r in d_rows)
+    if not stochastic:
+        abytes[fused_name] = abytes["tree_verify_greedy"] + abytes["kv_commit_path"]
     step_bytes = sum(abytes.values())
     dom = max(["tree_attn_fwd", verify_name], key=lambda n: kernel_us[n])
     attn_flops = attention_flops(inp)
@@ -773,7 +784,8 @@ def measure_workload(name, args, rank, world, dev, flush_l2, full, verify="greed
         "attention_tflops": round(attn_tflops, 1),
         "gpu_launches": launches,
         "wall_s_timed_region": round(t_wall, 4),
-        "kernel_sum_us": round(sum(kernel_us.values()), 3),
+        "kernel_sum_us": round(sum(kernel_us[n] for n in step_names), 3),
+        "step_calls": step_names,
         "mean_accept_len": float(A.float().mean().item()),
         "verify": (verify if not stochastic else
                    {"mode": "stochastic", "internal_rows": internal_rows,

@@ -381,6 +381,34 @@ int tsd_kv_commit_path(uint16_t *k_cache, uint16_t *v_cache, int num_layers, int
                        tsd_stream_t stream);
 
 /*
+ * a3 + a4 in one launch: tsd_tree_verify_greedy, and the block that finishes
+ * a sequence's acceptance search then commits that sequence's accepted path
+ * (every layer and kv head) exactly as tsd_kv_commit_path would from the
+ * accept_len / path it has just written, which spares the commit launch.
+ * Arguments: those of tsd_tree_verify_greedy (same workspace contract), then
+ * those of tsd_kv_commit_path without the ones the verification produces
+ * (accept_len, path) or shares (n_nodes, err, B, N_max, D_max); the tree sits
+ * right after the prefix.  num_layers 0: verification only.  Outputs and
+ * errors are those of the two calls; status gets the commit's BAD_PATH /
+ * BAD_PAGE / BAD_LEN bits.  The fused grid writes the cache, so it does not
+ * let the next kernel on the stream start before it ends (the attention pass
+ * may read the cache early).  With B == 1 the one sequence's commit would run
+ * in a single block: the call then launches the verification and the commit
+ * kernel back to back (two launches), which measured faster.
+ */
+int tsd_tree_verify_greedy_commit(const float *logits, const int32_t *tokens,
+                                  const int32_t *parent, const int32_t *anc, const int32_t *depth,
+                                  const uint32_t *mask, const int32_t *n_nodes,
+                                  const int32_t *err, int B, int N_max, int V, int D_max,
+                                  int32_t *argmax, int32_t *accept_len, int32_t *leaf,
+                                  int32_t *path, int32_t *bonus, void *workspace, size_t ws_bytes,
+                                  uint16_t *k_cache, uint16_t *v_cache, int num_layers,
+                                  int64_t layer_stride, const int32_t *block_table, int max_blocks,
+                                  int num_blocks, const int32_t *prefix_len, int Hkv, int D,
+                                  int32_t *new_len, int32_t *moved, int32_t *status,
+                                  tsd_stream_t stream);
+
+/*
  * a4 from a tree at its own base: as tsd_kv_commit_path, but real node i's
  * K/V are at slot tail_base[b] + i (REQUIRED, int32 [B]); slot P_b + k
  * receives the entry of slot tail_base[b] + path[b][k] - 1, the root too

@@ -46,6 +46,9 @@ SIGNATURES = {
     "tsd_tree_verify_workspace_bytes": (_SZ, [_I, _I, _I]),
     "tsd_tree_verify_greedy": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P,
                                     _P, _P, _SZ, _P]),
+    "tsd_tree_verify_greedy_commit": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P,
+                                           _P, _P, _P, _P, _SZ, _P, _P, _I, _I64, _P, _I, _I, _P,
+                                           _I, _I, _P, _P, _P, _P]),
     "tsd_tree_verify_static_capacity": (_SZ, []),
     "tsd_tree_verify_greedy_static": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P,
                                            _P, _P, _P, _P]),
@@ -246,6 +249,50 @@ def tree_verify_greedy(logits, tokens, parent, anc, depth, mask, n_nodes, err, D
         workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "tree_verify_greedy")
     return argmax, accept_len, leaf, path, bonus
+
+
+def tree_verify_greedy_commit(logits, tokens, parent, anc, depth, mask, n_nodes, err, D_max,
+                              k_cache, v_cache, block_table, prefix_len, num_layers=1,
+                              argmax=None, accept_len=None, leaf=None, path=None, bonus=None,
+                              new_len=None, moved=None, status=None, workspace=None, stream=None):
+    """tree_verify_greedy, then, in the same launch, kv_commit_path of the
+    accepted paths (caches as kv_commit_path takes them).  Returns (argmax,
+    accept_len, leaf, path, bonus, new_len, moved)."""
+    B, N_max, V = logits.shape
+    if k_cache.dim() == 5:
+        num_layers = k_cache.shape[0]
+        num_blocks, Hkv, _, D = k_cache.shape[1:]
+        layer_stride = k_cache.stride(0)
+    else:
+        num_blocks, Hkv, _, D = k_cache.shape
+        layer_stride = k_cache.numel()
+    max_blocks = block_table.shape[1]
+    argmax = argmax if argmax is not None else _empty((B, N_max), torch.int32, logits)
+    accept_len = accept_len if accept_len is not None else _empty((B,), torch.int32, logits)
+    leaf = leaf if leaf is not None else _empty((B,), torch.int32, logits)
+    path = path if path is not None else _empty((B, D_max + 1), torch.int32, logits)
+    bonus = bonus if bonus is not None else _empty((B,), torch.int32, logits)
+    new_len = new_len if new_len is not None else _empty((B,), torch.int32, logits)
+    moved = moved if moved is not None else _empty((B,), torch.int32, logits)
+    need = tree_verify_workspace_bytes(B, N_max, V)
+    if workspace is None:
+        workspace = torch.zeros((max(need, 1),), dtype=torch.uint8, device=logits.device)
+    rc = lib.tsd_tree_verify_greedy_commit(
+        _ptr(logits, torch.float32, "logits"), _ptr(tokens, torch.int32, "tokens"),
+        _ptr(parent, torch.int32, "parent"), _ptr(anc, torch.int32, "anc"),
+        _ptr(depth, torch.int32, "depth"), _ptr(mask, torch.int32, "mask"),
+        _ptr(n_nodes, torch.int32, "n_nodes"), _ptr(err, torch.int32, "err"), B, N_max, V, D_max,
+        _ptr(argmax, torch.int32, "argmax"), _ptr(accept_len, torch.int32, "accept_len"),
+        _ptr(leaf, torch.int32, "leaf"), _ptr(path, torch.int32, "path"),
+        _ptr(bonus, torch.int32, "bonus"), _ptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(),
+        _ptr(k_cache, torch.bfloat16, "k_cache"), _ptr(v_cache, torch.bfloat16, "v_cache"),
+        num_layers, layer_stride, _ptr(block_table, torch.int32, "block_table"), max_blocks,
+        num_blocks, _ptr(prefix_len, torch.int32, "prefix_len"), Hkv, D,
+        _ptr(new_len, torch.int32, "new_len"), _ptr(moved, torch.int32, "moved"),
+        _ptr(status, torch.int32, "status"), _stream(stream))
+    _check(rc, "tree_verify_greedy_commit")
+    return argmax, accept_len, leaf, path, bonus, new_len, moved
 
 
 def tree_verify_static_capacity() -> int:

@@ -24,6 +24,7 @@
 #include <cmath>
 #include <mutex>
 
+#include "commit_core.cuh"
 #include "sm100_ptx.cuh"
 #include "tsd_common.cuh"
 
@@ -33,6 +34,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kBatch = 8;        // 16-byte loads in flight per thread
 constexpr int kBlocksPerSm = 4;  // 1024 threads x 64 registers per SM
+constexpr int kFusedCap = 2 * kMaxMoves;  // staged (K, V) entries of the fused commit
 
 // (v, i) beats (bv, bi): larger value, or equal value and lower index.
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
@@ -55,6 +57,9 @@ __device__ __forceinline__ void take4(const float4 &a, int x, float &bv, int &bi
   if (better(a.w, x + 3, bv, bi)) { bv = a.w; bi = x + 3; }
 }
 
+// CD: 0, or the head dimension of the cache the block that finishes a
+// sequence also commits (the fused commit).
+template <int CD>
 __global__ void __launch_bounds__(kThreads, kBlocksPerSm)
 verify_greedy_kernel(const float *__restrict__ logits, const int32_t *__restrict__ tokens,
                      const int32_t *__restrict__ parent, const int32_t *__restrict__ anc,
@@ -64,13 +69,16 @@ verify_greedy_kernel(const float *__restrict__ logits, const int32_t *__restrict
                      int32_t *__restrict__ argmax_out, int32_t *__restrict__ accept_len,
                      int32_t *__restrict__ leaf_out, int32_t *__restrict__ path,
                      int32_t *__restrict__ bonus, unsigned long long *__restrict__ row_key,
-                     unsigned *__restrict__ counter) {
+                     unsigned *__restrict__ counter, const CommitArgs ca) {
   using namespace sm100;
   __shared__ float s_v[2][kThreads / 32];
   __shared__ int s_i[2][kThreads / 32];
   __shared__ bool s_last;
 
-  pdl_trigger();
+  // With the fused commit this grid writes the K/V cache, which the next
+  // attention pass reads before it waits for its own predecessor: no early
+  // release then.
+  if (CD == 0) pdl_trigger();
   const int g = blockIdx.x;
   const int Gs = gridDim.x;
   const int b = blockIdx.y;
@@ -90,6 +98,32 @@ verify_greedy_kernel(const float *__restrict__ logits, const int32_t *__restrict
       const char *base = reinterpret_cast<const char *>(seq);
       for (long off = lo * 4 + (long)t * 128; off < hi * 4; off += (long)kThreads * 128)
         prefetch_l2(base + off);
+      if constexpr (CD != 0) {
+        // the fused commit's inputs (lengths, the tree's block ids, the tree's
+        // K and V: the only entries a commit can move), each block a slice,
+        // so that the block that commits finds them in L2
+        const int P = ca.prefix_len[b];
+        if (P >= 0 && (long)P + nb_hint <= (long)ca.max_blocks * kPage) {
+          const int32_t *trow = ca.table + (size_t)b * ca.max_blocks;
+          const int pg0 = P / kPage, pg1 = (P + nb_hint - 1) / kPage;
+          const long entries = (long)(P + nb_hint - pg0 * kPage) * ca.Hkv;  // slots x heads
+          for (long x = (long)g * kThreads + t; x < entries * 4; x += (long)Gs * kThreads) {
+            const int line = (int)(x & 3);  // four 128-byte lines of K and of V per entry
+            const long en = x >> 2;
+            const int slot = pg0 * kPage + (int)(en / ca.Hkv), h = (int)(en % ca.Hkv);
+            const int page = trow[slot / kPage];
+            if (page < 0 || page >= ca.num_blocks || slot / kPage > pg1) continue;
+            const size_t off = (((size_t)page * ca.Hkv + h) * kPage + slot % kPage) * CD * 2;
+            for (int l = 0; l < ca.num_layers && l < 2; ++l) {
+              const size_t lb = (size_t)l * (size_t)ca.layer_stride * 2;
+              if (line * 128 < CD * 2) {
+                prefetch_l2(reinterpret_cast<const char *>(ca.k) + lb + off + line * 128);
+                prefetch_l2(reinterpret_cast<const char *>(ca.v) + lb + off + line * 128);
+              }
+            }
+          }
+        }
+      }
     }
   }
   pdl_wait();
@@ -291,6 +325,18 @@ verify_greedy_kernel(const float *__restrict__ logits, const int32_t *__restrict
       bonus[b] = -1;
     }
   }
+  if constexpr (CD != 0) {
+    // ---- phase 3 (fused commit): the accepted path's K/V of sequence b, every
+    // kv head and layer, exactly as tsd_kv_commit_path would commit it from
+    // the accept_len / path rows just written ----
+    __shared__ CommitMoves mv;
+    extern __shared__ uint4 stage[];
+    __syncthreads();  // this block's accept_len / path writes are visible to it
+    if (warp == 0)
+      commit_plan_warp(ca, b, N_max, D_max, n_nodes, err, accept_len, path, true, mv, lane);
+    __syncthreads();
+    commit_copy<CD>(ca, mv, 0, ca.Hkv, 0, ca.num_layers, stage, kFusedCap, t, kThreads);
+  }
 }
 
 struct VerifyPlan {
@@ -315,21 +361,37 @@ VerifyPlan plan_verify(int B, int N_max, int V) {
   return p;
 }
 
+// cd: 0 (no commit) or the cache's head dimension (64, 128) with `ca` set.
 int launch_verify(const float *logits, const int32_t *tokens, const int32_t *parent,
                   const int32_t *anc, const int32_t *depth, const uint32_t *mask,
                   const int32_t *n_nodes, const int32_t *err, int B, int N_max, int V, int D_max,
                   int32_t *argmax, int32_t *accept_len, int32_t *leaf, int32_t *path,
-                  int32_t *bonus, void *scratch, const VerifyPlan &p, cudaStream_t s) {
+                  int32_t *bonus, void *scratch, const VerifyPlan &p, cudaStream_t s,
+                  int cd = 0, const CommitArgs &ca = CommitArgs{}) {
   unsigned *counter = static_cast<unsigned *>(scratch);
   unsigned long long *keys =
       reinterpret_cast<unsigned long long *>(static_cast<char *>(scratch) + p.counter_bytes);
   const int W = (N_max + 31) / 32;
   const int vec = (V % 4 == 0) && aligned(logits, 16);
-  if (launch(verify_greedy_kernel, dim3(p.Gs, B), dim3(kThreads), 0, s, logits, tokens, parent,
-             anc, depth, mask, n_nodes, err, N_max, V, D_max, W, vec, argmax, accept_len, leaf,
-             path, bonus, keys, counter) != cudaSuccess)
-    return TSD_ERR_CUDA;
-  return TSD_OK;
+  const dim3 grid(p.Gs, B);
+  cudaError_t e;
+  if (cd == 0) {
+    e = launch(verify_greedy_kernel<0>, grid, dim3(kThreads), 0, s, logits, tokens, parent, anc,
+               depth, mask, n_nodes, err, N_max, V, D_max, W, vec, argmax, accept_len, leaf, path,
+               bonus, keys, counter, ca);
+  } else {
+    const size_t smem = 2 * (size_t)kFusedCap * (cd / 8) * sizeof(uint4);
+    const void *k = cd == 128 ? reinterpret_cast<const void *>(verify_greedy_kernel<128>)
+                              : reinterpret_cast<const void *>(verify_greedy_kernel<64>);
+    if (!set_smem(k, smem)) return TSD_ERR_CUDA;
+    e = cd == 128 ? launch(verify_greedy_kernel<128>, grid, dim3(kThreads), smem, s, logits, tokens,
+                           parent, anc, depth, mask, n_nodes, err, N_max, V, D_max, W, vec, argmax,
+                           accept_len, leaf, path, bonus, keys, counter, ca)
+                  : launch(verify_greedy_kernel<64>, grid, dim3(kThreads), smem, s, logits, tokens,
+                           parent, anc, depth, mask, n_nodes, err, N_max, V, D_max, W, vec, argmax,
+                           accept_len, leaf, path, bonus, keys, counter, ca);
+  }
+  return e == cudaSuccess ? TSD_OK : TSD_ERR_CUDA;
 }
 
 }  // namespace
@@ -360,6 +422,50 @@ TSD_API int tsd_tree_verify_greedy(const float *logits, const int32_t *tokens,
     return TSD_ERR_WORKSPACE;
   return launch_verify(logits, tokens, parent, anc, depth, mask, n_nodes, err, B, N_max, V, D_max,
                        argmax, accept_len, leaf, path, bonus, workspace, p, as_cuda(stream));
+}
+
+TSD_API int tsd_tree_verify_greedy_commit(
+    const float *logits, const int32_t *tokens, const int32_t *parent, const int32_t *anc,
+    const int32_t *depth, const uint32_t *mask, const int32_t *n_nodes, const int32_t *err, int B,
+    int N_max, int V, int D_max, int32_t *argmax, int32_t *accept_len, int32_t *leaf, int32_t *path,
+    int32_t *bonus, void *workspace, size_t ws_bytes, uint16_t *k_cache, uint16_t *v_cache,
+    int num_layers, int64_t layer_stride, const int32_t *block_table, int max_blocks,
+    int num_blocks, const int32_t *prefix_len, int Hkv, int D, int32_t *new_len, int32_t *moved,
+    int32_t *status, tsd_stream_t stream) {
+  using namespace tsd;
+  if (B < 0 || V < 1) return B < 0 ? TSD_ERR_ARG : TSD_ERR_LIMIT;
+  if (N_max < 1 || N_max > kMaxNodes || D_max < 0 || D_max > kMaxDepth || B > 65535)
+    return TSD_ERR_LIMIT;
+  if (num_layers < 0 || Hkv < 1 || max_blocks < 1 || num_blocks < 1) return TSD_ERR_ARG;
+  if (D != 64 && D != 128) return TSD_ERR_LIMIT;
+  if (B == 0) return TSD_OK;
+  if (!logits || !tokens || !parent || !anc || !depth || !mask || !argmax || !accept_len ||
+      !leaf || !path || !bonus)
+    return TSD_ERR_ARG;
+  if (num_layers > 0 && (!k_cache || !v_cache || !block_table || !prefix_len || !new_len))
+    return TSD_ERR_ARG;
+  if (num_layers > 0 && (!aligned(k_cache, 16) || !aligned(v_cache, 16))) return TSD_ERR_ARG;
+  const int64_t pool = (int64_t)num_blocks * Hkv * kPage * D;
+  if (num_layers > 1 && (layer_stride < pool || layer_stride % 8 != 0)) return TSD_ERR_ARG;
+  const VerifyPlan p = plan_verify(B, N_max, V);
+  if (!workspace || ws_bytes < p.counter_bytes + p.key_bytes || !aligned(workspace, 16))
+    return TSD_ERR_WORKSPACE;
+  if (num_layers == 0 || B == 1) {
+    // One sequence: its commit would run in a single block after the search
+    // (measured slower than the commit kernel's block per head), so the two
+    // kernels are launched back to back instead.
+    const int rc = launch_verify(logits, tokens, parent, anc, depth, mask, n_nodes, err, B, N_max,
+                                 V, D_max, argmax, accept_len, leaf, path, bonus, workspace, p,
+                                 as_cuda(stream));
+    if (rc != TSD_OK || num_layers == 0) return rc;
+    return tsd_kv_commit_path(k_cache, v_cache, num_layers, layer_stride, block_table, max_blocks,
+                              num_blocks, prefix_len, n_nodes, accept_len, path, err, B, N_max, Hkv,
+                              D, D_max, new_len, moved, status, stream);
+  }
+  const CommitArgs ca{k_cache, v_cache, num_layers, layer_stride, block_table, max_blocks,
+                      num_blocks, prefix_len, nullptr, Hkv, new_len, moved, status};
+  return launch_verify(logits, tokens, parent, anc, depth, mask, n_nodes, err, B, N_max, V, D_max,
+                       argmax, accept_len, leaf, path, bonus, workspace, p, as_cuda(stream), D, ca);
 }
 
 // ---------------------------------------------------------------------------
