@@ -26,6 +26,16 @@
  *   synchronises: all work is enqueued on `stream` (a cudaStream_t; NULL is
  *   the legacy default stream) in launch order, and results are ready when
  *   the stream reaches that point.
+ * - Kernels are launched with programmatic dependent launch: a kernel may
+ *   start while the previous kernel on the stream is still running, if that
+ *   kernel is one of this library's and releases its dependents early (every
+ *   kernel here does, except the commits, which release only when they end).
+ *   Each kernel waits for the previous one before it reads that kernel's
+ *   results and before its first global write.  tsd_tree_attn_fwd under the
+ *   uniform split reads its inputs (q, the caches, block table, lengths,
+ *   records) before that wait, and the mask and err after it: a library
+ *   kernel just before it must therefore not write those inputs, which holds
+ *   for tsd_tree_build_ancestors (the usual predecessor).
  * - Return value: a host-detected status (TSD_OK or a negative TSD_ERR_*).
  *   On a non-zero return nothing was launched (TSD_ERR_CUDA: a launch failed;
  *   the CUDA error is left for the caller to query).

@@ -32,10 +32,13 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Programmatic dependent launch: every kernel of the library is launched so
 // that it may start while the previous kernel on the stream finishes; each
-// kernel lets its own dependents launch at entry (pdl_trigger) and waits for
-// the previous grid's completion and memory (pdl_wait) before it touches
-// global memory.  After a kernel that does not trigger, this is an ordinary
-// stream-ordered launch.
+// kernel lets its own dependents launch at entry (pdl_trigger; the kernels
+// that write the K/V cache or the slot record release them only when they
+// end) and waits for the previous grid's completion and memory (pdl_wait)
+// before it reads that grid's results and before its first global write
+// (the attention under the uniform split reads its inputs before the wait).
+// After a kernel that does not trigger, this is an ordinary stream-ordered
+// launch.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::); }
 
