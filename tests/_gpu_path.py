@@ -72,12 +72,13 @@ def run_oracle(inp, sample_attention=None):
                 k=k1, v=v1)
 
 
-def attention_rows(inp, err, sample=None):
+def attention_rows(inp, err, sample=None, attn_skip=()):
     """Boolean [B][N_max][Hq] of rows to compare (valid nodes of sequences
-    without errors, restricted to the sample if given)."""
+    without errors and not in ``attn_skip``, restricted to the sample if
+    given)."""
     sel = np.zeros((inp.B, inp.N_max, inp.Hq), dtype=bool)
     for b in range(inp.B):
-        if err[b] == 0:
+        if err[b] == 0 and b not in attn_skip:
             sel[b, :int(inp.n_nodes[b]), :] = True
     if sample is not None:
         only = np.zeros_like(sel)
@@ -87,21 +88,23 @@ def attention_rows(inp, err, sample=None):
     return sel
 
 
-def compare(inp, g, o, sample=None, check_lse=True):
+def compare(inp, g, o, sample=None, check_lse=True, attn_skip=()):
+    """``attn_skip``: sequences the attention alone must skip (a key range
+    beyond the max_slots bound): their rows are checked to be zero / -inf."""
     for key in ["anc", "depth", "mask", "err"]:
         assert np.array_equal(g[key], o[key]), key
     for key in ["argmax", "accept_len", "leaf", "path", "bonus", "new_len", "moved"]:
         assert np.array_equal(g[key], o[key]), (key, g[key], o[key])
     assert np.array_equal(g["k"], o["k"]), "committed K cache"
     assert np.array_equal(g["v"], o["v"]), "committed V cache"
-    sel = attention_rows(inp, o["err"], sample)
+    sel = attention_rows(inp, o["err"], sample, attn_skip)
     got = oracle.bf16_to_f64(g["out"])
     diff = np.abs(got - o["out"])[sel]
     if diff.size:
         assert diff.max() <= ATOL_MAX, ("attention max-abs", diff.max())
         assert diff.mean() <= ATOL_MEAN, ("attention mean-abs", diff.mean())
     # skipped / padding rows are zero and -inf
-    skip = attention_rows(inp, o["err"]) == False  # noqa: E712
+    skip = attention_rows(inp, o["err"], None, attn_skip) == False  # noqa: E712
     assert (g["out"][skip] == 0).all()
     if check_lse and g["lse"] is not None:
         d = np.abs(g["lse"].astype(np.float64)[sel] - o["lse"][sel])

@@ -344,6 +344,45 @@ def test_malformed_trees_fail_closed(tsd):
     assert (g["new_len"][1:] == inp.prefix_len[1:]).all()
 
 
+@pytest.mark.parametrize("B,N,Hq,Hkv,P,mode,direct,dual", [
+    (6, 12, 4, 2, 40, 1, 1, 1),      # two blocks per SM, one piece per key range
+    (6, 12, 8, 2, 2900, 1, 0, 1),    # two blocks per SM, uniform split (23 pieces)
+    (7, 40, 64, 8, 3700, 1, 0, 1),   # the same with three row tiles per kv head
+    (6, 12, 16, 8, 12200, 2, 0, 1),  # two blocks per SM, device plan
+    (7, 40, 64, 8, 4300, 2, 0, 0)])  # 256-row blocks, device plan
+def test_failed_sequences_every_attention_plan(tsd, B, N, Hq, Hkv, P, mode, direct, dual):
+    """Failed sequences under each launch shape of the attention: a cyclic
+    tree and an empty tree (err != 0: skipped by every kernel) and a
+    sequence whose key range runs past the max_slots bound the caller
+    passed (TSD_STATUS_BAD_LEN from the attention, which skips it; the
+    verification and commit, which take no such bound, still run it).  The
+    uniform split's blocks read their inputs before the grid dependency on
+    the ancestors kernel resolves and the error words after it, so a stale
+    err would show here as rows written for a failed tree."""
+    prefix = np.full(B, P, dtype=np.int32)
+    prefix[::2] -= 37          # ragged lengths
+    prefix[3] = P + 300        # past the bound below
+    inp = gen.random_small(900 + B + N + P, B=B, N_max=N, Hq=Hq, Hkv=Hkv, D=128, V=80,
+                           prefix_lo=0, prefix_hi=1, max_depth=6, prefix_len=prefix)
+    inp.parent[1, int(inp.n_nodes[1]) - 1] = int(inp.n_nodes[1]) - 1  # self loop (or root cycle)
+    inp.n_nodes[2] = 0
+    others = [b for b in range(B) if b != 3]
+    max_slots = int((inp.prefix_len[others] + inp.n_nodes[others]).max())
+    assert int(inp.prefix_len[3] + inp.n_nodes[3]) > max_slots
+    plan = tsd.tree_attn_plan(B, N, Hq, Hkv, inp.D, max_slots)
+    assert (plan["mode"], plan["direct"], plan["two_blocks_per_sm"]) == (mode, direct, dual), plan
+    rng = np.random.default_rng(B * N)
+    sample = sorted({(b, int(rng.integers(inp.N_max)), int(rng.integers(Hq)))
+                     for b in range(B) for _ in range(10)}
+                    | {(0, i, h) for i in range(int(inp.n_nodes[0])) for h in (0, Hq - 1)})
+    g = run_gpu(tsd, inp, max_slots=max_slots)
+    o = run_oracle(inp, sample_attention=sample)
+    assert o["err"][1] != 0 and o["err"][2] != 0 and o["err"][3] == 0
+    compare(inp, g, o, sample=sample, attn_skip=(3,))
+    assert g["status"] == 2  # TSD_STATUS_BAD_LEN, from the attention alone
+    assert g["accept_len"][3] == o["accept_len"][3] and g["new_len"][3] > inp.prefix_len[3]
+
+
 def test_argmax_ties_across_chunks(tsd):
     """Maxima planted in several chunks of a long row: the lowest index wins;
     +0.0 and -0.0 tie; a non-multiple-of-4 vocabulary takes the scalar path."""
