@@ -57,6 +57,9 @@ struct AttnParams {
   int4 *plan_out;    // plan_mode 2: per sequence (first item, splits, chunk in key tiles, row tiles)
   int4 *plan_items;  // plan_mode 2: per block of the grid, its item (tree_attn_plan_kernel)
   uint16_t *part_o;  // fp16 partial rows [..][D]: the split's O / (l * c)
+  int part_keep;     // 1: more blocks than fit at once, so the K/V streamed after a
+                     // block's partial rows would evict them: they are stored with
+                     // an evict-last L2 policy and dropped from L2 by the merge
   float4 *part_ml;   // one per partial row: (reference max in log2 units, sum l, scale c, 0)
   uint16_t *out;
   float *lse;
@@ -1281,7 +1284,11 @@ tree_attn_split_tc(const AttnParams p, const __grid_constant__ CUtensorMap map_k
     if (!p.direct) {
       if (writer) asm volatile("bar.sync 1, %0;\n" ::"r"(nwr) : "memory");
       if (all_ok && warp == 2 && lane == 0) {
-        bulk_store(p.part_o + item_row0 * D, base + L::kStaging, (uint32_t)(nwr * D * 2));
+        if (p.part_keep)  // kept in L2 ahead of the K/V stream for the merge kernel
+          bulk_store_hint(p.part_o + item_row0 * D, base + L::kStaging, (uint32_t)(nwr * D * 2),
+                          l2_policy_evict_last());
+        else
+          bulk_store(p.part_o + item_row0 * D, base + L::kStaging, (uint32_t)(nwr * D * 2));
         bulk_wait_read();
       }
     }
@@ -1808,7 +1815,11 @@ tree_attn_split_dual(const AttnParams p, const __grid_constant__ CUtensorMap map
     if (!p.direct) {
       asm volatile("bar.sync 1, 128;\n" ::: "memory");
       if (all_ok && warp == 2 && lane == 0) {
-        bulk_store(p.part_o + item_row0 * D, base + L::kStaging, (uint32_t)(kTcBM * D * 2));
+        if (p.part_keep)
+          bulk_store_hint(p.part_o + item_row0 * D, base + L::kStaging, (uint32_t)(kTcBM * D * 2),
+                          l2_policy_evict_last());
+        else
+          bulk_store(p.part_o + item_row0 * D, base + L::kStaging, (uint32_t)(kTcBM * D * 2));
         bulk_wait_read();
       }
     }
@@ -1839,7 +1850,8 @@ tree_attn_split_dual(const AttnParams p, const __grid_constant__ CUtensorMap map
 // of split (l / (D/8)) + round * 32/(D/8).  Every load of every round is
 // issued before any is used, so the merge costs one memory round trip; lanes
 // holding the same chunk for different splits are then summed by shuffles.
-template <int D, int R>  // R: rounds of loads per batch (R * 32 / (D/8) splits)
+// kDrop: the partials were kept in L2 (part_keep) and are dropped once read.
+template <int D, int R, bool kDrop>  // R: rounds of loads per batch (R * 32 / (D/8) splits)
 __global__ void __launch_bounds__(256) tree_attn_combine_kernel(const AttnParams p, int B) {
   constexpr int kChunks = D / 8;            // 16-byte chunks of a partial row
   constexpr int kPerRound = 32 / kChunks;   // splits covered by one warp-wide load
@@ -1922,6 +1934,11 @@ __global__ void __launch_bounds__(256) tree_attn_combine_kernel(const AttnParams
           acc[2 * k] += f.x * ws;
           acc[2 * k + 1] += f.y * ws;
         }
+        // this row's 128-byte lines of split sp are read by no one else: kept
+        // partials are dropped from L2 without a write-back (by the lane
+        // holding a line's first chunk)
+        if (kDrop && (pc & 7) == 0)
+          sm100::discard_l2_line(p.part_o + (r0 + (size_t)sp * stride) * D + pc * 8);
       }
     }
     s0 += R * kPerRound;
@@ -1949,9 +1966,14 @@ cudaError_t launch_combine(const AttnParams &p, int B, cudaStream_t s) {
   // one batch for the uniform split's count; under the device plan (counts
   // known on the device only) batches of four rounds
   const int rounds = p.plan_mode == 2 ? 4 : (p.splits + kPerRound - 1) / kPerRound;
-  if (rounds <= 4) return launch(tree_attn_combine_kernel<D, 4>, grid, dim3(256), 0, s, p, B);
-  if (rounds <= 8) return launch(tree_attn_combine_kernel<D, 8>, grid, dim3(256), 0, s, p, B);
-  return launch(tree_attn_combine_kernel<D, 32 / kPerRound>, grid, dim3(256), 0, s, p, B);
+  if (p.part_keep) {
+    if (rounds <= 4) return launch(tree_attn_combine_kernel<D, 4, true>, grid, dim3(256), 0, s, p, B);
+    if (rounds <= 8) return launch(tree_attn_combine_kernel<D, 8, true>, grid, dim3(256), 0, s, p, B);
+    return launch(tree_attn_combine_kernel<D, 32 / kPerRound, true>, grid, dim3(256), 0, s, p, B);
+  }
+  if (rounds <= 4) return launch(tree_attn_combine_kernel<D, 4, false>, grid, dim3(256), 0, s, p, B);
+  if (rounds <= 8) return launch(tree_attn_combine_kernel<D, 8, false>, grid, dim3(256), 0, s, p, B);
+  return launch(tree_attn_combine_kernel<D, 32 / kPerRound, false>, grid, dim3(256), 0, s, p, B);
 }
 
 struct AttnPlan {
@@ -2191,6 +2213,10 @@ static int attn_fwd_impl(const uint16_t *q, const uint16_t *k_cache, const uint1
   p.plan_items = a.mode == 2 ? p.plan_out + B : nullptr;
   p.B = B;
   p.plan_mode = a.mode;
+  // blocks beyond one resident wave (the two-blocks-per-SM kernel fits two per
+  // SM); under the device plan, the host's uniform guess of the item count
+  p.part_keep = !a.direct && (long)a.row_tiles * a.splits * B * Hkv >
+                                 (long)sm_count() * (a.dual ? 2 : 1);
   p.nsm = sm_count() * (a.dual ? 2 : 1);  // block slots the plan spreads items over
   p.grid_items = (int)a.grid_items;
   p.out = out;

@@ -124,6 +124,26 @@ __device__ __forceinline__ void bulk_store(void *gdst, uint32_t ssrc, uint32_t b
                : "memory");
   asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
 }
+// L2 policy that evicts the lines it covers after lines of normal priority.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(pol));
+  return pol;
+}
+// bulk_store with an L2 cache policy for the written lines.
+__device__ __forceinline__ void bulk_store_hint(void *gdst, uint32_t ssrc, uint32_t bytes,
+                                                uint64_t policy) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;\n" ::"l"(
+                   gdst),
+               "r"(ssrc), "r"(bytes), "l"(policy)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+}
+// Drops the 128-byte L2 line at p (128-byte aligned) without writing it back:
+// for data that no one will read again.
+__device__ __forceinline__ void discard_l2_line(const void *p) {
+  asm volatile("discard.global.L2 [%0], 128;\n" ::"l"(p) : "memory");
+}
 __device__ __forceinline__ void bulk_wait() {
   asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
 }
