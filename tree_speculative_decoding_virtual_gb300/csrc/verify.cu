@@ -180,7 +180,10 @@ verify_greedy_kernel(const float *__restrict__ logits, const int32_t *__restrict
       const int x1 = (int)(lo - end0);          // ... and in row r0 + 1 (negative)
       constexpr int kStride = kBatch * kThreads;
       const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-      // passes of kBatch independent loads per thread
+      // passes of kBatch independent loads per thread; once a pass's loads
+      // are issued, one thread asks the copy engine to pull the next pass into
+      // L2 (inside a verify step the stream then holds its rate against the
+      // write-backs of the attention that ran before it)
       float4 a[kBatch];
       for (int p4 = 0; p4 < n4; p4 += kStride) {
 #pragma unroll
@@ -188,6 +191,8 @@ verify_greedy_kernel(const float *__restrict__ logits, const int32_t *__restrict
           const int q = p4 + u * kThreads + t;
           a[u] = q < n4 ? __ldcs(src + q) : ninf;
         }
+        if (t == 0 && p4 + kStride < n4)
+          bulk_prefetch_l2(src + p4 + kStride, (uint32_t)min(kStride, n4 - p4 - kStride) * 16u);
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
           const int q = p4 + u * kThreads + t;
