@@ -226,6 +226,28 @@ def test_two_blocks_per_sm_path(tsd, D, N, Hq, Hkv):
     assert g["status"] == 0
 
 
+def test_multi_wave_partials_kept_in_l2(tsd):
+    """More blocks than fit at once (80 sequences, three pieces per key
+    range): the partials are stored with an evict-last L2 policy and the
+    merge kernel drops each line once it has read it, so every row of every
+    piece must still be read before its line goes.  All rows against the
+    oracle."""
+    import torch
+    rng = np.random.default_rng(8080)
+    prefix = rng.integers(4300, 4990, size=80)
+    inp = gen.random_small(8080, B=80, N_max=6, Hq=4, Hkv=2, D=64, V=40, prefix_lo=0,
+                           prefix_hi=1, max_depth=4, prefix_len=prefix)
+    max_slots = int((inp.prefix_len + inp.n_nodes).max())
+    plan = tsd.tree_attn_plan(inp.B, inp.N_max, inp.Hq, inp.Hkv, inp.D, max_slots)
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    assert plan["mode"] == 1 and plan["direct"] == 0 and plan["two_blocks_per_sm"] == 1, plan
+    assert plan["grid_blocks"] > 2 * nsm, plan
+    g = run_gpu(tsd, inp, max_slots=max_slots)
+    o = run_oracle(inp)
+    compare(inp, g, o)
+    assert g["status"] == 0
+
+
 def test_attention_launch_count(tsd):
     """The launch count the library reports: split + merge, plus the plan
     kernel for ragged-capable batches with long blocks, and a single launch
