@@ -352,6 +352,37 @@ def bastion_marginals(seed: Optional[int] = None):
     return q, root
 
 
+def shaped_marginals(seed: int, B: int, K: int, V: int, shape: str):
+    """Draft marginals q[B][K][V] (fp32) of one of several shapes, for
+    best-first trees of different forms: "sharp" (softmax of 4 z: deep,
+    narrow trees), "flat" (softmax of 0.3 z: wide and deep), "tied" (softmax
+    of round(2 z): many equal probabilities), "pow2" (every probability a power
+    of two: many equal path scores), "dominant" (token 0 raised by 6: long
+    chains), "tiny_tail" (token 0 at 1/2, the rest of the mass 1e-7 spread
+    over the others: path scores spanning more than 2^53).  z ~ N(0, 1);
+    softmax in fp64, rounded once to fp32.  Also returns uniform root tokens."""
+    rng = np.random.default_rng(seed)
+    z = rng.standard_normal(size=(B, K, V))
+    if shape == "sharp":
+        z = 4.0 * z
+    elif shape == "flat":
+        z = 0.3 * z
+    elif shape == "tied":
+        z = np.round(2.0 * z)
+    elif shape == "dominant":
+        z[..., 0] += 6.0
+    elif shape not in ("pow2", "tiny_tail"):
+        raise ValueError(shape)
+    e = np.exp(z - z.max(axis=-1, keepdims=True))
+    q = e / e.sum(axis=-1, keepdims=True)
+    if shape == "pow2":
+        q = np.exp2(np.round(np.log2(q)))
+    if shape == "tiny_tail":
+        q = np.where(np.arange(V) == 0, 0.5, 1e-7 * q / max(V - 1, 1))
+    root = rng.integers(0, V, size=B).astype(np.int32)
+    return q.astype(np.float32), root
+
+
 def dynamic_draft_rows(seed: int, b: int, pool_ids, V: int, temp: float = 1.0) -> np.ndarray:
     """Stand-in for a drafter's per-node output in dynamic-tree construction:
     the row of node (b, pool id) is softmax(z / temp), z ~ N(0,1) drawn from

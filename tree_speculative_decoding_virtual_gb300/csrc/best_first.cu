@@ -18,7 +18,8 @@
 // rank at the next position); the child ranks of a node are consumed in
 // order because q is sorted.  Each step takes the best candidate with two
 // warp max-reductions (rho bits, then (depth, parent) as a tie key) over
-// candidate keys held in shared memory.
+// candidate keys held in shared memory, together with the run of its
+// next-ranked siblings that beat every other candidate.
 
 //
 // Dynamic draft trees ("Speculative Decoding Hierarquico: Medusa, EAGLE-2 e
@@ -192,12 +193,34 @@ __device__ __forceinline__ unsigned long long child_key(int node, float rho_node
          (unsigned long long)(((unsigned)(255 - d) << 16) | (unsigned)(0xFFFF - node));
 }
 
+__device__ __forceinline__ unsigned long long max_u64(unsigned long long a, unsigned long long b) {
+  return a > b ? a : b;
+}
+
+// Largest 64-bit key over the warp: two 32-bit max reductions (high word,
+// then the low word among the lanes holding that high word).
+__device__ __forceinline__ unsigned long long warp_max_key(unsigned long long k) {
+  const unsigned hi = (unsigned)(k >> 32), lo = (unsigned)k;
+  const unsigned H = __reduce_max_sync(0xffffffffu, hi);
+  const unsigned L = __reduce_max_sync(0xffffffffu, hi == H ? lo : 0u);
+  return ((unsigned long long)H << 32) | L;
+}
+
 // One warp per sequence.  Every inserted node owns one candidate key in
-// shared memory; per step each lane reduces the keys of its nodes, two warp
-// max-reductions pick the winner, and lane 0 alone inserts it: the new node's
-// state and both changed candidate keys are written with plain shared-memory
-// stores, so a step is one short dependent chain.  Outputs are written at the
-// end, coalesced.
+// shared memory (its best remaining child).  A step takes the best candidate,
+// a child (p, r) of node p at depth d, and with it the longest run of p's
+// next-ranked children (p, r+1), (p, r+2), ... that still beat every other
+// candidate: the best key outside p's slot, and the first child of (p, r),
+// which is the best of the run's own first children (their path scores do not
+// increase along the run and a later node loses ties on its parent index).
+// Inserting the run in one step therefore gives the order of one-at-a-time
+// insertion.  Lane i tests (p, r+i); the run is the ballot's leading ones.
+// A_hat, the fp64 sum of the non-root path scores in insertion order, is
+// order-independent when every partial sum is exact: all terms are multiples
+// of 2^b (b the lowest set bit over the terms) and the sum stays below
+// 2^(e+9) (e the largest term's exponent, at most 255 terms), so
+// e + 9 - b <= 53 makes every addition exact and the warp adds in any order;
+// otherwise lane 0 adds in insertion order.
 __global__ void __launch_bounds__(kExpandThreads)
 expand_kernel(const int32_t *__restrict__ top_tok, const float *__restrict__ top_q,
               const int32_t *__restrict__ root_token, int K, int M, int N,
@@ -213,9 +236,30 @@ expand_kernel(const int32_t *__restrict__ top_tok, const float *__restrict__ top
   pdl_trigger();
   pdl_wait();
   const int b = blockIdx.x, t = threadIdx.x;
-  for (int x = t; x < K * M; x += kExpandThreads) {
-    s_tq[x] = top_q[(size_t)b * K * M + x];
-    s_tt[x] = top_tok[(size_t)b * K * M + x];
+  {
+    // the ranked lists, eight loads of each kind in flight per thread
+    constexpr int kU = 8;
+    const int KM = K * M;
+    const float *gq = top_q + (size_t)b * KM;
+    const int32_t *gt = top_tok + (size_t)b * KM;
+    for (int x0 = t; x0 < KM; x0 += kU * kExpandThreads) {
+      float qv[kU];
+      int32_t tv[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int x = x0 + u * kExpandThreads;
+        qv[u] = x < KM ? __ldg(gq + x) : 0.f;
+        tv[u] = x < KM ? __ldg(gt + x) : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int x = x0 + u * kExpandThreads;
+        if (x < KM) {
+          s_tq[x] = qv[u];
+          s_tt[x] = tv[u];
+        }
+      }
+    }
   }
   for (int x = t; x < kMaxNodes; x += kExpandThreads) {
     s_key[x] = 0ull;
@@ -228,7 +272,6 @@ expand_kernel(const int32_t *__restrict__ top_tok, const float *__restrict__ top
   __syncthreads();
   if (t >= 32) return;
   const int lane = t;
-  double a_hat = 0.0;  // lane 0: sum of non-root rho in insertion order
   if (lane == 0) {
     s_rho[0] = 1.f;
     s_tok[0] = root_token[b];
@@ -236,43 +279,91 @@ expand_kernel(const int32_t *__restrict__ top_tok, const float *__restrict__ top
   }
   __syncwarp();
 
-  int filled = N;
-  for (int n = 1; n < N; ++n) {
-    unsigned long long best = 0ull;
+  int n = 1;
+  for (int step = 1; n < N && step < N; ++step) {  // a step inserts at least one node
+    unsigned long long k[kPerLane];
 #pragma unroll
-    for (int j = 0; j < kPerLane; ++j) {
-      const unsigned long long k = s_key[lane + 32 * j];
-      best = k > best ? k : best;
-    }
-    const unsigned bh = (unsigned)(best >> 32), bl = (unsigned)best;
-    const unsigned H = __reduce_max_sync(0xffffffffu, bh);
-    const unsigned Lo = __reduce_max_sync(0xffffffffu, bh == H ? bl : 0u);
-    if (H == 0u && Lo == 0u) {  // no valid node left (host checks make this unreachable)
-      filled = n;
-      break;
+    for (int j = 0; j < kPerLane; ++j) k[j] = s_key[lane + 32 * j];
+    const unsigned long long best =
+        warp_max_key(max_u64(max_u64(max_u64(k[0], k[1]), max_u64(k[2], k[3])),
+                             max_u64(max_u64(k[4], k[5]), max_u64(k[6], k[7]))));
+    if (best == 0ull) break;  // no valid node left (host checks make this unreachable)
+    const int p = 0xFFFF - (int)(best & 0xFFFFu);
+    const int d = 255 - (int)((best >> 16) & 0xFFu);
+    // the best key outside p's slot
+#pragma unroll
+    for (int j = 0; j < kPerLane; ++j) k[j] = lane + 32 * j == p ? 0ull : k[j];
+    const unsigned long long k2 =
+        warp_max_key(max_u64(max_u64(max_u64(k[0], k[1]), max_u64(k[2], k[3])),
+                             max_u64(max_u64(k[4], k[5]), max_u64(k[6], k[7]))));
+    const int r = s_nch[p];
+    const float rp = s_rho[p];
+    const float *q_row = s_tq + (d - 1) * M;
+    // the first child of (p, r), the run's first node
+    const unsigned long long fc0 =
+        child_key(n, __uint_as_float((unsigned)(best >> 32)), d, 0, s_tq, K, M, N);
+    const unsigned long long bound = max_u64(k2, fc0);
+    const int ri = r + lane;
+    const bool ok = ri < M && n + lane < N;
+    float rc = 0.f;
+    if (ok) rc = __fmul_rn(rp, q_row[ri]);
+    const unsigned long long key =
+        ok ? ((unsigned long long)__float_as_uint(rc) << 32) |
+                 (unsigned long long)(((unsigned)(255 - d) << 16) | (unsigned)(0xFFFF - p))
+           : 0ull;
+    const unsigned pass = __ballot_sync(0xffffffffu, key > bound);
+    const int run = ~pass ? __ffs(~pass) - 1 : 32;  // lane 0 (the best key) always passes
+    if (run == 0) break;
+    if (lane < run) {
+      const int node = n + lane;
+      s_par[node] = p;
+      s_tok[node] = s_tt[(d - 1) * M + ri];
+      s_dep[node] = d;
+      s_rho[node] = rc;
+      s_key[node] = child_key(node, rc, d, 0, s_tq, K, M, N);
     }
     if (lane == 0) {
-      const int p = 0xFFFF - (int)(Lo & 0xFFFFu);
-      const int d = 255 - (int)((Lo >> 16) & 0xFFu);
-      const float rn = __uint_as_float(H);
-      const int r = s_nch[p];
-      s_nch[p] = r + 1;
-      s_key[p] = child_key(p, s_rho[p], s_dep[p], r + 1, s_tq, K, M, N);
-      s_par[n] = p;
-      s_tok[n] = s_tt[(d - 1) * M + r];
-      s_dep[n] = d;
-      s_rho[n] = rn;
-      s_key[n] = child_key(n, rn, d, 0, s_tq, K, M, N);
-      a_hat += (double)rn;
+      s_nch[p] = r + run;
+      s_key[p] = child_key(p, rp, d - 1, r + run, s_tq, K, M, N);
     }
+    n += run;
     __syncwarp();
   }
-  for (int n = lane; n < N; n += 32) {
-    const bool ok = n < filled;
-    parent[(size_t)b * N + n] = ok ? s_par[n] : -1;
-    tokens[(size_t)b * N + n] = ok ? s_tok[n] : -1;
-    depth[(size_t)b * N + n] = ok ? s_dep[n] : 0;
-    rho[(size_t)b * N + n] = ok ? s_rho[n] : 0.f;
+  const int filled = n;
+
+  // A_hat
+  int e_max = -1000, b_min = 1000;
+  double part = 0.0;
+  for (int x = 1 + lane; x < filled; x += 32) {
+    const float v = s_rho[x];
+    const unsigned u = __float_as_uint(v) & 0x7FFFFFFFu;
+    part += (double)v;
+    if (u == 0u) continue;
+    const int e = (int)(u >> 23), m = (int)(u & 0x7FFFFFu);
+    const int sig = e ? (m | 0x800000) : m;
+    const int lo = (e ? e - 150 : -149) + __ffs(sig) - 1;
+    const int ex = e ? e - 127 : -149 + (31 - __clz(m));
+    e_max = ex > e_max ? ex : e_max;
+    b_min = lo < b_min ? lo : b_min;
+  }
+  e_max = __reduce_max_sync(0xffffffffu, e_max);
+  b_min = __reduce_min_sync(0xffffffffu, b_min);
+  double a_hat;
+  if (e_max == -1000 || e_max + 9 - b_min <= 53) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+    a_hat = part;
+  } else {
+    a_hat = 0.0;
+    if (lane == 0)
+      for (int x = 1; x < filled; ++x) a_hat += (double)s_rho[x];
+  }
+  for (int x = lane; x < N; x += 32) {
+    const bool ok = x < filled;
+    parent[(size_t)b * N + x] = ok ? s_par[x] : -1;
+    tokens[(size_t)b * N + x] = ok ? s_tok[x] : -1;
+    depth[(size_t)b * N + x] = ok ? s_dep[x] : 0;
+    rho[(size_t)b * N + x] = ok ? s_rho[x] : 0.f;
   }
   if (lane == 0) ahat[b] = a_hat;
 }
