@@ -158,12 +158,22 @@ def _code_only(text):
     return " ".join("".join(out).split())
 
 
-def kernel_sources_digest():
+# The sources each profiled kernel is built from (its translation unit and the
+# headers that unit includes); a kernel's profile figures are tied to these.
+KERNEL_SOURCES = {
+    "tree_attn_fwd": ["attention.cu", "sm100_ptx.cuh", "tsd_common.cuh"],
+    "tree_verify_greedy": ["verify.cu", "commit_core.cuh", "sm100_ptx.cuh", "tsd_common.cuh"],
+}
+
+
+def kernel_sources_digest(kernel_key=None):
     """Digest of the CUDA sources' code (comments and layout ignored), so
-    profile figures stay attached to the kernels they were taken on."""
+    profile figures stay attached to the kernels they were taken on: of the
+    sources of one profiled kernel (KERNEL_SOURCES), or of every source."""
     csrc = os.path.join(ROOT, "tree_speculative_decoding_virtual_gb300", "csrc")
+    names = sorted(KERNEL_SOURCES[kernel_key] if kernel_key else os.listdir(csrc))
     h = hashlib.sha256()
-    for f in sorted(os.listdir(csrc)):
+    for f in names:
         with open(os.path.join(csrc, f), encoding="utf-8") as fh:
             h.update(f.encode() + b"\0" + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
@@ -171,7 +181,7 @@ def kernel_sources_digest():
 
 def ncu_traffic(kernel_key, workload):
     """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
-    the current kernel sources."""
+    the kernel's current sources."""
     path = os.path.join(ROOT, "profiles", "traffic_%s_%s.md" % (kernel_key, workload))
     try:
         text = open(path).read()
@@ -179,7 +189,7 @@ def ncu_traffic(kernel_key, workload):
         return None
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
     d = re.search(r"kernel_sources_sha256_16:\s*([0-9a-f]+)", text)
-    if not m or not d or d.group(1) != kernel_sources_digest():
+    if not m or not d or d.group(1) != kernel_sources_digest(kernel_key):
         return None
     return float(m.group(1))
 

@@ -359,8 +359,9 @@ def shaped_marginals(seed: int, B: int, K: int, V: int, shape: str):
     of round(2 z): many equal probabilities), "pow2" (every probability a power
     of two: many equal path scores), "dominant" (token 0 raised by 6: long
     chains), "tiny_tail" (token 0 at 1/2, the rest of the mass 1e-7 spread
-    over the others: path scores spanning more than 2^53).  z ~ N(0, 1);
-    softmax in fp64, rounded once to fp32.  Also returns uniform root tokens."""
+    over the others: path scores spanning more than 2^53), "uniform" (every
+    probability 1/V: every rank a tie).  z ~ N(0, 1); softmax in fp64, rounded
+    once to fp32.  Also returns uniform root tokens."""
     rng = np.random.default_rng(seed)
     z = rng.standard_normal(size=(B, K, V))
     if shape == "sharp":
@@ -371,6 +372,8 @@ def shaped_marginals(seed: int, B: int, K: int, V: int, shape: str):
         z = np.round(2.0 * z)
     elif shape == "dominant":
         z[..., 0] += 6.0
+    elif shape == "uniform":
+        z = np.zeros_like(z)
     elif shape not in ("pow2", "tiny_tail"):
         raise ValueError(shape)
     e = np.exp(z - z.max(axis=-1, keepdims=True))

@@ -53,9 +53,19 @@ def test_digest_ignores_comments_but_not_code(tree):
 def test_traffic_lookup_follows_the_digest(tree):
     prof = tree / "profiles" / "traffic_tree_attn_fwd_8b.md"
     prof.write_text("traffic_bytes_per_launch: 123456\nkernel_sources_sha256_16: %s\n"
-                    % bench.kernel_sources_digest())
+                    % bench.kernel_sources_digest("tree_attn_fwd"))
+    assert bench.ncu_traffic("tree_attn_fwd", "8b") == 123456.0
+    # another kernel's source does not detach the attention figures
+    _edit(tree, "best_first.cu", lambda s: s + "\nstatic int other_kernel = 3;\n")
     assert bench.ncu_traffic("tree_attn_fwd", "8b") == 123456.0
     _edit(tree, "attention.cu", lambda s: s + "\nstatic int changed_code = 2;\n")
     assert bench.ncu_traffic("tree_attn_fwd", "8b") is None
     assert bench.ncu_traffic("tree_attn_fwd", "70b") is None  # no file
+
+
+def test_kernel_sources_exist():
+    csrc = os.path.join(bench.ROOT, "tree_speculative_decoding_virtual_gb300", "csrc")
+    for key, names in bench.KERNEL_SOURCES.items():
+        for n in names:
+            assert os.path.isfile(os.path.join(csrc, n)), (key, n)
 

@@ -2,8 +2,10 @@
 the oracle, bit for bit (parent, tokens, depth, rho, A_hat), on marginals of
 several shapes: deep and narrow, wide, many equal probabilities, powers of
 two (many equal path scores), long chains, path scores spanning more than
-2^53 (A_hat then has to be summed in insertion order), the largest number of
-positions, vocabularies smaller than the budget, and the smallest budgets."""
+2^53 (A_hat then has to be summed in insertion order), uniform rows (every
+rank a tie), the largest number of positions, vocabularies smaller than the
+budget, the smallest budgets, and rows longer than the shared-memory-staged
+top-M kernel takes."""
 
 import numpy as np
 import pytest
@@ -51,6 +53,11 @@ CASES = [
     ("flat", 19, 3, 4, 5, 2),
     ("flat", 20, 3, 4, 5, 1),
     ("dominant", 21, 4, 16, 32000, 64),
+    ("uniform", 22, 2, 4, 32000, 256),  # more ties at the filter's threshold than it keeps
+    ("uniform", 23, 2, 3, 1500, 100),   # every candidate tied: the select reaches the index bits
+    ("flat", 24, 2, 5, 40961, 64),      # a row longer than the staged kernel takes
+    ("sharp", 25, 2, 6, 500, 65),       # 64 ranked tokens: two full runs of the final sort
+    ("tied", 26, 2, 4, 1000, 33),       # 32 ranked tokens: one full run
 ]
 
 

@@ -7,12 +7,15 @@
 // adds the valid node with the largest rho.
 //
 // Kernel 1 (one block per (position, sequence)): the M = min(N-1, V) best
-// tokens of the position, ranked by (q desc, token id asc).  A threshold
+// tokens of the position, ranked by (q desc, token id asc).  Rows that fit in
+// shared memory: the staged threshold filter (topk_stage_kernel: the row
+// staged once, a threshold from the warps' sorted thread maxima, a radix
+// select over the candidates, warp-run sorts).  Longer rows: the threshold
 // filter (topk_filter_kernel: the M-th best of the threads' best keys bounds
 // the row's M-th best from below; a second pass keeps the keys above it; a
-// bitonic sort ranks them), with a 4-pass 8-bit radix select as the fallback
-// (radix_topk_block: the M-th largest key, a coalesced gather, a bitonic sort,
-// ties at the threshold beyond the budget resolved in index order).
+// bitonic sort ranks them).  Both fall back to a 4-pass 8-bit radix select
+// (radix_topk_block: the M-th largest key, a coalesced gather, a bitonic
+// sort, ties at the threshold beyond the budget resolved in index order).
 // Kernel 2 (one block per sequence, one warp expanding): every inserted node
 // owns exactly one candidate, its best not-yet-inserted child (the next
 // rank at the next position); the child ranks of a node are consumed in
@@ -25,12 +28,13 @@
 // Dynamic draft trees ("Speculative Decoding Hierarquico: Medusa, EAGLE-2 e
 // Multi-Token Prediction", EAGLE-2 section: deep where the drafter is
 // confident, wide where it is not), built level by level with the path score
-// above as node confidence: each frontier node's top-k tokens (topk_kernel on
+// above as node confidence: each frontier node's top-k tokens (a5's top-M kernels on
 // its draft row) become its children; one block per sequence scores them,
 // writes them to the node pool and keeps the level's k best as the next
 // frontier (bitonic sort in shared memory); the rerank kernel keeps the N-1
 // best pool nodes, in rank order, with parents re-indexed.
 
+#include "sm100_ptx.cuh"
 #include "tsd_common.cuh"
 
 namespace tsd {
@@ -237,8 +241,9 @@ expand_kernel(const int32_t *__restrict__ top_tok, const float *__restrict__ top
   pdl_wait();
   const int b = blockIdx.x, t = threadIdx.x;
   {
-    // the ranked lists, eight loads of each kind in flight per thread
-    constexpr int kU = 8;
+    // the ranked lists, sixteen loads of each kind in flight per thread (one
+    // round trip for K * M <= 4096)
+    constexpr int kU = 16;
     const int KM = K * M;
     const float *gq = top_q + (size_t)b * KM;
     const int32_t *gt = top_tok + (size_t)b * KM;
@@ -331,13 +336,13 @@ expand_kernel(const int32_t *__restrict__ top_tok, const float *__restrict__ top
   }
   const int filled = n;
 
-  // A_hat
+  // A_hat.  When the sum is exact (e_max + 9 - b_min <= 53) every term is an
+  // integer multiple of 2^b_min and the total below 2^53 of them: the terms
+  // are added as 64-bit integers (the warp's fp64 pipe is slow on this part)
+  // and the total scaled once; otherwise lane 0 adds in insertion order.
   int e_max = -1000, b_min = 1000;
-  double part = 0.0;
   for (int x = 1 + lane; x < filled; x += 32) {
-    const float v = s_rho[x];
-    const unsigned u = __float_as_uint(v) & 0x7FFFFFFFu;
-    part += (double)v;
+    const unsigned u = __float_as_uint(s_rho[x]) & 0x7FFFFFFFu;
     if (u == 0u) continue;
     const int e = (int)(u >> 23), m = (int)(u & 0x7FFFFFu);
     const int sig = e ? (m | 0x800000) : m;
@@ -348,15 +353,26 @@ expand_kernel(const int32_t *__restrict__ top_tok, const float *__restrict__ top
   }
   e_max = __reduce_max_sync(0xffffffffu, e_max);
   b_min = __reduce_min_sync(0xffffffffu, b_min);
-  double a_hat;
-  if (e_max == -1000 || e_max + 9 - b_min <= 53) {
+  double a_hat = 0.0;
+  if (e_max == -1000) {
+    // every term zero
+  } else if (e_max + 9 - b_min <= 53) {
+    long long part = 0;
+    for (int x = 1 + lane; x < filled; x += 32) {
+      const unsigned w = __float_as_uint(s_rho[x]);
+      const unsigned u = w & 0x7FFFFFFFu;
+      if (u == 0u) continue;
+      const int e = (int)(u >> 23), m = (int)(u & 0x7FFFFFu);
+      const long long sig = e ? (m | 0x800000) : m;
+      const int sh = (e ? e - 150 : -149) - b_min;  // term = sig * 2^sh, sh >= -(trailing zeros)
+      const long long term = sh >= 0 ? sig << sh : sig >> -sh;
+      part += (w >> 31) ? -term : term;
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-    a_hat = part;
-  } else {
-    a_hat = 0.0;
-    if (lane == 0)
-      for (int x = 1; x < filled; ++x) a_hat += (double)s_rho[x];
+    a_hat = ldexp((double)part, b_min);
+  } else if (lane == 0) {
+    for (int x = 1; x < filled; ++x) a_hat += (double)s_rho[x];
   }
   for (int x = lane; x < N; x += 32) {
     const bool ok = x < filled;
@@ -561,23 +577,42 @@ topk_filter_kernel(const float *__restrict__ q, int K, int V, int M, int32_t *__
   const float4 *row4 = reinterpret_cast<const float4 *>(row);
   const int V4 = V >> 2;
   unsigned long long best = 0ull;
+  // eight loads per thread issued before any is used
+  constexpr int kU = 8;
   if (vec) {
-#pragma unroll 8
-    for (int x4 = t; x4 < V4; x4 += kFiltThreads) {
-      const float4 v = __ldg(row4 + x4);
-      const int x = 4 * x4;
-      unsigned long long k0 = key2(v.x, x), k1 = key2(v.y, x + 1), k2 = key2(v.z, x + 2),
-                         k3 = key2(v.w, x + 3);
-      k0 = k1 > k0 ? k1 : k0;
-      k2 = k3 > k2 ? k3 : k2;
-      k0 = k2 > k0 ? k2 : k0;
-      best = k0 > best ? k0 : best;
+    for (int x0 = t; x0 < V4; x0 += kU * kFiltThreads) {
+      float4 v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u)
+        if (x0 + u * kFiltThreads < V4) v[u] = __ldg(row4 + x0 + u * kFiltThreads);
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int x4 = x0 + u * kFiltThreads;
+        if (x4 < V4) {
+          const int x = 4 * x4;
+          unsigned long long k0 = key2(v[u].x, x), k1 = key2(v[u].y, x + 1),
+                             k2 = key2(v[u].z, x + 2), k3 = key2(v[u].w, x + 3);
+          k0 = k1 > k0 ? k1 : k0;
+          k2 = k3 > k2 ? k3 : k2;
+          k0 = k2 > k0 ? k2 : k0;
+          best = k0 > best ? k0 : best;
+        }
+      }
     }
   } else {
-#pragma unroll 8
-    for (int x = t; x < V; x += kFiltThreads) {
-      const unsigned long long key = key2(__ldg(row + x), x);
-      best = key > best ? key : best;
+    for (int x0 = t; x0 < V; x0 += kU * kFiltThreads) {
+      float v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u)
+        if (x0 + u * kFiltThreads < V) v[u] = __ldg(row + x0 + u * kFiltThreads);
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int x = x0 + u * kFiltThreads;
+        if (x < V) {
+          const unsigned long long key = key2(v[u], x);
+          best = key > best ? key : best;
+        }
+      }
     }
   }
   s_best[t] = best;
@@ -592,18 +627,33 @@ topk_filter_kernel(const float *__restrict__ q, int K, int V, int M, int32_t *__
     }
   };
   if (vec) {
-#pragma unroll 4
-    for (int x4 = t; x4 < V4; x4 += kFiltThreads) {
-      const float4 v = __ldg(row4 + x4);
-      const int x = 4 * x4;
-      offer(key2(v.x, x));
-      offer(key2(v.y, x + 1));
-      offer(key2(v.z, x + 2));
-      offer(key2(v.w, x + 3));
+    for (int x0 = t; x0 < V4; x0 += kU * kFiltThreads) {
+      float4 v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u)
+        if (x0 + u * kFiltThreads < V4) v[u] = __ldg(row4 + x0 + u * kFiltThreads);
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int x4 = x0 + u * kFiltThreads;
+        if (x4 < V4) {
+          const int x = 4 * x4;
+          offer(key2(v[u].x, x));
+          offer(key2(v[u].y, x + 1));
+          offer(key2(v[u].z, x + 2));
+          offer(key2(v[u].w, x + 3));
+        }
+      }
     }
   } else {
-#pragma unroll 4
-    for (int x = t; x < V; x += kFiltThreads) offer(key2(__ldg(row + x), x));
+    for (int x0 = t; x0 < V; x0 += kU * kFiltThreads) {
+      float v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u)
+        if (x0 + u * kFiltThreads < V) v[u] = __ldg(row + x0 + u * kFiltThreads);
+#pragma unroll
+      for (int u = 0; u < kU; ++u)
+        if (x0 + u * kFiltThreads < V) offer(key2(v[u], x0 + u * kFiltThreads));
+    }
   }
   __syncthreads();
   const int n = (int)s_count;
@@ -623,10 +673,292 @@ topk_filter_kernel(const float *__restrict__ q, int K, int V, int M, int32_t *__
   }
 }
 
-// Ranked top M of every row of q [B][K][V]: the threshold filter, or the
-// radix select for M >= kFiltThreads.
+// The threshold filter with the row staged in shared memory (rows of at most
+// kStageMaxV floats): one block of 1024 threads per row.
+//  1. The row is read once (16-byte loads) and kept in shared memory; each
+//     thread keeps the largest of its values (NaN ignored).
+//  2. Each warp sorts its 32 thread maxima (shuffles) and takes the
+//     ceil(M/32)-th; tau, the least of the warps' values, has at least M
+//     non-NaN elements at or above it, so every one of the M best (by order
+//     key, index) passes !(v < tau) (NaN always passes).
+//  3. The passing elements become 64-bit keys (order key, 0xFFFFFFFF - index)
+//     in a candidate list, appended a warp at a time (one atomic per warp).
+//  4. A radix select over the candidates (8-bit digits from the top, ending
+//     once the digit's bin is taken whole) keeps exactly the M largest keys.
+//  5. The kept keys are sorted in runs of 32 (one warp each, shuffles); a key's
+//     rank is its place in its run plus, for every other run, the number of
+//     its keys above it (binary search).
+// More candidates than kStageCap (many ties at tau) fall back to the radix
+// select over the row.
+constexpr int kStageThreads = 1024;
+constexpr int kStageWarps = kStageThreads / 32;
+constexpr int kStageMaxV = 40960;  // 160 KB of staged row
+constexpr int kStageCap = 2048;
+constexpr int kStageMaxM = 511;
+
+// Bitonic sort of one key per lane across the warp, descending.
+template <typename T>
+__device__ __forceinline__ T warp_sort_desc(T x, int lane) {
+#pragma unroll
+  for (int kk = 2; kk <= 32; kk <<= 1) {
+#pragma unroll
+    for (int j = kk >> 1; j > 0; j >>= 1) {
+      const T y = __shfl_xor_sync(0xffffffffu, x, j);
+      const bool take_max = ((lane & kk) == 0) == ((lane & j) == 0);
+      x = take_max ? (x > y ? x : y) : (x < y ? x : y);
+    }
+  }
+  return x;
+}
+
+__global__ void __launch_bounds__(kStageThreads)
+topk_stage_kernel(const float *__restrict__ q, int K, int V, int M, int32_t *__restrict__ top_tok,
+                  float *__restrict__ top_q, unsigned long long wait_limit_ns) {
+  extern __shared__ __align__(16) float s_row[];  // [V]
+  __shared__ unsigned long long s_cand[kStageCap];
+  __shared__ unsigned long long s_sel[kStageMaxM + 1];
+  __shared__ __align__(16) float s_wtau[kStageWarps];
+  __shared__ unsigned s_hist[256];
+  __shared__ unsigned s_count, s_nsel, s_rem, s_bin_count;
+  __shared__ unsigned long long s_prefix;
+  __shared__ uint64_t s_bar;
+  pdl_trigger();
+  const int k = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
+  const int lane = t & 31, warp = t >> 5;
+  const float *row = q + ((size_t)b * K + k) * (size_t)V;
+  const size_t o = ((size_t)b * K + k) * M;
+  const unsigned lane_lt = (1u << lane) - 1u;
+  const bool vec = (V & 3) == 0 && ((reinterpret_cast<uintptr_t>(row) & 15) == 0);
+  const uint32_t bar = sm100::smem_addr(&s_bar);
+  if (vec && t == 0) {
+    sm100::mbar_init(bar, 1);
+    sm100::fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_wait();
+
+  // 1. stage the row, then each thread's largest value.  A row of whole
+  // 16-byte words arrives by bulk copies (the copy engine keeps far more of it
+  // in flight than the threads' own loads); other rows element by element.
+  float fmx = -INFINITY;
+  const int V4 = V >> 2;
+  if (vec) {
+    if (t == 0) {
+      constexpr uint32_t kChunk = 16384;
+      const uint32_t bytes = (uint32_t)V * 4u;
+      sm100::mbar_arrive_expect_tx(bar, bytes);
+      for (uint32_t off = 0; off < bytes; off += kChunk)
+        sm100::bulk_load(sm100::smem_addr(s_row) + off, reinterpret_cast<const char *>(row) + off,
+                         bytes - off < kChunk ? bytes - off : kChunk, bar);
+    }
+    const bool landed = sm100::mbar_wait(bar, 0, wait_limit_ns);
+    if (__syncthreads_or(!landed)) {
+      // the copy did not land in time: the result from global memory, and a
+      // second bounded wait so that no copy is left writing this block's
+      // shared memory after it exits
+      radix_topk_block(row, V, M, top_tok + o, top_q + o);
+      sm100::mbar_wait(bar, 0, wait_limit_ns);
+      return;
+    }
+    const float4 *s_row4 = reinterpret_cast<const float4 *>(s_row);
+#pragma unroll 4
+    for (int x4 = t; x4 < V4; x4 += kStageThreads) {
+      const float4 v = s_row4[x4];
+      fmx = fmaxf(fmx, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+    }
+  } else {
+    constexpr int kU = 8;  // eight loads per thread in flight
+    for (int x0 = t; x0 < V; x0 += kU * kStageThreads) {
+      float v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u)
+        if (x0 + u * kStageThreads < V) v[u] = __ldg(row + x0 + u * kStageThreads);
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        if (x0 + u * kStageThreads < V) {
+          s_row[x0 + u * kStageThreads] = v[u];
+          fmx = fmaxf(fmx, v[u]);
+        }
+      }
+    }
+  }
+  if (t == 0) {
+    s_count = 0u;
+    s_nsel = 0u;
+  }
+  // 2. the warp's ceil(M/32)-th largest thread maximum; tau the least of them
+  {
+    const float x = warp_sort_desc(fmx, lane);
+    const int mw = (M + kStageWarps - 1) / kStageWarps;  // 1..16 for M <= 511
+    const float wt = __shfl_sync(0xffffffffu, x, mw - 1);
+    if (lane == 0) s_wtau[warp] = wt;
+  }
+  __syncthreads();
+  float tau = INFINITY;
+#pragma unroll
+  for (int w = 0; w < kStageWarps; w += 4) {
+    const float4 w4 = *reinterpret_cast<const float4 *>(&s_wtau[w]);
+    tau = fminf(tau, fminf(fminf(w4.x, w4.y), fminf(w4.z, w4.w)));
+  }
+
+  // 3. candidates: every element with !(v < tau), appended a warp at a time
+  auto put = [&](unsigned i, float v, int x) {
+    if (i < (unsigned)kStageCap)
+      s_cand[i] = ((unsigned long long)order_key(v) << 32) | (unsigned long long)(0xFFFFFFFFu - (unsigned)x);
+  };
+  if (vec) {
+    const float4 *s_row4 = reinterpret_cast<const float4 *>(s_row);
+    // (kept rolled: the append path is long and rarely taken)
+#pragma unroll 1
+    for (int w0 = warp * 32; w0 < V4; w0 += kStageThreads) {
+      {
+        const int x4 = w0 + lane;
+        unsigned m = 0u;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (x4 < V4) {
+          v = s_row4[x4];
+          m = (unsigned)!(v.x < tau) | ((unsigned)!(v.y < tau) << 1) | ((unsigned)!(v.z < tau) << 2) |
+              ((unsigned)!(v.w < tau) << 3);
+        }
+        if (__any_sync(0xffffffffu, m != 0u)) {
+          const unsigned b0 = __ballot_sync(0xffffffffu, m & 1u), b1 = __ballot_sync(0xffffffffu, m & 2u);
+          const unsigned b2 = __ballot_sync(0xffffffffu, m & 4u), b3 = __ballot_sync(0xffffffffu, m & 8u);
+          const unsigned c0 = __popc(b0), c1 = __popc(b1), c2 = __popc(b2), c3 = __popc(b3);
+          unsigned base = 0u;
+          if (lane == 0) base = atomicAdd(&s_count, c0 + c1 + c2 + c3);
+          base = __shfl_sync(0xffffffffu, base, 0);
+          if (m & 1u) put(base + __popc(b0 & lane_lt), v.x, 4 * x4);
+          if (m & 2u) put(base + c0 + __popc(b1 & lane_lt), v.y, 4 * x4 + 1);
+          if (m & 4u) put(base + c0 + c1 + __popc(b2 & lane_lt), v.z, 4 * x4 + 2);
+          if (m & 8u) put(base + c0 + c1 + c2 + __popc(b3 & lane_lt), v.w, 4 * x4 + 3);
+        }
+      }
+    }
+  } else {
+    for (int w0 = warp * 32; w0 < V; w0 += kStageThreads) {
+      const int x = w0 + lane;
+      float v = 0.f;
+      bool pass = false;
+      if (x < V) {
+        v = s_row[x];
+        pass = !(v < tau);
+      }
+      const unsigned bal = __ballot_sync(0xffffffffu, pass);
+      if (bal) {
+        unsigned base = 0u;
+        if (lane == 0) base = atomicAdd(&s_count, (unsigned)__popc(bal));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        if (pass) put(base + __popc(bal & lane_lt), v, x);
+      }
+    }
+  }
+  __syncthreads();
+  const int n = (int)s_count;
+  if (n > kStageCap) {  // block-uniform
+    radix_topk_block(row, V, M, top_tok + o, top_q + o);
+    return;
+  }
+
+  // 4. the M largest candidates: radix select
+  unsigned long long prefix = 0ull, pmask = 0ull;
+  if (n > M) {
+    unsigned remaining = (unsigned)M;
+    for (int shift = 56; shift >= 0; shift -= 8) {
+      if (t < 256) s_hist[t] = 0u;
+      __syncthreads();
+      for (int i = t; i < n; i += kStageThreads) {
+        const unsigned long long kk = s_cand[i];
+        if ((kk & pmask) == prefix) atomicAdd(&s_hist[(unsigned)(kk >> shift) & 0xFFu], 1u);
+      }
+      __syncthreads();
+      if (warp == 0) {
+        // lane l owns bins 255-8l .. 248-8l (descending)
+        unsigned c[8], sum = 0u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          c[j] = s_hist[255 - 8 * lane - j];
+          sum += c[j];
+        }
+        unsigned incl = sum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const unsigned y = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += y;
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, incl >= remaining);
+        if (lane == __ffs(hit) - 1) {
+          // the first of this lane's bins where the running count reaches
+          // `remaining` (unrolled: the counts stay in registers)
+          unsigned cum = incl - sum, pick_cum = 0u, pick_c = 0u;
+          int pick_j = -1;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (pick_j < 0 && cum + c[j] >= remaining) {
+              pick_j = j;
+              pick_cum = cum;
+              pick_c = c[j];
+            }
+            cum += c[j];
+          }
+          s_prefix = prefix | ((unsigned long long)(255 - 8 * lane - pick_j) << shift);
+          s_rem = remaining - pick_cum;
+          s_bin_count = pick_c;
+        }
+      }
+      __syncthreads();
+      prefix = s_prefix;
+      remaining = s_rem;
+      pmask |= 0xFFull << shift;
+      if (s_bin_count == remaining) break;  // the bin is taken whole (block-uniform)
+    }
+  }
+  // kept: every key whose selected digits are >= the prefix (exactly M keys)
+  for (int i = t; i < n; i += kStageThreads) {
+    const unsigned long long kk = s_cand[i];
+    if ((kk & pmask) >= prefix) s_sel[atomicAdd(&s_nsel, 1u)] = kk;
+  }
+  __syncthreads();
+
+  // 5. runs of 32 sorted by one warp each (padding 0 sorts below every key:
+  // a key's low word 0xFFFFFFFF - index is never 0 for index < V), then ranks
+  const int runs = (M + 31) >> 5;
+  unsigned long long key = 0ull;
+  if (warp < runs) {
+    const int i = warp * 32 + lane;
+    key = warp_sort_desc(i < M ? s_sel[i] : 0ull, lane);
+    s_cand[i] = key;  // the candidates are no longer needed
+  }
+  __syncthreads();
+  if (warp < runs && key != 0ull) {
+    int rank = lane;
+    for (int r = 0; r < runs; ++r) {
+      if (r == warp) continue;
+      const unsigned long long *run = s_cand + r * 32;
+      int pos = 0;  // keys of run r above `key` (the run is descending)
+#pragma unroll
+      for (int step = 16; step > 0; step >>= 1)
+        if (run[pos + step - 1] > key) pos += step;
+      pos += run[pos] > key ? 1 : 0;  // the search reaches 31 at most; all 32 above
+      rank += pos;
+    }
+    const int idx = (int)(0xFFFFFFFFu - (unsigned)(key & 0xFFFFFFFFull));
+    top_tok[o + rank] = idx;
+    top_q[o + rank] = s_row[idx];
+  }
+}
+
+// Ranked top M of every row of q [B][K][V]: the staged threshold filter for
+// rows that fit in shared memory, else the threshold filter, or the radix
+// select for M >= kFiltThreads.
 cudaError_t launch_topk(const float *q, int K, int B, int V, int M, int32_t *top_tok, float *top_q,
                         cudaStream_t s) {
+  if (M <= kStageMaxM && V <= kStageMaxV) {
+    const size_t smem = align_up((size_t)V * sizeof(float), 16);
+    if (!set_smem((const void *)topk_stage_kernel, (size_t)kStageMaxV * sizeof(float)))
+      return cudaErrorInvalidValue;
+    return launch(topk_stage_kernel, dim3(K, B), dim3(kStageThreads), smem, s, q, K, V, M, top_tok,
+                  top_q, (unsigned long long)option(TSD_OPT_WAIT_LIMIT_NS));
+  }
   if (M < kFiltThreads)
     return launch(topk_filter_kernel, dim3(K, B), dim3(kFiltThreads), 0, s, q, K, V, M, top_tok,
                   top_q);

@@ -1,19 +1,27 @@
 // Host-side state shared by the entry points: device properties, process-wide
 // options, version.
 
+#include <atomic>
+#include <mutex>
+
 #include "tsd_common.cuh"
 
 namespace tsd {
 
 int sm_count() {
-  static int cached[64] = {0};
+  // one value per device; a relaxed atomic is enough (every thread that fills
+  // it stores the same number)
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
-  if (dev < 64 && cached[dev] > 0) return cached[dev];
+  if (dev < 64) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
     n = 148;
-  if (dev < 64) cached[dev] = n;
+  if (dev < 64) cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
@@ -25,14 +33,18 @@ static int64_t g_options[TSD_OPT_COUNT] = {
 int64_t option(int key) { return (key >= 0 && key < TSD_OPT_COUNT) ? g_options[key] : 0; }
 
 bool set_smem(const void *kernel, size_t bytes) {
+  // (kernel, device) pairs whose limit is already raised, under a mutex so
+  // that concurrent first calls from several host threads are safe
   struct Entry {
     const void *fn;
     int dev;
   };
+  static std::mutex mu;
   static Entry done[64];
   static int n_done = 0;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lock(mu);
   for (int i = 0; i < n_done; ++i)
     if (done[i].fn == kernel && done[i].dev == dev) return true;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
