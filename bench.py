@@ -163,6 +163,7 @@ def _code_only(text):
 KERNEL_SOURCES = {
     "tree_attn_fwd": ["attention.cu", "sm100_ptx.cuh", "tsd_common.cuh"],
     "tree_verify_greedy": ["verify.cu", "commit_core.cuh", "sm100_ptx.cuh", "tsd_common.cuh"],
+    "best_first_tree_build": ["best_first.cu", "sm100_ptx.cuh", "tsd_common.cuh"],
 }
 
 
