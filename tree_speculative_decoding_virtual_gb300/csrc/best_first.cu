@@ -675,8 +675,9 @@ topk_filter_kernel(const float *__restrict__ q, int K, int V, int M, int32_t *__
 
 // The threshold filter with the row staged in shared memory (rows of at most
 // kStageMaxV floats): one block of 1024 threads per row.
-//  1. The row is read once (16-byte loads) and kept in shared memory; each
-//     thread keeps the largest of its values (NaN ignored).
+//  1. The row is read once into shared memory (bulk copies for rows of whole
+//     16-byte words, else element loads); each thread keeps the largest of
+//     its values (NaN ignored).
 //  2. Each warp sorts its 32 thread maxima (shuffles) and takes the
 //     ceil(M/32)-th; tau, the least of the warps' values, has at least M
 //     non-NaN elements at or above it, so every one of the M best (by order
