@@ -69,3 +69,20 @@ def test_kernel_sources_exist():
         for n in names:
             assert os.path.isfile(os.path.join(csrc, n)), (key, n)
 
+
+
+def test_reference_arm_line_contract(capsys):
+    """The reference arm (the oracle timed on the host cores) prints one JSON
+    line with the metric, the oracle's baseline block and a zero-copy e2e."""
+    import json
+    rc = bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "3", "--warmup", "3"])
+    assert rc in (None, 0)
+    line = [l for l in capsys.readouterr().out.strip().splitlines() if l.startswith("{")][-1]
+    d = json.loads(line)
+    assert d["impl"] == "reference" and d["steps"] == 3 and d["warmup"] == 3
+    assert d["unit"] == "steps/s" and d["higher_is_better"] is True and d["value"] > 0
+    assert d["config"]["workload"]
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
